@@ -1,0 +1,266 @@
+"""CPU oracle of the forward pass of one sparse Mixture-of-Experts FFN layer.
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the package's smoke check and the
+benchmark's CPU-baseline leg may import this module.  It shares no code with the CUDA library
+and the library never calls it.
+
+Everything is computed in float64 from the exact (bf16 or fp32) tensors the GPU consumes,
+with an explicit loop over experts, in the order the sources describe the layer:
+
+  1. router logits  z = x W_r^T (+ a fixed logit bias)      -- mini-moe tutorial, sec. 3.1
+     (MoELayer: the router is a bias-free Linear); GPT-4 2%-parameters article, sec. 3.2
+  2. P = softmax(z) per token, lse = logsumexp(z)            -- mini-moe tutorial, sec. 3.1
+  3. top-k experts by descending logit                       -- mini-moe tutorial, sec. 3.1
+     (torch.topk); the pages fix no tie rule, so equal logits go to the lower expert index
+  4. weights renormalised over the k selected, w = P_sel / sum P_sel
+                                                              -- mini-moe tutorial, sec. 3.1;
+     OpenMythos article, sec. 3.1 (routing pseudo-code); equal to the GPT-4 article's softmax
+     over the k selected logits (sec. 4.1 MoELayer)
+  5. capacity C = ceil(cf * T * k / E) (exact rational ceil), assignments of each expert ranked in
+     token order, rank >= C dropped (weight 0, no renormalisation)
+                                                              -- OpenMythos article, sec. 3.1
+     (capacity factor and overflow handling)
+  6. expert FFN: GELU(erf) form  W2 gelu(W1 x + b1) + b2      -- mini-moe tutorial, sec. 3.1
+                 SwiGLU form     Wd (silu(Wg x) * (Wu x))     -- GPT-4 article, sec. 3.1
+  7. y_t = sum over kept slots of w_tj FFN_{e_tj}(x_t) + sum over shared experts FFN_s(x_t)
+                                                              -- FLAME-MoE summary, sec. 2
+     (weighted sum of the selected experts; 2 shared experts active for every token)
+  8. load-balance loss  lb = alpha * E * sum_e f_e * Pbar_e, f_e = counts_e / (T k),
+     Pbar_e = mean_t P_te                                     -- OpenMythos article, sec. 3.1
+     router z-loss      zl = beta * mean_t lse_t^2            -- named but not written out in the
+     FLAME-MoE summary, sec. 2; the formula used is the standard router z-loss
+
+Pins (tests/test_oracle_pins.py): each function here is checked against something other than
+itself -- brute-force sorting, closed forms, library routines (torch.nn.functional) on special
+cases that reduce to a dense FFN, and hand-worked fixtures under tests/golden/.  The numeric
+value of a full layer on random inputs has no worked example on the pages: beyond those
+reductions it is "parity unpinned" by the pages and rests on the pinned parts.
+"""
+from __future__ import annotations
+
+import math
+from fractions import Fraction
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+from scipy import special as _sp
+
+
+def _f64(a) -> Optional[np.ndarray]:
+    """Widen a torch tensor or array-like to a float64 numpy array (exact for bf16/fp32)."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        import torch  # local: only for the dtype conversion
+        return a.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------- routing
+def router_logits(x, w_router, logit_bias=None) -> np.ndarray:
+    """z[t, e] = sum_i x[t, i] W_r[e, i] (+ logit_bias[e]).
+
+    mini-moe tutorial, sec. 3.1: the router is one Linear(hidden_dim -> num_experts) without
+    bias; the optional fixed bias vector models the skewed-routing workload (routing collapse,
+    Naive-N0.5-Flash article sec. 2.2)."""
+    z = _f64(x) @ _f64(w_router).T
+    if logit_bias is not None:
+        z = z + _f64(logit_bias)[None, :]
+    return z
+
+
+def softmax_lse(z: np.ndarray):
+    """Row softmax P and log-sum-exp lse of the logits (max-subtracted)."""
+    if z.shape[0] == 0:
+        return np.zeros_like(z), np.zeros(0)
+    m = z.max(axis=1, keepdims=True)
+    ex = np.exp(z - m)
+    s = ex.sum(axis=1, keepdims=True)
+    return ex / s, (m + np.log(s))[:, 0]
+
+
+def topk_select(z: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, in descending order; equal logits are ordered
+    by ascending expert index (so the lower index wins a tie at the k-th place)."""
+    T, E = z.shape
+    if T == 0:
+        return np.zeros((0, k), dtype=np.int64)
+    order = np.lexsort((np.broadcast_to(np.arange(E), (T, E)), -z), axis=-1)
+    return order[:, :k].astype(np.int64)
+
+
+def topk_gap(z: np.ndarray, k: int) -> np.ndarray:
+    """z_(k) - z_(k+1): the logit margin at the selection boundary (+inf when k == E)."""
+    T, E = z.shape
+    if k >= E:
+        return np.full(T, np.inf)
+    zs = -np.sort(-z, axis=1)
+    return zs[:, k - 1] - zs[:, k]
+
+
+def renormalise(P: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """w_tj = P[t, idx_tj] / sum_j P[t, idx_tj]."""
+    sel = np.take_along_axis(P, idx, axis=1)
+    return sel / sel.sum(axis=1, keepdims=True)
+
+
+# ----------------------------------------------------------------------------- dispatch
+def capacity(cf: float, T: int, k: int, E: int) -> Optional[int]:
+    """Expert capacity ceil(cf * T * k / E), exact in rationals (cf taken as the float32 value
+    the C struct carries); None when cf <= 0 (dropless)."""
+    if cf <= 0:
+        return None
+    cf32 = float(np.float32(cf))
+    return int(math.ceil(Fraction(cf32) * T * k / E))
+
+
+def dispatch(idx: np.ndarray, E: int, cap: Optional[int]) -> Dict[str, np.ndarray]:
+    """Expert-sorted layout of the routed (token, slot) assignments.
+
+    Each expert's assignments are ranked in increasing token order; rank >= cap is dropped.
+    Kept rows are laid out expert after expert, tokens ascending inside an expert."""
+    T, k = idx.shape
+    counts = np.zeros(E, dtype=np.int64)
+    rank = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            rank[t, j] = counts[e]
+            counts[e] += 1
+    kept_counts = counts.copy() if cap is None else np.minimum(counts, cap)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(kept_counts)
+    row_of = np.full((T, k), -1, dtype=np.int64)
+    tok_of = np.zeros(int(offsets[E]), dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            if cap is None or rank[t, j] < cap:
+                r = int(offsets[e] + rank[t, j])
+                row_of[t, j] = r
+                tok_of[r] = t
+    return dict(counts=counts, kept_counts=kept_counts, offsets=offsets, row_of=row_of,
+                tok_of=tok_of, drops=int(T * k - offsets[E]))
+
+
+# ----------------------------------------------------------------------------- experts
+def gelu_erf(u: np.ndarray) -> np.ndarray:
+    """GELU in its exact erf form, u * (1 + erf(u / sqrt 2)) / 2 (torch's nn.GELU default)."""
+    return 0.5 * u * (1.0 + _sp.erf(u / math.sqrt(2.0)))
+
+
+def silu(u: np.ndarray) -> np.ndarray:
+    """SiLU u * sigmoid(u)."""
+    return u * _sp.expit(u)
+
+
+def expert_ffn(xr, act: str, w_up, w_down, w_gate=None, b_up=None, b_down=None) -> np.ndarray:
+    """One expert on rows xr [n, d]; weights in nn.Linear layout [out, in].
+
+    gelu:   W_down gelu(W_up x + b_up) + b_down   (mini-moe tutorial, sec. 3.1 experts)
+    swiglu: W_down (silu(W_gate x) * (W_up x))     (GPT-4 article, sec. 3.1)"""
+    xr = _f64(xr)
+    if act == "gelu":
+        u = xr @ _f64(w_up).T
+        if b_up is not None:
+            u = u + _f64(b_up)[None, :]
+        h = gelu_erf(u)
+    elif act == "swiglu":
+        h = silu(xr @ _f64(w_gate).T) * (xr @ _f64(w_up).T)
+    else:
+        raise ValueError(act)
+    y = h @ _f64(w_down).T
+    if b_down is not None:
+        y = y + _f64(b_down)[None, :]
+    return y
+
+
+def combine(idx, w, row_of, y_perm, tokens: Sequence[int], y_shared=None) -> np.ndarray:
+    """y_t = sum over kept slots j (row_of >= 0) of w_tj * y_perm[row_of_tj]  (+ shared output)."""
+    d = y_perm.shape[1] if y_perm.ndim == 2 and y_perm.shape[0] else (
+        y_shared.shape[1] if y_shared is not None else 0)
+    y = np.zeros((len(tokens), d))
+    for i, t in enumerate(tokens):
+        for j in range(idx.shape[1]):
+            r = row_of[t, j]
+            if r >= 0:
+                y[i] += w[t, j] * y_perm[r]
+        if y_shared is not None:
+            y[i] += y_shared[i]
+    return y
+
+
+# ----------------------------------------------------------------------------- losses
+def aux_losses(P: np.ndarray, lse: np.ndarray, counts: np.ndarray, k: int,
+               lb_coef: float, z_coef: float):
+    """(load-balance loss, router z-loss).  lb = alpha E sum_e f_e Pbar_e with f_e = counts_e/(T k)
+    (pre-drop router counts) and Pbar_e = mean_t P_te; zl = beta mean_t lse_t^2.  Both are 0 for
+    an empty batch."""
+    T, E = P.shape
+    if T == 0:
+        return 0.0, 0.0
+    f = counts / float(T * k)
+    pbar = P.sum(axis=0) / T
+    lb = lb_coef * E * float(np.sum(f * pbar))
+    zl = z_coef * float(np.sum(lse * lse)) / T
+    return lb, zl
+
+
+def lb_loss_squared_mean_form(P: np.ndarray, lb_coef: float) -> float:
+    """Diagnostic variant from the mini-moe tutorial, sec. 3.1 (its auxiliary loss): alpha E sum_e Pbar_e^2."""
+    E = P.shape[1]
+    pbar = P.mean(axis=0)
+    return lb_coef * E * float(np.sum(pbar * pbar))
+
+
+def expert_param_count(d: int, dff: int, act: str = "gelu", bias: bool = False) -> int:
+    """Weights of one expert: 2 d dff for the two-matrix form (Naive-N0.5-Flash article sec. 3.3),
+    3 d dff for SwiGLU; biases add dff + d."""
+    n = (3 if act == "swiglu" else 2) * d * dff
+    return n + ((dff + d) if bias else 0)
+
+
+# ----------------------------------------------------------------------------- whole layer
+def moe_layer(inp: Dict, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
+              lb_coef: float = 0.01, z_coef: float = 0.001,
+              tokens: Optional[Sequence[int]] = None) -> Dict:
+    """Forward pass of the layer on ``inp`` (the tensors of ``synth.make_inputs``).
+
+    Routing, dispatch and losses are computed for every token; the FFNs and the combine only for
+    ``tokens`` (all tokens when None).  Returns routing, layout, losses and y [len(tokens), d]."""
+    x = _f64(inp["x"])
+    T = x.shape[0]
+    z = router_logits(x, inp["w_router"], inp.get("logit_bias"))
+    P, lse = softmax_lse(z)
+    idx = topk_select(z, k)
+    w = renormalise(P, idx) if T else np.zeros((0, k))
+    cap = capacity(cf, T, k, E)
+    lay = dispatch(idx, E, cap)
+    lb, zl = aux_losses(P, lse, lay["counts"], k, lb_coef, z_coef)
+    if tokens is None:
+        tokens = list(range(T))
+    tokens = [int(t) for t in tokens]
+    want = set(tokens)
+
+    A = int(lay["offsets"][E])
+    d = x.shape[1]
+    y_perm = np.zeros((A, d))
+    for e in range(E):
+        lo, hi = int(lay["offsets"][e]), int(lay["offsets"][e + 1])
+        rows = [r for r in range(lo, hi) if int(lay["tok_of"][r]) in want]
+        if not rows:
+            continue
+        xr = x[lay["tok_of"][rows]]
+        g = lambda name: None if inp.get(name) is None else inp[name][e]
+        y_perm[rows] = expert_ffn(xr, act, g("w_up"), g("w_down"), g("w_gate"), g("b_up"), g("b_down"))
+
+    y_shared = None
+    if n_shared > 0:
+        xs = x[tokens]
+        y_shared = np.zeros((len(tokens), d))
+        for s in range(n_shared):
+            gs = None if inp.get("ws_gate") is None else inp["ws_gate"][s]
+            y_shared += expert_ffn(xs, act, inp["ws_up"][s], inp["ws_down"][s], gs)
+    y = combine(idx, w, lay["row_of"], y_perm, tokens, y_shared)
+    return dict(z=z, P=P, lse=lse, idx=idx, w=w, gap=topk_gap(z, k), cap=cap, lb=lb, zl=zl,
+                y=y, tokens=np.asarray(tokens, dtype=np.int64), y_perm=y_perm, **lay)

@@ -1,0 +1,324 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each ``check_*`` takes the oracle module, so the same checks can be re-run on the oracle with
+one planted mistake: ``test_planted_mistakes_are_caught`` shows that a dropped term, a wrong
+index, a transposed operand or a wrong rounding rule fails a pin.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special as sps
+import torch
+import torch.nn.functional as F
+
+from oracle import moe_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------------------- checks
+def check_router(o):
+    # library routine: torch's Linear without bias, on a non-square shape
+    x = RNG.standard_normal((5, 7))
+    w = RNG.standard_normal((3, 7))
+    ref = F.linear(torch.from_numpy(x), torch.from_numpy(w)).numpy()
+    np.testing.assert_allclose(o.router_logits(x, w), ref, rtol=1e-13, atol=1e-13)
+    # hand case: x = (1, 2, 3), rows of W_r pick x1 and x2 + x3
+    z = o.router_logits(np.array([[1.0, 2.0, 3.0]]), np.array([[1.0, 0, 0], [0, 1.0, 1.0]]))
+    assert z.tolist() == [[1.0, 5.0]]
+    # the fixed logit bias shifts only its own column
+    zb = o.router_logits(x, w, np.array([2.0, 0.0, 0.0]))
+    np.testing.assert_allclose(zb - ref, np.tile([2.0, 0.0, 0.0], (5, 1)), atol=1e-13)
+
+
+def check_softmax(o):
+    z = RNG.standard_normal((9, 6)) * 3
+    P, lse = o.softmax_lse(z)
+    assert np.all(np.abs(P.sum(1) - 1) <= 1e-12)
+    np.testing.assert_allclose(P, sps.softmax(z, axis=1), rtol=1e-13)
+    np.testing.assert_allclose(lse, sps.logsumexp(z, axis=1), rtol=1e-13)
+    P2, lse2 = o.softmax_lse(np.array([[0.0, math.log(3.0)]]))
+    np.testing.assert_allclose(P2, [[0.25, 0.75]], rtol=1e-14)
+    np.testing.assert_allclose(lse2, [math.log(4.0)], rtol=1e-14)
+    P0, lse0 = o.softmax_lse(np.zeros((2, 8)))
+    assert np.all(P0 == 1.0 / 8) and np.allclose(lse0, math.log(8.0), rtol=1e-15)
+
+
+def check_topk(o):
+    # explicit tie cases
+    assert o.topk_select(np.array([[1.0, 3.0, 3.0, 0.0]]), 2).tolist() == [[1, 2]]
+    assert o.topk_select(np.array([[2.0, 2.0]]), 1).tolist() == [[0]]
+    assert o.topk_select(np.array([[0.0, 5.0, 1.0, 5.0]]), 3).tolist() == [[1, 3, 2]]
+    # brute force: full Python sort by (-z, e) on tiny integer logits (many exact ties)
+    for T, E, k in [(64, 8, 2), (40, 5, 5), (30, 4, 1), (25, 8, 6)]:
+        z = RNG.integers(-2, 3, size=(T, E)).astype(np.float64)
+        got = o.topk_select(z, k)
+        for t in range(T):
+            ref = sorted(range(E), key=lambda e: (-z[t, e], e))[:k]
+            assert got[t].tolist() == ref, (t, z[t])
+        gap = o.topk_gap(z, k)
+        for t in range(T):
+            zs = sorted(z[t], reverse=True)
+            assert gap[t] == (math.inf if k == E else zs[k - 1] - zs[k])
+
+
+def check_renormalise(o):
+    z = RNG.standard_normal((20, 8))
+    P, _ = o.softmax_lse(z)
+    idx = o.topk_select(z, 3)
+    w = o.renormalise(P, idx)
+    assert np.all(np.abs(w.sum(1) - 1) <= 1e-12)
+    # equals the softmax over the selected logits (the GPT-4 article's form)
+    np.testing.assert_allclose(w, sps.softmax(np.take_along_axis(z, idx, 1), axis=1), rtol=1e-12)
+
+
+def check_capacity(o):
+    assert o.capacity(1.25, 8192, 2, 16) == 1280
+    assert o.capacity(1.0, 16384, 2, 128) == 256
+    assert o.capacity(1.0, 10, 1, 3) == 4          # ceil(10/3)
+    assert o.capacity(0.5, 3, 1, 1) == 2           # ceil(1.5)
+    assert o.capacity(0.1, 10, 1, 1) == 2          # float32(0.1) > 0.1, so 10 cf > 1
+    assert o.capacity(0.0, 10, 2, 4) is None and o.capacity(-1.0, 10, 2, 4) is None
+
+
+def _brute_dispatch(idx, E, cap):
+    T, k = idx.shape
+    per = [[(t, j) for t in range(T) for j in range(k) if idx[t, j] == e] for e in range(E)]
+    kept = [p if cap is None else p[:cap] for p in per]
+    rows = [a for e in range(E) for a in kept[e]]
+    return per, kept, rows
+
+
+def check_dispatch(o):
+    for T, E, k, cap in [(50, 6, 2, None), (50, 6, 2, 7), (33, 4, 3, 1), (16, 8, 8, 2), (1, 3, 1, 1)]:
+        z = RNG.standard_normal((T, E))
+        z[:, 0] += 1.5   # skew so that capacity bites
+        idx = o.topk_select(z, k)
+        lay = o.dispatch(idx, E, cap)
+        per, kept, rows = _brute_dispatch(idx, E, cap)
+        assert lay["counts"].tolist() == [len(p) for p in per]
+        assert int(lay["counts"].sum()) == T * k
+        assert lay["kept_counts"].tolist() == [len(p) for p in kept]
+        assert int(lay["kept_counts"].sum()) == T * k - lay["drops"]
+        if cap is not None:
+            assert lay["kept_counts"].tolist() == [min(len(p), cap) for p in per]
+        assert lay["offsets"].tolist() == [0] + list(np.cumsum([len(p) for p in kept]))
+        assert lay["tok_of"].tolist() == [t for (t, _) in rows]
+        for r, (t, j) in enumerate(rows):
+            assert lay["row_of"][t, j] == r
+        n_kept = int((lay["row_of"] >= 0).sum())
+        assert n_kept == len(rows)
+        for e in range(E):
+            toks = lay["tok_of"][lay["offsets"][e]:lay["offsets"][e + 1]]
+            assert np.all(np.diff(toks) > 0)
+
+
+def check_activations(o):
+    u = np.linspace(-9, 9, 1001)
+    np.testing.assert_allclose(o.gelu_erf(u), F.gelu(torch.from_numpy(u)).numpy(), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(o.silu(u), F.silu(torch.from_numpy(u)).numpy(), rtol=1e-12, atol=1e-15)
+    assert o.gelu_erf(np.array([0.0]))[0] == 0.0 and o.silu(np.array([0.0]))[0] == 0.0
+    assert abs(o.gelu_erf(np.array([1.0]))[0] - 0.5 * (1 + math.erf(1 / math.sqrt(2)))) < 1e-15
+
+
+def _torch_ffn(xr, act, w_up, w_down, w_gate=None, b_up=None, b_down=None):
+    t = lambda a: None if a is None else torch.as_tensor(np.asarray(a, np.float64))
+    x = t(xr)
+    if act == "gelu":
+        h = F.gelu(F.linear(x, t(w_up), t(b_up)))
+    else:
+        h = F.silu(F.linear(x, t(w_gate))) * F.linear(x, t(w_up))
+    return F.linear(h, t(w_down), t(b_down)).numpy()
+
+
+def check_expert_ffn(o):
+    d, f = 12, 20
+    xr = RNG.standard_normal((7, d))
+    wu, wd, wg = RNG.standard_normal((f, d)), RNG.standard_normal((d, f)), RNG.standard_normal((f, d))
+    bu, bd = RNG.standard_normal(f), RNG.standard_normal(d)
+    np.testing.assert_allclose(o.expert_ffn(xr, "gelu", wu, wd, None, bu, bd),
+                               _torch_ffn(xr, "gelu", wu, wd, None, bu, bd), rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(o.expert_ffn(xr, "swiglu", wu, wd, wg),
+                               _torch_ffn(xr, "swiglu", wu, wd, wg), rtol=1e-11, atol=1e-11)
+
+
+def _identical_expert_inputs(T, d, E, f, act, S=0, bias=True):
+    x = RNG.standard_normal((T, d))
+    wr = RNG.standard_normal((E, d))
+    wu, wd, wg = RNG.standard_normal((f, d)), RNG.standard_normal((d, f)), RNG.standard_normal((f, d))
+    bu, bd = RNG.standard_normal(f), RNG.standard_normal(d)
+    rep = lambda a: np.repeat(a[None], E, 0)
+    inp = dict(x=x, w_router=wr, logit_bias=None, w_up=rep(wu), w_down=rep(wd),
+               w_gate=rep(wg) if act == "swiglu" else None,
+               b_up=rep(bu) if (bias and act == "gelu") else None,
+               b_down=rep(bd) if (bias and act == "gelu") else None)
+    if S:
+        inp.update(ws_up=np.repeat(wu[None], S, 0), ws_down=np.repeat(wd[None], S, 0),
+                   ws_gate=np.repeat(wg[None], S, 0) if act == "swiglu" else None)
+    dense = _torch_ffn(x, act, wu, wd, wg if act == "swiglu" else None,
+                       inp["b_up"][0] if inp["b_up"] is not None else None,
+                       inp["b_down"][0] if inp["b_down"] is not None else None)
+    return inp, dense
+
+
+def check_layer_reductions(o):
+    # k = E with identical experts: the renormalised weights sum to 1, so y is one dense FFN
+    for act in ("gelu", "swiglu"):
+        inp, dense = _identical_expert_inputs(T=24, d=10, E=4, f=16, act=act)
+        out = o.moe_layer(inp, E=4, k=4, act=act)
+        np.testing.assert_allclose(out["y"], dense, rtol=1e-10, atol=1e-10)
+    # E = 1, k = 1: a dense FFN
+    inp, dense = _identical_expert_inputs(T=9, d=8, E=1, f=8, act="gelu")
+    np.testing.assert_allclose(o.moe_layer(inp, E=1, k=1, act="gelu")["y"], dense, rtol=1e-10, atol=1e-10)
+    # shared experts identical to the routed ones, no biases: y = (1 + S) dense FFN
+    inp, dense = _identical_expert_inputs(T=11, d=8, E=3, f=16, act="swiglu", S=2, bias=False)
+    np.testing.assert_allclose(o.moe_layer(inp, E=3, k=2, act="swiglu", n_shared=2)["y"], 3 * dense,
+                               rtol=1e-10, atol=1e-10)
+    # capacity: all tokens forced onto expert 0 with k = 1 and cap = 3; later tokens get nothing
+    inp, dense = _identical_expert_inputs(T=10, d=6, E=3, f=8, act="gelu")
+    inp["logit_bias"] = np.array([1e3, 0.0, 0.0])
+    out = o.moe_layer(inp, E=3, k=1, act="gelu", cf=0.9)  # cap = ceil(0.9 * 10 / 3) = 3
+    assert out["cap"] == 3 and out["drops"] == 7
+    np.testing.assert_allclose(out["y"][:3], dense[:3], rtol=1e-10, atol=1e-10)
+    assert np.all(out["y"][3:] == 0)
+    # subset evaluation equals the rows of the full evaluation
+    inp, _ = _identical_expert_inputs(T=15, d=6, E=5, f=8, act="gelu")
+    inp["w_up"] = RNG.standard_normal(inp["w_up"].shape)
+    full = o.moe_layer(inp, E=5, k=2, act="gelu")
+    sub = o.moe_layer(inp, E=5, k=2, act="gelu", tokens=[3, 0, 14])
+    np.testing.assert_allclose(sub["y"], full["y"][[3, 0, 14]], rtol=1e-13, atol=1e-13)
+
+
+def check_losses(o):
+    E, T, k = 8, 32, 2
+    # zero router weights: every Pbar_e = 1/E exactly, so lb = alpha for any counts; zl = beta (ln E)^2
+    P, lse = o.softmax_lse(np.zeros((T, E)))
+    for counts in (np.full(E, T * k // E), np.array([T * k] + [0] * (E - 1))):
+        lb, zl = o.aux_losses(P, lse, counts, k, 0.01, 0.001)
+        assert abs(lb - 0.01) < 1e-15
+        assert abs(zl - 0.001 * math.log(E) ** 2) < 1e-15
+    assert abs(o.lb_loss_squared_mean_form(P, 0.01) - 0.01) < 1e-15
+    # two experts, every assignment on expert 0, Pbar = (p, 1-p): lb = alpha * 2 * p
+    z = np.array([[math.log(3.0), 0.0]] * 4)     # P = (3/4, 1/4)
+    P, lse = o.softmax_lse(z)
+    lb, zl = o.aux_losses(P, lse, np.array([4, 0]), 1, 0.5, 1.0)
+    assert abs(lb - 0.5 * 2 * 0.75) < 1e-14
+    assert abs(zl - math.log(4.0) ** 2) < 1e-14
+    assert o.aux_losses(np.zeros((0, 4)), np.zeros(0), np.zeros(4), 2, 0.01, 0.001) == (0.0, 0.0)
+
+
+ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
+              check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
+              check_losses]
+
+
+@pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
+def test_oracle_pin(check):
+    check(O)
+
+
+def test_param_count_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "param_count_example.json")))
+    M = 2 ** 20
+    d, n, k = g["d_model"], g["n_expert"], g["top_k"]
+    per = O.expert_param_count(d, g["d_ff_expert"], "gelu")
+    assert round(per / M) == g["params_per_expert_M"]
+    assert round(n * per / M) == g["params_all_experts_M"]
+    assert round(O.expert_param_count(d, g["d_ff_dense"], "gelu") / M) == g["params_dense_ffn_M"]
+    assert round(k * per / M) == g["params_active_M"]
+
+
+def test_shape_contract_example():
+    g = json.load(open(os.path.join(GOLDEN, "shape_contract_example.json")))
+    T = g["batch_size"] * g["seq_len"]
+    d, E, f, k = g["d_model"], g["num_experts"], g["expert_hidden_dim"], g["k"]
+    rng = np.random.default_rng(7)
+    inp = dict(x=rng.standard_normal((T, d)), w_router=rng.standard_normal((E, d)) * 0.02,
+               w_up=rng.standard_normal((E, f, d)) * 0.02, w_down=rng.standard_normal((E, d, f)) * 0.02)
+    out = O.moe_layer(inp, E=E, k=k, act="gelu")
+    assert out["y"].reshape(g["batch_size"], g["seq_len"], d).shape == (g["batch_size"], g["seq_len"], d)
+
+
+def test_flame_moe_config_matches_pages():
+    from synth import WORKLOADS
+    g = json.load(open(os.path.join(GOLDEN, "flame_moe_layer.json")))
+    wl = WORKLOADS["finegrained_bf16"]
+    assert wl.E == g["experts_per_layer"] and wl.n_shared == g["shared_experts"]
+    assert wl.k == g["routed_top_k"] == g["active_per_token"] - g["shared_experts"]
+    assert wl.lb_coef == g["load_balance_coef"] and wl.z_coef == g["router_z_loss_coef"]
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+def _mut_router_transposed(x, w, b=None):
+    z = np.asarray(x, np.float64) @ np.asarray(w, np.float64).T[::-1]
+    return z
+
+
+def _mut_topk_high_index(z, k):
+    T, E = z.shape
+    order = np.lexsort((-np.broadcast_to(np.arange(E), (T, E)), -z), axis=-1)
+    return order[:, :k]
+
+
+def _mut_no_renorm(P, idx):
+    return np.take_along_axis(P, idx, axis=1)
+
+
+_REAL = dict(dispatch=O.dispatch, aux_losses=O.aux_losses, expert_ffn=O.expert_ffn)
+
+
+def _mut_dispatch_reverse(idx, E, cap):
+    return _REAL["dispatch"](idx[::-1].copy(), E, cap)
+
+
+def _mut_lb_without_E(P, lse, counts, k, a, b):
+    lb, zl = _REAL["aux_losses"](P, lse, counts, k, a, b)
+    return lb / P.shape[1] if P.shape[0] else lb, zl
+
+
+def _mut_gelu_tanh(u):
+    return 0.5 * u * (1 + np.tanh(math.sqrt(2 / math.pi) * (u + 0.044715 * u ** 3)))
+
+
+def _mut_ffn_no_bias(xr, act, w_up, w_down, w_gate=None, b_up=None, b_down=None):
+    return _REAL["expert_ffn"](xr, act, w_up, w_down, w_gate, b_up, None)
+
+
+def _mut_capacity_floor(cf, T, k, E):
+    return None if cf <= 0 else int(cf * T * k // E)
+
+
+def _mut_combine_unweighted(idx, w, row_of, y_perm, tokens, y_shared=None):
+    return O_combine(idx, np.ones_like(w), row_of, y_perm, tokens, y_shared)
+
+
+def _mut_silu_sigmoid(u):
+    return sps.expit(u)
+
+
+O_combine = O.combine
+
+
+@pytest.mark.parametrize("name,fn,check", [
+    ("router_logits", _mut_router_transposed, check_router),
+    ("topk_select", _mut_topk_high_index, check_topk),
+    ("renormalise", _mut_no_renorm, check_renormalise),
+    ("dispatch", _mut_dispatch_reverse, check_dispatch),
+    ("aux_losses", _mut_lb_without_E, check_losses),
+    ("gelu_erf", _mut_gelu_tanh, check_activations),
+    ("expert_ffn", _mut_ffn_no_bias, check_expert_ffn),
+    ("capacity", _mut_capacity_floor, check_capacity),
+    ("combine", _mut_combine_unweighted, check_layer_reductions),
+    ("silu", _mut_silu_sigmoid, check_expert_ffn),
+])
+def test_planted_mistakes_are_caught(name, fn, check, monkeypatch):
+    """Plant one mistake in the oracle module itself (so its internal callers see it too)."""
+    real = getattr(O, name)
+    monkeypatch.setattr(O, name, fn)
+    with pytest.raises((AssertionError, ValueError, IndexError)):
+        check(O)
+    monkeypatch.setattr(O, name, real)
