@@ -1,0 +1,386 @@
+"""Benchmark of the sparse MoE FFN layer forward on B300 (one JSON line on stdout, rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one full ``moe_layer_forward`` (route, dispatch, expert FFNs, combine, losses) over one
+batch of synthetic tokens already resident in HBM.  Per-GPU work is fixed (``"scaling": "weak"``):
+under torchrun every rank runs an independent replica of the layer on its own GPU (the layer
+needs no exchange between replicas), and the value counts the tokens of all ranks over the
+slowest rank's time.
+
+``--impl reference`` times the CPU oracle (fp64 NumPy, explicit per-expert loop) on a bounded
+token sample of the same workload; only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from synth import WORKLOADS, make_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "flash_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM bytes per launch of the routed up-projection kernel, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload; valid only while the kernel
+# source hash matches the one the capture was taken with.
+NCU_TRAFFIC = {
+    # "flash_bf16": {"bytes": ..., "src_sha1": "..."},
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_src_sha1():
+    h = hashlib.sha1()
+    for name in ("gemm_tc.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "mixture_experts_layer_89_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+def expert_flops(wl, kept_rows: int, T: int):
+    """Algorithmic expert FLOPs: 2 * rows * (matrices * d * dff) for the kept routed rows plus the
+    shared experts on every token; (up, down) split."""
+    m_up = 2 if wl.act == "swiglu" else 1
+    up = 2.0 * kept_rows * m_up * wl.d * wl.dff
+    down = 2.0 * kept_rows * wl.d * wl.dff
+    sh_up = 2.0 * T * wl.n_shared * m_up * wl.d * wl.dff
+    sh_down = 2.0 * T * wl.n_shared * wl.d * wl.dff
+    return up, down, sh_up, sh_down
+
+
+# ------------------------------------------------------------------------------ our arm
+def run_ours(args, wl, ws_n, rank, local):
+    from mixture_experts_layer_89_b300 import moe
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = make_inputs(wl, str(dev))
+    cfg = moe.config_from_workload(wl)
+    layer = moe.MoELayer(cfg, inp, device=dev)
+    T, d = wl.T, wl.d
+    y = torch.empty_like(inp["x"])
+    losses = torch.empty(2, dtype=torch.float32, device=dev)
+    counts = torch.empty(wl.E, dtype=torch.int32, device=dev)
+    drops = torch.empty(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_ev = 7
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+
+    def step(i=None):
+        if i is None:
+            moe.moe_layer_forward(cfg, layer.weights, inp["x"], y, losses, counts, drops, layer.ws, stream)
+        else:
+            moe.moe_layer_forward_timed(cfg, layer.weights, inp["x"], y, losses, counts, drops, layer.ws, evs[i],
+                                        stream)
+
+    for _ in range(args.warmup):
+        step()
+    st = moe.moe_read_device_status(layer.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {moe.moe_status_string(st)}")
+    kept_rows = int(wl.T * wl.k - drops.item())
+
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(ms_total)
+    ms_step = ms_total / args.steps
+    stages = ["route", "dispatch", "up", "down", "shared", "combine"]
+    stage_ms = {s: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+                for j, s in enumerate(stages)}
+
+    up, down, sh_up, sh_down = expert_flops(wl, kept_rows, T)
+    total_expert = up + down + sh_up + sh_down
+    peaks, peak_src = load_peaks()
+    up_tflops = up / (stage_ms["up"] * 1e-3) / 1e12
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = None
+    rec = NCU_TRAFFIC.get(wl.name)
+    if rec and rec.get("src_sha1") == kernel_src_sha1():
+        traffic = rec["bytes"]
+    roofline = {"bound": "tensor", "kernel": "k_proj_tc<SwiGLU|GELU> routed up-projection",
+                "achieved": round(up_tflops, 2), "peak": peak_sus, "unit": "TFLOP/s",
+                "frac": round(up_tflops / peak_sus, 4), "frac_of_burst_peak": round(up_tflops / peak_burst, 4),
+                "peak_source": f"{peak_src} bf16_tflops_sustained", "traffic": traffic,
+                "algorithmic_flops_per_launch": up}
+    expert_ms = stage_ms["up"] + stage_ms["down"] + stage_ms["shared"]
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    l_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    for _ in range(max(1, args.warmup // 2)):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(cfg, layer.weights, x_dev, y, losses, counts, drops, layer.ws, stream)
+        y_host.copy_(y, non_blocking=True)
+        l_host.copy_(losses, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(cfg, layer.weights, x_dev, y, losses, counts, drops, layer.ws, stream)
+        y_host.copy_(y, non_blocking=True)
+        l_host.copy_(losses, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+    h2d = x_host.numel() * x_host.element_size()
+    d2h = y_host.numel() * y_host.element_size() + 8
+    st = moe.moe_read_device_status(layer.ws)
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {moe.moe_status_string(st)}")
+
+    tokens_all = T * ws_n
+    res = {
+        "metric": "MoE-layer fwd tokens/s (expert-GEMM TFLOP/s alongside)",
+        "value": round(tokens_all / (ms_step * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, random-init)",
+        "config": {"workload": wl.name, "T": wl.T, "d_model": wl.d, "experts": wl.E, "top_k": wl.k,
+                   "d_ffn": wl.dff, "act": wl.act, "shared_experts": wl.n_shared,
+                   "capacity_factor": wl.cf if wl.cf > 0 else None,
+                   "parallelism": f"replicas x{ws_n} (no collective)",
+                   "l2": "inputs larger than L2 (expert weights %.0f MB per step)" % (
+                       (wl.E + wl.n_shared) * (3 if wl.act == "swiglu" else 2) * wl.d * wl.dff * 2 / 1e6)},
+        "expert_tflops": round(total_expert / (expert_ms * 1e-3) / 1e12, 2),
+        "expert_frac_of_sustained_peak": round(total_expert / (expert_ms * 1e-3) / 1e12 / peak_sus, 4),
+        "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+        "kept_rows": kept_rows, "drops": int(wl.T * wl.k - kept_rows),
+        "roofline": roofline,
+        "e2e": {"value": round(tokens_all / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "moe_layer_forward with pinned host x/y"},
+        "gpu_launches": moe.moe_layer_forward_launches(cfg) * args.steps,
+        "clocks": clk.summary(),
+    }
+    return res
+
+
+# ------------------------------------------------------------------------------ oracle (CPU)
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p.get("num_threads", 1) for p in threadpool_info() if p.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_step_fn(wl, tokens: int):
+    """One oracle pass over the first ``tokens`` tokens of the workload (a bounded sample)."""
+    from oracle import moe_oracle as O
+
+    inp = make_inputs(wl.replace(T=tokens), "cpu")
+    return lambda: O.moe_layer(inp, E=wl.E, k=wl.k, act=wl.act, n_shared=wl.n_shared, cf=wl.cf,
+                               lb_coef=wl.lb_coef, z_coef=wl.z_coef)
+
+
+def cpu_sample_tokens(wl, flops: float):
+    """Tokens whose fp64 expert work is about ``flops``."""
+    per_token = 2.0 * (wl.k + wl.n_shared) * (3 if wl.act == "swiglu" else 2) * wl.d * wl.dff
+    return int(max(16, min(wl.T, flops / per_token)))
+
+
+def run_reference(args, wl):
+    n = cpu_sample_tokens(wl, 3.0e10)      # ~1-3 s per step on a few cores
+    fn = oracle_step_fn(wl, n)
+    per_step = []
+    for i in range(args.warmup + max(1, args.steps)):
+        t = time.perf_counter()
+        fn()
+        if i >= args.warmup:
+            per_step.append(time.perf_counter() - t)
+    ms = statistics.median(per_step) * 1e3
+    value = n / (ms * 1e-3)
+    cores = oracle_threads()
+    sample = f"first {n} of {wl.T} tokens of {wl.name}, full layer in fp64 per step"
+    return {
+        "impl": "reference", "metric": "MoE-layer fwd tokens/s (expert-GEMM TFLOP/s alongside)",
+        "value": round(value, 2), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name, "T": n},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_leg(wl):
+    n = cpu_sample_tokens(wl, 6.0e11)      # ~10-30 s of fp64 work on a few cores (capped at T)
+    fn = oracle_step_fn(wl, n)
+    t = time.perf_counter()
+    fn()
+    sec = time.perf_counter() - t
+    return {"value": round(n / sec, 2), "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"first {n} of {wl.T} tokens of {wl.name}, one full layer pass in fp64 ({sec:.1f} s)"}
+
+
+# ------------------------------------------------------------------------------ distributed glue
+_PG = False
+
+
+def barrier():
+    if _PG:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    if not _PG:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    global _PG
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    ws_n, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, wl)), flush=True)
+        return 0
+
+    # the CPU oracle leg runs first, before any GPU work, on rank 0 at N=1 only
+    cpu = None
+    if ws_n == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_leg(wl)
+
+    from mixture_experts_layer_89_b300 import build
+    if rank == 0:
+        build.build()
+    if ws_n > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+        _PG = True
+        barrier()
+    res = run_ours(args, wl, ws_n, rank, local)
+    if cpu is not None:
+        res["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if _PG:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN layer, forward pass.
+ *
+ * The layer (mini-moe tutorial, sec. 3.1 MoELayer; OpenMythos article, sec. 3.1; FLAME-MoE
+ * summary, sec. 2) maps T tokens x[T,d] to y[T,d]:
+ *   z = x W_r^T (+ fixed logit bias)        P = softmax(z)      S_t = top-k of z_t
+ *   w_tj = P_t[e_j] / sum_{e in S_t} P_t[e]
+ *   per-expert capacity C = ceil(cf T k / E) (cf <= 0: dropless), assignments ranked in token
+ *   order, rank >= C dropped (weight 0)
+ *   y_t = sum_{kept j} w_tj FFN_{e_j}(x_t) + sum_s FFN^shared_s(x_t)
+ *   lb = lb_coef E sum_e f_e Pbar_e  (f_e = counts_e/(T k), Pbar_e = mean_t P_te)
+ *   zl = z_coef mean_t logsumexp(z_t)^2
+ * The residual add x + y is not part of the layer.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers allocated and owned by the caller; the library
+ *    allocates no memory and keeps no per-call state.  Tensors are dense row-major.
+ *  - Weights use the nn.Linear layout [out, in], stacked on a leading expert axis.
+ *  - Activations and weights share the dtype of moe_config.dtype (fp32 or bf16); router logits,
+ *    softmax and routing weights are fp32; indices and counts are int32.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream); calls return
+ *    without synchronising.  The return value reports argument validation and launch errors.
+ *    Errors detected on the device (non-finite logits, inconsistent counts, a bounded wait
+ *    that gave up) are recorded in a status word inside the workspace; read it with
+ *    moe_read_device_status.
+ *  - `ws` is a device workspace of at least moe_workspace_size bytes, 256-byte aligned, owned
+ *    by the caller; the same workspace must not be used by two calls that may run concurrently.
+ *  - A_max = T*k (dropless) or min(T*k, E*C): the row capacity of the expert-sorted buffers.
+ *  - Shape limits: 1 <= k <= min(E, 8), 1 <= E <= 256, T >= 0, d >= 1, dff >= 1.  bf16 layers
+ *    also need d % 64 == 0 and dff % 64 == 0 (tensor-core tiles), and with n_shared > 1 also
+ *    dff % 128 == 0 (SwiGLU) or dff % 256 == 0 (GELU).  Violations return MOE_ERR_UNSUPPORTED.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* NULL pointer, negative size, misaligned pointer          */
+  MOE_ERR_UNSUPPORTED = -2,   /* shape outside the limits above                           */
+  MOE_ERR_CUDA = -3,          /* a CUDA runtime/driver call failed                        */
+  MOE_ERR_TIMEOUT = -4,       /* device: a bounded wait inside a kernel gave up           */
+  MOE_ERR_DEVICE_STATUS = -5  /* device: non-finite logits or inconsistent inputs         */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  MOE_ACT_GELU_ERF = 0,  /* W_down gelu(W_up x + b_up) + b_down   (mini-moe tutorial, sec. 3.1) */
+  MOE_ACT_SWIGLU = 1     /* W_down (silu(W_gate x) * W_up x)      (GPT-4 2% article, sec. 3.1)  */
+} moe_act;
+
+typedef struct {
+  int32_t T;               /* tokens                                                        */
+  int32_t d;               /* model width                                                   */
+  int32_t E;               /* routed experts                                                */
+  int32_t k;               /* experts per token                                             */
+  int32_t dff;             /* expert hidden width                                           */
+  int32_t n_shared;        /* always-on shared experts (same act, no biases)                */
+  int32_t act;             /* moe_act                                                       */
+  int32_t dtype;           /* moe_dtype of activations and weights                          */
+  int32_t has_bias;        /* routed GELU experts carry b_up [E,dff] and b_down [E,d]       */
+  float capacity_factor;   /* <= 0: dropless                                                */
+  float lb_coef;           /* load-balance loss coefficient (alpha)                         */
+  float z_coef;            /* router z-loss coefficient (beta)                              */
+} moe_config;
+
+typedef struct {
+  const void* w_router;           /* [E,d]                                                  */
+  const float* router_logit_bias; /* [E] fp32 added to the logits, or NULL                   */
+  const void* w_up;               /* [E,dff,d]                                              */
+  const void* w_gate;             /* [E,dff,d] (SwiGLU) or NULL                              */
+  const void* w_down;             /* [E,d,dff]                                              */
+  const void* b_up;               /* [E,dff] or NULL (has_bias)                              */
+  const void* b_down;             /* [E,d]   or NULL (has_bias)                              */
+  const void* ws_up;              /* shared [S,dff,d] or NULL when n_shared == 0             */
+  const void* ws_gate;            /* shared [S,dff,d] (SwiGLU) or NULL                       */
+  const void* ws_down;            /* shared [S,d,dff] or NULL                                */
+} moe_weights;
+
+/* Workspace bytes needed by every call below for this config (host only, no GPU work).
+ * Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad config. */
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Expert capacity C (-1 when dropless) and A_max for this config, exactly as the kernels use
+ * them: C = ceil(cf * T * k / E) evaluated exactly on the float32 value of cf. Host only. */
+moe_status moe_capacity(const moe_config* cfg, int32_t* cap, int32_t* a_max);
+
+/* Router (mini-moe tutorial, sec. 3.1; OpenMythos article, sec. 3.1; losses: OpenMythos
+ * article sec. 3.1 and FLAME-MoE summary sec. 2).
+ *   x [T,d], w_router [E,d], logit_bias [E] fp32 or NULL
+ *   -> topk_idx [T,k] int32 (descending logit, ties to the lower expert index),
+ *      topk_w [T,k] fp32 (renormalised over the k), counts [E] int32 (pre-drop assignments),
+ *      losses [2] fp32 = {load-balance loss, router z-loss}.
+ * Logits are accumulated in fp32. */
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
+                     const float* logit_bias, int32_t* topk_idx, float* topk_w,
+                     int32_t* counts, float* losses, void* ws, void* stream);
+
+/* Dispatch (Naive-N0.5-Flash article sec. 4.2: group tokens by target expert; OpenMythos
+ * article sec. 3.1: flatten + index reorder, capacity and overflow).
+ *   x [T,d], topk_idx [T,k], counts [E] (as produced by moe_route)
+ *   -> offsets [E+1] (expert e owns rows offsets[e]..offsets[e+1]-1 of the sorted layout),
+ *      kept [E] = min(counts, C), row_of [T,k] (sorted row of slot j of token t, -1 if dropped),
+ *      tok_of [A_max] (token of each sorted row), x_perm [A_max,d] = x[tok_of[r]].
+ * Rows of an expert are in increasing token order; rows >= offsets[E] are left untouched.
+ * A counts vector that disagrees with topk_idx sets MOE_ERR_DEVICE_STATUS in the status word. */
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
+                       const int32_t* counts, int32_t* offsets, int32_t* kept,
+                       int32_t* row_of, int32_t* tok_of, void* x_perm, void* ws, void* stream);
+
+/* Expert FFNs (mini-moe tutorial sec. 3.1; GPT-4 2% article sec. 3.1; shared experts:
+ * FLAME-MoE summary sec. 2).
+ *   x_perm [A_max,d] with offsets [E+1] from moe_permute -> y_perm [A_max,d] (rows < offsets[E]);
+ *   when n_shared > 0 also x [T,d] -> y_shared [T,d] = sum_s FFN^shared_s(x) (else both NULL).
+ * Hidden activations are kept in the workspace; bf16 layers round them to bf16. */
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                          const moe_weights* w, void* y_perm, const void* x, void* y_shared,
+                          void* ws, void* stream);
+
+/* Combine (FLAME-MoE summary sec. 2: output = routing-weighted sum of the selected experts).
+ *   y[t] = sum_{j: row_of[t,j] >= 0} topk_w[t,j] * y_perm[row_of[t,j]]  (+ y_shared[t])
+ * accumulated in fp32 in slot order and rounded once.  y_shared may be NULL. */
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
+                       const float* topk_w, const void* y_shared, void* y, void* stream);
+
+/* The whole layer: route -> permute -> expert FFNs -> combine, on one stream, no host sync.
+ *   x [T,d] -> y [T,d]; losses [2]; counts_out [E] (nullable); drops_out [1] (nullable,
+ *   number of dropped assignments).  Intermediates live in ws. */
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
+                             void* y, float* losses, int32_t* counts_out, int32_t* drops_out,
+                             void* ws, void* stream);
+
+/* Same as moe_layer_forward, and records caller-created CUDA events (cudaEvent_t, cast to
+ * void*) on `stream` at the stage boundaries, for timing:
+ *   events[0] before routing, [1] after routing, [2] after dispatch, [3] after the routed
+ *   up-projection, [4] after the routed down-projection, [5] after the shared experts,
+ *   [6] after the combine.  n_events must be 7. */
+moe_status moe_layer_forward_timed(const moe_config* cfg, const moe_weights* w, const void* x,
+                                   void* y, float* losses, int32_t* counts_out,
+                                   int32_t* drops_out, void* ws, void* stream,
+                                   void* const* events, int32_t n_events);
+
+/* Synchronises `stream`, returns the device status word of `ws` as a moe_status (MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_STATUS) and clears it. */
+moe_status moe_read_device_status(void* ws, void* stream);
+
+/* Number of kernels moe_layer_forward launches for this config (for launch accounting). */
+int32_t moe_layer_forward_launches(const moe_config* cfg);
+
+/* Static string for a status code. */
+const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_B300_H */

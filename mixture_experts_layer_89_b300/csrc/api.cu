@@ -1,0 +1,397 @@
+// C ABI of the MoE layer (declared in include/moe.h): argument validation, exact capacity,
+// workspace layout and the stream-ordered launch sequence of each step.
+#include <limits.h>
+#include <math.h>
+#include <string.h>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+struct WsLayout {
+  size_t status, r_hist, r_psum, r_lse2, p_hist, p_base, drops;
+  size_t topk_idx, topk_w, counts, offsets, kept, row_of, tok_of;
+  size_t x_perm, h, y_perm, h_sh, y_sh;
+  size_t total;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+inline size_t elt(const moe_config* c) { return c->dtype == MOE_BF16 ? 2 : 4; }
+inline bool is_bf16(const moe_config* c) { return c->dtype == MOE_BF16; }
+
+// cap = ceil(cf T k / E) computed exactly from the binary value of the float32 cf; -1 = dropless.
+int64_t capacity_exact(float cf, int64_t T, int64_t k, int64_t E) {
+  if (!(cf > 0.f)) return -1;
+  if (isinf(cf)) return T * k;
+  int ex = 0;
+  const float m = frexpf(cf, &ex);                         // cf = m 2^ex, m in [0.5, 1)
+  const int64_t mi = (int64_t)ldexpf(m, 24);               // cf = mi 2^(ex - 24), exactly
+  const int sh = ex - 24;
+  __int128 num = (__int128)mi * T * k;
+  __int128 den = E;
+  if (sh >= 0) {
+    if (sh > 40) return T * k;                             // cap >= T k: nothing can drop
+    num <<= sh;
+  } else {
+    if (-sh > 90) return num > 0 ? 1 : 0;                  // 0 < cf T k / E < 1
+    den <<= -sh;
+  }
+  __int128 c = (num + den - 1) / den;
+  if (c > (__int128)T * k) c = (__int128)T * k;            // identical behaviour, keeps it in range
+  return (int64_t)c;
+}
+
+int64_t a_max_of(const moe_config* c) {
+  const int64_t tk = (int64_t)c->T * c->k;
+  const int64_t cap = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
+  if (cap < 0) return tk;
+  const int64_t ec = cap * c->E;
+  return ec < tk ? ec : tk;
+}
+
+moe_status validate(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d < 1 || c->E < 1 || c->k < 1 || c->dff < 1 || c->n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_GELU_ERF && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (isnan(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (c->E > 256 || c->k > 8 || c->k > c->E || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
+  if (c->has_bias && c->act != MOE_ACT_GELU_ERF) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->k > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->n_shared * c->dff > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
+  if (is_bf16(c)) {
+    if (c->d % 64 || c->dff % 64) return MOE_ERR_UNSUPPORTED;
+    if (c->n_shared > 1 && (c->dff % (c->act == MOE_ACT_SWIGLU ? 128 : 256))) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+WsLayout layout(const moe_config* c) {
+  WsLayout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  const size_t T = (size_t)c->T, E = (size_t)c->E, k = (size_t)c->k, d = (size_t)c->d, f = (size_t)c->dff;
+  const size_t S = (size_t)c->n_shared;
+  const size_t nrb = (size_t)route_blocks(c->T), npb = (size_t)perm_blocks(c->T);
+  const size_t A = (size_t)a_max_of(c);
+  L.status = take(256);
+  L.r_hist = take(nrb * E * 4);
+  L.r_psum = take(nrb * E * 4);
+  L.r_lse2 = take(nrb * 4);
+  L.p_hist = take(npb * E * 4);
+  L.p_base = take(npb * E * 4);
+  L.drops = take(4);
+  L.topk_idx = take(T * k * 4);
+  L.topk_w = take(T * k * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.kept = take(E * 4);
+  L.row_of = take(T * k * 4);
+  L.tok_of = take(A * 4);
+  L.x_perm = take(A * d * elt(c));
+  L.h = take(A * f * elt(c));
+  L.y_perm = take(A * d * elt(c));
+  L.h_sh = take(T * S * f * elt(c));
+  L.y_sh = take(S ? T * d * elt(c) : 0);
+  L.total = off;
+  return L;
+}
+
+template <typename P>
+inline P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+inline bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                      \
+  do {                                     \
+    const moe_status _s = (expr);          \
+    if (_s != MOE_OK) return _s;           \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+
+// ------------------------------------------------------------------------------ steps
+moe_status route_impl(const moe_config* c, const void* x, const void* wr, const float* lbias, int32_t* topk_idx,
+                      float* topk_w, int32_t* counts, float* losses, void* ws, cudaStream_t st) {
+  const WsLayout L = layout(c);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  MOE_CUDA(launch_route(is_bf16(c), x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w, at<int32_t>(ws, L.r_hist),
+                        at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2), status, st));
+  MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
+                                 route_blocks(c->T), c->T, c->E, c->k, c->lb_coef, c->z_coef, counts, losses, st));
+  return MOE_OK;
+}
+
+moe_status permute_impl(const moe_config* c, const void* x, const int32_t* topk_idx, const int32_t* counts,
+                        int32_t* offsets, int32_t* kept, int32_t* row_of, int32_t* tok_of, void* x_perm,
+                        int32_t* drops, void* ws, cudaStream_t st) {
+  const WsLayout L = layout(c);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  const int64_t cap64 = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
+  const int cap = cap64 < 0 ? INT_MAX : (int)cap64;
+  const int npb = perm_blocks(c->T);
+  MOE_CUDA(launch_perm_hist(topk_idx, c->T, c->E, c->k, at<int32_t>(ws, L.p_hist), status, st));
+  MOE_CUDA(launch_perm_scan(at<int32_t>(ws, L.p_hist), npb, counts, c->E, c->T * c->k, cap,
+                            at<int32_t>(ws, L.p_base), offsets, kept, drops, status, st));
+  MOE_CUDA(launch_perm_rank(topk_idx, at<int32_t>(ws, L.p_base), offsets, c->T, c->E, c->k, cap, row_of, tok_of,
+                            st));
+  MOE_CUDA(launch_gather_rows(is_bf16(c), x, tok_of, offsets + c->E, (int)a_max_of(c), c->d, x_perm, st));
+  return MOE_OK;
+}
+
+moe_status run_projection(const moe_config* c, const Projection& p, uint32_t* status, cudaStream_t st) {
+  cudaError_t e = is_bf16(c) ? launch_projection_tc(p, status, num_sms_current(), st)
+                             : launch_projection_simt(false, p, st);
+  return cuda_status(e);
+}
+
+moe_status ffn_routed_impl(const moe_config* c, const void* x_perm, const int32_t* offsets, const moe_weights* w,
+                           void* y_perm, void* ws, cudaStream_t st, cudaEvent_t ev_mid) {
+  const WsLayout L = layout(c);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  const int A = (int)a_max_of(c);
+  const bool swiglu = c->act == MOE_ACT_SWIGLU;
+  void* h = at<char>(ws, L.h);
+  if (A > 0) {
+    Projection up{};
+    up.A = x_perm; up.lda = c->d; up.rows_alloc = A;
+    up.offsets = offsets; up.G = c->E; up.rows_static = 0;
+    up.B0 = swiglu ? w->w_gate : w->w_up; up.B1 = w->w_up;
+    up.bias = c->has_bias ? w->b_up : nullptr;
+    up.N = c->dff; up.K = c->d; up.N_w = c->dff; up.K_w = c->d; up.G_w = c->E;
+    up.act = swiglu ? ACT_SWIGLU : ACT_GELU;
+    up.out = h; up.ldc = c->dff;
+    MOE_TRY(run_projection(c, up, status, st));
+  }
+  if (ev_mid) MOE_CUDA(cudaEventRecord(ev_mid, st));
+  if (A > 0) {
+    Projection dn{};
+    dn.A = h; dn.lda = c->dff; dn.rows_alloc = A;
+    dn.offsets = offsets; dn.G = c->E; dn.rows_static = 0;
+    dn.B0 = w->w_down; dn.B1 = nullptr;
+    dn.bias = c->has_bias ? w->b_down : nullptr;
+    dn.N = c->d; dn.K = c->dff; dn.N_w = c->d; dn.K_w = c->dff; dn.G_w = c->E;
+    dn.act = ACT_NONE;
+    dn.out = y_perm; dn.ldc = c->d;
+    MOE_TRY(run_projection(c, dn, status, st));
+  }
+  return MOE_OK;
+}
+
+// Shared experts, concatenated: the S hidden layers form one hidden layer of width S dff.
+moe_status ffn_shared_impl(const moe_config* c, const void* x, const moe_weights* w, void* y_shared, void* ws,
+                           cudaStream_t st) {
+  if (c->n_shared <= 0 || c->T <= 0) return MOE_OK;
+  const WsLayout L = layout(c);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+  const bool swiglu = c->act == MOE_ACT_SWIGLU;
+  const int S = c->n_shared;
+  void* hs = at<char>(ws, L.h_sh);
+  Projection up{};
+  up.A = x; up.lda = c->d; up.rows_alloc = c->T;
+  up.offsets = nullptr; up.G = 1; up.rows_static = c->T;
+  up.B0 = swiglu ? w->ws_gate : w->ws_up; up.B1 = w->ws_up;
+  up.bias = nullptr;
+  up.N = S * c->dff; up.K = c->d; up.N_w = c->dff; up.K_w = c->d; up.G_w = S;
+  up.act = swiglu ? ACT_SWIGLU : ACT_GELU;
+  up.out = hs; up.ldc = (int64_t)S * c->dff;
+  MOE_TRY(run_projection(c, up, status, st));
+  Projection dn{};
+  dn.A = hs; dn.lda = (int64_t)S * c->dff; dn.rows_alloc = c->T;
+  dn.offsets = nullptr; dn.G = 1; dn.rows_static = c->T;
+  dn.B0 = w->ws_down; dn.B1 = nullptr; dn.bias = nullptr;
+  dn.N = c->d; dn.K = S * c->dff; dn.N_w = c->d; dn.K_w = c->dff; dn.G_w = S;
+  dn.act = ACT_NONE;
+  dn.out = y_shared; dn.ldc = c->d;
+  return run_projection(c, dn, status, st);
+}
+
+moe_status check_weights(const moe_config* c, const moe_weights* w) {
+  if (!w || !w->w_router || !w->w_up || !w->w_down) return MOE_ERR_INVALID_ARG;
+  if (c->act == MOE_ACT_SWIGLU && !w->w_gate) return MOE_ERR_INVALID_ARG;
+  if (c->has_bias && (!w->b_up || !w->b_down)) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared > 0 && (!w->ws_up || !w->ws_down || (c->act == MOE_ACT_SWIGLU && !w->ws_gate)))
+    return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {w->w_router, w->w_up, w->w_gate, w->w_down, w->b_up, w->b_down, w->ws_up, w->ws_gate, w->ws_down};
+  for (const void* p : ps)
+    if (p && misaligned(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, void* y, float* losses,
+                      int32_t* counts_out, int32_t* drops_out, void* ws, cudaStream_t st, cudaEvent_t const* ev) {
+  MOE_TRY(validate(c));
+  MOE_TRY(check_weights(c, w));
+  if (!ws || !losses || (c->T > 0 && (!x || !y))) return MOE_ERR_INVALID_ARG;
+  if (misaligned(ws) || misaligned(x) || misaligned(y)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(c);
+  int32_t* topk_idx = at<int32_t>(ws, L.topk_idx);
+  float* topk_w = at<float>(ws, L.topk_w);
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(ws, L.counts);
+  int32_t* drops = drops_out ? drops_out : at<int32_t>(ws, L.drops);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* row_of = at<int32_t>(ws, L.row_of);
+  void* x_perm = at<char>(ws, L.x_perm);
+  void* y_perm = at<char>(ws, L.y_perm);
+  void* y_sh = c->n_shared > 0 ? at<char>(ws, L.y_sh) : nullptr;
+  auto rec = [&](int i) -> moe_status { return ev ? cuda_status(cudaEventRecord(ev[i], st)) : MOE_OK; };
+
+  MOE_TRY(rec(0));
+  MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st));
+  MOE_TRY(rec(1));
+  MOE_TRY(permute_impl(c, x, topk_idx, counts, offsets, at<int32_t>(ws, L.kept), row_of, at<int32_t>(ws, L.tok_of),
+                       x_perm, drops, ws, st));
+  MOE_TRY(rec(2));
+  MOE_TRY(ffn_routed_impl(c, x_perm, offsets, w, y_perm, ws, st, ev ? ev[3] : nullptr));
+  MOE_TRY(rec(4));
+  MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, st));
+  MOE_TRY(rec(5));
+  MOE_CUDA(launch_combine(is_bf16(c), y_perm, row_of, topk_w, y_sh, y, c->T, c->d, c->k, st));
+  MOE_TRY(rec(6));
+  return MOE_OK;
+}
+
+}  // namespace
+
+// ================================================================================ C ABI
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = layout(cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_capacity(const moe_config* cfg, int32_t* cap, int32_t* a_max) {
+  MOE_TRY(validate(cfg));
+  if (cap) {
+    const int64_t c = capacity_exact(cfg->capacity_factor, cfg->T, cfg->k, cfg->E);
+    *cap = c < 0 ? -1 : (int32_t)c;
+  }
+  if (a_max) *a_max = (int32_t)a_max_of(cfg);
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
+                     int32_t* topk_idx, float* topk_w, int32_t* counts, float* losses, void* ws, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (!w_router || !counts || !losses || !ws) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!x || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (misaligned(ws) || misaligned(x) || misaligned(w_router)) return MOE_ERR_INVALID_ARG;
+  return route_impl(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, ws,
+                    static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* counts,
+                       int32_t* offsets, int32_t* kept, int32_t* row_of, int32_t* tok_of, void* x_perm, void* ws,
+                       void* stream) {
+  MOE_TRY(validate(cfg));
+  if (!offsets || !kept || !ws) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!x || !topk_idx || !row_of || !tok_of || !x_perm)) return MOE_ERR_INVALID_ARG;
+  if (misaligned(ws) || misaligned(x) || misaligned(x_perm)) return MOE_ERR_INVALID_ARG;
+  return permute_impl(cfg, x, topk_idx, counts, offsets, kept, row_of, tok_of, x_perm, nullptr, ws,
+                      static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets, const moe_weights* w,
+                          void* y_perm, const void* x, void* y_shared, void* ws, void* stream) {
+  MOE_TRY(validate(cfg));
+  MOE_TRY(check_weights(cfg, w));
+  if (!offsets || !ws) return MOE_ERR_INVALID_ARG;
+  if (a_max_of(cfg) > 0 && (!x_perm || !y_perm)) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared > 0 && cfg->T > 0 && (!x || !y_shared)) return MOE_ERR_INVALID_ARG;
+  if (misaligned(ws) || misaligned(x_perm) || misaligned(y_perm) || misaligned(x) || misaligned(y_shared))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(ffn_routed_impl(cfg, x_perm, offsets, w, y_perm, ws, st, nullptr));
+  return ffn_shared_impl(cfg, x, w, y_shared, ws, st);
+}
+
+moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of, const float* topk_w,
+                       const void* y_shared, void* y, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0 && (!row_of || !topk_w || !y || (!y_perm && a_max_of(cfg) > 0))) return MOE_ERR_INVALID_ARG;
+  if (misaligned(y_perm) || misaligned(y_shared) || misaligned(y)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(is_bf16(cfg), y_perm, row_of, topk_w, y_shared, y, cfg->T, cfg->d, cfg->k,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, float* losses,
+                             int32_t* counts_out, int32_t* drops_out, void* ws, void* stream) {
+  return layer_impl(cfg, w, x, y, losses, counts_out, drops_out, ws, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+moe_status moe_layer_forward_timed(const moe_config* cfg, const moe_weights* w, const void* x, void* y,
+                                   float* losses, int32_t* counts_out, int32_t* drops_out, void* ws, void* stream,
+                                   void* const* events, int32_t n_events) {
+  if (!events || n_events != 7) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[7];
+  for (int i = 0; i < 7; ++i) {
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+    ev[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  return layer_impl(cfg, w, x, y, losses, counts_out, drops_out, ws, static_cast<cudaStream_t>(stream), ev);
+}
+
+moe_status moe_read_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v == 0) return MOE_OK;
+  if (cudaMemset(ws, 0, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & DEV_TIMEOUT) return MOE_ERR_TIMEOUT;
+  return MOE_ERR_DEVICE_STATUS;
+}
+
+int32_t moe_layer_forward_launches(const moe_config* cfg) {
+  if (validate(cfg) != MOE_OK) return -1;
+  int n = 0;
+  const bool tokens = cfg->T > 0;
+  n += tokens ? 2 : 1;                        // router + finalize
+  n += tokens ? 4 : 1;                        // histogram, scan, rank, gather
+  if (a_max_of(cfg) > 0) n += 2;              // routed up + down projections
+  if (cfg->n_shared > 0 && tokens) n += 2;    // shared up + down projections
+  if (tokens) n += 1;                         // combine
+  return n;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_STATUS: return "device reported bad data";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

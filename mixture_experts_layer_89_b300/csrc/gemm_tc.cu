@@ -1,0 +1,430 @@
+// Grouped expert projection on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// The expert FFNs are dense contractions once tokens are grouped by expert (Naive-N0.5-Flash
+// article, sec. 4.2: "one big matmul per expert"), so they run here as one persistent grouped
+// GEMM per projection:
+//   up:   h = GELU(x_perm W_up^T + b_up)          or  h = SiLU(x_perm W_gate^T) * (x_perm W_up^T)
+//   down: y_perm = h W_down^T (+ b_down)
+// (expert forms: mini-moe tutorial, sec. 3.1; GPT-4 2% article, sec. 3.1).
+//
+// Tile: 128 rows x 256 accumulator columns, K step 64 (one 128-byte swizzle row of bf16).  For
+// SwiGLU the 256 columns are 128 gate columns followed by the same 128 up columns, so one MMA
+// (M=128, N=256, K=16) produces both halves and the epilogue multiplies them in registers.
+// Warp roles (256 threads, one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: A tile (rows of one expert) + B tile (that expert's weights), 4 stages
+//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma per stage into a TMEM accumulator
+//   warp 2      TMEM allocator (512 columns = two 256-column accumulators, double buffered)
+//   warps 4..7  epilogue: tcgen05.ld (thread = row), bias/activation, bf16 stores
+// Tiles are enumerated m-tile-major with n fastest, so CTAs running at the same time share the A
+// tile and the expert's weight slab through L2.  The tile table is built inside every CTA from the
+// device-side expert offsets; no count returns to the host.
+#include <stdio.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int BNB = 256;  // B rows per stage (accumulator columns)
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BNB * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MAXG = 256;
+constexpr int NTHREADS = 256;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = umma_idesc_bf16(BM, BNB);
+
+struct TcArgs {
+  const int32_t* offsets;
+  int G;
+  int rows_static;
+  int N, K, N_w, K_w;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;
+  int64_t ldc;
+  uint32_t* status;
+};
+
+struct SmemCtl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int row_lo[MAXG + 1];
+  int mt_pre[MAXG + 1];
+};
+constexpr size_t SMEM_TOTAL = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
+
+// Wait that ignores the abort flag (used to drain in-flight async operations before exit).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erff(u * 0.70710678118654752f)); }
+__device__ __forceinline__ float silu(float u) { return u / (1.f + expf(-u)); }
+
+template <int ACT>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+              const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+  constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)STAGES * STAGE_BYTES);
+  volatile int* abort_flag = &ctl->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.offsets ? args.G : 1;
+  const int n_tiles = (args.N + NOUT - 1) / NOUT;
+  const int kblocks = args.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&ctl->tfull[a]), 1);
+      mbar_init(smem_u32(&ctl->tempty[a]), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(smem_u32(&ctl->mma_done), 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    if (ACT == ACT_SWIGLU) tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 3) {
+    // m-tile prefix over groups: lane owns groups [8 lane, 8 lane + 8)
+    int cnt[8];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      cnt[i] = 0;
+      if (g < G) {
+        const int lo = args.offsets ? args.offsets[g] : 0;
+        const int hi = args.offsets ? args.offsets[g + 1] : args.rows_static;
+        ctl->row_lo[g] = lo;
+        if (g == G - 1) ctl->row_lo[G] = hi;
+        cnt[i] = hi > lo ? (hi - lo + BM - 1) / BM : 0;
+        local += cnt[i];
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      if (g < G) ctl->mt_pre[g] = run;
+      run += cnt[i];
+    }
+    if (lane == 31) ctl->mt_pre[G] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int total_tiles = ctl->mt_pre[G] * n_tiles;
+
+  auto decode = [&](int t, int& g, int& m0, int& m_end, int& n0) {
+    const int mt = t / n_tiles;
+    const int nt = t - mt * n_tiles;
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (ctl->mt_pre[mid] <= mt) lo = mid; else hi = mid;
+    }
+    g = lo;
+    m0 = ctl->row_lo[g] + (mt - ctl->mt_pre[g]) * BM;
+    m_end = ctl->row_lo[g + 1];
+    n0 = nt * NOUT;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      bool aborted = false;
+      for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+        int g, m0, m_end, n0;
+        decode(t, g, m0, m_end, n0);
+        const int nn = n0 % args.N_w;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          const int k0 = kb * BK;
+          const int gw = g + n0 / args.N_w + k0 / args.K_w;
+          const int kk = k0 % args.K_w;
+          uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
+          if (ACT == ACT_SWIGLU) {
+            tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
+            tma_load_3d(smem_u32(sb + B_BYTES / 2), &tmB1, fb, kk, nn, gw);
+          } else {
+            tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
+          }
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {  // let every armed copy land before the CTA leaves
+        for (int i = 0; i < STAGES; ++i)
+          if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0, it = 0;
+      uint32_t ph = 0;
+      bool aborted = false;
+      for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNB);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)s * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC,
+                      (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&ctl->empty[s]));
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (aborted) break;
+        umma_commit(smem_u32(&ctl->tfull[acc]));
+      }
+      umma_commit(smem_u32(&ctl->mma_done));
+      drain_wait(smem_u32(&ctl->mma_done), 0);
+    }
+  } else if (warp >= 4) {
+    const int q = warp - 4;
+    int it = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      int g, m0, m_end, n0;
+      decode(t, g, m0, m_end, n0);
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      // lane 0 waits, the warp follows its verdict (tcgen05.ld needs the whole warp converged)
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), aph, abort_flag, args.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+      const bool valid = row < m_end;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNB);
+      __nv_bfloat16* orow = args.out + (size_t)(valid ? row : 0) * args.ldc;
+      if (ACT == ACT_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < NOUT; c += 32) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tb + c, gv);
+          tmem_ld32(tb + 128 + c, uv);
+          tmem_wait_ld();
+          if (valid && n0 + c < args.N) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = silu(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]);
+              const float h1 = silu(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
+              pk[i] = pack_bf16x2(h0, h1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < NOUT; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tb + c, v);
+          tmem_wait_ld();
+          if (valid && n0 + c < args.N) {
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            if (args.bias) {
+              const int col = n0 + c;
+              const int gw = g + col / args.N_w;
+              const uint4* bp = reinterpret_cast<const uint4*>(args.bias + (size_t)gw * args.N_w + col % args.N_w);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint4 bq = bp[i];
+                const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  f[8 * i + 2 * j] += __uint_as_float(bw[j] << 16);
+                  f[8 * i + 2 * j + 1] += __uint_as_float(bw[j] & 0xffff0000u);
+                }
+              }
+            }
+            if (ACT == ACT_GELU) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+char g_err[256] = "";
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+              const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) {
+    snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled unavailable");
+    return false;
+  }
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled failed (%d) rank %d dims %llu %llu %llu", (int)r, rank,
+             (unsigned long long)dims[0], (unsigned long long)dims[1],
+             rank > 2 ? (unsigned long long)dims[2] : 0ull);
+    return false;
+  }
+  return true;
+}
+
+template <int ACT>
+cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
+  constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
+  const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
+  if (rows_alloc <= 0 || p.N <= 0) return cudaSuccess;
+  CUtensorMap mA, mB0, mB1;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)rows_alloc};
+    const cuuint64_t str[1] = {(cuuint64_t)p.lda * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    if (!make_map(&mA, p.A, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)p.K_w, (cuuint64_t)p.N_w, (cuuint64_t)p.G_w};
+    const cuuint64_t str[2] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)p.N_w * p.K_w * 2};
+    const cuuint32_t box[3] = {BK, (cuuint32_t)(ACT == ACT_SWIGLU ? BNB / 2 : BNB), 1};
+    if (!make_map(&mB0, p.B0, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (ACT == ACT_SWIGLU) {
+      if (!make_map(&mB1, p.B1, 3, dims, str, box)) return cudaErrorInvalidValue;
+    } else {
+      mB1 = mB0;
+    }
+  }
+  TcArgs a;
+  a.offsets = p.offsets;
+  a.G = p.G;
+  a.rows_static = p.rows_static;
+  a.N = p.N;
+  a.K = p.K;
+  a.N_w = p.N_w;
+  a.K_w = p.K_w;
+  a.bias = static_cast<const __nv_bfloat16*>(p.bias);
+  a.out = static_cast<__nv_bfloat16*>(p.out);
+  a.ldc = p.ldc;
+  a.status = status;
+  const long n_tiles = (p.N + NOUT - 1) / NOUT;
+  const long ub_mt = p.offsets ? (rows_alloc + BM - 1) / BM + p.G : (p.rows_static + BM - 1) / BM;
+  long grid = ub_mt * n_tiles;
+  if (grid > num_sms) grid = num_sms;
+  if (grid < 1) grid = 1;
+  cudaError_t err = cudaFuncSetAttribute(k_proj_tc<ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
+  if (err != cudaSuccess) return err;
+  k_proj_tc<ACT><<<(unsigned)grid, NTHREADS, SMEM_TOTAL, st>>>(mA, mB0, mB1, a);
+  return cudaGetLastError();
+}
+}  // namespace
+
+const char* tc_last_error() { return g_err; }
+
+cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
+  switch (p.act) {
+    case ACT_GELU: return launch_t<ACT_GELU>(p, status, num_sms, st);
+    case ACT_SWIGLU: return launch_t<ACT_SWIGLU>(p, status, num_sms, st);
+    default: return launch_t<ACT_NONE>(p, status, num_sms, st);
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,61 @@
+// Host-side launchers of the MoE kernels (internal to the library; the public ABI is moe.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- router (route.cu)
+constexpr int kRouteTokens = 32;  // tokens per router CTA
+int route_blocks(int T);
+// x [T,d] and w_router [E,d] of type `bf16` (else fp32).  Writes top-k, per-CTA histograms,
+// per-CTA softmax column sums and per-CTA sums of lse^2.
+cudaError_t launch_route(bool bf16, const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
+                         int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2,
+                         uint32_t* status, cudaStream_t st);
+// Reduces the per-CTA partials: counts [E] and losses [2].
+cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,
+                                  int k, float lb_coef, float z_coef, int32_t* counts, float* losses,
+                                  cudaStream_t st);
+
+// ---------------------------------------------------------------- dispatch (permute.cu)
+constexpr int kPermTokens = 64;  // tokens per dispatch CTA
+int perm_blocks(int T);
+cudaError_t launch_perm_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* phist, uint32_t* status,
+                             cudaStream_t st);
+cudaError_t launch_perm_scan(const int32_t* phist, int npb, const int32_t* counts, int E, int Tk, int cap,
+                             int32_t* pbase, int32_t* offsets, int32_t* kept, int32_t* drops, uint32_t* status,
+                             cudaStream_t st);
+cudaError_t launch_perm_rank(const int32_t* topk_idx, const int32_t* pbase, const int32_t* offsets, int T, int E,
+                             int k, int cap, int32_t* row_of, int32_t* tok_of, cudaStream_t st);
+cudaError_t launch_gather_rows(bool bf16, const void* x, const int32_t* tok_of, const int32_t* n_rows_dev,
+                               int max_rows, int d, void* x_perm, cudaStream_t st);
+
+// ---------------------------------------------------------------- combine (combine.cu)
+cudaError_t launch_combine(bool bf16, const void* y_perm, const int32_t* row_of, const float* topk_w,
+                           const void* y_shared, void* y, int T, int d, int k, cudaStream_t st);
+
+// ---------------------------------------------------------------- grouped FFN GEMMs
+// One grouped projection  out[r, n] = act(sum_k A[r, k] B_{g(r)}[n, k] (+ bias)).
+// Rows of A are split into G groups by offsets (device, [G+1]); offsets == NULL means one group of
+// rows [0, rows_static).  Weights are viewed as [G_w][N_w][K_w]; the weight matrix used for output
+// column n and reduction index kk of group g is g + n / N_w + kk / K_w, at (n % N_w, kk % K_w), so
+// routed experts (N_w = N, K_w = K) and concatenated shared experts (spanning N or K) share code.
+enum Act { ACT_NONE = 0, ACT_GELU = 1, ACT_SWIGLU = 2 };
+struct Projection {
+  const void* A; int64_t lda; int rows_alloc;      // A [rows_alloc, K] (lda elements)
+  const int32_t* offsets; int G; int rows_static;
+  const void* B0; const void* B1;                  // B1: the W_up half of SwiGLU
+  const void* bias;                                // [G_w][N_w] or NULL
+  int N, K, N_w, K_w, G_w;
+  int act;
+  void* out; int64_t ldc;
+};
+cudaError_t launch_projection_simt(bool bf16, const Projection& p, cudaStream_t st);
+cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st);
+const char* tc_last_error();
+
+}  // namespace moe

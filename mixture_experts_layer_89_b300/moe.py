@@ -1,0 +1,210 @@
+"""ctypes binding of ``libmoe.so`` with the same names as the C ABI in ``include/moe.h``.
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.  PyTorch
+supplies device memory and the current CUDA stream.  There is no CPU fallback: if the library
+is missing or was built without a GPU-capable toolchain, loading fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_STATUS = 0, -1, -2, -3, -4, -5
+MOE_F32, MOE_BF16 = 0, 1
+MOE_ACT_GELU_ERF, MOE_ACT_SWIGLU = 0, 1
+
+_c_i32 = ctypes.c_int32
+_c_p = ctypes.c_void_p
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("T", _c_i32), ("d", _c_i32), ("E", _c_i32), ("k", _c_i32), ("dff", _c_i32),
+                ("n_shared", _c_i32), ("act", _c_i32), ("dtype", _c_i32), ("has_bias", _c_i32),
+                ("capacity_factor", ctypes.c_float), ("lb_coef", ctypes.c_float), ("z_coef", ctypes.c_float)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [("w_router", _c_p), ("router_logit_bias", _c_p), ("w_up", _c_p), ("w_gate", _c_p),
+                ("w_down", _c_p), ("b_up", _c_p), ("b_down", _c_p), ("ws_up", _c_p), ("ws_gate", _c_p),
+                ("ws_down", _c_p)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {moe_status_string(status)} ({status})")
+        self.status = status
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m mixture_experts_layer_89_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER
+        cfgp = P(MoeConfig)
+        L.moe_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
+        L.moe_capacity.argtypes = [cfgp, P(_c_i32), P(_c_i32)]
+        L.moe_route.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_permute.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_expert_ffn.argtypes = [cfgp, _c_p, _c_p, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_combine.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_layer_forward.argtypes = [cfgp, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_layer_forward_timed.argtypes = [cfgp, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                              P(_c_p), _c_i32]
+        L.moe_read_device_status.argtypes = [_c_p, _c_p]
+        L.moe_layer_forward_launches.argtypes = [cfgp]
+        L.moe_status_string.argtypes = [_c_i32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_permute", "moe_expert_ffn",
+                     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
+                     "moe_layer_forward_launches"):
+            getattr(L, name).restype = _c_i32
+        _LIB = L
+    return _LIB
+
+
+EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
+            "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
+            "moe_layer_forward_launches", "moe_status_string")
+
+
+# ----------------------------------------------------------------------------- marshalling
+def _p(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _s(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def make_config(T: int, d: int, E: int, k: int, dff: int, act: str = "gelu", dtype: str = "bf16",
+                n_shared: int = 0, has_bias: bool = False, capacity_factor: float = 0.0,
+                lb_coef: float = 0.01, z_coef: float = 0.001) -> MoeConfig:
+    return MoeConfig(T, d, E, k, dff, n_shared, MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_GELU_ERF,
+                     MOE_BF16 if dtype == "bf16" else MOE_F32, int(bool(has_bias)), float(capacity_factor),
+                     float(lb_coef), float(z_coef))
+
+
+def config_from_workload(wl, T: Optional[int] = None) -> MoeConfig:
+    return make_config(wl.T if T is None else T, wl.d, wl.E, wl.k, wl.dff, wl.act, wl.dtype, wl.n_shared,
+                       wl.bias, wl.cf, wl.lb_coef, wl.z_coef)
+
+
+def make_weights(t: Dict[str, Optional[torch.Tensor]]) -> MoeWeights:
+    """MoeWeights over the tensors of ``t`` (keys as produced by ``synth.make_inputs``)."""
+    w = MoeWeights(*[_p(t.get(n)) for n in ("w_router", "logit_bias", "w_up", "w_gate", "w_down", "b_up", "b_down",
+                                            "ws_up", "ws_gate", "ws_down")])
+    w._keep = t  # keep the tensors alive as long as the struct
+    return w
+
+
+# ----------------------------------------------------------------------------- C ABI, same names
+def moe_status_string(s: int) -> str:
+    return lib().moe_status_string(int(s)).decode()
+
+
+def moe_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return int(n.value)
+
+
+def moe_capacity(cfg: MoeConfig):
+    cap, amax = _c_i32(0), _c_i32(0)
+    _check(lib().moe_capacity(ctypes.byref(cfg), ctypes.byref(cap), ctypes.byref(amax)), "moe_capacity")
+    return int(cap.value), int(amax.value)
+
+
+def moe_route(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, ws, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx), _p(topk_w),
+                           _p(counts), _p(losses), _p(ws), _s(stream)), "moe_route")
+
+
+def moe_permute(cfg, x, topk_idx, counts, offsets, kept, row_of, tok_of, x_perm, ws, stream=None):
+    _check(lib().moe_permute(ctypes.byref(cfg), _p(x), _p(topk_idx), _p(counts), _p(offsets), _p(kept),
+                             _p(row_of), _p(tok_of), _p(x_perm), _p(ws), _s(stream)), "moe_permute")
+
+
+def moe_expert_ffn(cfg, x_perm, offsets, weights: MoeWeights, y_perm, x, y_shared, ws, stream=None):
+    _check(lib().moe_expert_ffn(ctypes.byref(cfg), _p(x_perm), _p(offsets), ctypes.byref(weights), _p(y_perm),
+                                _p(x), _p(y_shared), _p(ws), _s(stream)), "moe_expert_ffn")
+
+
+def moe_combine(cfg, y_perm, row_of, topk_w, y_shared, y, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), _p(y_perm), _p(row_of), _p(topk_w), _p(y_shared), _p(y),
+                             _s(stream)), "moe_combine")
+
+
+def moe_layer_forward(cfg, weights: MoeWeights, x, y, losses, counts_out, drops_out, ws, stream=None):
+    _check(lib().moe_layer_forward(ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(y), _p(losses),
+                                   _p(counts_out), _p(drops_out), _p(ws), _s(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_timed(cfg, weights: MoeWeights, x, y, losses, counts_out, drops_out, ws,
+                            events: Sequence[torch.cuda.Event], stream=None):
+    arr = (_c_p * len(events))(*[ev.cuda_event for ev in events])
+    _check(lib().moe_layer_forward_timed(ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(y), _p(losses),
+                                         _p(counts_out), _p(drops_out), _p(ws), _s(stream), arr, len(events)),
+           "moe_layer_forward_timed")
+
+
+def moe_read_device_status(ws, stream=None) -> int:
+    """Synchronise and return (and clear) the device status word of ``ws`` as a status code."""
+    return int(lib().moe_read_device_status(_p(ws), _s(stream)))
+
+
+def moe_layer_forward_launches(cfg) -> int:
+    return int(lib().moe_layer_forward_launches(ctypes.byref(cfg)))
+
+
+# ----------------------------------------------------------------------------- convenience
+def alloc_workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace (the status word must start at zero)."""
+    return torch.zeros(max(moe_workspace_size(cfg), 256), dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    """Holds a config, the weights and a workspace; ``forward(x)`` runs ``moe_layer_forward``."""
+
+    def __init__(self, cfg: MoeConfig, tensors: Dict[str, Optional[torch.Tensor]], device="cuda"):
+        self.cfg = cfg
+        self.weights = make_weights(tensors)
+        self.ws = alloc_workspace(cfg, device)
+        self.device = device
+
+    def forward(self, x: torch.Tensor, stream=None):
+        c = self.cfg
+        y = torch.empty_like(x)
+        losses = torch.empty(2, dtype=torch.float32, device=x.device)
+        counts = torch.empty(c.E, dtype=torch.int32, device=x.device)
+        drops = torch.empty(1, dtype=torch.int32, device=x.device)
+        moe_layer_forward(c, self.weights, x, y, losses, counts, drops, self.ws, stream)
+        return y, losses, counts, drops
