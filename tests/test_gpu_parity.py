@@ -95,7 +95,8 @@ def check_all_steps(wl, inp_cpu, inp_gpu, tokens=None):
     if n_b == 0:
         assert same.all()
         # expert outputs per sorted row (oracle rows of the sampled tokens)
-        rows = [r for r in range(A) if int(ref["tok_of"][r]) in set(toks.tolist())]
+        tokset = set(toks.tolist())
+        rows = [r for r in range(A) if int(ref["tok_of"][r]) in tokset]
         if rows:
             check_output(to_np(got["y_perm"][rows]), ref["y_perm"][rows], wl.dtype, "y_perm")
     ys_ref = _shared_ref(wl, inp_cpu, toks)
