@@ -24,7 +24,9 @@
  *    that gave up) are recorded in a status word inside the workspace; read it with
  *    moe_read_device_status.
  *  - `ws` is a device workspace of at least moe_workspace_size bytes, 256-byte aligned, owned
- *    by the caller; the same workspace must not be used by two calls that may run concurrently.
+ *    by the caller and zero-filled before its first use (its first word is the device status
+ *    word); the same workspace must not be used by two calls that may run concurrently.
+ *  - Every tensor pointer must be 16-byte aligned (MOE_ERR_INVALID_ARG otherwise).
  *  - A_max = T*k (dropless) or min(T*k, E*C): the row capacity of the expert-sorted buffers.
  *  - Shape limits: 1 <= k <= min(E, 8), 1 <= E <= 256, T >= 0, d >= 1, dff >= 1.  bf16 layers
  *    also need d % 64 == 0 and dff % 64 == 0 (tensor-core tiles), and with n_shared > 1 also
@@ -117,16 +119,20 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
 
 /* Expert FFNs (mini-moe tutorial sec. 3.1; GPT-4 2% article sec. 3.1; shared experts:
  * FLAME-MoE summary sec. 2).
- *   x_perm [A_max,d] with offsets [E+1] from moe_permute -> y_perm [A_max,d] (rows < offsets[E]);
- *   when n_shared > 0 also x [T,d] -> y_shared [T,d] = sum_s FFN^shared_s(x) (else both NULL).
- * Hidden activations are kept in the workspace; bf16 layers round them to bf16. */
+ *   x_perm [A_max,d] with offsets [E+1] from moe_permute -> y_perm [A_max,d] fp32 (rows < offsets[E]);
+ *   when n_shared > 0 also x [T,d] -> y_shared [T,d] fp32 = sum_s FFN^shared_s(x) (else both NULL).
+ * y_perm and y_shared keep the fp32 accumulators so that the layer output is rounded only once.
+ * Hidden activations are kept in the workspace; bf16 layers round them to bf16 (they are the
+ * operand of the down-projection's bf16 tensor-core MMA). */
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
                           const moe_weights* w, void* y_perm, const void* x, void* y_shared,
                           void* ws, void* stream);
 
 /* Combine (FLAME-MoE summary sec. 2: output = routing-weighted sum of the selected experts).
  *   y[t] = sum_{j: row_of[t,j] >= 0} topk_w[t,j] * y_perm[row_of[t,j]]  (+ y_shared[t])
- * accumulated in fp32 in slot order and rounded once.  y_shared may be NULL. */
+ * y_perm [A_max,d] and y_shared [T,d] are fp32 (as moe_expert_ffn writes them); y [T,d] has the
+ * layer dtype.  Accumulated in fp32 in slot order, shared output last, rounded once.
+ * y_shared may be NULL. */
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
                        const float* topk_w, const void* y_shared, void* y, void* stream);
 

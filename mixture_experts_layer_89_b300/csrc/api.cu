@@ -98,9 +98,9 @@ WsLayout layout(const moe_config* c) {
   L.tok_of = take(A * 4);
   L.x_perm = take(A * d * elt(c));
   L.h = take(A * f * elt(c));
-  L.y_perm = take(A * d * elt(c));
+  L.y_perm = take(A * d * 4);
   L.h_sh = take(T * S * f * elt(c));
-  L.y_sh = take(S ? T * d * elt(c) : 0);
+  L.y_sh = take(S ? T * d * 4 : 0);
   L.total = off;
   return L;
 }
@@ -196,7 +196,7 @@ moe_status ffn_routed_impl(const moe_config* c, const void* x_perm, const int32_
     dn.bias = c->has_bias ? w->b_down : nullptr;
     dn.N = c->d; dn.K = c->dff; dn.N_w = c->d; dn.K_w = c->dff; dn.G_w = c->E;
     dn.act = ACT_NONE;
-    dn.out = y_perm; dn.ldc = c->d;
+    dn.out = y_perm; dn.ldc = c->d; dn.out_f32 = true;
     MOE_TRY(run_projection(c, dn, status, st));
   }
   return MOE_OK;
@@ -226,7 +226,7 @@ moe_status ffn_shared_impl(const moe_config* c, const void* x, const moe_weights
   dn.B0 = w->ws_down; dn.B1 = nullptr; dn.bias = nullptr;
   dn.N = c->d; dn.K = S * c->dff; dn.N_w = c->d; dn.K_w = c->dff; dn.G_w = S;
   dn.act = ACT_NONE;
-  dn.out = y_shared; dn.ldc = c->d;
+  dn.out = y_shared; dn.ldc = c->d; dn.out_f32 = true;
   return run_projection(c, dn, status, st);
 }
 
@@ -270,7 +270,8 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
   MOE_TRY(rec(4));
   MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, st));
   MOE_TRY(rec(5));
-  MOE_CUDA(launch_combine(is_bf16(c), y_perm, row_of, topk_w, y_sh, y, c->T, c->d, c->k, st));
+  MOE_CUDA(launch_combine(is_bf16(c), static_cast<const float*>(y_perm), row_of, topk_w,
+                          static_cast<const float*>(y_sh), y, c->T, c->d, c->k, st));
   MOE_TRY(rec(6));
   return MOE_OK;
 }
@@ -337,7 +338,8 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
   MOE_TRY(validate(cfg));
   if (cfg->T > 0 && (!row_of || !topk_w || !y || (!y_perm && a_max_of(cfg) > 0))) return MOE_ERR_INVALID_ARG;
   if (misaligned(y_perm) || misaligned(y_shared) || misaligned(y)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(launch_combine(is_bf16(cfg), y_perm, row_of, topk_w, y_shared, y, cfg->T, cfg->d, cfg->k,
+  return cuda_status(launch_combine(is_bf16(cfg), static_cast<const float*>(y_perm), row_of, topk_w,
+                                    static_cast<const float*>(y_shared), y, cfg->T, cfg->d, cfg->k,
                                     static_cast<cudaStream_t>(stream)));
 }
 

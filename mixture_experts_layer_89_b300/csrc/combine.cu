@@ -5,55 +5,36 @@
 // always-on shared experts.  A dropped slot (row -1) contributes nothing and the surviving
 // weights are not renormalised (OpenMythos article, sec. 3.1, overflow handling).
 //
-// One warp per token; each lane moves 16-byte vectors; fp32 accumulation in slot order, one
-// rounding at the store.  All k source rows of a chunk are loaded before any is accumulated so a
-// lane keeps up to k+1 independent 16-byte loads in flight.
+// The expert outputs arrive in fp32 (the projections keep their accumulators), so the layer output
+// is rounded once.  One warp per token; fp32 accumulation in slot order, then + shared.  All k
+// source rows of a chunk are loaded before any is accumulated so a lane keeps up to 2(k+1)
+// independent 16-byte loads in flight.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 
 namespace {
-template <typename T>
-struct Vec;  // 16 bytes of T
-template <>
-struct Vec<float> {
-  static constexpr int N = 4;
-  static __device__ __forceinline__ void load(const void* p, float (&v)[4]) {
-    const float4 q = *reinterpret_cast<const float4*>(p);
-    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-  }
-  static __device__ __forceinline__ void store(void* p, const float (&v)[4]) {
-    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-  }
-};
-template <>
-struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-  static __device__ __forceinline__ void load(const void* p, float (&v)[8]) {
-    const uint4 q = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = __uint_as_float(w[i] << 16);
-      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
-  static __device__ __forceinline__ void store(void* p, const float (&v)[8]) {
-    uint4 q;
-    q.x = pack_bf16x2(v[0], v[1]);
-    q.y = pack_bf16x2(v[2], v[3]);
-    q.z = pack_bf16x2(v[4], v[5]);
-    q.w = pack_bf16x2(v[6], v[7]);
-    *reinterpret_cast<uint4*>(p) = q;
-  }
-};
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  *reinterpret_cast<uint4*>(p) =
+      make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
 
+// One warp per token, 8 consecutive columns per lane and step (two 16-byte loads per source row).
 template <typename T, int KMAX>
-__global__ void __launch_bounds__(256) k_combine(const T* __restrict__ y_perm, const int32_t* __restrict__ row_of,
-                                                 const float* __restrict__ topk_w, const T* __restrict__ y_shared,
+__global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ row_of,
+                                                 const float* __restrict__ topk_w, const float* __restrict__ y_shared,
                                                  T* __restrict__ y, int Tn, int d, int k) {
-  constexpr int N = Vec<T>::N;
   const int warps = gridDim.x * 8;
   const int lane = threadIdx.x & 31;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += warps) {
@@ -64,37 +45,37 @@ __global__ void __launch_bounds__(256) k_combine(const T* __restrict__ y_perm, c
       rows[j] = (j < k) ? row_of[(size_t)t * k + j] : -1;
       ws[j] = (j < k) ? topk_w[(size_t)t * k + j] : 0.f;
     }
-    for (int c = lane * N; c < d; c += 32 * N) {
-      float acc[N];
-#pragma unroll
-      for (int i = 0; i < N; ++i) acc[i] = 0.f;
-      float v[KMAX][N];
+    for (int c = lane * 8; c < d; c += 32 * 8) {
+      float v[KMAX][8];
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (rows[j] >= 0) Vec<T>::load(y_perm + (size_t)rows[j] * d + c, v[j]);
-      float sv[N];
-      if (y_shared) Vec<T>::load(y_shared + (size_t)t * d + c, sv);
+        if (rows[j] >= 0) load8(y_perm + (size_t)rows[j] * d + c, v[j]);
+      float sv[8];
+      if (y_shared) load8(y_shared + (size_t)t * d + c, sv);
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
         if (rows[j] >= 0) {
 #pragma unroll
-          for (int i = 0; i < N; ++i) acc[i] = fmaf(ws[j], v[j][i], acc[i]);
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(ws[j], v[j][i], acc[i]);
         }
       if (y_shared) {
 #pragma unroll
-        for (int i = 0; i < N; ++i) acc[i] += sv[i];
+        for (int i = 0; i < 8; ++i) acc[i] += sv[i];
       }
-      Vec<T>::store(y + (size_t)t * d + c, acc);
+      store8(y + (size_t)t * d + c, acc);
     }
   }
 }
 
-// Any d: one element per lane step.
+// Any d: one element per lane step (same accumulation order).
 template <typename T>
-__global__ void __launch_bounds__(256) k_combine_scalar(const T* __restrict__ y_perm,
+__global__ void __launch_bounds__(256) k_combine_scalar(const float* __restrict__ y_perm,
                                                         const int32_t* __restrict__ row_of,
                                                         const float* __restrict__ topk_w,
-                                                        const T* __restrict__ y_shared, T* __restrict__ y, int Tn,
+                                                        const float* __restrict__ y_shared, T* __restrict__ y, int Tn,
                                                         int d, int k) {
   const int warps = gridDim.x * 8;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += warps) {
@@ -102,37 +83,35 @@ __global__ void __launch_bounds__(256) k_combine_scalar(const T* __restrict__ y_
       float acc = 0.f;
       for (int j = 0; j < k; ++j) {
         const int r = row_of[(size_t)t * k + j];
-        if (r >= 0) acc = fmaf(topk_w[(size_t)t * k + j], to_f(y_perm[(size_t)r * d + c]), acc);
+        if (r >= 0) acc = fmaf(topk_w[(size_t)t * k + j], y_perm[(size_t)r * d + c], acc);
       }
-      if (y_shared) acc += to_f(y_shared[(size_t)t * d + c]);
+      if (y_shared) acc += y_shared[(size_t)t * d + c];
       y[(size_t)t * d + c] = from_f<T>(acc);
     }
   }
 }
 
 template <typename T>
-cudaError_t launch_t(const void* y_perm, const int32_t* row_of, const float* topk_w, const void* y_shared, void* y,
+cudaError_t launch_t(const float* y_perm, const int32_t* row_of, const float* topk_w, const float* y_shared, void* y,
                      int Tn, int d, int k, cudaStream_t st) {
   int blocks = (Tn + 7) / 8;
   if (blocks > 148 * 32) blocks = 148 * 32;
-  const T* yp = static_cast<const T*>(y_perm);
-  const T* ys = static_cast<const T*>(y_shared);
   T* yo = static_cast<T*>(y);
-  if (((size_t)d * sizeof(T)) % 16 != 0) {
-    k_combine_scalar<T><<<blocks, 256, 0, st>>>(yp, row_of, topk_w, ys, yo, Tn, d, k);
+  if (d % 8 != 0) {
+    k_combine_scalar<T><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
   } else if (k <= 2) {
-    k_combine<T, 2><<<blocks, 256, 0, st>>>(yp, row_of, topk_w, ys, yo, Tn, d, k);
+    k_combine<T, 2><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
   } else if (k <= 4) {
-    k_combine<T, 4><<<blocks, 256, 0, st>>>(yp, row_of, topk_w, ys, yo, Tn, d, k);
+    k_combine<T, 4><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
   } else {
-    k_combine<T, 8><<<blocks, 256, 0, st>>>(yp, row_of, topk_w, ys, yo, Tn, d, k);
+    k_combine<T, 8><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
   }
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_combine(bool bf16, const void* y_perm, const int32_t* row_of, const float* topk_w,
-                           const void* y_shared, void* y, int T, int d, int k, cudaStream_t st) {
+cudaError_t launch_combine(bool bf16, const float* y_perm, const int32_t* row_of, const float* topk_w,
+                           const float* y_shared, void* y, int T, int d, int k, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (bf16) return launch_t<__nv_bfloat16>(y_perm, row_of, topk_w, y_shared, y, T, d, k, st);
   return launch_t<float>(y_perm, row_of, topk_w, y_shared, y, T, d, k, st);

@@ -13,12 +13,12 @@ namespace {
 __device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erff(u * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float u) { return u / (1.f + expf(-u)); }
 
-template <typename T, int ACT>
+template <typename T, typename TO, int ACT>
 __global__ void __launch_bounds__(128) k_proj_simt(const T* __restrict__ A, int64_t lda,
                                                    const int32_t* __restrict__ offsets, int G, int rows_static,
                                                    const T* __restrict__ B0, const T* __restrict__ B1,
                                                    const T* __restrict__ bias, int N, int K, int N_w, int K_w,
-                                                   T* __restrict__ out, int64_t ldc) {
+                                                   TO* __restrict__ out, int64_t ldc) {
   const int row = blockIdx.x;
   const int n = blockIdx.y * blockDim.x + threadIdx.x;
   if (n >= N) return;
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(128) k_proj_simt(const T* __restrict__ A, int6
     if (bias) acc0 += to_f(bias[(size_t)gn * N_w + nn]);
     r = (ACT == ACT_GELU) ? gelu_erf(acc0) : acc0;
   }
-  out[(size_t)row * ldc + n] = from_f<T>(r);
+  out[(size_t)row * ldc + n] = from_f<TO>(r);
 }
 
 template <typename T>
@@ -67,19 +67,23 @@ cudaError_t launch_t(const Projection& p, cudaStream_t st) {
   const T* B0 = static_cast<const T*>(p.B0);
   const T* B1 = static_cast<const T*>(p.B1);
   const T* bias = static_cast<const T*>(p.bias);
-  T* out = static_cast<T*>(p.out);
   switch (p.act) {
     case ACT_GELU:
-      k_proj_simt<T, ACT_GELU><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias, p.N, p.K,
-                                                     p.N_w, p.K_w, out, p.ldc);
+      k_proj_simt<T, T, ACT_GELU><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias, p.N,
+                                                        p.K, p.N_w, p.K_w, static_cast<T*>(p.out), p.ldc);
       break;
     case ACT_SWIGLU:
-      k_proj_simt<T, ACT_SWIGLU><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias, p.N,
-                                                       p.K, p.N_w, p.K_w, out, p.ldc);
+      k_proj_simt<T, T, ACT_SWIGLU><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias,
+                                                          p.N, p.K, p.N_w, p.K_w, static_cast<T*>(p.out), p.ldc);
       break;
     default:
-      k_proj_simt<T, ACT_NONE><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias, p.N, p.K,
-                                                     p.N_w, p.K_w, out, p.ldc);
+      if (p.out_f32)
+        k_proj_simt<T, float, ACT_NONE><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias,
+                                                              p.N, p.K, p.N_w, p.K_w, static_cast<float*>(p.out),
+                                                              p.ldc);
+      else
+        k_proj_simt<T, T, ACT_NONE><<<grid, 128, 0, st>>>(A, p.lda, p.offsets, p.G, p.rows_static, B0, B1, bias, p.N,
+                                                          p.K, p.N_w, p.K_w, static_cast<T*>(p.out), p.ldc);
   }
   return cudaGetLastError();
 }

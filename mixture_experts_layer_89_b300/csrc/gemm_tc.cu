@@ -44,7 +44,7 @@ struct TcArgs {
   int rows_static;
   int N, K, N_w, K_w;
   const __nv_bfloat16* bias;
-  __nv_bfloat16* out;
+  void* out;  // bf16, or fp32 when the kernel's OUTF32 is set
   int64_t ldc;
   uint32_t* status;
 };
@@ -74,7 +74,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erff(u * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float u) { return u / (1.f + expf(-u)); }
 
-template <int ACT>
+template <int ACT, bool OUTF32>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
               const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int row = m0 + q * 32 + lane;
       const bool valid = row < m_end;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNB);
-      __nv_bfloat16* orow = args.out + (size_t)(valid ? row : 0) * args.ldc;
+      const size_t orow = (size_t)(valid ? row : 0) * args.ldc;
       if (ACT == ACT_SWIGLU) {
 #pragma unroll 1
         for (int c = 0; c < NOUT; c += 32) {
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const float h1 = silu(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
               pk[i] = pack_bf16x2(h0, h1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
@@ -307,12 +307,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
             }
-            uint32_t pk[16];
+            if (OUTF32) {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.out) + orow + n0 + c);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(orow + n0 + c);
+              for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            } else {
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
         }
       }
@@ -370,7 +377,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
   return true;
 }
 
-template <int ACT>
+template <int ACT, bool OUTF32>
 cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
   const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
@@ -402,7 +409,7 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
   a.N_w = p.N_w;
   a.K_w = p.K_w;
   a.bias = static_cast<const __nv_bfloat16*>(p.bias);
-  a.out = static_cast<__nv_bfloat16*>(p.out);
+  a.out = p.out;
   a.ldc = p.ldc;
   a.status = status;
   const long n_tiles = (p.N + NOUT - 1) / NOUT;
@@ -410,9 +417,10 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
   long grid = ub_mt * n_tiles;
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
-  cudaError_t err = cudaFuncSetAttribute(k_proj_tc<ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
+  cudaError_t err =
+      cudaFuncSetAttribute(k_proj_tc<ACT, OUTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
   if (err != cudaSuccess) return err;
-  k_proj_tc<ACT><<<(unsigned)grid, NTHREADS, SMEM_TOTAL, st>>>(mA, mB0, mB1, a);
+  k_proj_tc<ACT, OUTF32><<<(unsigned)grid, NTHREADS, SMEM_TOTAL, st>>>(mA, mB0, mB1, a);
   return cudaGetLastError();
 }
 }  // namespace
@@ -420,10 +428,13 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
 const char* tc_last_error() { return g_err; }
 
 cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
+  // hidden layers are bf16 (the next projection's MMA operand); projections to the model width
+  // keep the fp32 accumulator so the layer output is rounded once
   switch (p.act) {
-    case ACT_GELU: return launch_t<ACT_GELU>(p, status, num_sms, st);
-    case ACT_SWIGLU: return launch_t<ACT_SWIGLU>(p, status, num_sms, st);
-    default: return launch_t<ACT_NONE>(p, status, num_sms, st);
+    case ACT_GELU: return launch_t<ACT_GELU, false>(p, status, num_sms, st);
+    case ACT_SWIGLU: return launch_t<ACT_SWIGLU, false>(p, status, num_sms, st);
+    default: return p.out_f32 ? launch_t<ACT_NONE, true>(p, status, num_sms, st)
+                              : launch_t<ACT_NONE, false>(p, status, num_sms, st);
   }
 }
 

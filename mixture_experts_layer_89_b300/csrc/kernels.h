@@ -35,8 +35,9 @@ cudaError_t launch_gather_rows(bool bf16, const void* x, const int32_t* tok_of, 
                                int max_rows, int d, void* x_perm, cudaStream_t st);
 
 // ---------------------------------------------------------------- combine (combine.cu)
-cudaError_t launch_combine(bool bf16, const void* y_perm, const int32_t* row_of, const float* topk_w,
-                           const void* y_shared, void* y, int T, int d, int k, cudaStream_t st);
+// y_perm [rows, d] and y_shared [T, d] are fp32; y is bf16 or fp32.
+cudaError_t launch_combine(bool bf16, const float* y_perm, const int32_t* row_of, const float* topk_w,
+                           const float* y_shared, void* y, int T, int d, int k, cudaStream_t st);
 
 // ---------------------------------------------------------------- grouped FFN GEMMs
 // One grouped projection  out[r, n] = act(sum_k A[r, k] B_{g(r)}[n, k] (+ bias)).
@@ -53,6 +54,7 @@ struct Projection {
   int N, K, N_w, K_w, G_w;
   int act;
   void* out; int64_t ldc;
+  bool out_f32;                                    // out is fp32 (else the layer dtype)
 };
 cudaError_t launch_projection_simt(bool bf16, const Projection& p, cudaStream_t st);
 cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st);
