@@ -18,7 +18,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -69,61 +68,69 @@ def kernel_src_sha1():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """Samples SM clock, power and clock-event (throttle) reasons through NVML (read-only queries)
+    every ~2 ms in a background thread while the timed region runs."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-         "clocks_event_reasons.sw_power_cap")
+    def __init__(self, torch_device: int):
+        self.dev = torch_device
+        self.rows = []
+        self.err = None
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"moe_bench_clocks_{os.getpid()}.csv")
+    def _handle(self, nv):
+        try:
+            p = torch.cuda.get_device_properties(self.dev)
+            bus = "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            return nv.nvmlDeviceGetHandleByPciBusId(bus)
+        except Exception:
+            return nv.nvmlDeviceGetHandleByIndex(self.dev)
+
+    def _run(self):
+        nv = self.nv
+        h = self._handle(nv)
+        smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
+        while not self.stop.is_set():
+            try:
+                self.rows.append((nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM), smax,
+                                  nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
+                                  nv.nvmlDeviceGetCurrentClocksEventReasons(h)))
+            except Exception as e:  # pragma: no cover
+                self.err = str(e)
+                return
+            time.sleep(0.002)
 
     def __enter__(self):
+        import threading
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+            import pynvml as nv
+            nv.nvmlInit()
+            self.nv = nv
+            self.stop = threading.Event()
+            self.th = threading.Thread(target=self._run, daemon=True)
+            self.th.start()
+            time.sleep(0.02)  # first samples before the timed work starts
+        except Exception as e:
+            self.nv = None
+            self.err = str(e)
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
-            self.f.close()
+        if self.nv is not None:
+            self.stop.set()
+            self.th.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
-                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
-                except ValueError:
-                    continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        reasons = set()
-        for r in rows:
-            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
-                              ("pcap", "sw_power_cap")):
-                if r[key].lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["smax"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w_max": max(r["power"] for r in rows)}
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"no samples ({self.err})"]}
+        nv = self.nv
+        names = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
+                 "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
+                 "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
+                 "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap,
+                 "hw_power_brake_slowdown": nv.nvmlClocksEventReasonHwPowerBrakeSlowdown}
+        reasons = sorted({n for n, bit in names.items() for r in self.rows if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows), "sm_max_mhz": max(r[1] for r in self.rows),
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": round(max(r[2] for r in self.rows), 1),
+                "source": "NVML, ~2 ms period, timed region only"}
 
 
 def expert_flops(wl, kept_rows: int, T: int):
@@ -154,6 +161,10 @@ def run_ours(args, wl, ws_n, rank, local):
     stream = torch.cuda.current_stream(dev)
     n_ev = 7
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    for row in evs:          # torch creates the CUDA event on first record: make the handles exist
+        for ev in row:
+            ev.record(stream)
+    torch.cuda.synchronize(dev)
 
     def step(i=None):
         if i is None:

@@ -170,7 +170,10 @@ def moe_layer_forward(cfg, weights: MoeWeights, x, y, losses, counts_out, drops_
 
 def moe_layer_forward_timed(cfg, weights: MoeWeights, x, y, losses, counts_out, drops_out, ws,
                             events: Sequence[torch.cuda.Event], stream=None):
-    arr = (_c_p * len(events))(*[ev.cuda_event for ev in events])
+    handles = [ev.cuda_event for ev in events]
+    if not all(handles):
+        raise ValueError("events must have been recorded once (torch creates them lazily)")
+    arr = (_c_p * len(events))(*handles)
     _check(lib().moe_layer_forward_timed(ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(y), _p(losses),
                                          _p(counts_out), _p(drops_out), _p(ws), _s(stream), arr, len(events)),
            "moe_layer_forward_timed")
