@@ -67,47 +67,75 @@ def kernel_src_sha1():
     return h.hexdigest()
 
 
+class _Nvml:
+    """Minimal read-only NVML access through ctypes (libnvidia-ml ships with the driver)."""
+
+    SM = 1  # NVML_CLOCK_SM
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, torch_device: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        p = torch.cuda.get_device_properties(torch_device)
+        bus = ("%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)).encode()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) != 0:
+            raise RuntimeError(f"no NVML handle for PCI bus {bus.decode()}")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _u32(self, fn, *args):
+        v = self.c.c_uint(0)
+        if fn(self.h, *args, self.c.byref(v)) != 0:
+            raise RuntimeError(fn.__name__)
+        return v.value
+
+    def sample(self):
+        r = self.c.c_ulonglong(0)
+        if self._reasons(self.h, self.c.byref(r)) != 0:
+            raise RuntimeError("clock event reasons")
+        return (self._u32(self.lib.nvmlDeviceGetClockInfo, self.SM), self._u32(self.lib.nvmlDeviceGetPowerUsage) / 1e3,
+                r.value)
+
+    def max_sm(self):
+        return self._u32(self.lib.nvmlDeviceGetMaxClockInfo, self.SM)
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """Samples SM clock, power and clock-event (throttle) reasons through NVML (read-only queries)
-    every ~2 ms in a background thread while the timed region runs."""
+    """Samples the SM clock, power and clock-event (throttle) reasons through NVML (read-only
+    queries) every ~1 ms in a background thread while the timed region runs."""
 
     def __init__(self, torch_device: int):
         self.dev = torch_device
         self.rows = []
         self.err = None
-
-    def _handle(self, nv):
-        try:
-            p = torch.cuda.get_device_properties(self.dev)
-            bus = "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
-            return nv.nvmlDeviceGetHandleByPciBusId(bus)
-        except Exception:
-            return nv.nvmlDeviceGetHandleByIndex(self.dev)
+        self.nv = None
 
     def _run(self):
-        nv = self.nv
-        h = self._handle(nv)
-        smax = nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)
         while not self.stop.is_set():
             try:
-                self.rows.append((nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM), smax,
-                                  nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
-                                  nv.nvmlDeviceGetCurrentClocksEventReasons(h)))
+                self.rows.append(self.nv.sample())
             except Exception as e:  # pragma: no cover
                 self.err = str(e)
                 return
-            time.sleep(0.002)
+            time.sleep(0.001)
 
     def __enter__(self):
         import threading
         try:
-            import pynvml as nv
-            nv.nvmlInit()
-            self.nv = nv
+            self.nv = _Nvml(self.dev)
+            self.smax = self.nv.max_sm()
             self.stop = threading.Event()
             self.th = threading.Thread(target=self._run, daemon=True)
             self.th.start()
-            time.sleep(0.02)  # first samples before the timed work starts
+            time.sleep(0.01)  # first samples before the timed work starts
         except Exception as e:
             self.nv = None
             self.err = str(e)
@@ -117,20 +145,15 @@ class ClockSampler:
         if self.nv is not None:
             self.stop.set()
             self.th.join(timeout=5)
+            self.nv.close()
 
     def summary(self):
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"no samples ({self.err})"]}
-        nv = self.nv
-        names = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
-                 "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
-                 "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
-                 "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap,
-                 "hw_power_brake_slowdown": nv.nvmlClocksEventReasonHwPowerBrakeSlowdown}
-        reasons = sorted({n for n, bit in names.items() for r in self.rows if r[3] & bit})
-        return {"sm_mhz": statistics.median(r[0] for r in self.rows), "sm_max_mhz": max(r[1] for r in self.rows),
-                "reasons": reasons, "samples": len(self.rows), "power_w_max": round(max(r[2] for r in self.rows), 1),
-                "source": "NVML, ~2 ms period, timed region only"}
+        reasons = sorted({n for n, bit in _Nvml.REASONS.items() for r in self.rows if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows), "sm_max_mhz": self.smax,
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": round(max(r[1] for r in self.rows), 1),
+                "source": "NVML (libnvidia-ml via ctypes), ~1 ms period, timed region only"}
 
 
 def expert_flops(wl, kept_rows: int, T: int):
@@ -355,7 +378,7 @@ def main():
     global _PG
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
