@@ -160,6 +160,31 @@ moe_status moe_read_device_status(void* ws, void* stream);
 /* Number of kernels moe_layer_forward launches for this config (for launch accounting). */
 int32_t moe_layer_forward_launches(const moe_config* cfg);
 
+/* Router without a caller-supplied workspace (no counterpart in the pages: an addition of this
+ * library for callers that cannot allocate device memory, such as an engine that reserves all of
+ * HBM for weights and caches at start-up and forbids later cudaMalloc calls (they synchronise the
+ * device and fragment its memory), or a plug-in running inside another framework's operator with
+ * no handle on that framework's allocator).
+ *   Same arguments, results and error codes as moe_route, without `ws`.  Its scratch (the status
+ *   word and the per-CTA partial sums of the router) lives in a fixed device array of
+ *   MOE_ROUTE_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads the library
+ *   holds until the process exits.  This call allocates nothing.
+ *   Limits: T <= MOE_ROUTE_NOALLOC_MAX_T and T * E <= MOE_ROUTE_NOALLOC_MAX_TE, else
+ *   MOE_ERR_UNSUPPORTED (before any GPU work).
+ *   The first call on a device looks up that array's device address (once per device, with that
+ *   device current); make that first call outside any CUDA stream capture.
+ *   All calls share the one array and it keeps the previous call's contents: each call clears the
+ *   status word itself, but two calls whose GPU work may overlap (different streams, or different
+ *   host threads, without ordering between them) race on the array and must not be issued.
+ *   Device-side error flags (non-finite logits) are cleared at the start of every call and are
+ *   not reported back; use moe_route with a workspace when they are needed. */
+#define MOE_ROUTE_NOALLOC_SCRATCH_BYTES (2u << 20)
+#define MOE_ROUTE_NOALLOC_MAX_T (1 << 20)
+#define MOE_ROUTE_NOALLOC_MAX_TE (1 << 22)
+moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w_router,
+                             const float* logit_bias, int32_t* topk_idx, float* topk_w,
+                             int32_t* counts, float* losses, void* stream);
+
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);
 

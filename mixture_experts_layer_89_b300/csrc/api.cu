@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/moe.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -278,6 +280,33 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
 
 }  // namespace
 
+
+// ------------------------------------------------------------------ router without a workspace
+// Scratch of moe_route_noalloc: a file-scope device array.  Host code must not hand the array's
+// name to a kernel (in host code it names a host-side shadow, not device memory); its device
+// address is looked up once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) unsigned char g_route_scratch[MOE_ROUTE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_route_scratch_mu;
+void* g_route_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_route_scratch on the current device (looked up on first use).
+moe_status route_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_route_scratch_mu);
+  if (!g_route_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_route_scratch_ptr[dev] = p;
+  }
+  *out = g_route_scratch_ptr[dev];
+  return MOE_OK;
+}
+}  // namespace
+
 // ================================================================================ C ABI
 extern "C" {
 
@@ -306,6 +335,23 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
   if (misaligned(ws) || misaligned(x) || misaligned(w_router)) return MOE_ERR_INVALID_ARG;
   return route_impl(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, ws,
                     static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
+                             int32_t* topk_idx, float* topk_w, int32_t* counts, float* losses, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (!w_router || !counts || !losses) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!x || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
+  if (misaligned(x) || misaligned(w_router)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > MOE_ROUTE_NOALLOC_MAX_T || (int64_t)cfg->T * cfg->E > MOE_ROUTE_NOALLOC_MAX_TE)
+    return MOE_ERR_UNSUPPORTED;
+  // the router's scratch is the front of the workspace layout, up to the dispatch's first buffer
+  if (layout(cfg).p_hist > (size_t)MOE_ROUTE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  MOE_TRY(route_scratch_address(&scratch));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_CUDA(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st));  // status word starts at zero
+  return route_impl(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, scratch, st);
 }
 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* counts,

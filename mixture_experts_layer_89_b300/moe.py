@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
         L.moe_capacity.argtypes = [cfgp, P(_c_i32), P(_c_i32)]
         L.moe_route.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_route_noalloc.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_permute.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_expert_ffn.argtypes = [cfgp, _c_p, _c_p, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_combine.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
@@ -66,16 +67,16 @@ def lib() -> ctypes.CDLL:
         L.moe_layer_forward_launches.argtypes = [cfgp]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
-        for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_permute", "moe_expert_ffn",
-                     "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
-                     "moe_layer_forward_launches"):
+        for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute",
+                     "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
+                     "moe_read_device_status", "moe_layer_forward_launches"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
 
 
-EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_permute", "moe_expert_ffn", "moe_combine",
-            "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
+EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
+            "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
             "moe_layer_forward_launches", "moe_status_string")
 
 
@@ -146,6 +147,12 @@ def moe_capacity(cfg: MoeConfig):
 def moe_route(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, ws, stream=None):
     _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx), _p(topk_w),
                            _p(counts), _p(losses), _p(ws), _s(stream)), "moe_route")
+
+
+def moe_route_noalloc(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, stream=None):
+    """moe_route without a workspace: the library's fixed device scratch array is used instead."""
+    _check(lib().moe_route_noalloc(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx),
+                                   _p(topk_w), _p(counts), _p(losses), _s(stream)), "moe_route_noalloc")
 
 
 def moe_permute(cfg, x, topk_idx, counts, offsets, kept, row_of, tok_of, x_perm, ws, stream=None):
