@@ -100,7 +100,12 @@ moe_status moe_capacity(const moe_config* cfg, int32_t* cap, int32_t* a_max);
  *   -> topk_idx [T,k] int32 (descending logit, ties to the lower expert index),
  *      topk_w [T,k] fp32 (renormalised over the k), counts [E] int32 (pre-drop assignments),
  *      losses [2] fp32 = {load-balance loss, router z-loss}.
- * Logits are accumulated in fp32. */
+ * Logits are accumulated in fp32: bf16 layers on the tensor cores (one launch; the reduction of
+ * the per-CTA partials into counts and losses is done by the last CTA to finish), fp32 layers on
+ * CUDA cores.  A bf16 token whose leading k+1 logits lie closer together than a bound on the
+ * tensor cores' accumulation error (about 2^-22 (d/16) max(1, |z|)) is re-decided from logits
+ * recomputed with compensated fp32 sums, so the selection and its order do not depend on the
+ * tensor cores' accumulation order. */
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
                      const float* logit_bias, int32_t* topk_idx, float* topk_w,
                      int32_t* counts, float* losses, void* ws, void* stream);

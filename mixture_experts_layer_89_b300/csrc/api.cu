@@ -141,7 +141,12 @@ moe_status route_impl(const moe_config* c, const void* x, const void* wr, const 
                       float* topk_w, int32_t* counts, float* losses, void* ws, cudaStream_t st) {
   const WsLayout L = layout(c);
   uint32_t* status = at<uint32_t>(ws, L.status);
-  MOE_CUDA(launch_route(is_bf16(c), x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w, at<int32_t>(ws, L.r_hist),
+  if (is_bf16(c)) {  // tensor-core router; the last CTA reduces the partials (counter: status block word 1)
+    return cuda_status(launch_route_tc(x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w,
+                                       at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
+                                       status + 1, counts, losses, c->lb_coef, c->z_coef, status, st));
+  }
+  MOE_CUDA(launch_route(false, x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w, at<int32_t>(ws, L.r_hist),
                         at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2), status, st));
   MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
                                  route_blocks(c->T), c->T, c->E, c->k, c->lb_coef, c->z_coef, counts, losses, st));
@@ -350,7 +355,7 @@ moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w
   void* scratch = nullptr;
   MOE_TRY(route_scratch_address(&scratch));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(cudaMemsetAsync(scratch, 0, sizeof(uint32_t), st));  // status word starts at zero
+  MOE_CUDA(cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), st));  // status word and CTA counter start at zero
   return route_impl(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, scratch, st);
 }
 
@@ -422,7 +427,8 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   if (validate(cfg) != MOE_OK) return -1;
   int n = 0;
   const bool tokens = cfg->T > 0;
-  n += tokens ? 2 : 1;                        // router + finalize
+  if (is_bf16(cfg)) n += tokens ? 1 : 0;      // tensor-core router (finalize fused; T = 0: memsets only)
+  else n += tokens ? 2 : 1;                   // router + finalize
   n += tokens ? 4 : 1;                        // histogram, scan, rank, gather
   if (a_max_of(cfg) > 0) n += 2;              // routed up + down projections
   if (cfg->n_shared > 0 && tokens) n += 2;    // shared up + down projections

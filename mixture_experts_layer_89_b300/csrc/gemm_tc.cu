@@ -10,15 +10,21 @@
 // Tile: 128 rows x 256 accumulator columns, K step 64 (one 128-byte swizzle row of bf16).  For
 // SwiGLU the 256 columns are 128 gate columns followed by the same 128 up columns, so one MMA
 // (M=128, N=256, K=16) produces both halves and the epilogue multiplies them in registers.
-// Warp roles (256 threads, one CTA per SM, persistent over tiles):
+// Warp roles (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: A tile (rows of one expert) + B tile (that expert's weights), 4 stages
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma per stage into a TMEM accumulator
 //   warp 2      TMEM allocator (512 columns = two 256-column accumulators, double buffered)
-//   warps 4..7  epilogue: tcgen05.ld (thread = row), bias/activation, bf16 stores
-// Tiles are enumerated m-tile-major with n fastest, so CTAs running at the same time share the A
-// tile and the expert's weight slab through L2.  The tile table is built inside every CTA from the
-// device-side expert offsets; no count returns to the host.
+//   warp 3      builds the tile table from the device-side expert offsets (no count returns to
+//               the host)
+//   warps 4..   EPIW epilogue warps: tcgen05.ld (thread = row), bias/activation, stores.  Warp w
+//               reaches TMEM lanes 32 (w % 4)..; with 8 warps, w and w + 4 split the columns.
+// Paired mode (PAIR): CTAs run in clusters of two that take the two 128-row halves of a 256-row
+// tile of one expert with the same weight tile.  Each CTA loads half of that B tile and multicasts
+// it to both, so B crosses L2 once per 256 rows; each CTA's MMA signals the stage free in both
+// CTAs.  Tiles are enumerated m-tile-major with n fastest (measured faster than n-major here).
 #include <stdio.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -34,9 +40,9 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BNB * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MAXG = 256;
-constexpr int NTHREADS = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = umma_idesc_bf16(BM, BNB);
+constexpr uint16_t PAIR_MASK = 0x3;
 
 struct TcArgs {
   const int32_t* offsets;
@@ -58,7 +64,7 @@ struct SmemCtl {
   uint32_t tmem_base;
   int abort_flag;
   int row_lo[MAXG + 1];
-  int mt_pre[MAXG + 1];
+  int u_pre[MAXG + 1];  // prefix over groups of row units (m-tiles, or m-tile pairs in PAIR mode)
 };
 constexpr size_t SMEM_TOTAL = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
 
@@ -71,14 +77,28 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erff(u * 0.70710678118654752f)); }
-__device__ __forceinline__ float silu(float u) { return u / (1.f + expf(-u)); }
+// Epilogue activations.  Their outputs are rounded to bf16 (relative spacing 2^-8), so they use
+// the hardware exp2/reciprocal approximations (relative error ~1e-7) instead of IEEE expf/erff
+// and division.
+// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26
+// (|error| <= 1.5e-7): erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
+// t = 1 / (1 + p x), x >= 0, odd continuation for x < 0.
+__device__ __forceinline__ float erf_as7126(float x) {
+  const float ax = fabsf(x);
+  const float t = __fdividef(1.f, fmaf(0.3275911f, ax, 1.f));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  return copysignf(1.f - poly * __expf(-ax * ax), x);
+}
+__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erf_as7126(u * 0.70710678118654752f)); }
+__device__ __forceinline__ float silu(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
-template <int ACT, bool OUTF32>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int ACT, bool OUTF32, int EPIW, bool PAIR>
+__global__ void __launch_bounds__(128 + 32 * EPIW, 1)
     k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
               const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
+  constexpr int CW = NOUT / (EPIW / 4);  // output columns per epilogue warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)STAGES * STAGE_BYTES);
@@ -87,15 +107,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int G = args.offsets ? args.G : 1;
   const int n_tiles = (args.N + NOUT - 1) / NOUT;
   const int kblocks = args.K / BK;
+  const int crank = PAIR ? (int)cluster_ctarank() : 0;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs read the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), 4);  // one arrive per epilogue warp
+      mbar_init(smem_u32(&ctl->tempty[a]), EPIW);  // one arrive per epilogue warp
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     ctl->abort_flag = 0;
@@ -111,7 +134,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_relinquish();
   }
   if (warp == 3) {
-    // m-tile prefix over groups: lane owns groups [8 lane, 8 lane + 8)
+    // unit prefix over groups: lane owns groups [8 lane, 8 lane + 8)
     int cnt[8];
     int local = 0;
 #pragma unroll
@@ -123,7 +146,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int hi = args.offsets ? args.offsets[g + 1] : args.rows_static;
         ctl->row_lo[g] = lo;
         if (g == G - 1) ctl->row_lo[G] = hi;
-        cnt[i] = hi > lo ? (hi - lo + BM - 1) / BM : 0;
+        const int mt = hi > lo ? (hi - lo + BM - 1) / BM : 0;
+        cnt[i] = PAIR ? (mt + 1) >> 1 : mt;
         local += cnt[i];
       }
     }
@@ -137,28 +161,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int g = lane * 8 + i;
-      if (g < G) ctl->mt_pre[g] = run;
+      if (g < G) ctl->u_pre[g] = run;
       run += cnt[i];
     }
-    if (lane == 31) ctl->mt_pre[G] = incl;
+    if (lane == 31) ctl->u_pre[G] = incl;
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any remote signal
   tc_fence_after();
 
   const uint32_t tmem_base = ctl->tmem_base;
-  const int total_tiles = ctl->mt_pre[G] * n_tiles;
+  const int total_units = ctl->u_pre[G] * n_tiles;
 
-  auto decode = [&](int t, int& g, int& m0, int& m_end, int& n0) {
-    const int mt = t / n_tiles;
-    const int nt = t - mt * n_tiles;
+  // unit -> (group, first row, end of the group's rows, first output column); m-major, n fastest
+  auto decode = [&](int u, int& g, int& m0, int& m_end, int& n0) {
+    const int mu = u / n_tiles;
+    const int nt = u - mu * n_tiles;
     int lo = 0, hi = G;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (ctl->mt_pre[mid] <= mt) lo = mid; else hi = mid;
+      if (ctl->u_pre[mid] <= mu) lo = mid; else hi = mid;
     }
     g = lo;
-    m0 = ctl->row_lo[g] + (mt - ctl->mt_pre[g]) * BM;
+    const int mt_local = PAIR ? 2 * (mu - ctl->u_pre[g]) + crank : mu - ctl->u_pre[g];
+    m0 = ctl->row_lo[g] + mt_local * BM;   // may lie past m_end in PAIR mode: nothing is stored
     m_end = ctl->row_lo[g + 1];
     n0 = nt * NOUT;
   };
@@ -168,9 +195,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
       bool aborted = false;
-      for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      for (int u = unit0; u < total_units && !aborted; u += ustep) {
         int g, m0, m_end, n0;
-        decode(t, g, m0, m_end, n0);
+        decode(u, g, m0, m_end, n0);
         const int nn = n0 % args.N_w;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status)) {
@@ -178,7 +205,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);  // A + the whole B tile (both halves in PAIR mode)
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           const int k0 = kb * BK;
@@ -187,7 +214,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
-          if (ACT == ACT_SWIGLU) {
+          if (PAIR) {
+            // half `crank` of the B tile, into both CTAs: SwiGLU gate / up halves, else rows
+            // [128 crank, 128 crank + 128) of the tile
+            const uint32_t dst = smem_u32(sb + crank * (B_BYTES / 2));
+            if (ACT == ACT_SWIGLU)
+              tma_load_3d_mc(dst, crank ? &tmB1 : &tmB0, fb, kk, nn, gw, PAIR_MASK);
+            else
+              tma_load_3d_mc(dst, &tmB0, fb, kk, nn + crank * (BNB / 2), gw, PAIR_MASK);
+          } else if (ACT == ACT_SWIGLU) {
             tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
             tma_load_3d(smem_u32(sb + B_BYTES / 2), &tmB1, fb, kk, nn, gw);
           } else {
@@ -209,7 +244,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool aborted = false;
-      for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x, ++it) {
+      for (int u = unit0; u < total_units && !aborted; u += ustep, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, args.status)) break;
@@ -228,7 +263,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC,
                       (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&ctl->empty[s]));
+          if (PAIR)
+            umma_commit_mc(smem_u32(&ctl->empty[s]), PAIR_MASK);  // the stage holds the peer's half too
+          else
+            umma_commit(smem_u32(&ctl->empty[s]));
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
@@ -241,11 +279,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       drain_wait(smem_u32(&ctl->mma_done), 0);
     }
   } else if (warp >= 4) {
-    const int q = warp - 4;
+    const int q = warp & 3;                      // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
+    const int c_lo = ((warp - 4) >> 2) * CW;     // this warp's share of the output columns
     int it = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+    for (int u = unit0; u < total_units; u += ustep, ++it) {
       int g, m0, m_end, n0;
-      decode(t, g, m0, m_end, n0);
+      decode(u, g, m0, m_end, n0);
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       // lane 0 waits, the warp follows its verdict (tcgen05.ld needs the whole warp converged)
@@ -260,7 +299,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const size_t orow = (size_t)(valid ? row : 0) * args.ldc;
       if (ACT == ACT_SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < NOUT; c += 32) {
+        for (int c = c_lo; c < c_lo + CW; c += 32) {
           uint32_t gv[32], uv[32];
           tmem_ld32(tb + c, gv);
           tmem_ld32(tb + 128 + c, uv);
@@ -280,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < NOUT; c += 32) {
+        for (int c = c_lo; c < c_lo + CW; c += 32) {
           uint32_t v[32];
           tmem_ld32(tb + c, v);
           tmem_wait_ld();
@@ -335,16 +374,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if (PAIR) cluster_sync_all();  // no signal from the peer can still be in flight towards this CTA
 }
 
 // ------------------------------------------------------------------------------- host side
+}  // namespace
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-char g_err[256] = "";
+static char g_err[256] = "";
 
-EncodeTiledFn encode_fn() {
+static EncodeTiledFn encode_fn() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* p = nullptr;
@@ -357,8 +399,26 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
+  // cudaFuncSetAttribute once per (kernel, device, size): it is a host call that need not repeat on
+  // every launch (and is then also kept out of any stream capture after the first call).
+  struct Entry { const void* k; int dev; size_t bytes; };
+  static Entry seen[256];
+  static int n_seen = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i].k == kernel && seen[i].dev == dev && seen[i].bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && n_seen < 256) seen[n_seen++] = Entry{kernel, dev, bytes};
+  return e;
+}
+
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                    const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled unavailable");
@@ -377,25 +437,97 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
   return true;
 }
 
+namespace {
+// Largest number of co-resident 2-CTA clusters of a paired kernel (0 if none), per device.
+template <typename K>
+int max_pair_clusters(K kernel, int threads) {
+  struct Entry { const void* k; int dev; int n; };
+  static Entry seen[64];
+  static int n_seen = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_seen; ++i)
+    if (seen[i].k == reinterpret_cast<const void*>(kernel) && seen[i].dev == dev) return seen[i].n;
+  int n = 0;
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kernel), SMEM_TOTAL) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (n_seen < 64) seen[n_seen++] = Entry{reinterpret_cast<const void*>(kernel), dev, n};
+  return n;
+}
+
+template <int ACT, bool OUTF32, int EPIW, bool PAIR>
+cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1, const TcArgs& a,
+                     long grid, cudaStream_t st) {
+  auto kern = k_proj_tc<ACT, OUTF32, EPIW, PAIR>;
+  constexpr int threads = 128 + 32 * EPIW;
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_TOTAL);
+  if (err != cudaSuccess) return err;
+  if (!PAIR) {
+    kern<<<(unsigned)grid, threads, SMEM_TOTAL, st>>>(mA, mB0, mB1, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, a);
+}
+
 template <int ACT, bool OUTF32>
 cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
+  constexpr int EPIW = (ACT == ACT_GELU) ? 8 : 4;  // the erf epilogue is ALU-bound; the others are not
   const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
   if (rows_alloc <= 0 || p.N <= 0) return cudaSuccess;
+  const int G = p.offsets ? p.G : 1;
+  // Pairs pay off when groups average two or more row tiles (otherwise half the pair idles) and
+  // the epilogue is light: the two CTAs of a pair advance in lock-step, so the ALU-bound GELU
+  // epilogue of one stalls both (measured slower there).
+  int n_clusters = 0;
+  if (ACT != ACT_GELU && (long)rows_alloc >= 2L * BM * G)
+    n_clusters = max_pair_clusters(k_proj_tc<ACT, OUTF32, EPIW, true>, 128 + 32 * EPIW);
+  const bool pair = n_clusters > 0;
   CUtensorMap mA, mB0, mB1;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)rows_alloc};
     const cuuint64_t str[1] = {(cuuint64_t)p.lda * 2};
     const cuuint32_t box[2] = {BK, BM};
-    if (!make_map(&mA, p.A, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_tmap_bf16(&mA, p.A, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)p.K_w, (cuuint64_t)p.N_w, (cuuint64_t)p.G_w};
     const cuuint64_t str[2] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)p.N_w * p.K_w * 2};
-    const cuuint32_t box[3] = {BK, (cuuint32_t)(ACT == ACT_SWIGLU ? BNB / 2 : BNB), 1};
-    if (!make_map(&mB0, p.B0, 3, dims, str, box)) return cudaErrorInvalidValue;
+    const cuuint32_t box[3] = {BK, (cuuint32_t)((ACT == ACT_SWIGLU || pair) ? BNB / 2 : BNB), 1};
+    if (!make_tmap_bf16(&mB0, p.B0, 3, dims, str, box)) return cudaErrorInvalidValue;
     if (ACT == ACT_SWIGLU) {
-      if (!make_map(&mB1, p.B1, 3, dims, str, box)) return cudaErrorInvalidValue;
+      if (!make_tmap_bf16(&mB1, p.B1, 3, dims, str, box)) return cudaErrorInvalidValue;
     } else {
       mB1 = mB0;
     }
@@ -413,15 +545,17 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
   a.ldc = p.ldc;
   a.status = status;
   const long n_tiles = (p.N + NOUT - 1) / NOUT;
-  const long ub_mt = p.offsets ? (rows_alloc + BM - 1) / BM + p.G : (p.rows_static + BM - 1) / BM;
+  const long ub_mt = (rows_alloc + BM - 1) / BM + (p.offsets ? G : 0);  // each group adds <= 1 partial tile
+  if (pair) {
+    long units = (ub_mt + G + 1) / 2 * n_tiles;
+    long clusters = units < n_clusters ? units : n_clusters;
+    if (clusters < 1) clusters = 1;
+    return launch_k<ACT, OUTF32, EPIW, true>(mA, mB0, mB1, a, 2 * clusters, st);
+  }
   long grid = ub_mt * n_tiles;
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
-  cudaError_t err =
-      cudaFuncSetAttribute(k_proj_tc<ACT, OUTF32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_TOTAL);
-  if (err != cudaSuccess) return err;
-  k_proj_tc<ACT, OUTF32><<<(unsigned)grid, NTHREADS, SMEM_TOTAL, st>>>(mA, mB0, mB1, a);
-  return cudaGetLastError();
+  return launch_k<ACT, OUTF32, EPIW, false>(mA, mB0, mB1, a, grid, st);
 }
 }  // namespace
 

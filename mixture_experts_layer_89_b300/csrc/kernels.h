@@ -16,6 +16,14 @@ int route_blocks(int T);
 cudaError_t launch_route(bool bf16, const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                          int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2,
                          uint32_t* status, cudaStream_t st);
+// Tensor-core router of bf16 layers (one launch, 128 tokens per CTA): writes top-k, and through
+// the last CTA to finish, counts [E] and losses [2].  hist/psum/lse2 hold route_tc_blocks(T) rows
+// of partials; *done must be zero before the launch and is zero again after it.
+int route_tc_blocks(int T);
+cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
+                            int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
+                            int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
+                            cudaStream_t st);
 // Reduces the per-CTA partials: counts [E] and losses [2].
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,
                                   int k, float lb_coef, float z_coef, int32_t* counts, float* losses,
@@ -59,5 +67,13 @@ struct Projection {
 cudaError_t launch_projection_simt(bool bf16, const Projection& p, cudaStream_t st);
 cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st);
 const char* tc_last_error();
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` (once per kernel and device).
+cudaError_t ensure_smem_attr(const void* kernel, size_t bytes);
+
+// bf16 tensor map with the 128-byte swizzle (tiles of 64 bf16 along the innermost dimension);
+// out-of-range elements of a box read as zero.  False (message in tc_last_error) on failure.
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                    const cuuint32_t* box);
 
 }  // namespace moe

@@ -221,7 +221,7 @@ cudaError_t launch_route_t(const void* x, const void* wr, const float* lbias, in
                            cudaStream_t st) {
   const size_t smem = sizeof(float) * ((size_t)RT * (RDC + 1) + (size_t)E * (RDC + 1) + (size_t)RT * (E + 1) + RT) +
                       sizeof(int) * (size_t)E;
-  cudaError_t err = cudaFuncSetAttribute(k_route<T, NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(k_route<T, NI>), smem);
   if (err != cudaSuccess) return err;
   k_route<T, NI><<<route_blocks(Tn), RTHREADS, smem, st>>>(static_cast<const T*>(x), static_cast<const T*>(wr), lbias,
                                                             Tn, d, E, k, topk_idx, topk_w, hist, psum, lse2, status);
