@@ -66,7 +66,9 @@ struct SmemCtl {
   int row_lo[MAXG + 1];
   int u_pre[MAXG + 1];  // prefix over groups of row units (m-tiles, or m-tile pairs in PAIR mode)
 };
-constexpr size_t SMEM_TOTAL = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
+constexpr int STG_BYTES = 32 * 32 * 4;  // fp32-output epilogue: one 32 x 32 staging tile per warp
+constexpr size_t SMEM_BASE = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
+constexpr size_t smem_total(bool outf32, int epiw) { return SMEM_BASE + (outf32 ? (size_t)epiw * STG_BYTES + 1024 : 0); }
 
 // Wait that ignores the abort flag (used to drain in-flight async operations before exit).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -96,12 +98,15 @@ __device__ __forceinline__ float silu(float u) { return __fdividef(u, 1.f + __ex
 template <int ACT, bool OUTF32, int EPIW, bool PAIR>
 __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
     k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-              const __grid_constant__ CUtensorMap tmB1, const TcArgs args) {
+              const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut, const TcArgs args) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
   constexpr int CW = NOUT / (EPIW / 4);  // output columns per epilogue warp
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)STAGES * STAGE_BYTES);
+  // fp32 staging tiles (1024-byte aligned for the 128-byte swizzle), one per epilogue warp
+  uint8_t* stg_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(ctl) + sizeof(SmemCtl) + 1023) & ~uintptr_t(1023));
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.offsets ? args.G : 1;
@@ -281,6 +286,7 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   } else if (warp >= 4) {
     const int q = warp & 3;                      // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
     const int c_lo = ((warp - 4) >> 2) * CW;     // this warp's share of the output columns
+    uint8_t* stg = stg_base + (size_t)(warp - 4) * STG_BYTES;
     int it = 0;
     for (int u = unit0; u < total_units; u += ustep, ++it) {
       int g, m0, m_end, n0;
@@ -295,6 +301,7 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       tc_fence_after();
       const int row = m0 + q * 32 + lane;
       const bool valid = row < m_end;
+      const bool full_rows = m0 + q * 32 + 32 <= m_end;  // all 32 rows of this warp are output rows
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNB);
       const size_t orow = (size_t)(valid ? row : 0) * args.ldc;
       if (ACT == ACT_SWIGLU) {
@@ -346,7 +353,22 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
             }
-            if (OUTF32) {
+            if (OUTF32 && full_rows) {
+              // the warp's 32 rows x 32 columns go out as one TMA tile store through shared
+              // memory (128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8))
+              if (lane == 0) bulk_wait_read0();  // the previous store has finished reading stg
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmOut, smem_u32(stg), n0 + c, m0 + q * 32);
+                bulk_commit();
+              }
+            } else if (OUTF32) {
               float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.out) + orow + n0 + c);
 #pragma unroll
               for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
@@ -366,6 +388,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
     }
+    if (OUTF32 && lane == 0) bulk_wait_all();  // tile stores complete before the CTA leaves
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -417,16 +441,16 @@ cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
   return e;
 }
 
-bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                    const cuuint32_t* box) {
+static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int rank, const cuuint64_t* dims,
+                      const cuuint64_t* strides, const cuuint32_t* box) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled unavailable");
     return false;
   }
   const cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled failed (%d) rank %d dims %llu %llu %llu", (int)r, rank,
@@ -437,10 +461,15 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t*
   return true;
 }
 
+bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                    const cuuint32_t* box) {
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
+}
+
 namespace {
 // Largest number of co-resident 2-CTA clusters of a paired kernel (0 if none), per device.
 template <typename K>
-int max_pair_clusters(K kernel, int threads) {
+int max_pair_clusters(K kernel, int threads, size_t smem) {
   struct Entry { const void* k; int dev; int n; };
   static Entry seen[64];
   static int n_seen = 0;
@@ -451,7 +480,7 @@ int max_pair_clusters(K kernel, int threads) {
   for (int i = 0; i < n_seen; ++i)
     if (seen[i].k == reinterpret_cast<const void*>(kernel) && seen[i].dev == dev) return seen[i].n;
   int n = 0;
-  if (ensure_smem_attr(reinterpret_cast<const void*>(kernel), SMEM_TOTAL) != cudaSuccess) {
+  if (ensure_smem_attr(reinterpret_cast<const void*>(kernel), smem) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -463,7 +492,7 @@ int max_pair_clusters(K kernel, int threads) {
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
@@ -475,14 +504,15 @@ int max_pair_clusters(K kernel, int threads) {
 }
 
 template <int ACT, bool OUTF32, int EPIW, bool PAIR>
-cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1, const TcArgs& a,
-                     long grid, cudaStream_t st) {
+cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1, const CUtensorMap& mO,
+                     const TcArgs& a, long grid, cudaStream_t st) {
   auto kern = k_proj_tc<ACT, OUTF32, EPIW, PAIR>;
   constexpr int threads = 128 + 32 * EPIW;
-  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), SMEM_TOTAL);
+  constexpr size_t smem = smem_total(OUTF32, EPIW);
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   if (!PAIR) {
-    kern<<<(unsigned)grid, threads, SMEM_TOTAL, st>>>(mA, mB0, mB1, a);
+    kern<<<(unsigned)grid, threads, smem, st>>>(mA, mB0, mB1, mO, a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -493,11 +523,11 @@ cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = SMEM_TOTAL;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, a);
+  return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, mO, a);
 }
 
 template <int ACT, bool OUTF32>
@@ -512,7 +542,7 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
   // epilogue of one stalls both (measured slower there).
   int n_clusters = 0;
   if (ACT != ACT_GELU && (long)rows_alloc >= 2L * BM * G)
-    n_clusters = max_pair_clusters(k_proj_tc<ACT, OUTF32, EPIW, true>, 128 + 32 * EPIW);
+    n_clusters = max_pair_clusters(k_proj_tc<ACT, OUTF32, EPIW, true>, 128 + 32 * EPIW, smem_total(OUTF32, EPIW));
   const bool pair = n_clusters > 0;
   CUtensorMap mA, mB0, mB1;
   {
@@ -532,6 +562,13 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
       mB1 = mB0;
     }
   }
+  CUtensorMap mO = mA;
+  if (OUTF32) {  // output tile map for the TMA stores of the epilogue: 32 x 32 fp32 boxes
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)rows_alloc};
+    const cuuint64_t str[1] = {(cuuint64_t)p.ldc * 4};
+    const cuuint32_t box[2] = {32, 32};
+    if (!make_tmap(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.out, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
   TcArgs a;
   a.offsets = p.offsets;
   a.G = p.G;
@@ -550,12 +587,12 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
     long units = (ub_mt + G + 1) / 2 * n_tiles;
     long clusters = units < n_clusters ? units : n_clusters;
     if (clusters < 1) clusters = 1;
-    return launch_k<ACT, OUTF32, EPIW, true>(mA, mB0, mB1, a, 2 * clusters, st);
+    return launch_k<ACT, OUTF32, EPIW, true>(mA, mB0, mB1, mO, a, 2 * clusters, st);
   }
   long grid = ub_mt * n_tiles;
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
-  return launch_k<ACT, OUTF32, EPIW, false>(mA, mB0, mB1, a, grid, st);
+  return launch_k<ACT, OUTF32, EPIW, false>(mA, mB0, mB1, mO, a, grid, st);
 }
 }  // namespace
 
