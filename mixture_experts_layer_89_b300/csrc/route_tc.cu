@@ -6,24 +6,24 @@
 // tutorial, sec. 3.1 (MoELayer) and the routing pseudo-code of the OpenMythos article, sec. 3.1;
 // the load-balance loss is that article's alpha E sum_e f_e P_e, the z-loss the one the FLAME-MoE
 // summary, sec. 2, names.  The logit GEMM is a dense contraction (T x d x E), so it runs on
-// tcgen05 with N = E (rounded up to 16) and the whole logit row of 128 tokens in TMEM; it then
-// costs one HBM read of x.
+// tcgen05 with N = E (rounded up to 16) and the whole logit row of 128 tokens in TMEM; the main
+// loop then streams x from HBM once, at the HBM roofline.
 //
-// CTA = 128 tokens, 256 threads:
+// CTA = 128 tokens, 256 threads.  Main loop:
 //   warp 0     TMA producer: x tile [128 x 64] and W_r tile [Npad x 64] per stage
 //   warp 1     MMA issuer: 4 x tcgen05.mma (M=128, N=Npad, K=16) per stage
-//   warp 2     TMEM allocator
-//   warp 3     copies the logit bias to shared memory
-//   warps 4-7  epilogue, thread = token: three passes over its TMEM row
-//              (1) top-(k+1) by logit, ties to the lower expert index,
-//              (2) softmax denominator; near-tie candidates,
-//              (3) probabilities, reduced over the CTA's tokens per expert (fixed order).
-// Exactness of the selection: the tensor cores accumulate in fp32 but round differently from a
-// sequential sum, so a token whose top-(k+1) logits are closer than a band (a bound on that
-// accumulation error, scaled with d and the logits' magnitude) is re-decided from logits
-// recomputed with compensated fp32 sums (near fp64 accuracy) for every expert within the band of
-// the boundary.  The last CTA to finish (a counter in the workspace) reduces the
-// per-CTA partials in a fixed order into counts and losses, so results are deterministic.
+//   warp 2     TMEM allocator;   warp 3   logit bias and counters
+// Epilogue, all 8 warps, the pipeline buffers reused as scratch:
+//   A  TMEM -> shared memory (warp w reads TMEM lane quarter w % 4)
+//   B  thread per (token, expert half): sorted top-(k+1) insertion lists, ties to the lower
+//      expert index, merged per token; near-tie candidates; softmax denominators
+//   C  exact re-decision of near ties: the tensor cores accumulate in fp32 but round differently
+//      from a sequential sum, so a token whose leading k+1 logits lie closer than a bound on that
+//      accumulation error is re-decided from compensated fp32 (Neumaier) dot products of every
+//      expert within the band, shared out over the warps
+//   D  outputs per token; per-expert sums of P over the CTA's tokens in token order
+// The last CTA to finish (a counter in the workspace) reduces the per-CTA partials in block order
+// into counts and losses, so results do not depend on scheduling.
 #include <float.h>
 #include <stdio.h>
 
@@ -36,15 +36,19 @@ namespace {
 constexpr int RM = 128;                 // tokens per CTA (MMA M)
 constexpr int RBK = 64;                 // K per stage: one 128-byte swizzle row of bf16
 constexpr int RTHREADS = 256;
+constexpr int RWARPS = RTHREADS / 32;
 constexpr int A_TILE = RM * RBK * 2;    // 16 KB
 constexpr int SMEM_STAGES_BYTES = 192 * 1024;
 constexpr int MAX_STAGES = 8;
+constexpr int KLMAX = 9;                // top-(k+1) list, k <= 8
 constexpr int CMAX = 16;                // near-tie candidates kept per token (more: all experts)
 // Near-tie band of a token: a bound on the difference between the tensor cores' fp32 accumulation
 // and an exactly rounded sum, |error| <~ (d / 16 MMA steps) x ulp(|partial sums|), taken twice
 // over with |partial sums| <= max(1, |logits|); measured errors stay ~10x below it.
 constexpr float kBandFloor = 2e-5f;
 constexpr float kBadLogit = -3.0e38f;
+
+enum : int { F_FEW = 2, F_ALL = 4, F_BAD = 8 };
 
 struct RouteCtl {
   uint64_t full[MAX_STAGES];
@@ -53,16 +57,48 @@ struct RouteCtl {
   uint32_t tmem_base;
   int abort_flag;
   int is_last;
+  int npairs;
   int hist[256];
   float bias[256];
-  float red[4][256];
-  float lse2[4];
+  float lse[RM];
+  float mx[RM];       // top (tensor-core) logit of each token
+  float sinv[RM];     // 1 / softmax denominator (0 for rows past T)
+  float spart[2][RM]; // denominators of the two expert halves
+  int flags[RM];
+  int ncand[RM];
+  float lse2w[RWARPS];
   double lbterm[256];
-  int npairs;
-  uint8_t cand[RM][CMAX];
-  float cexact[RM][CMAX];
-  uint16_t pairs[RM * CMAX];   // (row << 4) | candidate slot
+  double red[RWARPS];
 };
+
+// Epilogue scratch laid over the pipeline buffers once the main loop is done.
+constexpr int PPARTS = 8;  // row (or block) slices of the per-expert column sums
+struct EpiScratch {
+  float* Z;          // [RM][E+1] logits, then exp(z - max)
+  float* tlv;        // [2][RM][KLMAX] top lists of the two expert halves (merged list in half 0)
+  int* tle;          // [2][RM][KLMAX]
+  float* cexact;     // [RM][CMAX] recomputed logits of near-tie candidates
+  float* ppart;      // [PPARTS][256] partial column sums
+  int* hpart;        // [PPARTS][256] partial counts (last CTA)
+  uint16_t* pairs;   // [RM*CMAX] (row << 4) | candidate slot
+  uint8_t* cand;     // [RM][CMAX] candidate experts, ascending
+};
+__host__ __device__ inline size_t epi_scratch_bytes(int E) {
+  return (size_t)RM * (E + 1) * 4 + 2 * (size_t)RM * KLMAX * 8 + (size_t)RM * CMAX * 4 + 2 * (size_t)PPARTS * 256 * 4 +
+         (size_t)RM * CMAX * (2 + 1);
+}
+__device__ inline EpiScratch epi_scratch(uint8_t* base, int E) {
+  EpiScratch s;
+  s.Z = reinterpret_cast<float*>(base);
+  s.tlv = s.Z + (size_t)RM * (E + 1);
+  s.tle = reinterpret_cast<int*>(s.tlv + 2 * RM * KLMAX);
+  s.cexact = reinterpret_cast<float*>(s.tle + 2 * RM * KLMAX);
+  s.ppart = s.cexact + RM * CMAX;
+  s.hpart = reinterpret_cast<int*>(s.ppart + PPARTS * 256);
+  s.pairs = reinterpret_cast<uint16_t*>(s.hpart + PPARTS * 256);
+  s.cand = reinterpret_cast<uint8_t*>(s.pairs + RM * CMAX);
+  return s;
+}
 
 struct RouteArgs {
   const __nv_bfloat16* x;
@@ -89,8 +125,6 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitLimitNs) return;
   }
 }
-
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Insert (v, e) into the descending list lv/le of length n (elements arrive in increasing e, so a
 // strict comparison leaves an equal earlier element in front: ties go to the lower index).
@@ -154,21 +188,6 @@ __device__ __forceinline__ float exact_dot(const __nv_bfloat16* __restrict__ a, 
   return __fadd_rn(s, c);
 }
 
-// Sum over the 32 lanes of 32 values per lane: afterwards lane l holds sum over lanes of v[l].
-__device__ __forceinline__ float warp_transpose_sum(float (&v)[32], int lane) {
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-    const bool upper = (lane & w) != 0;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = upper ? v[i] : v[i + w];
-      const float keep = upper ? v[i + w] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-    }
-  }
-  return v[0];
-}
-
 template <int KL>  // list length >= k + 1
 __global__ void __launch_bounds__(RTHREADS, 1)
     k_route_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const RouteArgs a) {
@@ -177,14 +196,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const int stage_bytes = A_TILE + a.npad * RBK * 2;
   RouteCtl* ctl = reinterpret_cast<RouteCtl*>(smem + (size_t)a.stages * stage_bytes);
   volatile int* abort_flag = &ctl->abort_flag;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k;
   const int kblocks = a.d / RBK;
   const int t0 = blockIdx.x * RM;
   uint32_t tmem_cols = 32;
   while ((int)tmem_cols < a.npad) tmem_cols <<= 1;
 
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
@@ -207,78 +226,105 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       ctl->bias[e] = (e < E && a.lbias) ? a.lbias[e] : 0.f;
       ctl->hist[e] = 0;
     }
+    for (int r = lane; r < RM; r += 32) ctl->flags[r] = 0;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0, armed = 0, armed_ph = 0;
-      bool aborted = false;
-      // every CTA reads all of W_r: start each at a different k-block so that they do not all ask
-      // the same L2 lines for the same tile at the same moment
-      const int kb0 = (int)(blockIdx.x % (unsigned)kblocks);
-      for (int i = 0; i < kblocks; ++i) {
-        const int kb = kb0 + i < kblocks ? kb0 + i : kb0 + i - kblocks;
-        if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.status)) {
-          aborted = true;
-          break;
-        }
-        const uint32_t fb = smem_u32(&ctl->full[s]);
-        mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
-        armed |= 1u << s;
-        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-        uint8_t* sa = smem + (size_t)s * stage_bytes;
-        tma_load_2d(smem_u32(sa), &tmX, fb, kb * RBK, t0);
-        tma_load_2d(smem_u32(sa + A_TILE), &tmW, fb, kb * RBK, 0);
-        if (++s == a.stages) {
-          s = 0;
-          ph ^= 1u;
-        }
+  // ------------------------------------------------------------------ main loop
+  if (warp == 0 && lane == 0) {
+    int s = 0;
+    uint32_t ph = 0, armed = 0, armed_ph = 0;
+    bool aborted = false;
+    // every CTA reads all of W_r: start each at a different k-block so that they do not all ask
+    // the same L2 lines for the same tile at the same moment
+    const int kb0 = (int)(blockIdx.x % (unsigned)kblocks);
+    for (int i = 0; i < kblocks; ++i) {
+      const int kb = kb0 + i < kblocks ? kb0 + i : kb0 + i - kblocks;
+      if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.status)) {
+        aborted = true;
+        break;
       }
-      if (aborted) {
-        for (int i = 0; i < a.stages; ++i)
-          if ((armed >> i) & 1u) drain(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
+      const uint32_t fb = smem_u32(&ctl->full[s]);
+      mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+      armed |= 1u << s;
+      armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+      uint8_t* sa = smem + (size_t)s * stage_bytes;
+      tma_load_2d(smem_u32(sa), &tmX, fb, kb * RBK, t0);
+      tma_load_2d(smem_u32(sa + A_TILE), &tmW, fb, kb * RBK, 0);
+      if (++s == a.stages) {
+        s = 0;
+        ph ^= 1u;
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(RM, a.npad);
-      int s = 0;
-      uint32_t ph = 0;
-      for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, a.status)) break;
-        tc_fence_after();
-        const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-        const uint32_t sb = sa + A_TILE;
+    if (aborted) {
+      for (int i = 0; i < a.stages; ++i)
+        if ((armed >> i) & 1u) drain(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = umma_idesc_bf16(RM, a.npad);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int kb = 0; kb < kblocks; ++kb) {
+      if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, a.status)) break;
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
+      const uint32_t sb = sa + A_TILE;
 #pragma unroll
-        for (int kk = 0; kk < RBK / 16; ++kk)
-          umma_bf16(tmem_base, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc, (kb | kk) != 0);
-        umma_commit(smem_u32(&ctl->empty[s]));
-        if (++s == a.stages) {
-          s = 0;
-          ph ^= 1u;
+      for (int kk = 0; kk < RBK / 16; ++kk)
+        umma_bf16(tmem_base, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc, (kb | kk) != 0);
+      umma_commit(smem_u32(&ctl->empty[s]));
+      if (++s == a.stages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    umma_commit(smem_u32(&ctl->mma_done));
+    drain(smem_u32(&ctl->mma_done), 0);  // every MMA has completed: the logits are in TMEM
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const EpiScratch S = epi_scratch(smem, E);  // the pipeline buffers are free from here on
+  const int ZP = E + 1;                       // padded row pitch: conflict-free column accesses
+
+  // ------------------------------------------------------------------ A: TMEM -> shared memory
+  {
+    const int q = warp & 3, r = q * 32 + lane;
+    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+    bool bad = false;
+    for (int c0 = (warp >> 2) * 32; c0 < E; c0 += 64) {
+      uint32_t v[32];
+      tmem_ld32(trow + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if (c0 + i < E) {
+          float z = __fadd_rn(__uint_as_float(v[i]), ctl->bias[c0 + i]);
+          if (!isfinite(z)) {
+            bad = true;
+            z = kBadLogit;
+          }
+          S.Z[r * ZP + c0 + i] = z;
         }
       }
-      umma_commit(smem_u32(&ctl->mma_done));
-      drain(smem_u32(&ctl->mma_done), 0);
     }
-  } else if (warp >= 4) {
-    const int q = warp - 4;
-    const int r = q * 32 + lane;          // row of the tile = TMEM lane
-    const int t = t0 + r;
-    const bool valid = t < a.T;
-    int ok = 1;
-    if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->mma_done), 0, abort_flag, a.status) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    tc_fence_after();
-    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
-    const int nl = min(k + 1, E);         // list entries in use
+    if (bad) atomicOr(&ctl->flags[r], F_BAD);
+  }
+  tc_fence_before();
+  __syncthreads();
 
-    // ---- pass 1: top-(k+1) by logit
+  // ------------------------------------------------------------------ B: top-(k+1) per token
+  // Thread per (token, expert half): a sorted insertion list over the half's experts in increasing
+  // index (measured faster here than warp-cooperative argmax rounds, whose shuffle round trips
+  // dominate), then the lower half's thread merges the upper half's list into its own.
+  const int nl = min(k + 1, E);
+  const int ehalf = (E + 1) >> 1;
+  {
+    const int h = tid >> 7, r = tid & (RM - 1);
     float lv[KL];
     int le[KL];
 #pragma unroll
@@ -286,28 +332,33 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       lv[j] = -FLT_MAX;
       le[j] = 0x7fffffff;
     }
-    bool bad = false;
-    if (ok) {
-      for (int c0 = 0; c0 < E; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(trow + c0, v);
-        tmem_wait_ld();
+    const int e_hi = h ? E : ehalf;
+    for (int e = h ? ehalf : 0; e < e_hi; ++e) list_insert(lv, le, nl, S.Z[r * ZP + e], e);
+    float* tv = S.tlv + (size_t)(h * RM + r) * KLMAX;
+    int* te = S.tle + (size_t)(h * RM + r) * KLMAX;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = c0 + i;
-          if (e < E) {
-            float z = __fadd_rn(__uint_as_float(v[i]), ctl->bias[e]);
-            if (!isfinite(z)) {
-              bad = true;
-              z = kBadLogit;
-            }
-            list_insert(lv, le, nl, z, e);
-          }
-        }
-      }
+    for (int j = 0; j < KL; ++j) {
+      tv[j] = lv[j];
+      te[j] = le[j];
     }
+  }
+  __syncthreads();
+  if (tid < RM) {
+    const int r = tid;
+    float lv[KL];
+    int le[KL];
+#pragma unroll
+    for (int j = 0; j < KL; ++j) {
+      lv[j] = S.tlv[r * KLMAX + j];
+      le[j] = S.tle[r * KLMAX + j];
+    }
+    // the upper half's experts all have higher indices: insert them in their list order
+#pragma unroll
+    for (int j = 0; j < KL; ++j)
+      if (j < nl && S.tle[(RM + r) * KLMAX + j] != 0x7fffffff)
+        list_insert(lv, le, nl, S.tlv[(RM + r) * KLMAX + j], S.tle[(RM + r) * KLMAX + j]);
     const float m = lv[0];
-    float last = lv[0];  // smallest list entry in use (the list is sorted)
+    float last = lv[0];
 #pragma unroll
     for (int j = 1; j < KL; ++j)
       if (j < nl) last = fminf(last, lv[j]);
@@ -316,179 +367,229 @@ __global__ void __launch_bounds__(RTHREADS, 1)
 #pragma unroll
     for (int j = 0; j + 1 < KL; ++j)
       if (j + 1 < nl && lv[j] - lv[j + 1] < band) flagged = true;
-    flagged = flagged && valid && ok && !bad;
-
-    // ---- pass 2: softmax denominator; near-tie candidates of flagged tokens
-    const float thr = last - band;
-    float s = 0.f;
+    flagged = flagged && (t0 + r < a.T) && !(ctl->flags[r] & F_BAD);
     int nc = 0;
-    if (ok) {
-      for (int c0 = 0; c0 < E; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(trow + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = c0 + i;
-          if (e < E) {
-            float z = __fadd_rn(__uint_as_float(v[i]), ctl->bias[e]);
-            if (!isfinite(z)) z = kBadLogit;
-            s += __expf(z - m);
-            if (flagged && z >= thr) {
-              if (nc < CMAX) ctl->cand[r][nc] = (uint8_t)e;
-              ++nc;
-            }
-          }
+    if (flagged) {  // near-tie candidates: every expert within the band of the (k+1)-th logit
+      const float thr = last - band;
+      for (int e = 0; e < E; ++e) {
+        if (S.Z[r * ZP + e] >= thr) {
+          if (nc < CMAX) S.cand[r * CMAX + nc] = (uint8_t)e;
+          ++nc;
         }
       }
+      if (nc <= CMAX) {
+        const int p0 = atomicAdd(&ctl->npairs, nc);
+        for (int c = 0; c < nc; ++c) S.pairs[p0 + c] = (uint16_t)((r << 4) | c);
+        ctl->flags[r] |= F_FEW;
+      } else {
+        ctl->flags[r] |= F_ALL;
+      }
     }
+    ctl->ncand[r] = nc;
+    ctl->mx[r] = m;
+#pragma unroll
+    for (int j = 0; j < KL; ++j) {
+      S.tlv[r * KLMAX + j] = lv[j];
+      S.tle[r * KLMAX + j] = le[j];
+    }
+  }
+  __syncthreads();
+  {  // softmax denominators, per expert half; Z becomes exp(z - max)
+    const int h = tid >> 7, r = tid & (RM - 1);
+    const float m = ctl->mx[r];
+    float s0 = 0.f, s1 = 0.f;
+    const int e_lo = h ? ehalf : 0, e_hi = h ? E : ehalf;
+    int e = e_lo;
+    for (; e + 1 < e_hi; e += 2) {
+      const float p0 = __expf(S.Z[r * ZP + e] - m), p1 = __expf(S.Z[r * ZP + e + 1] - m);
+      S.Z[r * ZP + e] = p0;
+      S.Z[r * ZP + e + 1] = p1;
+      s0 += p0;
+      s1 += p1;
+    }
+    if (e < e_hi) {
+      const float p0 = __expf(S.Z[r * ZP + e] - m);
+      S.Z[r * ZP + e] = p0;
+      s0 += p0;
+    }
+    ctl->spart[h][r] = s0 + s1;
+  }
+  __syncthreads();
+  if (tid < RM) {
+    const int r = tid;
+    const float s = ctl->spart[0][r] + ctl->spart[1][r];
+    const bool valid = t0 + r < a.T;
+    ctl->sinv[r] = valid ? 1.f / s : 0.f;
+    ctl->lse[r] = valid ? ctl->mx[r] + __logf(s) : 0.f;
+  }
 
-    // ---- exact re-decision of flagged tokens.  The (token, candidate) pairs of the CTA are shared
-    // out over the 4 epilogue warps (one warp per dot product); a token with more than CMAX
-    // candidates (degenerate inputs, e.g. a row of zeros) is re-decided over all experts by its own
-    // warp.
-    const bool few = flagged && nc <= CMAX;
-    if (few) {
-      const int p0 = atomicAdd(&ctl->npairs, nc);
-      for (int c = 0; c < nc; ++c) ctl->pairs[p0 + c] = (uint16_t)((r << 4) | c);
-    }
-    epi_bar();
+  // ------------------------------------------------------------------ C: exact re-decision of near ties
+  {
     const int np = ctl->npairs;
-    for (int pi = q; pi < np; pi += 4) {
-      const int pr = ctl->pairs[pi] >> 4, pc = ctl->pairs[pi] & 15;
-      const int e = ctl->cand[pr][pc];
+    for (int pi = warp; pi < np; pi += RWARPS) {
+      const int pr = S.pairs[pi] >> 4, pc = S.pairs[pi] & 15;
+      const int e = S.cand[pr * CMAX + pc];
       float z = exact_dot(a.x + (size_t)(t0 + pr) * a.d, a.wr + (size_t)e * a.d, a.d, lane);
       z = __fadd_rn(z, ctl->bias[e]);
-      if (lane == 0) ctl->cexact[pr][pc] = isfinite(z) ? z : kBadLogit;
+      if (lane == 0) S.cexact[pr * CMAX + pc] = isfinite(z) ? z : kBadLogit;
     }
-    epi_bar();
-    if (few) {
+    // tokens with more candidates than CMAX (degenerate inputs, e.g. a row of zeros): all experts
+    for (int r = warp; r < RM; r += RWARPS) {
+      if (!(ctl->flags[r] & F_ALL)) continue;
+      float lv[KL];
+      int le[KL];
 #pragma unroll
       for (int j = 0; j < KL; ++j) {
         lv[j] = -FLT_MAX;
         le[j] = 0x7fffffff;
       }
-      for (int c = 0; c < nc; ++c) list_insert(lv, le, nl, ctl->cexact[r][c], (int)ctl->cand[r][c]);
-    }
-    unsigned fl = __ballot_sync(0xffffffffu, flagged && !few);
-    while (fl) {
-      const int f = __ffs(fl) - 1;
-      fl &= fl - 1;
-      const int tf = t0 + q * 32 + f;
-      if (lane == f) {
-#pragma unroll
-        for (int j = 0; j < KL; ++j) {
-          lv[j] = -FLT_MAX;
-          le[j] = 0x7fffffff;
-        }
-      }
       for (int e = 0; e < E; ++e) {
-        float z = exact_dot(a.x + (size_t)tf * a.d, a.wr + (size_t)e * a.d, a.d, lane);
+        float z = exact_dot(a.x + (size_t)(t0 + r) * a.d, a.wr + (size_t)e * a.d, a.d, lane);
         z = __fadd_rn(z, ctl->bias[e]);
         if (!isfinite(z)) z = kBadLogit;
-        if (lane == f) list_insert(lv, le, nl, z, e);
+        list_insert(lv, le, nl, z, e);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < KL; ++j) {
+          S.tlv[r * KLMAX + j] = lv[j];
+          S.tle[r * KLMAX + j] = le[j];
+        }
       }
     }
+  }
+  __syncthreads();
 
-    // ---- outputs of the token: indices, renormalised weights, histogram
-    const float inv_s = 1.f / s;
-    float lse = 0.f;
-    if (valid && ok) {
-      float wsum = 0.f;
-      float p[KL];
+  // ------------------------------------------------------------------ D: outputs and per-CTA partials
+  if (tid < RM) {
+    const int r = tid, t = t0 + r;
+    const int fl = ctl->flags[r];
+    float lv[KL];
+    int le[KL];
+#pragma unroll
+    for (int j = 0; j < KL; ++j) {
+      lv[j] = S.tlv[r * KLMAX + j];
+      le[j] = S.tle[r * KLMAX + j];
+    }
+    if (fl & F_FEW) {
 #pragma unroll
       for (int j = 0; j < KL; ++j) {
-        p[j] = (j < k) ? __expf(lv[j] - lv[0]) : 0.f;
-        wsum += p[j];
+        lv[j] = -FLT_MAX;
+        le[j] = 0x7fffffff;
       }
+      const int nc = ctl->ncand[r];
+      for (int c = 0; c < nc; ++c) list_insert(lv, le, nl, S.cexact[r * CMAX + c], (int)S.cand[r * CMAX + c]);
+    }
+    float l2 = 0.f;
+    if (t < a.T) {
+      float wsum = 0.f;
+#pragma unroll
+      for (int j = 0; j < KL; ++j) wsum += (j < k) ? __expf(lv[j] - lv[0]) : 0.f;
       const float inv_w = 1.f / wsum;
 #pragma unroll
       for (int j = 0; j < KL; ++j) {
         if (j < k) {
           a.topk_idx[(size_t)t * k + j] = le[j];
-          a.topk_w[(size_t)t * k + j] = p[j] * inv_w;
+          a.topk_w[(size_t)t * k + j] = __expf(lv[j] - lv[0]) * inv_w;
           atomicAdd(&ctl->hist[le[j]], 1);
         }
       }
-      lse = m + __logf(s);
-      if (bad) atomicOr(a.status, DEV_NONFINITE);
+      if (fl & F_BAD) atomicOr(a.status, DEV_NONFINITE);
+      l2 = ctl->lse[r] * ctl->lse[r];
     }
-
-    // ---- pass 3: P = exp(z - m) / s, summed over the CTA's tokens per expert
-    if (ok) {
-      for (int c0 = 0; c0 < E; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(trow + c0, v);
-        tmem_wait_ld();
-        float pv[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float z = __fadd_rn(__uint_as_float(v[i]), ctl->bias[min(c0 + i, 255)]);
-          if (!isfinite(z)) z = kBadLogit;
-          pv[i] = (valid && c0 + i < E) ? __expf(z - m) * inv_s : 0.f;
-        }
-        const float colsum = warp_transpose_sum(pv, lane);
-        if (c0 + lane < E) ctl->red[q][c0 + lane] = colsum;
-      }
-    }
-    float l2 = valid ? lse * lse : 0.f;
 #pragma unroll
     for (int o = 16; o; o >>= 1) l2 += __shfl_xor_sync(0xffffffffu, l2, o);
-    if (lane == 0) ctl->lse2[q] = l2;
-    epi_bar();
-
-    // ---- per-CTA partials, then the last CTA reduces all of them
-    const int te = threadIdx.x - 128;
-    for (int e = te; e < E; e += 128) {
-      a.psum[(size_t)blockIdx.x * E + e] = ((ctl->red[0][e] + ctl->red[1][e]) + ctl->red[2][e]) + ctl->red[3][e];
-      a.hist[(size_t)blockIdx.x * E + e] = ctl->hist[e];
+    if (lane == 0) ctl->lse2w[warp] = l2;
+  }
+  // per-expert sums of P = exp(z - max) / denominator over the CTA's tokens: row slices, then the
+  // slices in order
+  int parts = 1;  // a power of two (so it divides RM), with parts * E <= RTHREADS
+  while (parts < PPARTS && 2 * parts * E <= RTHREADS) parts <<= 1;
+  {
+    const int e = tid % E, part = tid / E;
+    if (part < parts) {
+      const int rows = RM / parts;
+      float ps = 0.f;
+      for (int r = part * rows; r < (part + 1) * rows; ++r) ps = fmaf(S.Z[r * ZP + e], ctl->sinv[r], ps);
+      S.ppart[part * 256 + e] = ps;
     }
-    if (te == 0) a.lse2[blockIdx.x] = ((ctl->lse2[0] + ctl->lse2[1]) + ctl->lse2[2]) + ctl->lse2[3];
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += RTHREADS) {
+    float ps = 0.f;
+    for (int part = 0; part < parts; ++part) ps += S.ppart[part * 256 + e];
+    a.psum[(size_t)blockIdx.x * E + e] = ps;
+    a.hist[(size_t)blockIdx.x * E + e] = ctl->hist[e];
+  }
+  if (tid == 0) a.lse2[blockIdx.x] = ((ctl->lse2w[0] + ctl->lse2w[1]) + ctl->lse2w[2]) + ctl->lse2w[3];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) ctl->is_last = (atomicAdd(a.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+
+  // ------------------------------------------------------------------ last CTA: counts and losses
+  if (ctl->is_last) {
     __threadfence();
-    epi_bar();
-    if (te == 0) ctl->is_last = (atomicAdd(a.done, 1u) == gridDim.x - 1) ? 1 : 0;
-    epi_bar();
-    if (ctl->is_last) {
-      __threadfence();
-      const int nb = gridDim.x;
-      // one thread per expert; partials are loaded 16 at a time (independent loads in flight) and
-      // summed in block order, so the result does not depend on which CTA finished last
-      constexpr int U = 16;
-      for (int e = te; e < E; e += 128) {
+    const int nb = gridDim.x;
+    // block slices per expert (fixed boundaries), fp32 sums in block order, slices in order
+    {
+      const int e = tid % E, part = tid / E;
+      if (part < parts) {
+        const int b_lo = (int)((long)nb * part / parts), b_hi = (int)((long)nb * (part + 1) / parts);
         int cnt = 0;
-        double ps = 0.0;
-        for (int b0 = 0; b0 < nb; b0 += U) {
+        float ps = 0.f;
+        constexpr int U = 8;
+        for (int b0 = b_lo; b0 < b_hi; b0 += U) {
           int hv[U];
           float pv[U];
 #pragma unroll
           for (int u = 0; u < U; ++u) {
-            const bool in = b0 + u < nb;
+            const bool in = b0 + u < b_hi;
             hv[u] = in ? __ldcg(a.hist + (size_t)(b0 + u) * E + e) : 0;
             pv[u] = in ? __ldcg(a.psum + (size_t)(b0 + u) * E + e) : 0.f;
           }
 #pragma unroll
           for (int u = 0; u < U; ++u) {
             cnt += hv[u];
-            ps += (double)pv[u];
+            ps += pv[u];
           }
         }
-        a.counts[e] = cnt;
-        ctl->lbterm[e] = (double)cnt * ps;
+        S.ppart[part * 256 + e] = ps;
+        S.hpart[part * 256 + e] = cnt;
       }
-      double l = 0.0;
-      if (te < 32) {
-        for (int b = te; b < nb; b += 32) l += (double)__ldcg(a.lse2 + b);
+    }
+    float l = 0.f;
+    if (warp == 1) {
+      for (int b = lane; b < nb; b += 32) l += __ldcg(a.lse2 + b);
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += RTHREADS) {
+      int cnt = 0;
+      float ps = 0.f;
+      for (int part = 0; part < parts; ++part) {
+        cnt += S.hpart[part * 256 + e];
+        ps += S.ppart[part * 256 + e];
+      }
+      a.counts[e] = cnt;
+      ctl->lbterm[e] = (double)cnt * (double)ps;
+    }
+    if (warp == 1) {
+      double dl = (double)l;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      }
-      epi_bar();
-      if (te == 0) {
-        double lb = 0.0;
-        for (int e = 0; e < E; ++e) lb += ctl->lbterm[e];
+      for (int o = 16; o; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+      if (lane == 0) ctl->red[1] = dl;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      double lb = 0.0;
+      for (int e = lane; e < E; e += 32) lb += ctl->lbterm[e];
+#pragma unroll
+      for (int o = 16; o; o >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+      if (lane == 0) {
         const double Tn = (double)a.T;
         // lb = alpha E sum_e (c_e / (T k)) (psum_e / T);  zl = beta mean_t lse_t^2
         a.losses[0] = (float)((double)a.lb_coef * E * lb / (Tn * k * Tn));
-        a.losses[1] = (float)((double)a.z_coef * l / Tn);
+        a.losses[1] = (float)((double)a.z_coef * ctl->red[1] / Tn);
         *a.done = 0;  // ready for the next call
       }
     }
@@ -541,6 +642,7 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   const int stage_bytes = A_TILE + npad * RBK * 2;
   int stages = SMEM_STAGES_BYTES / stage_bytes;
   if (stages > MAX_STAGES) stages = MAX_STAGES;
+  if ((size_t)stages * stage_bytes < epi_scratch_bytes(E)) return cudaErrorInvalidValue;  // never for E <= 256
   const size_t smem = (size_t)stages * stage_bytes + sizeof(RouteCtl) + 1024;
   RouteArgs a;
   a.x = static_cast<const __nv_bfloat16*>(x);
