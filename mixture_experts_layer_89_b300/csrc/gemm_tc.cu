@@ -18,10 +18,14 @@
 //               the host)
 //   warps 4..   EPIW epilogue warps: tcgen05.ld (thread = row), bias/activation, stores.  Warp w
 //               reaches TMEM lanes 32 (w % 4)..; with 8 warps, w and w + 4 split the columns.
-// Paired mode (PAIR): CTAs run in clusters of two that take the two 128-row halves of a 256-row
-// tile of one expert with the same weight tile.  Each CTA loads half of that B tile and multicasts
-// it to both, so B crosses L2 once per 256 rows; each CTA's MMA signals the stage free in both
-// CTAs.  Tiles are enumerated m-tile-major with n fastest (measured faster than n-major here).
+// Paired mode (PAIR): 2-SM MMAs.  CTAs run in clusters of two that take the two 128-row halves of a
+// 256-row tile of one expert; each holds its own 128 A rows and half of the 256 B rows in shared
+// memory (32 KB per stage instead of 48, so 6 stages), and the even CTA issues
+// tcgen05.mma.cta_group::2 (M=256) that reads both CTAs' operands and writes both CTAs' TMEM.
+// Both CTAs' loads signal the leader's stage barriers; the leader's commits signal both CTAs'
+// "stage free" and "accumulator full" barriers; both epilogues signal the leader's "accumulator
+// free" barrier.  Per SM, operand traffic drops by a third for the same FLOPs.  Tiles are
+// enumerated m-tile-major with n fastest (measured faster than n-major here).
 #include <stdio.h>
 
 #include <mutex>
@@ -34,14 +38,19 @@ namespace moe {
 namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int BNB = 256;  // B rows per stage (accumulator columns)
+constexpr int BNB = 256;  // B rows per tile (accumulator columns)
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BNB * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MAX_STAGES = 6;
+// single CTA: A + the whole B tile per stage, 4 stages; pair: A + half of B per CTA, 6 stages
+constexpr int stages_of(bool pair) { return pair ? 6 : 4; }
+constexpr int stage_bytes_of(bool pair) { return A_BYTES + (pair ? B_BYTES / 2 : B_BYTES); }
+constexpr int STAGE_REGION = 4 * (A_BYTES + B_BYTES);
+static_assert(6 * (A_BYTES + B_BYTES / 2) == STAGE_REGION, "both stage layouts fill the same region");
 constexpr int MAXG = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = umma_idesc_bf16(BM, BNB);
+constexpr uint32_t IDESC_PAIR = umma_idesc_bf16(2 * BM, BNB);  // 2-SM MMA: M = 256 across the pair
 constexpr uint16_t PAIR_MASK = 0x3;
 
 struct TcArgs {
@@ -56,8 +65,8 @@ struct TcArgs {
 };
 
 struct SmemCtl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -67,7 +76,7 @@ struct SmemCtl {
   int u_pre[MAXG + 1];  // prefix over groups of row units (m-tiles, or m-tile pairs in PAIR mode)
 };
 constexpr int STG_BYTES = 32 * 32 * 4;  // fp32-output epilogue: one 32 x 32 staging tile per warp
-constexpr size_t SMEM_BASE = (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl) + 1024;
+constexpr size_t SMEM_BASE = (size_t)STAGE_REGION + sizeof(SmemCtl) + 1024;
 constexpr size_t smem_total(bool outf32, int epiw) { return SMEM_BASE + (outf32 ? (size_t)epiw * STG_BYTES + 1024 : 0); }
 
 // Wait that ignores the abort flag (used to drain in-flight async operations before exit).
@@ -101,9 +110,11 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut, const TcArgs args) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
   constexpr int CW = NOUT / (EPIW / 4);  // output columns per epilogue warp
+  constexpr int STAGES = stages_of(PAIR);
+  constexpr int STAGE_BYTES = stage_bytes_of(PAIR);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)STAGES * STAGE_BYTES);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)STAGE_REGION);
   // fp32 staging tiles (1024-byte aligned for the 128-byte swizzle), one per epilogue warp
   uint8_t* stg_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(ctl) + sizeof(SmemCtl) + 1023) & ~uintptr_t(1023));
@@ -115,15 +126,16 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   const int crank = PAIR ? (int)cluster_ctarank() : 0;
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const bool leader = crank == 0;  // PAIR: the even CTA issues the 2-SM MMAs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), PAIR ? 2 : 1);  // PAIR: both CTAs' MMAs read the stage
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), EPIW);  // one arrive per epilogue warp
+      mbar_init(smem_u32(&ctl->tempty[a]), PAIR ? 2 * EPIW : EPIW);  // one arrive per epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     ctl->abort_flag = 0;
@@ -135,8 +147,13 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
     if (ACT == ACT_SWIGLU) tma_prefetch_desc(&tmB1);
   }
   if (warp == 2) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {  // both CTAs of the pair allocate together and receive the same address
+      tmem_alloc_cg2(smem_u32(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish_cg2();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 3) {
     // unit prefix over groups: lane owns groups [8 lane, 8 lane + 8)
@@ -210,7 +227,6 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);  // A + the whole B tile (both halves in PAIR mode)
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           const int k0 = kb * BK;
@@ -218,19 +234,24 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
           const int kk = k0 % args.K_w;
           uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
-          tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
           if (PAIR) {
-            // half `crank` of the B tile, into both CTAs: SwiGLU gate / up halves, else rows
-            // [128 crank, 128 crank + 128) of the tile
-            const uint32_t dst = smem_u32(sb + crank * (B_BYTES / 2));
+            // this CTA's 128 A rows and its half of the B tile (SwiGLU: the gate or the up half;
+            // else rows [128 crank, 128 crank + 128)), both signalling the leader's stage barrier
+            const uint32_t lb = mapa_rank(fb, 0);
+            if (leader) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
+            tma_load_2d_cg2(smem_u32(sa), &tmA, lb, k0, m0);
             if (ACT == ACT_SWIGLU)
-              tma_load_3d_mc(dst, crank ? &tmB1 : &tmB0, fb, kk, nn, gw, PAIR_MASK);
+              tma_load_3d_cg2(smem_u32(sb), crank ? &tmB1 : &tmB0, lb, kk, nn, gw);
             else
-              tma_load_3d_mc(dst, &tmB0, fb, kk, nn + crank * (BNB / 2), gw, PAIR_MASK);
+              tma_load_3d_cg2(smem_u32(sb), &tmB0, lb, kk, nn + crank * (BNB / 2), gw);
           } else if (ACT == ACT_SWIGLU) {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);  // A + the whole B tile
+            tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
             tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
             tma_load_3d(smem_u32(sb + B_BYTES / 2), &tmB1, fb, kk, nn, gw);
           } else {
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
             tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
           }
           if (++s == STAGES) {
@@ -239,13 +260,13 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
           }
         }
       }
-      if (aborted) {  // let every armed copy land before the CTA leaves
+      if (aborted && leader) {  // let every armed copy (of both CTAs of a pair) land before leaving
         for (int i = 0; i < STAGES; ++i)
           if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool aborted = false;
@@ -265,11 +286,15 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC,
-                      (kb | kk) != 0 ? 1u : 0u);
+            if (PAIR)
+              umma_bf16_cg2(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC_PAIR,
+                            (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC,
+                        (kb | kk) != 0 ? 1u : 0u);
           }
           if (PAIR)
-            umma_commit_mc(smem_u32(&ctl->empty[s]), PAIR_MASK);  // the stage holds the peer's half too
+            umma_commit_cg2_mc(smem_u32(&ctl->empty[s]), PAIR_MASK);  // both CTAs' copies of the stage are free
           else
             umma_commit(smem_u32(&ctl->empty[s]));
           if (++s == STAGES) {
@@ -278,9 +303,15 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
           }
         }
         if (aborted) break;
-        umma_commit(smem_u32(&ctl->tfull[acc]));
+        if (PAIR)
+          umma_commit_cg2_mc(smem_u32(&ctl->tfull[acc]), PAIR_MASK);  // both CTAs' accumulators are full
+        else
+          umma_commit(smem_u32(&ctl->tfull[acc]));
       }
-      umma_commit(smem_u32(&ctl->mma_done));
+      if (PAIR)
+        umma_commit_cg2_mc(smem_u32(&ctl->mma_done), PAIR_MASK);
+      else
+        umma_commit(smem_u32(&ctl->mma_done));
       drain_wait(smem_u32(&ctl->mma_done), 0);
     }
   } else if (warp >= 4) {
@@ -386,7 +417,12 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(mapa_rank(smem_u32(&ctl->tempty[acc]), 0));  // the leader reuses the accumulator
+        else
+          mbar_arrive(smem_u32(&ctl->tempty[acc]));
+      }
     }
     if (OUTF32 && lane == 0) bulk_wait_all();  // tile stores complete before the CTA leaves
     __syncwarp();
@@ -394,11 +430,16 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
 
   tc_fence_before();
   __syncthreads();
+  // PAIR: no signal of the peer can still be in flight towards this CTA, and neither CTA's TMEM is
+  // in use, when the pair frees its TMEM together
+  if (PAIR) cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_cg2(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  if (PAIR) cluster_sync_all();  // no signal from the peer can still be in flight towards this CTA
 }
 
 // ------------------------------------------------------------------------------- host side
