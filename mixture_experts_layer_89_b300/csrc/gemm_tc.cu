@@ -75,9 +75,11 @@ struct SmemCtl {
   int row_lo[MAXG + 1];
   int u_pre[MAXG + 1];  // prefix over groups of row units (m-tiles, or m-tile pairs in PAIR mode)
 };
-constexpr int STG_BYTES = 32 * 32 * 4;  // fp32-output epilogue: one 32 x 32 staging tile per warp
+// Epilogue staging for TMA tile stores: one 32 x 32 tile per warp (fp32 4 KB with the 128-byte
+// swizzle, bf16 2 KB with the 64-byte swizzle).
+constexpr int stg_bytes(bool outf32) { return outf32 ? 32 * 32 * 4 : 32 * 32 * 2; }
 constexpr size_t SMEM_BASE = (size_t)STAGE_REGION + sizeof(SmemCtl) + 1024;
-constexpr size_t smem_total(bool outf32, int epiw) { return SMEM_BASE + (outf32 ? (size_t)epiw * STG_BYTES + 1024 : 0); }
+constexpr size_t smem_total(bool outf32, int epiw) { return SMEM_BASE + (size_t)epiw * stg_bytes(outf32) + 1024; }
 
 // Wait that ignores the abort flag (used to drain in-flight async operations before exit).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -103,6 +105,32 @@ __device__ __forceinline__ float erf_as7126(float x) {
 }
 __device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erf_as7126(u * 0.70710678118654752f)); }
 __device__ __forceinline__ float silu(float u) { return __fdividef(u, 1.f + __expf(-u)); }
+
+// One warp's 32 rows x 32 bf16 columns (16 packed words per lane, lane = row): a TMA tile store
+// through the warp's staging tile when all 32 rows are output rows (64-byte swizzle: 16-byte chunk
+// j of row r sits at chunk j ^ ((r / 2) % 4), conflict-free), else direct row stores.
+__device__ __forceinline__ void store_bf16_chunk(const uint32_t (&pk)[16], bool full_rows, uint8_t* stg,
+                                                 const CUtensorMap* tm, int col, int row0, __nv_bfloat16* dst_row,
+                                                 int lane) {
+  if (full_rows) {
+    if (lane == 0) bulk_wait_read0();  // the previous store has finished reading stg
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+          make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm, smem_u32(stg), col, row0);
+      bulk_commit();
+    }
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  }
+}
 
 template <int ACT, bool OUTF32, int EPIW, bool PAIR>
 __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
@@ -317,7 +345,7 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   } else if (warp >= 4) {
     const int q = warp & 3;                      // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
     const int c_lo = ((warp - 4) >> 2) * CW;     // this warp's share of the output columns
-    uint8_t* stg = stg_base + (size_t)(warp - 4) * STG_BYTES;
+    uint8_t* stg = stg_base + (size_t)(warp - 4) * stg_bytes(OUTF32);
     int it = 0;
     for (int u = unit0; u < total_units; u += ustep, ++it) {
       int g, m0, m_end, n0;
@@ -350,9 +378,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
               const float h1 = silu(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
               pk[i] = pack_bf16x2(h0, h1);
             }
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            store_bf16_chunk(pk, full_rows, stg, &tmOut, n0 + c, m0 + q * 32,
+                             static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
           }
         }
       } else {
@@ -407,10 +434,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
               uint32_t pk[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              store_bf16_chunk(pk, full_rows, stg, &tmOut, n0 + c, m0 + q * 32,
+                               static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
             }
           }
         }
@@ -424,7 +449,7 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
           mbar_arrive(smem_u32(&ctl->tempty[acc]));
       }
     }
-    if (OUTF32 && lane == 0) bulk_wait_all();  // tile stores complete before the CTA leaves
+    if (lane == 0) bulk_wait_all();  // tile stores complete before the CTA leaves
     __syncwarp();
   }
 
@@ -483,7 +508,8 @@ cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
 }
 
 static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int rank, const cuuint64_t* dims,
-                      const cuuint64_t* strides, const cuuint32_t* box) {
+                      const cuuint64_t* strides, const cuuint32_t* box,
+                      CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled unavailable");
@@ -491,7 +517,7 @@ static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, i
   }
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled failed (%d) rank %d dims %llu %llu %llu", (int)r, rank,
@@ -603,12 +629,14 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
       mB1 = mB0;
     }
   }
-  CUtensorMap mO = mA;
-  if (OUTF32) {  // output tile map for the TMA stores of the epilogue: 32 x 32 fp32 boxes
+  CUtensorMap mO;
+  {  // output tile map for the TMA stores of the epilogue: 32 x 32 boxes (fp32: 128-byte rows, bf16: 64-byte)
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)rows_alloc};
-    const cuuint64_t str[1] = {(cuuint64_t)p.ldc * 4};
+    const cuuint64_t str[1] = {(cuuint64_t)p.ldc * (OUTF32 ? 4 : 2)};
     const cuuint32_t box[2] = {32, 32};
-    if (!make_tmap(&mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.out, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!make_tmap(&mO, OUTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2, dims,
+                   str, box, OUTF32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+      return cudaErrorInvalidValue;
   }
   TcArgs a;
   a.offsets = p.offsets;
