@@ -137,14 +137,16 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 #define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
 
 // ------------------------------------------------------------------------------ steps
+// scan != NULL: the tensor-core router may also do the dispatch scan (route_tc_fuses_scan).
 moe_status route_impl(const moe_config* c, const void* x, const void* wr, const float* lbias, int32_t* topk_idx,
-                      float* topk_w, int32_t* counts, float* losses, void* ws, cudaStream_t st) {
+                      float* topk_w, int32_t* counts, float* losses, void* ws, cudaStream_t st,
+                      const RouteScan* scan = nullptr) {
   const WsLayout L = layout(c);
   uint32_t* status = at<uint32_t>(ws, L.status);
   if (is_bf16(c)) {  // tensor-core router; the last CTA reduces the partials (counter: status block word 1)
     return cuda_status(launch_route_tc(x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w,
                                        at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
-                                       status + 1, counts, losses, c->lb_coef, c->z_coef, status, st));
+                                       status + 1, counts, losses, c->lb_coef, c->z_coef, status, st, scan));
   }
   MOE_CUDA(launch_route(false, x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w, at<int32_t>(ws, L.r_hist),
                         at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2), status, st));
@@ -153,20 +155,22 @@ moe_status route_impl(const moe_config* c, const void* x, const void* wr, const 
   return MOE_OK;
 }
 
+// scanned: the router already wrote the rank bases (p_base), kept, offsets and drops.
 moe_status permute_impl(const moe_config* c, const void* x, const int32_t* topk_idx, const int32_t* counts,
                         int32_t* offsets, int32_t* kept, int32_t* row_of, int32_t* tok_of, void* x_perm,
-                        int32_t* drops, void* ws, cudaStream_t st) {
+                        int32_t* drops, void* ws, cudaStream_t st, bool scanned = false) {
   const WsLayout L = layout(c);
   uint32_t* status = at<uint32_t>(ws, L.status);
   const int64_t cap64 = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
   const int cap = cap64 < 0 ? INT_MAX : (int)cap64;
   const int npb = perm_blocks(c->T);
-  MOE_CUDA(launch_perm_hist(topk_idx, c->T, c->E, c->k, at<int32_t>(ws, L.p_hist), status, st));
-  MOE_CUDA(launch_perm_scan(at<int32_t>(ws, L.p_hist), npb, counts, c->E, c->T * c->k, cap,
-                            at<int32_t>(ws, L.p_base), offsets, kept, drops, status, st));
-  MOE_CUDA(launch_perm_rank(topk_idx, at<int32_t>(ws, L.p_base), offsets, c->T, c->E, c->k, cap, row_of, tok_of,
-                            st));
-  MOE_CUDA(launch_gather_rows(is_bf16(c), x, tok_of, offsets + c->E, (int)a_max_of(c), c->d, x_perm, st));
+  if (!scanned) {
+    MOE_CUDA(launch_perm_hist(topk_idx, c->T, c->E, c->k, at<int32_t>(ws, L.p_hist), status, st));
+    MOE_CUDA(launch_perm_scan(at<int32_t>(ws, L.p_hist), npb, counts, c->E, c->T * c->k, cap,
+                              at<int32_t>(ws, L.p_base), offsets, kept, drops, status, st));
+  }
+  MOE_CUDA(launch_dispatch(is_bf16(c), topk_idx, at<int32_t>(ws, L.p_base), offsets, c->T, c->E, c->k, cap, x, c->d,
+                           row_of, tok_of, x_perm, (int)a_max_of(c), status, st));
   return MOE_OK;
 }
 
@@ -267,11 +271,20 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
   void* y_sh = c->n_shared > 0 ? at<char>(ws, L.y_sh) : nullptr;
   auto rec = [&](int i) -> moe_status { return ev ? cuda_status(cudaEventRecord(ev[i], st)) : MOE_OK; };
 
+  // bf16 layers: the router's last CTA also does the dispatch scan over its per-block histograms
+  const int64_t cap64 = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
+  RouteScan scan;
+  scan.cap = cap64 < 0 ? INT_MAX : (int)cap64;
+  scan.pbase = at<int32_t>(ws, L.p_base);
+  scan.kept = at<int32_t>(ws, L.kept);
+  scan.offsets = offsets;
+  scan.drops = drops;
+  const bool scanned = is_bf16(c) && route_tc_fuses_scan(c->T, c->E);
   MOE_TRY(rec(0));
-  MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st));
+  MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st, &scan));
   MOE_TRY(rec(1));
   MOE_TRY(permute_impl(c, x, topk_idx, counts, offsets, at<int32_t>(ws, L.kept), row_of, at<int32_t>(ws, L.tok_of),
-                       x_perm, drops, ws, st));
+                       x_perm, drops, ws, st, scanned));
   MOE_TRY(rec(2));
   MOE_TRY(ffn_routed_impl(c, x_perm, offsets, w, y_perm, ws, st, ev ? ev[3] : nullptr));
   MOE_TRY(rec(4));
@@ -429,7 +442,9 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   const bool tokens = cfg->T > 0;
   if (is_bf16(cfg)) n += tokens ? 1 : 0;      // tensor-core router (finalize fused; T = 0: memsets only)
   else n += tokens ? 2 : 1;                   // router + finalize
-  n += tokens ? 4 : 1;                        // histogram, scan, rank, gather
+  const bool scanned = is_bf16(cfg) && route_tc_fuses_scan(cfg->T, cfg->E);
+  if (!tokens) n += 1;                        // scan (writes zero offsets)
+  else n += (scanned ? 0 : 2) + dispatch_launches(true, cfg->d, is_bf16(cfg) ? 2 : 4);  // [hist, scan,] dispatch
   if (a_max_of(cfg) > 0) n += 2;              // routed up + down projections
   if (cfg->n_shared > 0 && tokens) n += 2;    // shared up + down projections
   if (tokens) n += 1;                         // combine

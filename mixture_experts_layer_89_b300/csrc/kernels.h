@@ -19,28 +19,40 @@ cudaError_t launch_route(bool bf16, const void* x, const void* wr, const float* 
 // Tensor-core router of bf16 layers (one launch, 128 tokens per CTA): writes top-k, and through
 // the last CTA to finish, counts [E] and losses [2].  hist/psum/lse2 hold route_tc_blocks(T) rows
 // of partials; *done must be zero before the launch and is zero again after it.
+// With `scan`, and when route_tc_fuses_scan(T, E), the last CTA also does the dispatch scan over
+// the router's per-block histograms (blocks of kPermTokens tokens).
+struct RouteScan {
+  int cap;          // expert capacity (INT_MAX when dropless)
+  int32_t* pbase;   // [nb][E] exclusive prefix of each expert's histogram over blocks
+  int32_t* kept;    // [E]
+  int32_t* offsets; // [E+1]
+  int32_t* drops;   // [1]
+};
 int route_tc_blocks(int T);
+bool route_tc_fuses_scan(int T, int E);
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
-                            cudaStream_t st);
+                            cudaStream_t st, const RouteScan* scan);
 // Reduces the per-CTA partials: counts [E] and losses [2].
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,
                                   int k, float lb_coef, float z_coef, int32_t* counts, float* losses,
                                   cudaStream_t st);
 
 // ---------------------------------------------------------------- dispatch (permute.cu)
-constexpr int kPermTokens = 64;  // tokens per dispatch CTA
+constexpr int kPermTokens = 128;  // tokens per dispatch block (= the tensor-core router's block)
 int perm_blocks(int T);
 cudaError_t launch_perm_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* phist, uint32_t* status,
                              cudaStream_t st);
 cudaError_t launch_perm_scan(const int32_t* phist, int npb, const int32_t* counts, int E, int Tk, int cap,
                              int32_t* pbase, int32_t* offsets, int32_t* kept, int32_t* drops, uint32_t* status,
                              cudaStream_t st);
-cudaError_t launch_perm_rank(const int32_t* topk_idx, const int32_t* pbase, const int32_t* offsets, int T, int E,
-                             int k, int cap, int32_t* row_of, int32_t* tok_of, cudaStream_t st);
-cudaError_t launch_gather_rows(bool bf16, const void* x, const int32_t* tok_of, const int32_t* n_rows_dev,
-                               int max_rows, int d, void* x_perm, cudaStream_t st);
+// Ranks and row_of / tok_of (one CTA per block), then (x_perm != NULL) the row copy x -> x_perm.
+cudaError_t launch_dispatch(bool bf16, const int32_t* topk_idx, const int32_t* pbase, const int32_t* offsets, int T,
+                            int E, int k, int cap, const void* x, int d, int32_t* row_of, int32_t* tok_of,
+                            void* x_perm, int max_rows, uint32_t* status, cudaStream_t st);
+// Kernels launch_dispatch launches (2 with the row copy, else 1).
+int dispatch_launches(bool with_rows, int d, int elt_bytes);
 
 // ---------------------------------------------------------------- combine (combine.cu)
 // y_perm [rows, d] and y_shared [T, d] are fp32; y is bf16 or fp32.

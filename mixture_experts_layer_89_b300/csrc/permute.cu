@@ -5,11 +5,13 @@
 // the Naive-N0.5-Flash article, sec. 4.2; the flatten-and-reorder formulation and the capacity
 // C = cf * tokens / E with overflow dropped are the OpenMythos article, sec. 3.1.
 //
-// Deterministic, atomics-free ordering: (1) each CTA of 64 tokens histograms its assignments per
-// expert; (2) one CTA scans the histograms per expert over CTAs (the rank base of every CTA),
-// applies the capacity and scans the kept counts over experts (offsets); (3) each CTA walks its
-// assignments in token order with one warp, ranking equal experts inside a 32-wide chunk with
-// __match_any_sync, and writes row_of / tok_of; (4) a row-parallel copy gathers x into x_perm.
+// Deterministic, atomics-free ordering over blocks of 128 tokens: (1) a per-block histogram of the
+// assignments per expert (for bf16 layers the router already writes it); (2) an exclusive scan of
+// each expert's histogram over blocks gives every block its rank base, the capacity gives the kept
+// counts and a scan over experts the offsets (for bf16 layers the router's last CTA does this);
+// (3) one kernel per block ranks its assignments in token order (one warp, equal experts inside a
+// 32-wide chunk ranked with __match_any_sync) and writes row_of / tok_of; (4) a row-parallel copy
+// gathers x into x_perm.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -38,7 +40,8 @@ __global__ void __launch_bounds__(256) k_perm_hist(const int32_t* __restrict__ t
   for (int e = tid; e < E; e += 256) phist[(size_t)blockIdx.x * E + e] = h[e];
 }
 
-// One CTA: per-expert scan over the dispatch CTAs, capacity, exclusive scan over experts.
+// One CTA: per-expert exclusive scan over the blocks (16 loads in flight per thread), capacity,
+// exclusive scan over experts.
 __global__ void __launch_bounds__(256) k_perm_scan(const int32_t* __restrict__ phist, int npb,
                                                    const int32_t* __restrict__ counts, int E, int Tk, int cap,
                                                    int32_t* __restrict__ pbase, int32_t* __restrict__ offsets,
@@ -48,10 +51,17 @@ __global__ void __launch_bounds__(256) k_perm_scan(const int32_t* __restrict__ p
   const int tid = threadIdx.x;
   int kp = 0;
   if (tid < E) {
+    constexpr int U = 16;
     int run = 0;
-    for (int b = 0; b < npb; ++b) {
-      pbase[(size_t)b * E + tid] = run;
-      run += phist[(size_t)b * E + tid];
+    for (int b0 = 0; b0 < npb; b0 += U) {
+      int hv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) hv[u] = b0 + u < npb ? phist[(size_t)(b0 + u) * E + tid] : 0;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (b0 + u < npb) pbase[(size_t)(b0 + u) * E + tid] = run;
+        run += hv[u];
+      }
     }
     if (counts && counts[tid] != run) atomicOr(status, DEV_BADCOUNTS);
     kp = min(run, cap);
@@ -73,40 +83,57 @@ __global__ void __launch_bounds__(256) k_perm_scan(const int32_t* __restrict__ p
   }
 }
 
-// Ranks of each CTA's assignments in token order -> row_of, tok_of.
-__global__ void __launch_bounds__(32) k_perm_rank(const int32_t* __restrict__ topk_idx,
+// One CTA per block of PT tokens: the block's assignments ranked in token order (warp 0; equal
+// experts inside a 32-wide chunk ranked with __match_any_sync), then row_of / tok_of.
+template <int KMAX>
+__global__ void __launch_bounds__(256) k_dispatch(const int32_t* __restrict__ topk_idx,
                                                   const int32_t* __restrict__ pbase,
                                                   const int32_t* __restrict__ offsets, int Tn, int E, int k, int cap,
-                                                  int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of) {
+                                                  int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
+                                                  uint32_t* status) {
   __shared__ int run[256];
-  const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) run[e] = pbase[(size_t)blockIdx.x * E + e];
-  __syncwarp();
-  const long a0 = (long)blockIdx.x * PT * k;
-  const long a1 = min(a0 + (long)PT * k, (long)Tn * k);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (long c0 = a0; c0 < a1; c0 += 32) {
-    const long a = c0 + lane;
-    const bool valid = a < a1;
-    int e = valid ? topk_idx[a] : -1;
-    if (e < 0 || e >= E) e = -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    int row = -1;
-    if (e >= 0) {
-      const int r = run[e] + __popc(peers & lt_mask);
-      if (r < cap) row = offsets[e] + r;
+  __shared__ int eidx[PT * KMAX];
+  __shared__ int rows[PT * KMAX];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * PT;
+  const int nt = min(PT, Tn - t0), na = nt * k;
+  for (int e = tid; e < E; e += 256) run[e] = pbase[(size_t)blockIdx.x * E + e];
+  for (int i = tid; i < na; i += 256) {
+    int e = topk_idx[(size_t)t0 * k + i];
+    if (e < 0 || e >= E) {
+      atomicOr(status, DEV_BADINDEX);
+      e = -1;
     }
-    __syncwarp();
-    if (e >= 0 && (__ffs(peers) - 1) == lane) run[e] += __popc(peers);
-    __syncwarp();
-    if (valid) {
-      row_of[a] = row;
-      if (row >= 0) tok_of[row] = (int)(a / k);
+    eidx[i] = e;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int c0 = 0; c0 < na; c0 += 32) {
+      const int a = c0 + lane;
+      const int e = a < na ? eidx[a] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int row = -1;
+      if (e >= 0) {
+        const int r = run[e] + __popc(peers & lt_mask);
+        if (r < cap) row = offsets[e] + r;
+      }
+      __syncwarp();
+      if (e >= 0 && (__ffs(peers) - 1) == lane) run[e] += __popc(peers);
+      __syncwarp();
+      if (a < na) rows[a] = row;
     }
+  }
+  __syncthreads();
+  for (int i = tid; i < na; i += 256) {
+    const int row = rows[i];
+    row_of[(size_t)t0 * k + i] = row;
+    if (row >= 0) tok_of[row] = t0 + i / k;
   }
 }
 
-// x_perm[r] = x[tok_of[r]] for r < n_rows (device count); one warp per row, 16-byte vectors.
+// x_perm[r] = x[tok_of[r]] for r < n_rows (device count); one warp per row, 16-byte vectors, a
+// grid far larger than the SM count so that many loads are in flight.
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ tok_of,
                                                      const int32_t* __restrict__ n_rows_dev, int max_rows,
                                                      int row_vecs, uint4* __restrict__ x_perm) {
@@ -120,7 +147,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x
   }
 }
 
-// Scalar fallback of the gather for rows whose byte length is not a multiple of 16.
+// Scalar row copy for rows whose byte length is not a multiple of 16: x_perm[r] = x[tok_of[r]].
 template <typename T>
 __global__ void __launch_bounds__(256) k_gather_rows_scalar(const T* __restrict__ x,
                                                             const int32_t* __restrict__ tok_of,
@@ -151,30 +178,38 @@ cudaError_t launch_perm_scan(const int32_t* phist, int npb, const int32_t* count
   return cudaGetLastError();
 }
 
-cudaError_t launch_perm_rank(const int32_t* topk_idx, const int32_t* pbase, const int32_t* offsets, int T, int E,
-                             int k, int cap, int32_t* row_of, int32_t* tok_of, cudaStream_t st) {
-  if (T <= 0) return cudaSuccess;
-  k_perm_rank<<<perm_blocks(T), 32, 0, st>>>(topk_idx, pbase, offsets, T, E, k, cap, row_of, tok_of);
-  return cudaGetLastError();
+int dispatch_launches(bool with_rows, int d, int elt_bytes) {
+  (void)d;
+  (void)elt_bytes;
+  return with_rows ? 2 : 1;
 }
 
-cudaError_t launch_gather_rows(bool bf16, const void* x, const int32_t* tok_of, const int32_t* n_rows_dev,
-                               int max_rows, int d, void* x_perm, cudaStream_t st) {
-  if (max_rows <= 0) return cudaSuccess;
+cudaError_t launch_dispatch(bool bf16, const int32_t* topk_idx, const int32_t* pbase, const int32_t* offsets, int T,
+                            int E, int k, int cap, const void* x, int d, int32_t* row_of, int32_t* tok_of,
+                            void* x_perm, int max_rows, uint32_t* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int nb = perm_blocks(T);
+  if (k <= 2)
+    k_dispatch<2><<<nb, 256, 0, st>>>(topk_idx, pbase, offsets, T, E, k, cap, row_of, tok_of, status);
+  else if (k <= 4)
+    k_dispatch<4><<<nb, 256, 0, st>>>(topk_idx, pbase, offsets, T, E, k, cap, row_of, tok_of, status);
+  else
+    k_dispatch<8><<<nb, 256, 0, st>>>(topk_idx, pbase, offsets, T, E, k, cap, row_of, tok_of, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !x_perm || max_rows <= 0) return e;
   const size_t row_bytes = (size_t)d * (bf16 ? 2 : 4);
   int blocks = (max_rows + 7) / 8;
   if (blocks > 148 * 32) blocks = 148 * 32;
-  if (row_bytes % 16 == 0) {
-    k_gather_rows<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, n_rows_dev, max_rows,
+  if (row_bytes % 16 == 0)
+    k_gather_rows<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, offsets + E, max_rows,
                                           (int)(row_bytes / 16), static_cast<uint4*>(x_perm));
-  } else if (bf16) {
+  else if (bf16)
     k_gather_rows_scalar<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), tok_of,
-                                                                n_rows_dev, max_rows, d,
+                                                                offsets + E, max_rows, d,
                                                                 static_cast<__nv_bfloat16*>(x_perm));
-  } else {
-    k_gather_rows_scalar<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(x), tok_of, n_rows_dev, max_rows,
+  else
+    k_gather_rows_scalar<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(x), tok_of, offsets + E, max_rows,
                                                         d, static_cast<float*>(x_perm));
-  }
   return cudaGetLastError();
 }
 

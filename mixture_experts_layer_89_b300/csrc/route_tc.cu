@@ -47,6 +47,7 @@ constexpr int CMAX = 16;                // near-tie candidates kept per token (m
 // over with |partial sums| <= max(1, |logits|); measured errors stay ~10x below it.
 constexpr float kBandFloor = 2e-5f;
 constexpr float kBadLogit = -3.0e38f;
+constexpr int kScanSmemInts = 32768;    // per-block histograms the last CTA scans in shared memory
 
 enum : int { F_FEW = 2, F_ALL = 4, F_BAD = 8 };
 
@@ -115,6 +116,13 @@ struct RouteArgs {
   float* losses;
   float lb_coef, z_coef;
   float band_scale;   // 2^-22 * d / 16
+  // dispatch scan fused into the last CTA (pbase == NULL: not done here): per-block rank bases
+  // [nb][E], kept counts [E], offsets [E+1], dropped assignments; cap = capacity (INT_MAX dropless)
+  int cap;
+  int32_t* pbase;
+  int32_t* kept;
+  int32_t* offsets;
+  int32_t* drops;
   uint32_t* status;
 };
 
@@ -580,6 +588,65 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       if (lane == 0) ctl->red[1] = dl;
     }
     __syncthreads();
+    if (a.pbase) {
+      // dispatch scan: each expert's histogram over the blocks (exclusive: the block's rank base),
+      // kept counts under the capacity, offsets over experts, drops
+      int* H = reinterpret_cast<int*>(smem);  // the pipeline buffers are free
+      {
+        constexpr int U = 16;  // independent loads in flight per thread
+        const int n = nb * E;
+        for (int i0 = tid; i0 < n; i0 += RTHREADS * U) {
+          int hv[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * RTHREADS;
+            hv[u] = i < n ? __ldcg(a.hist + i) : 0;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = i0 + u * RTHREADS;
+            if (i < n) H[i] = hv[u];
+          }
+        }
+      }
+      __syncthreads();
+      for (int e = tid; e < E; e += RTHREADS) {
+        int run = 0;
+        for (int b = 0; b < nb; ++b) {
+          const int h = H[b * E + e];
+          a.pbase[(size_t)b * E + e] = run;
+          run += h;
+        }
+        const int kp = min(run, a.cap);
+        a.kept[e] = kp;
+        ctl->hist[e] = kp;
+      }
+      __syncthreads();
+      if (warp == 2) {  // exclusive scan of the kept counts over experts, 8 per lane
+        int v[8], sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = lane * 8 + i;
+          v[i] = e < E ? ctl->hist[e] : 0;
+          sum += v[i];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        int run = incl - sum;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = lane * 8 + i;
+          run += v[i];
+          if (e < E) a.offsets[e + 1] = run;
+        }
+        if (lane == 0) a.offsets[0] = 0;
+        if (lane == 31) *a.drops = a.T * k - incl;
+      }
+    }
     if (warp == 0) {
       double lb = 0.0;
       for (int e = lane; e < E; e += 32) lb += ctl->lbterm[e];
@@ -615,10 +682,12 @@ cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, const RouteA
 
 int route_tc_blocks(int T) { return (T + RM - 1) / RM; }
 
+bool route_tc_fuses_scan(int T, int E) { return T > 0 && (long)route_tc_blocks(T) * E <= kScanSmemInts; }
+
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
-                            cudaStream_t st) {
+                            cudaStream_t st, const RouteScan* scan) {
   if (T <= 0) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (e != cudaSuccess) return e;
@@ -654,6 +723,12 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   a.counts = counts; a.losses = losses; a.lb_coef = lb_coef; a.z_coef = z_coef;
   a.band_scale = ldexpf((float)d / 16.f, -22);
   a.status = status;
+  const bool fuse = scan && route_tc_fuses_scan(T, E);
+  a.cap = fuse ? scan->cap : 0;
+  a.pbase = fuse ? scan->pbase : nullptr;
+  a.kept = fuse ? scan->kept : nullptr;
+  a.offsets = fuse ? scan->offsets : nullptr;
+  a.drops = fuse ? scan->drops : nullptr;
   const int nb = route_tc_blocks(T);
   cudaError_t err;
   if (k + 1 <= 3) err = launch_kl<3>(mx, mw, a, nb, smem, st);

@@ -113,6 +113,8 @@ def test_misaligned_pointer_rejected_on_host(L):
 def test_launch_count(L, name):
     wl = WORKLOADS[name]
     n = moe.moe_layer_forward_launches(moe.config_from_workload(wl))
-    router = 1 if wl.dtype == "bf16" else 2        # bf16: one tensor-core launch with the reduction fused
-    assert n == router + 4 + 2 + (2 if wl.n_shared else 0) + 1
+    # bf16: one tensor-core router launch whose last CTA also scans the dispatch histograms, then the
+    # rank kernel and the row gather; fp32: router + reduction, histogram + scan + rank + gather
+    router, dispatch = (1, 2) if wl.dtype == "bf16" else (2, 4)
+    assert n == router + dispatch + 2 + (2 if wl.n_shared else 0) + 1
     assert moe.moe_layer_forward_launches(moe.config_from_workload(wl, T=0)) == router - 1 + 1
