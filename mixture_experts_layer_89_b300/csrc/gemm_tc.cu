@@ -72,14 +72,18 @@ struct SmemCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  int row_lo[MAXG + 1];
   int u_pre[MAXG + 1];  // prefix over groups of row units (m-tiles, or m-tile pairs in PAIR mode)
 };
-// Epilogue staging for TMA tile stores: one 32 x 32 tile per warp (fp32 4 KB with the 128-byte
-// swizzle, bf16 2 KB with the 64-byte swizzle).
+// Epilogue staging for TMA tile stores: 32 x 32 tiles per warp (fp32 4 KB with the 128-byte
+// swizzle, bf16 2 KB with the 64-byte swizzle), two per warp (the store of one chunk overlaps the
+// staging of the next) except with 16 epilogue warps.  Shared memory: [alignment slack][stage
+// region][staging][control].
 constexpr int stg_bytes(bool outf32) { return outf32 ? 32 * 32 * 4 : 32 * 32 * 2; }
-constexpr size_t SMEM_BASE = (size_t)STAGE_REGION + sizeof(SmemCtl) + 1024;
-constexpr size_t smem_total(bool outf32, int epiw) { return SMEM_BASE + (size_t)epiw * stg_bytes(outf32) + 1024; }
+constexpr int stg_bufs(int epiw) { return epiw > 8 ? 1 : 2; }
+constexpr size_t smem_total(bool outf32, int epiw) {
+  return 1024 + (size_t)STAGE_REGION + (size_t)epiw * stg_bufs(epiw) * stg_bytes(outf32) + sizeof(SmemCtl);
+}
+static_assert(smem_total(true, 4) <= 232448 && smem_total(false, 16) <= 232448, "shared memory per CTA");
 
 // Wait that ignores the abort flag (used to drain in-flight async operations before exit).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -109,11 +113,12 @@ __device__ __forceinline__ float silu(float u) { return __fdividef(u, 1.f + __ex
 // One warp's 32 rows x 32 bf16 columns (16 packed words per lane, lane = row): a TMA tile store
 // through the warp's staging tile when all 32 rows are output rows (64-byte swizzle: 16-byte chunk
 // j of row r sits at chunk j ^ ((r / 2) % 4), conflict-free), else direct row stores.
+template <int NBUF>
 __device__ __forceinline__ void store_bf16_chunk(const uint32_t (&pk)[16], bool full_rows, uint8_t* stg,
                                                  const CUtensorMap* tm, int col, int row0, __nv_bfloat16* dst_row,
                                                  int lane) {
   if (full_rows) {
-    if (lane == 0) bulk_wait_read0();  // the previous store has finished reading stg
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last used stg has read it
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -142,10 +147,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   constexpr int STAGE_BYTES = stage_bytes_of(PAIR);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(smem + (size_t)STAGE_REGION);
-  // fp32 staging tiles (1024-byte aligned for the 128-byte swizzle), one per epilogue warp
-  uint8_t* stg_base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(ctl) + sizeof(SmemCtl) + 1023) & ~uintptr_t(1023));
+  uint8_t* stg_base = smem + (size_t)STAGE_REGION;  // 1024-byte aligned (the swizzle atoms)
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * stg_bufs(EPIW) * stg_bytes(OUTF32));
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.offsets ? args.G : 1;
@@ -194,8 +197,6 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       if (g < G) {
         const int lo = args.offsets ? args.offsets[g] : 0;
         const int hi = args.offsets ? args.offsets[g + 1] : args.rows_static;
-        ctl->row_lo[g] = lo;
-        if (g == G - 1) ctl->row_lo[G] = hi;
         const int mt = hi > lo ? (hi - lo + BM - 1) / BM : 0;
         cnt[i] = PAIR ? (mt + 1) >> 1 : mt;
         local += cnt[i];
@@ -235,8 +236,9 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
     }
     g = lo;
     const int mt_local = PAIR ? 2 * (mu - ctl->u_pre[g]) + crank : mu - ctl->u_pre[g];
-    m0 = ctl->row_lo[g] + mt_local * BM;   // may lie past m_end in PAIR mode: nothing is stored
-    m_end = ctl->row_lo[g + 1];
+    const int row_lo = args.offsets ? __ldg(args.offsets + g) : 0;
+    m0 = row_lo + mt_local * BM;   // may lie past m_end in PAIR mode: nothing is stored
+    m_end = args.offsets ? __ldg(args.offsets + g + 1) : args.rows_static;
     n0 = nt * NOUT;
   };
 
@@ -345,7 +347,9 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   } else if (warp >= 4) {
     const int q = warp & 3;                      // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
     const int c_lo = ((warp - 4) >> 2) * CW;     // this warp's share of the output columns
-    uint8_t* stg = stg_base + (size_t)(warp - 4) * stg_bytes(OUTF32);
+    constexpr int NBUF = stg_bufs(EPIW);
+    uint8_t* stg_w = stg_base + (size_t)(warp - 4) * NBUF * stg_bytes(OUTF32);
+    int chunk = 0;  // running chunk count of this warp: selects the staging buffer
     int it = 0;
     for (int u = unit0; u < total_units; u += ustep, ++it) {
       int g, m0, m_end, n0;
@@ -378,8 +382,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
               const float h1 = silu(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
               pk[i] = pack_bf16x2(h0, h1);
             }
-            store_bf16_chunk(pk, full_rows, stg, &tmOut, n0 + c, m0 + q * 32,
-                             static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
+            store_bf16_chunk<NBUF>(pk, full_rows, stg_w + (chunk++ % NBUF) * stg_bytes(OUTF32), &tmOut, n0 + c,
+                                   m0 + q * 32, static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
           }
         }
       } else {
@@ -414,7 +418,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
             if (OUTF32 && full_rows) {
               // the warp's 32 rows x 32 columns go out as one TMA tile store through shared
               // memory (128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8))
-              if (lane == 0) bulk_wait_read0();  // the previous store has finished reading stg
+              uint8_t* stg = stg_w + (chunk++ % NBUF) * stg_bytes(OUTF32);
+              if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last used stg has read it
               __syncwarp();
 #pragma unroll
               for (int j = 0; j < 8; ++j)
@@ -434,8 +439,8 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
               uint32_t pk[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-              store_bf16_chunk(pk, full_rows, stg, &tmOut, n0 + c, m0 + q * 32,
-                               static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
+              store_bf16_chunk<NBUF>(pk, full_rows, stg_w + (chunk++ % NBUF) * stg_bytes(OUTF32), &tmOut, n0 + c,
+                                     m0 + q * 32, static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
             }
           }
         }
@@ -600,7 +605,7 @@ cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
 template <int ACT, bool OUTF32>
 cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
-  constexpr int EPIW = (ACT == ACT_GELU) ? 8 : 4;  // the erf epilogue is ALU-bound; the others are not
+  constexpr int EPIW = (ACT == ACT_GELU) ? 16 : 4;  // the erf epilogue is ALU-bound; the others are not
   const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
   if (rows_alloc <= 0 || p.N <= 0) return cudaSuccess;
   const int G = p.offsets ? p.G : 1;
