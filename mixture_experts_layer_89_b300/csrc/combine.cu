@@ -6,9 +6,9 @@
 // weights are not renormalised (OpenMythos article, sec. 3.1, overflow handling).
 //
 // The expert outputs arrive in fp32 (the projections keep their accumulators), so the layer output
-// is rounded once.  One warp per token; fp32 accumulation in slot order, then + shared.  All k
-// source rows of a chunk are loaded before any is accumulated so a lane keeps up to 2(k+1)
-// independent 16-byte loads in flight.
+// is rounded once.  One warp per (token, 256-column chunk); fp32 accumulation in slot order, then
+// + shared.  All k source rows of a chunk are loaded before any is accumulated so a lane keeps up
+// to 2(k+1) independent 16-byte loads in flight.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,14 +30,19 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
       make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
 }
 
-// One warp per token, 8 consecutive columns per lane and step (two 16-byte loads per source row).
+// One warp per (token, 256-column chunk), 8 consecutive columns per lane (two 16-byte loads per
+// source row), so that a call with few tokens still spreads over many SMs.
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ row_of,
                                                  const float* __restrict__ topk_w, const float* __restrict__ y_shared,
                                                  T* __restrict__ y, int Tn, int d, int k) {
-  const int warps = gridDim.x * 8;
+  const int nch = (d + 255) / 256;
+  const long items = (long)Tn * nch;
+  const long warps = (long)gridDim.x * 8;
   const int lane = threadIdx.x & 31;
-  for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += warps) {
+  for (long it = (long)blockIdx.x * 8 + (threadIdx.x >> 5); it < items; it += warps) {
+    const int t = (int)(it / nch);
+    const int c = (int)(it - (long)t * nch) * 256 + lane * 8;
     int rows[KMAX];
     float ws[KMAX];
 #pragma unroll
@@ -45,28 +50,27 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_per
       rows[j] = (j < k) ? row_of[(size_t)t * k + j] : -1;
       ws[j] = (j < k) ? topk_w[(size_t)t * k + j] : 0.f;
     }
-    for (int c = lane * 8; c < d; c += 32 * 8) {
-      float v[KMAX][8];
+    if (c >= d) continue;
+    float v[KMAX][8];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (rows[j] >= 0) load8(y_perm + (size_t)rows[j] * d + c, v[j]);
-      float sv[8];
-      if (y_shared) load8(y_shared + (size_t)t * d + c, sv);
-      float acc[8];
+    for (int j = 0; j < KMAX; ++j)
+      if (rows[j] >= 0) load8(y_perm + (size_t)rows[j] * d + c, v[j]);
+    float sv[8];
+    if (y_shared) load8(y_shared + (size_t)t * d + c, sv);
+    float acc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (rows[j] >= 0) {
+    for (int j = 0; j < KMAX; ++j)
+      if (rows[j] >= 0) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = fmaf(ws[j], v[j][i], acc[i]);
-        }
-      if (y_shared) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += sv[i];
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(ws[j], v[j][i], acc[i]);
       }
-      store8(y + (size_t)t * d + c, acc);
+    if (y_shared) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += sv[i];
     }
+    store8(y + (size_t)t * d + c, acc);
   }
 }
 
@@ -94,7 +98,8 @@ __global__ void __launch_bounds__(256) k_combine_scalar(const float* __restrict_
 template <typename T>
 cudaError_t launch_t(const float* y_perm, const int32_t* row_of, const float* topk_w, const float* y_shared, void* y,
                      int Tn, int d, int k, cudaStream_t st) {
-  int blocks = (Tn + 7) / 8;
+  const long items = (long)Tn * ((d + 255) / 256);
+  int blocks = (int)((items + 7) / 8);
   if (blocks > 148 * 32) blocks = 148 * 32;
   T* yo = static_cast<T*>(y);
   if (d % 8 != 0) {

@@ -106,6 +106,7 @@ struct RouteArgs {
   const __nv_bfloat16* wr;
   const float* lbias;
   int T, d, E, k, npad, stages;
+  int xrows;  // rows of the x box: 128, or fewer (a multiple of 8) when the layer has fewer tokens
   int32_t* topk_idx;
   float* topk_w;
   int32_t* hist;      // [nb][E] per-CTA expert histograms
@@ -201,13 +202,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     k_route_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_bytes = A_TILE + a.npad * RBK * 2;
+  const int stage_bytes = A_TILE + a.npad * RBK * 2;  // layout; a stage receives xrows * 128 + npad * 128 bytes
   RouteCtl* ctl = reinterpret_cast<RouteCtl*>(smem + (size_t)a.stages * stage_bytes);
   volatile int* abort_flag = &ctl->abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k;
   const int kblocks = a.d / RBK;
   const int t0 = blockIdx.x * RM;
+  const int nvalid = min(RM, a.T - t0);  // rows of the tile that are tokens
   uint32_t tmem_cols = 32;
   while ((int)tmem_cols < a.npad) tmem_cols <<= 1;
 
@@ -256,7 +258,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         break;
       }
       const uint32_t fb = smem_u32(&ctl->full[s]);
-      mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+      // fewer than 128 tokens: only their rows of x are loaded; the MMA rows past them read stale
+      // shared memory and produce logits that are never used
+      mbar_arrive_expect_tx(fb, (uint32_t)((a.xrows + a.npad) * RBK * 2));
       armed |= 1u << s;
       armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
       uint8_t* sa = smem + (size_t)s * stage_bytes;
@@ -340,7 +344,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       lv[j] = -FLT_MAX;
       le[j] = 0x7fffffff;
     }
-    const int e_hi = h ? E : ehalf;
+    const int e_hi = r < nvalid ? (h ? E : ehalf) : 0;  // rows past T: no list
     for (int e = h ? ehalf : 0; e < e_hi; ++e) list_insert(lv, le, nl, S.Z[r * ZP + e], e);
     float* tv = S.tlv + (size_t)(h * RM + r) * KLMAX;
     int* te = S.tle + (size_t)(h * RM + r) * KLMAX;
@@ -407,6 +411,10 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const float m = ctl->mx[r];
     float s0 = 0.f, s1 = 0.f;
     const int e_lo = h ? ehalf : 0, e_hi = h ? E : ehalf;
+    if (r >= nvalid) {  // rows past T: zero probabilities
+      for (int e = e_lo; e < e_hi; ++e) S.Z[r * ZP + e] = 0.f;
+      s0 = 1.f;
+    } else {
     int e = e_lo;
     for (; e + 1 < e_hi; e += 2) {
       const float p0 = __expf(S.Z[r * ZP + e] - m), p1 = __expf(S.Z[r * ZP + e + 1] - m);
@@ -419,6 +427,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       const float p0 = __expf(S.Z[r * ZP + e] - m);
       S.Z[r * ZP + e] = p0;
       s0 += p0;
+    }
     }
     ctl->spart[h][r] = s0 + s1;
   }
@@ -699,7 +708,7 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   {
     const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)T};
     const cuuint64_t str[1] = {(cuuint64_t)d * 2};
-    const cuuint32_t box[2] = {RBK, RM};
+    const cuuint32_t box[2] = {RBK, (cuuint32_t)(T < RM ? (T + 7) / 8 * 8 : RM)};
     if (!make_tmap_bf16(&mx, x, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
@@ -718,6 +727,7 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   a.wr = static_cast<const __nv_bfloat16*>(wr);
   a.lbias = lbias;
   a.T = T; a.d = d; a.E = E; a.k = k; a.npad = npad; a.stages = stages;
+  a.xrows = T < RM ? (T + 7) / 8 * 8 : RM;
   a.topk_idx = topk_idx; a.topk_w = topk_w;
   a.hist = hist; a.psum = psum; a.lse2 = lse2; a.done = done;
   a.counts = counts; a.losses = losses; a.lb_coef = lb_coef; a.z_coef = z_coef;
