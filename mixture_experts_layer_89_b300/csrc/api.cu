@@ -253,6 +253,50 @@ moe_status check_weights(const moe_config* c, const moe_weights* w) {
   return MOE_OK;
 }
 
+// A second stream per (host thread, device) on which the shared experts run beside the router,
+// the dispatch and the routed projections, forked from and joined back to the caller's stream
+// with events (which stream capture records as graph edges).  Created on first use; never
+// created while the caller's stream is being captured.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kSideDevices = 64;
+thread_local SideStream t_side[kSideDevices];
+
+SideStream* side_stream(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideDevices) return nullptr;
+  SideStream& ss = t_side[dev];
+  if (ss.s) return &ss;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+  cudaStream_t s = nullptr;
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+    if (a) cudaEventDestroy(a);
+    cudaStreamDestroy(s);
+    return nullptr;
+  }
+  ss.s = s;
+  ss.fork = a;
+  ss.join = b;
+  return &ss;
+}
+
+// The shared experts go to the side stream only when their two projections together occupy at
+// most a third of the SMs: then they run on otherwise idle SMs.  Larger ones fill the GPU by
+// themselves and stay on the caller's stream.
+bool shared_on_side_stream(const moe_config* c) {
+  if (c->n_shared <= 0 || c->T <= 0 || !is_bf16(c)) return false;
+  const int64_t mt = (c->T + 127) / 128;
+  const int64_t hid = (int64_t)c->n_shared * c->dff * (c->act == MOE_ACT_SWIGLU ? 2 : 1);
+  const int64_t tiles = mt * ((hid + 255) / 256) + mt * ((c->d + 255) / 256);
+  return tiles * 3 <= num_sms_current();
+}
+
 moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, void* y, float* losses,
                       int32_t* counts_out, int32_t* drops_out, void* ws, cudaStream_t st, cudaEvent_t const* ev) {
   MOE_TRY(validate(c));
@@ -280,6 +324,14 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
   scan.offsets = offsets;
   scan.drops = drops;
   const bool scanned = is_bf16(c) && route_tc_fuses_scan(c->T, c->E);
+  // stage timing (ev) keeps every step on the caller's stream so that each stage is timed alone
+  SideStream* side = (!ev && shared_on_side_stream(c)) ? side_stream(st) : nullptr;
+  if (side) {
+    MOE_CUDA(cudaEventRecord(side->fork, st));
+    MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
+    MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, side->s));
+    MOE_CUDA(cudaEventRecord(side->join, side->s));
+  }
   MOE_TRY(rec(0));
   MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st, &scan));
   MOE_TRY(rec(1));
@@ -288,7 +340,10 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
   MOE_TRY(rec(2));
   MOE_TRY(ffn_routed_impl(c, x_perm, offsets, w, y_perm, ws, st, ev ? ev[3] : nullptr));
   MOE_TRY(rec(4));
-  MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, st));
+  if (side)
+    MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
+  else
+    MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, st));
   MOE_TRY(rec(5));
   MOE_CUDA(launch_combine(is_bf16(c), static_cast<const float*>(y_perm), row_of, topk_w,
                           static_cast<const float*>(y_sh), y, c->T, c->d, c->k, st));

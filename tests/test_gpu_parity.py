@@ -183,6 +183,29 @@ def test_repeat_calls_are_deterministic():
     assert torch.equal(a["y"], b["y"]) and torch.equal(a["losses"], b["losses"])
 
 
+def test_graph_replay_matches_eager():
+    """The layer captured in a CUDA graph (small shared experts fork onto a second stream and join
+    back before the combine) reproduces the eager result bit for bit, also after new inputs are
+    copied into the captured buffer."""
+    wl = CASES["bf16_swiglu_shared"]
+    inp = _to(make_inputs(wl, "cpu"), "cuda")
+    layer = moe.MoELayer(moe.config_from_workload(wl), inp)
+    x = inp["x"].clone()
+    ref1 = layer.forward(x)
+    ref2 = layer.forward(x.flip(0).contiguous())
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = layer.forward(x, stream=torch.cuda.current_stream())
+    for ref, src in ((ref1, inp["x"]), (ref2, inp["x"].flip(0))):
+        x.copy_(src)
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(layer.ws) == moe.MOE_OK
+        for a, b in zip(out, ref):
+            assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------------------------ full workloads
 def _full(name, n_sample, seed=0):
     wl = WORKLOADS[name]
