@@ -97,17 +97,40 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Epilogue activations.  Their outputs are rounded to bf16 (relative spacing 2^-8), so they use
 // the hardware exp2/reciprocal approximations (relative error ~1e-7) instead of IEEE expf/erff
 // and division.
-// erf by Abramowitz & Stegun, Handbook of Mathematical Functions, formula 7.1.26
-// (|error| <= 1.5e-7): erf(x) = 1 - t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-x^2),
-// t = 1 / (1 + p x), x >= 0, odd continuation for x < 0.
-__device__ __forceinline__ float erf_as7126(float x) {
-  const float ax = fabsf(x);
-  const float t = __fdividef(1.f, fmaf(0.3275911f, ax, 1.f));
-  const float poly =
-      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
-  return copysignf(1.f - poly * __expf(-ax * ax), x);
+// GELU(u) = u Phi(u) with the complementary error function of Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 7.1.26 (|error| <= 1.5e-7): for z >= 0,
+// erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2), t = 1 / (1 + p z).  With
+// z = |u| / sqrt 2 and g = |u| erfc(z) / 2:  u Phi(u) = u - g for u >= 0 and -g for u < 0, i.e.
+// max(u, 0) - g in both cases.  Two columns at a time with the packed fp32x2 multiply-adds
+// (the halved a_i fold the 1/2 into the polynomial); |u| is capped at 16 inside g, where
+// erfc(16 / sqrt 2) underflows, so that u = +-inf gives inf / 0 rather than inf * 0.
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
-__device__ __forceinline__ float gelu_erf(float u) { return 0.5f * u * (1.f + erf_as7126(u * 0.70710678118654752f)); }
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float2 gelu_erf2(float2 u) {
+  const float2 ax = make_float2(fabsf(u.x), fabsf(u.y));
+  const float2 den = __ffma2_rn(ax, make_float2(0.3275911f * 0.70710678118654752f, 0.3275911f * 0.70710678118654752f),
+                                make_float2(1.f, 1.f));
+  const float2 t = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+  float2 poly = __ffma2_rn(t, make_float2(0.5f * 1.061405429f, 0.5f * 1.061405429f),
+                           make_float2(0.5f * -1.453152027f, 0.5f * -1.453152027f));
+  poly = __ffma2_rn(poly, t, make_float2(0.5f * 1.421413741f, 0.5f * 1.421413741f));
+  poly = __ffma2_rn(poly, t, make_float2(0.5f * -0.284496736f, 0.5f * -0.284496736f));
+  poly = __ffma2_rn(poly, t, make_float2(0.5f * 0.254829592f, 0.5f * 0.254829592f));
+  poly = __fmul2_rn(poly, t);
+  // exp(-z^2) = 2^(-u^2 log2(e) / 2)
+  const float2 arg = __fmul2_rn(__fmul2_rn(u, u), make_float2(-0.72134752044448170f, -0.72134752044448170f));
+  const float2 e = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+  const float2 g = __fmul2_rn(__fmul2_rn(make_float2(fminf(ax.x, 16.f), fminf(ax.y, 16.f)), poly), e);
+  return __fadd2_rn(make_float2(fmaxf(u.x, 0.f), fmaxf(u.y, 0.f)), make_float2(-g.x, -g.y));
+}
 __device__ __forceinline__ float silu(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
 // One warp's 32 rows x 32 bf16 columns (16 packed words per lane, lane = row): a TMA tile store
@@ -139,7 +162,8 @@ __device__ __forceinline__ void store_bf16_chunk(const uint32_t (&pk)[16], bool 
 
 template <int ACT, bool OUTF32, int EPIW, bool PAIR>
 __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
-    k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+    k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
+              const __grid_constant__ CUtensorMap tmB0,
               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut, const TcArgs args) {
   constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
   constexpr int CW = NOUT / (EPIW / 4);  // output columns per epilogue warp
@@ -174,6 +198,7 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
+    if (!PAIR) tma_prefetch_desc(&tmA32);
     tma_prefetch_desc(&tmB0);
     if (ACT == ACT_SWIGLU) tma_prefetch_desc(&tmB1);
   }
@@ -251,6 +276,18 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
         int g, m0, m_end, n0;
         decode(u, g, m0, m_end, n0);
         const int nn = n0 % args.N_w;
+        // single CTA: a tile with few rows (an expert with few tokens) loads only its 32-row groups
+        // of A; the MMA rows past them read stale shared memory and give accumulator rows that are
+        // never stored
+        const int n32 = PAIR ? 4 : min(4, (max(m_end - m0, 1) + 31) >> 5);
+        const uint32_t tx_bytes = (uint32_t)(STAGE_BYTES - (4 - n32) * (A_BYTES / 4));
+        auto load_a = [&](uint8_t* sa, uint32_t fb, int k0) {
+          if (n32 == 4) {
+            tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
+          } else {
+            for (int j = 0; j < n32; ++j) tma_load_2d(smem_u32(sa + j * (A_BYTES / 4)), &tmA32, fb, k0, m0 + 32 * j);
+          }
+        };
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status)) {
             aborted = true;
@@ -275,13 +312,13 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
             else
               tma_load_3d_cg2(smem_u32(sb), &tmB0, lb, kk, nn + crank * (BNB / 2), gw);
           } else if (ACT == ACT_SWIGLU) {
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);  // A + the whole B tile
-            tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
+            mbar_arrive_expect_tx(fb, tx_bytes);  // A (its existing rows) + the whole B tile
+            load_a(sa, fb, k0);
             tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
             tma_load_3d(smem_u32(sb + B_BYTES / 2), &tmB1, fb, kk, nn, gw);
           } else {
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
+            mbar_arrive_expect_tx(fb, tx_bytes);
+            load_a(sa, fb, k0);
             tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
           }
           if (++s == STAGES) {
@@ -413,7 +450,11 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
             }
             if (ACT == ACT_GELU) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) f[i] = gelu_erf(f[i]);
+              for (int i = 0; i < 32; i += 2) {
+                const float2 h2 = gelu_erf2(make_float2(f[i], f[i + 1]));
+                f[i] = h2.x;
+                f[i + 1] = h2.y;
+              }
             }
             if (OUTF32 && full_rows) {
               // the warp's 32 rows x 32 columns go out as one TMA tile store through shared
@@ -576,7 +617,8 @@ int max_pair_clusters(K kernel, int threads, size_t smem) {
 }
 
 template <int ACT, bool OUTF32, int EPIW, bool PAIR>
-cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtensorMap& mB1, const CUtensorMap& mO,
+cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mA32, const CUtensorMap& mB0, const CUtensorMap& mB1,
+                     const CUtensorMap& mO,
                      const TcArgs& a, long grid, cudaStream_t st) {
   auto kern = k_proj_tc<ACT, OUTF32, EPIW, PAIR>;
   constexpr int threads = 128 + 32 * EPIW;
@@ -584,7 +626,7 @@ cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   if (!PAIR) {
-    kern<<<(unsigned)grid, threads, smem, st>>>(mA, mB0, mB1, mO, a);
+    kern<<<(unsigned)grid, threads, smem, st>>>(mA, mA32, mB0, mB1, mO, a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -599,7 +641,7 @@ cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mB0, const CUtens
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mA, mB0, mB1, mO, a);
+  return cudaLaunchKernelEx(&cfg, kern, mA, mA32, mB0, mB1, mO, a);
 }
 
 template <int ACT, bool OUTF32>
@@ -609,19 +651,21 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
   const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
   if (rows_alloc <= 0 || p.N <= 0) return cudaSuccess;
   const int G = p.offsets ? p.G : 1;
-  // Pairs pay off when groups average two or more row tiles (otherwise half the pair idles) and
-  // the epilogue is light: the two CTAs of a pair advance in lock-step, so the ALU-bound GELU
-  // epilogue of one stalls both (measured slower there).
+  // Pairs pay off when groups average two or more row tiles (otherwise half the pair idles): a CTA
+  // then holds 6 stages of half a B tile instead of 4 of a whole one, so more MMA work is in
+  // flight per byte of shared memory while the tile loads are on their way.
   int n_clusters = 0;
-  if (ACT != ACT_GELU && (long)rows_alloc >= 2L * BM * G)
+  if ((long)rows_alloc >= 2L * BM * G)
     n_clusters = max_pair_clusters(k_proj_tc<ACT, OUTF32, EPIW, true>, 128 + 32 * EPIW, smem_total(OUTF32, EPIW));
   const bool pair = n_clusters > 0;
-  CUtensorMap mA, mB0, mB1;
+  CUtensorMap mA, mA32, mB0, mB1;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)rows_alloc};
     const cuuint64_t str[1] = {(cuuint64_t)p.lda * 2};
     const cuuint32_t box[2] = {BK, BM};
     if (!make_tmap_bf16(&mA, p.A, 2, dims, str, box)) return cudaErrorInvalidValue;
+    const cuuint32_t box32[2] = {BK, 32};  // 32-row groups of A for tiles with few rows
+    if (!make_tmap_bf16(&mA32, p.A, 2, dims, str, box32)) return cudaErrorInvalidValue;
   }
   {
     const cuuint64_t dims[3] = {(cuuint64_t)p.K_w, (cuuint64_t)p.N_w, (cuuint64_t)p.G_w};
@@ -661,12 +705,12 @@ cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStr
     long units = (ub_mt + G + 1) / 2 * n_tiles;
     long clusters = units < n_clusters ? units : n_clusters;
     if (clusters < 1) clusters = 1;
-    return launch_k<ACT, OUTF32, EPIW, true>(mA, mB0, mB1, mO, a, 2 * clusters, st);
+    return launch_k<ACT, OUTF32, EPIW, true>(mA, mA32, mB0, mB1, mO, a, 2 * clusters, st);
   }
   long grid = ub_mt * n_tiles;
   if (grid > num_sms) grid = num_sms;
   if (grid < 1) grid = 1;
-  return launch_k<ACT, OUTF32, EPIW, false>(mA, mB0, mB1, mO, a, grid, st);
+  return launch_k<ACT, OUTF32, EPIW, false>(mA, mA32, mB0, mB1, mO, a, grid, st);
 }
 }  // namespace
 

@@ -133,7 +133,9 @@ __global__ void __launch_bounds__(256) k_dispatch(const int32_t* __restrict__ to
 }
 
 // x_perm[r] = x[tok_of[r]] for r < n_rows (device count); one warp per row, 16-byte vectors, a
-// grid far larger than the SM count so that many loads are in flight.
+// grid far larger than the SM count so that many loads are in flight.  The rows are written with
+// streaming (evict-first) stores so that they do not push x, which every one of its k rows
+// re-reads, out of L2.
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ tok_of,
                                                      const int32_t* __restrict__ n_rows_dev, int max_rows,
                                                      int row_vecs, uint4* __restrict__ x_perm) {
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x
     const int t = tok_of[r];
     const uint4* src = x + (size_t)t * row_vecs;
     uint4* dst = x_perm + (size_t)r * row_vecs;
-    for (int c = threadIdx.x & 31; c < row_vecs; c += 32) dst[c] = src[c];
+    for (int c = threadIdx.x & 31; c < row_vecs; c += 32) __stcs(dst + c, src[c]);
   }
 }
 

@@ -39,7 +39,7 @@ constexpr int RTHREADS = 256;
 constexpr int RWARPS = RTHREADS / 32;
 constexpr int A_TILE = RM * RBK * 2;    // 16 KB
 constexpr int SMEM_STAGES_BYTES = 192 * 1024;
-constexpr int MAX_STAGES = 8;
+constexpr int MAX_STAGES = 16;
 constexpr int KLMAX = 9;                // top-(k+1) list, k <= 8
 constexpr int CMAX = 16;                // near-tie candidates kept per token (more: all experts)
 // Near-tie band of a token: a bound on the difference between the tensor cores' fp32 accumulation
@@ -47,9 +47,9 @@ constexpr int CMAX = 16;                // near-tie candidates kept per token (m
 // over with |partial sums| <= max(1, |logits|); measured errors stay ~10x below it.
 constexpr float kBandFloor = 2e-5f;
 constexpr float kBadLogit = -3.0e38f;
-constexpr int kScanSmemInts = 32768;    // per-block histograms the last CTA scans in shared memory
 
 enum : int { F_FEW = 2, F_ALL = 4, F_BAD = 8 };
+constexpr int PPARTS_LAST = 8;
 
 struct RouteCtl {
   uint64_t full[MAX_STAGES];
@@ -68,8 +68,10 @@ struct RouteCtl {
   int flags[RM];
   int ncand[RM];
   float lse2w[RWARPS];
-  double lbterm[256];
-  double red[RWARPS];
+  float lbterm[256];
+  float red[RWARPS];
+  int lcnt[PPARTS_LAST][256];   // last CTA: per-slice counts and sums of P
+  float lps[PPARTS_LAST][256];
 };
 
 // Epilogue scratch laid over the pipeline buffers once the main loop is done.
@@ -106,6 +108,7 @@ struct RouteArgs {
   const __nv_bfloat16* wr;
   const float* lbias;
   int T, d, E, k, npad, stages;
+  int region;  // bytes before RouteCtl: the stages, or the epilogue scratch if that is larger
   int xrows;  // rows of the x box: 128, or fewer (a multiple of 8) when the layer has fewer tokens
   int32_t* topk_idx;
   float* topk_w;
@@ -202,8 +205,12 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     k_route_tc(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const RouteArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_bytes = A_TILE + a.npad * RBK * 2;  // layout; a stage receives xrows * 128 + npad * 128 bytes
-  RouteCtl* ctl = reinterpret_cast<RouteCtl*>(smem + (size_t)a.stages * stage_bytes);
+  // a stage holds the x rows of the tile (xrows x 128 bytes) and W_r (npad x 128 bytes); with fewer
+  // than 128 tokens the MMA's A rows past xrows read the following bytes of shared memory (still
+  // inside the allocation: RouteCtl follows the stages) and give logits that are never used
+  const int a_bytes = a.xrows * RBK * 2;
+  const int stage_bytes = a_bytes + a.npad * RBK * 2;
+  RouteCtl* ctl = reinterpret_cast<RouteCtl*>(smem + (size_t)a.region);
   volatile int* abort_flag = &ctl->abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k;
@@ -265,7 +272,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
       uint8_t* sa = smem + (size_t)s * stage_bytes;
       tma_load_2d(smem_u32(sa), &tmX, fb, kb * RBK, t0);
-      tma_load_2d(smem_u32(sa + A_TILE), &tmW, fb, kb * RBK, 0);
+      tma_load_2d(smem_u32(sa + a_bytes), &tmW, fb, kb * RBK, 0);
       if (++s == a.stages) {
         s = 0;
         ph ^= 1u;
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
       if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
-      const uint32_t sb = sa + A_TILE;
+      const uint32_t sb = sa + a_bytes;
 #pragma unroll
       for (int kk = 0; kk < RBK / 16; ++kk)
         umma_bf16(tmem_base, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc, (kb | kk) != 0);
@@ -411,8 +418,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const float m = ctl->mx[r];
     float s0 = 0.f, s1 = 0.f;
     const int e_lo = h ? ehalf : 0, e_hi = h ? E : ehalf;
-    if (r >= nvalid) {  // rows past T: zero probabilities
-      for (int e = e_lo; e < e_hi; ++e) S.Z[r * ZP + e] = 0.f;
+    if (r >= nvalid) {  // rows past T: no token, nothing to normalise
       s0 = 1.f;
     } else {
     int e = e_lo;
@@ -526,8 +532,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const int e = tid % E, part = tid / E;
     if (part < parts) {
       const int rows = RM / parts;
+      const int r_hi = min((part + 1) * rows, nvalid);  // rows past T hold no token
       float ps = 0.f;
-      for (int r = part * rows; r < (part + 1) * rows; ++r) ps = fmaf(S.Z[r * ZP + e], ctl->sinv[r], ps);
+      for (int r = part * rows; r < r_hi; ++r) ps = fmaf(S.Z[r * ZP + e], ctl->sinv[r], ps);
       S.ppart[part * 256 + e] = ps;
     }
   }
@@ -548,87 +555,108 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   if (ctl->is_last) {
     __threadfence();
     const int nb = gridDim.x;
-    // block slices per expert (fixed boundaries), fp32 sums in block order, slices in order
+    const int n = nb * E;
+    // Expert e's blocks are cut into `parts` slices with fixed boundaries; each slice is summed in
+    // block order and the slices in slice order, so the sums do not depend on scheduling.  When the
+    // per-block partials fit in the (now free) pipeline buffers they are first loaded there with
+    // many loads in flight, and the dispatch scan runs over the slices in parallel.
+    const bool staged = 8L * n <= (long)a.region;
+    int* H = reinterpret_cast<int*>(smem);             // [nb][E] per-block counts
+    float* PS = reinterpret_cast<float*>(smem) + n;    // [nb][E] per-block sums of P
+    float l = 0.f;
+    if (staged) {
+      constexpr int U = 16;  // independent loads in flight per thread
+      for (int i0 = tid; i0 < n; i0 += RTHREADS * U) {
+        int hv[U];
+        float pv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * RTHREADS;
+          hv[u] = i < n ? __ldcg(a.hist + i) : 0;
+          pv[u] = i < n ? __ldcg(a.psum + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + u * RTHREADS;
+          if (i < n) {
+            H[i] = hv[u];
+            PS[i] = pv[u];
+          }
+        }
+      }
+    }
+    if (warp == 1) {
+      for (int b = lane; b < nb; b += 32) l += __ldcg(a.lse2 + b);
+    }
+    __syncthreads();
     {
       const int e = tid % E, part = tid / E;
       if (part < parts) {
         const int b_lo = (int)((long)nb * part / parts), b_hi = (int)((long)nb * (part + 1) / parts);
         int cnt = 0;
         float ps = 0.f;
-        constexpr int U = 8;
-        for (int b0 = b_lo; b0 < b_hi; b0 += U) {
-          int hv[U];
-          float pv[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const bool in = b0 + u < b_hi;
-            hv[u] = in ? __ldcg(a.hist + (size_t)(b0 + u) * E + e) : 0;
-            pv[u] = in ? __ldcg(a.psum + (size_t)(b0 + u) * E + e) : 0.f;
+        if (staged) {
+          for (int b = b_lo; b < b_hi; ++b) {
+            cnt += H[b * E + e];
+            ps += PS[b * E + e];
           }
+        } else {
+          constexpr int U = 8;
+          for (int b0 = b_lo; b0 < b_hi; b0 += U) {
+            int hv[U];
+            float pv[U];
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            cnt += hv[u];
-            ps += pv[u];
+            for (int u = 0; u < U; ++u) {
+              const bool in = b0 + u < b_hi;
+              hv[u] = in ? __ldcg(a.hist + (size_t)(b0 + u) * E + e) : 0;
+              pv[u] = in ? __ldcg(a.psum + (size_t)(b0 + u) * E + e) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              cnt += hv[u];
+              ps += pv[u];
+            }
           }
         }
-        S.ppart[part * 256 + e] = ps;
-        S.hpart[part * 256 + e] = cnt;
+        ctl->lps[part][e] = ps;
+        ctl->lcnt[part][e] = cnt;
       }
-    }
-    float l = 0.f;
-    if (warp == 1) {
-      for (int b = lane; b < nb; b += 32) l += __ldcg(a.lse2 + b);
     }
     __syncthreads();
     for (int e = tid; e < E; e += RTHREADS) {
       int cnt = 0;
       float ps = 0.f;
       for (int part = 0; part < parts; ++part) {
-        cnt += S.hpart[part * 256 + e];
-        ps += S.ppart[part * 256 + e];
+        cnt += ctl->lcnt[part][e];
+        ps += ctl->lps[part][e];
       }
       a.counts[e] = cnt;
-      ctl->lbterm[e] = (double)cnt * (double)ps;
+      ctl->lbterm[e] = (float)cnt * ps;
+      if (a.pbase) {  // capacity: the kept count of the expert
+        const int kp = min(cnt, a.cap);
+        a.kept[e] = kp;
+        ctl->hist[e] = kp;
+      }
     }
     if (warp == 1) {
-      double dl = (double)l;
+      float dl = l;
 #pragma unroll
       for (int o = 16; o; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
       if (lane == 0) ctl->red[1] = dl;
     }
-    __syncthreads();
     if (a.pbase) {
-      // dispatch scan: each expert's histogram over the blocks (exclusive: the block's rank base),
-      // kept counts under the capacity, offsets over experts, drops
-      int* H = reinterpret_cast<int*>(smem);  // the pipeline buffers are free
-      {
-        constexpr int U = 16;  // independent loads in flight per thread
-        const int n = nb * E;
-        for (int i0 = tid; i0 < n; i0 += RTHREADS * U) {
-          int hv[U];
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * RTHREADS;
-            hv[u] = i < n ? __ldcg(a.hist + i) : 0;
-          }
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int i = i0 + u * RTHREADS;
-            if (i < n) H[i] = hv[u];
-          }
-        }
-      }
-      __syncthreads();
-      for (int e = tid; e < E; e += RTHREADS) {
+      // dispatch scan: each expert's exclusive scan over the blocks (the block's rank base), one
+      // slice per thread, starting from the sum of the earlier slices
+      const int e = tid % E, part = tid / E;
+      if (part < parts) {
+        const int b_lo = (int)((long)nb * part / parts), b_hi = (int)((long)nb * (part + 1) / parts);
         int run = 0;
-        for (int b = 0; b < nb; ++b) {
-          const int h = H[b * E + e];
+        for (int q = 0; q < part; ++q) run += ctl->lcnt[q][e];
+        for (int b = b_lo; b < b_hi; ++b) {
+          const int h = staged ? H[b * E + e] : __ldcg(a.hist + (size_t)b * E + e);
           a.pbase[(size_t)b * E + e] = run;
           run += h;
         }
-        const int kp = min(run, a.cap);
-        a.kept[e] = kp;
-        ctl->hist[e] = kp;
       }
       __syncthreads();
       if (warp == 2) {  // exclusive scan of the kept counts over experts, 8 per lane
@@ -655,17 +683,22 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         if (lane == 0) a.offsets[0] = 0;
         if (lane == 31) *a.drops = a.T * k - incl;
       }
+    } else {
+      __syncthreads();
     }
     if (warp == 0) {
-      double lb = 0.0;
+      float lb = 0.f;
       for (int e = lane; e < E; e += 32) lb += ctl->lbterm[e];
 #pragma unroll
       for (int o = 16; o; o >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
       if (lane == 0) {
-        const double Tn = (double)a.T;
-        // lb = alpha E sum_e (c_e / (T k)) (psum_e / T);  zl = beta mean_t lse_t^2
-        a.losses[0] = (float)((double)a.lb_coef * E * lb / (Tn * k * Tn));
-        a.losses[1] = (float)((double)a.z_coef * ctl->red[1] / Tn);
+        const float Tn = (float)a.T;
+        // lb = alpha E sum_e (c_e / (T k)) (psum_e / T);  zl = beta mean_t lse_t^2.  All in fp32:
+        // B300's FP64 pipe is narrow and slow enough that a few dependent FP64 operations cost
+        // microseconds here, and fp32 sums of <= 256 expert terms (and of the per-block z
+        // partials) stay within ~1e-5 relative
+        a.losses[0] = a.lb_coef * (float)E * (lb / (Tn * Tn * (float)k));
+        a.losses[1] = a.z_coef * (ctl->red[1] / Tn);
         *a.done = 0;  // ready for the next call
       }
     }
@@ -691,7 +724,18 @@ cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, const RouteA
 
 int route_tc_blocks(int T) { return (T + RM - 1) / RM; }
 
-bool route_tc_fuses_scan(int T, int E) { return T > 0 && (long)route_tc_blocks(T) * E <= kScanSmemInts; }
+// Bytes of the pipeline buffers for E experts and tiles of 128 tokens (the last CTA stages the
+// per-block partials there).
+static long route_stage_region(int E) {
+  const int npad = ((E < 16 ? 16 : E) + 15) / 16 * 16;
+  const int stage_bytes = A_TILE + npad * RBK * 2;
+  const int stages = SMEM_STAGES_BYTES / stage_bytes < MAX_STAGES ? SMEM_STAGES_BYTES / stage_bytes : MAX_STAGES;
+  return (long)stages * stage_bytes;
+}
+
+bool route_tc_fuses_scan(int T, int E) {
+  return T > 0 && E >= 1 && E <= 256 && 8L * route_tc_blocks(T) * E <= route_stage_region(E);
+}
 
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
@@ -717,17 +761,19 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
     const cuuint32_t box[2] = {RBK, (cuuint32_t)npad};
     if (!make_tmap_bf16(&mw, wr, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  const int stage_bytes = A_TILE + npad * RBK * 2;
+  const int xrows = T < RM ? (T + 7) / 8 * 8 : RM;  // a multiple of 8: whole 1024-byte swizzle atoms
+  const int stage_bytes = xrows * RBK * 2 + npad * RBK * 2;
   int stages = SMEM_STAGES_BYTES / stage_bytes;
   if (stages > MAX_STAGES) stages = MAX_STAGES;
-  if ((size_t)stages * stage_bytes < epi_scratch_bytes(E)) return cudaErrorInvalidValue;  // never for E <= 256
-  const size_t smem = (size_t)stages * stage_bytes + sizeof(RouteCtl) + 1024;
+  size_t region = (size_t)stages * stage_bytes;
+  if (region < epi_scratch_bytes(E)) region = (epi_scratch_bytes(E) + 1023) / 1024 * 1024;  // few tokens, many experts
+  const size_t smem = region + sizeof(RouteCtl) + 1024;
   RouteArgs a;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.wr = static_cast<const __nv_bfloat16*>(wr);
   a.lbias = lbias;
-  a.T = T; a.d = d; a.E = E; a.k = k; a.npad = npad; a.stages = stages;
-  a.xrows = T < RM ? (T + 7) / 8 * 8 : RM;
+  a.T = T; a.d = d; a.E = E; a.k = k; a.npad = npad; a.stages = stages; a.region = (int)region;
+  a.xrows = xrows;
   a.topk_idx = topk_idx; a.topk_w = topk_w;
   a.hist = hist; a.psum = psum; a.lse2 = lse2; a.done = done;
   a.counts = counts; a.losses = losses; a.lb_coef = lb_coef; a.z_coef = z_coef;
