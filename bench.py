@@ -36,9 +36,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # source hash matches the one the capture was taken with.
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the routed up-projection, one ncu --set full
-    # capture per workload (second layer pass); valid while gemm_tc.cu and common.cuh hash to src_sha1
-    "flash_bf16": {"bytes": 168043008 + 97550592, "src_sha1": "4c12824bc7e31a772eb43f444c232b1be1313939"},
-    "finegrained_bf16": {"bytes": 939648512 + 190960384, "src_sha1": "4c12824bc7e31a772eb43f444c232b1be1313939"},
+    # capture per workload; valid while gemm_tc.cu and common.cuh hash to src_sha1
+    "flash_bf16": {"bytes": 167972096 + 100669952, "src_sha1": "870db42f187b8f499b602a3517b481edb5018537"},
+    "finegrained_bf16": {"bytes": 940023808 + 190816256, "src_sha1": "870db42f187b8f499b602a3517b481edb5018537"},
+    "decode_bf16": {"bytes": 512892928 + 3781120, "src_sha1": "870db42f187b8f499b602a3517b481edb5018537"},
 }
 
 

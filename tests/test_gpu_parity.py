@@ -41,6 +41,9 @@ CASES = {
                              seed=19, wseed=19),
     "bf16_gelu_shared3": Workload("bf16_gelu_shared3", T=260, d=192, E=5, k=2, dff=256, act="gelu",
                                   dtype="bf16", n_shared=3, seed=21, wseed=21),
+    # enough rows per expert for the paired (2-SM) projections, with non-zero biases and drops
+    "bf16_gelu_bias_pair": Workload("bf16_gelu_bias_pair", T=2100, d=256, E=4, k=2, dff=512, act="gelu",
+                                    dtype="bf16", bias=True, bias_std=0.02, cf=1.05, seed=22, wseed=22),
 }
 
 
