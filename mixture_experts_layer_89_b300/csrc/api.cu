@@ -140,13 +140,14 @@ inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK 
 // scan != NULL: the tensor-core router may also do the dispatch scan (route_tc_fuses_scan).
 moe_status route_impl(const moe_config* c, const void* x, const void* wr, const float* lbias, int32_t* topk_idx,
                       float* topk_w, int32_t* counts, float* losses, void* ws, cudaStream_t st,
-                      const RouteScan* scan = nullptr) {
+                      const RouteScan* scan = nullptr, bool finalize = true) {
   const WsLayout L = layout(c);
   uint32_t* status = at<uint32_t>(ws, L.status);
   if (is_bf16(c)) {  // tensor-core router; the last CTA reduces the partials (counter: status block word 1)
     return cuda_status(launch_route_tc(x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w,
                                        at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
-                                       status + 1, counts, losses, c->lb_coef, c->z_coef, status, st, scan));
+                                       status + 1, counts, losses, c->lb_coef, c->z_coef, status, st, scan,
+                                       finalize));
   }
   MOE_CUDA(launch_route(false, x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w, at<int32_t>(ws, L.r_hist),
                         at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2), status, st));
@@ -323,7 +324,10 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
   scan.kept = at<int32_t>(ws, L.kept);
   scan.offsets = offsets;
   scan.drops = drops;
-  const bool scanned = is_bf16(c) && route_tc_fuses_scan(c->T, c->E);
+  // bf16 layers: the dispatch kernel finalises the router (counts, losses, scan) when the per-block
+  // histograms fit its shared memory; else the router's last CTA does, scan included when it fits
+  const bool dfused = is_bf16(c) && dispatch_fuses_scan(c->T, c->E);
+  const bool scanned = !dfused && is_bf16(c) && route_tc_fuses_scan(c->T, c->E);
   // stage timing (ev) keeps every step on the caller's stream so that each stage is timed alone
   SideStream* side = (!ev && shared_on_side_stream(c)) ? side_stream(st) : nullptr;
   if (side) {
@@ -333,10 +337,19 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
     MOE_CUDA(cudaEventRecord(side->join, side->s));
   }
   MOE_TRY(rec(0));
-  MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st, &scan));
+  MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st,
+                     dfused ? nullptr : &scan, !dfused));
   MOE_TRY(rec(1));
-  MOE_TRY(permute_impl(c, x, topk_idx, counts, offsets, at<int32_t>(ws, L.kept), row_of, at<int32_t>(ws, L.tok_of),
-                       x_perm, drops, ws, st, scanned));
+  if (dfused) {
+    MOE_CUDA(launch_dispatch_fused(true, topk_idx, at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum),
+                                   at<float>(ws, L.r_lse2), c->T, c->E, c->k, scan.cap, c->lb_coef, c->z_coef, x, c->d,
+                                   counts, losses, offsets, at<int32_t>(ws, L.kept), drops, row_of,
+                                   at<int32_t>(ws, L.tok_of), x_perm, (int)a_max_of(c), at<uint32_t>(ws, L.status),
+                                   st));
+  } else {
+    MOE_TRY(permute_impl(c, x, topk_idx, counts, offsets, at<int32_t>(ws, L.kept), row_of, at<int32_t>(ws, L.tok_of),
+                         x_perm, drops, ws, st, scanned));
+  }
   MOE_TRY(rec(2));
   MOE_TRY(ffn_routed_impl(c, x_perm, offsets, w, y_perm, ws, st, ev ? ev[3] : nullptr));
   MOE_TRY(rec(4));
@@ -497,7 +510,8 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   const bool tokens = cfg->T > 0;
   if (is_bf16(cfg)) n += tokens ? 1 : 0;      // tensor-core router (finalize fused; T = 0: memsets only)
   else n += tokens ? 2 : 1;                   // router + finalize
-  const bool scanned = is_bf16(cfg) && route_tc_fuses_scan(cfg->T, cfg->E);
+  const bool dfused = is_bf16(cfg) && dispatch_fuses_scan(cfg->T, cfg->E);
+  const bool scanned = dfused || (is_bf16(cfg) && route_tc_fuses_scan(cfg->T, cfg->E));
   if (!tokens) n += 1;                        // scan (writes zero offsets)
   else n += (scanned ? 0 : 2) + dispatch_launches(true, cfg->d, is_bf16(cfg) ? 2 : 4);  // [hist, scan,] dispatch
   if (a_max_of(cfg) > 0) n += 2;              // routed up + down projections

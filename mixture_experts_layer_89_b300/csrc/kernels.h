@@ -33,7 +33,7 @@ bool route_tc_fuses_scan(int T, int E);
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
-                            cudaStream_t st, const RouteScan* scan);
+                            cudaStream_t st, const RouteScan* scan, bool finalize = true);
 // Reduces the per-CTA partials: counts [E] and losses [2].
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,
                                   int k, float lb_coef, float z_coef, int32_t* counts, float* losses,
@@ -51,6 +51,17 @@ cudaError_t launch_perm_scan(const int32_t* phist, int npb, const int32_t* count
 cudaError_t launch_dispatch(bool bf16, const int32_t* topk_idx, const int32_t* pbase, const int32_t* offsets, int T,
                             int E, int k, int cap, const void* x, int d, int32_t* row_of, int32_t* tok_of,
                             void* x_perm, int max_rows, uint32_t* status, cudaStream_t st);
+// Dispatch that also finalises the router (bf16 layers): the router ran with finalize = false and
+// left its per-block partials (hist, psum [nb][E], lse2 [nb]); every dispatch CTA stages the
+// histograms, derives its rank bases, the kept counts and the offsets, and CTA 0 also writes
+// offsets, kept, drops, counts and both losses.  Usable when dispatch_fuses_scan(T, E).
+bool dispatch_fuses_scan(int T, int E);
+cudaError_t launch_dispatch_fused(bool bf16, const int32_t* topk_idx, const int32_t* hist, const float* psum,
+                                  const float* lse2, int T, int E, int k, int cap, float lb_coef, float z_coef,
+                                  const void* x, int d, int32_t* counts, float* losses, int32_t* offsets,
+                                  int32_t* kept, int32_t* drops, int32_t* row_of, int32_t* tok_of, void* x_perm,
+                                  int max_rows, uint32_t* status, cudaStream_t st);
+
 // Kernels launch_dispatch launches (2 with the row copy, else 1).
 int dispatch_launches(bool with_rows, int d, int elt_bytes);
 

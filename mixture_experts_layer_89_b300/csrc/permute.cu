@@ -14,11 +14,35 @@
 // gathers x into x_perm.
 #include "common.cuh"
 #include "kernels.h"
+#include "route_losses.cuh"
 
 namespace moe {
 
 namespace {
 constexpr int PT = kPermTokens;
+
+// Ranks one block's assignments in token order from the per-expert rank bases in run[] (warp 0;
+// equal experts inside a 32-wide chunk ranked with __match_any_sync); row = offsets[e] + rank while
+// the rank is under the capacity, else -1 (dropped).
+__device__ __forceinline__ void rank_block(const int* eidx, int na, int* run, const int* offs, int cap, int* rows) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < na; c0 += 32) {
+    const int a = c0 + lane;
+    const int e = a < na ? eidx[a] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int row = -1;
+    if (e >= 0) {
+      const int r = run[e] + __popc(peers & lt_mask);
+      if (r < cap) row = offs[e] + r;
+    }
+    __syncwarp();
+    if (e >= 0 && (__ffs(peers) - 1) == lane) run[e] += __popc(peers);
+    __syncwarp();
+    if (a < na) rows[a] = row;
+  }
+}
+
 
 __global__ void __launch_bounds__(256) k_perm_hist(const int32_t* __restrict__ topk_idx, int Tn, int E, int k,
                                                    int32_t* __restrict__ phist, uint32_t* status) {
@@ -94,7 +118,7 @@ __global__ void __launch_bounds__(256) k_dispatch(const int32_t* __restrict__ to
   __shared__ int run[256];
   __shared__ int eidx[PT * KMAX];
   __shared__ int rows[PT * KMAX];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int t0 = blockIdx.x * PT;
   const int nt = min(PT, Tn - t0), na = nt * k;
   for (int e = tid; e < E; e += 256) run[e] = pbase[(size_t)blockIdx.x * E + e];
@@ -107,23 +131,7 @@ __global__ void __launch_bounds__(256) k_dispatch(const int32_t* __restrict__ to
     eidx[i] = e;
   }
   __syncthreads();
-  if (warp == 0) {
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int c0 = 0; c0 < na; c0 += 32) {
-      const int a = c0 + lane;
-      const int e = a < na ? eidx[a] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      int row = -1;
-      if (e >= 0) {
-        const int r = run[e] + __popc(peers & lt_mask);
-        if (r < cap) row = offsets[e] + r;
-      }
-      __syncwarp();
-      if (e >= 0 && (__ffs(peers) - 1) == lane) run[e] += __popc(peers);
-      __syncwarp();
-      if (a < na) rows[a] = row;
-    }
-  }
+  if (warp == 0) rank_block(eidx, na, run, offsets, cap, rows);
   __syncthreads();
   for (int i = tid; i < na; i += 256) {
     const int row = rows[i];
@@ -132,13 +140,144 @@ __global__ void __launch_bounds__(256) k_dispatch(const int32_t* __restrict__ to
   }
 }
 
+// Per-block histograms staged by the fused dispatch: at most this many (blocks x experts) ints.
+constexpr int kDispatchScanInts = 16384;
+
+struct DispatchFusedArgs {
+  const int32_t* topk_idx;
+  const int32_t* hist;  // [nb][E] router per-block expert histograms
+  const float* psum;    // [nb][E] router per-block sums of P
+  const float* lse2;    // [nb]
+  int T, E, k, cap;
+  float lb_coef, z_coef;
+  int32_t* counts;
+  float* losses;
+  int32_t* offsets;
+  int32_t* kept;
+  int32_t* drops;
+  int32_t* row_of;
+  int32_t* tok_of;
+  uint32_t* status;
+};
+
+// One CTA per block of PT tokens.  Every CTA stages all per-block histograms in shared memory and
+// derives what the router's last CTA would otherwise compute for it: its rank base per expert
+// (the sum over the earlier blocks), the kept counts under the capacity and the offsets (exclusive
+// scan over experts).  CTA 0 also writes offsets, kept, drops, and the counts and losses (the same
+// reduction, in the same order, as the router's last CTA).
+template <int KMAX>
+__global__ void __launch_bounds__(256) k_dispatch_fused(const DispatchFusedArgs a) {
+  extern __shared__ int H[];  // [nb][E]
+  __shared__ int run[256];
+  __shared__ int kp_s[256];
+  __shared__ int offs[257];
+  __shared__ int eidx[PT * KMAX];
+  __shared__ int rows[PT * KMAX];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.x, nb = gridDim.x, E = a.E, k = a.k;
+  const int n = nb * E;
+  const int t0 = b * PT;
+  const int nt = min(PT, a.T - t0), na = nt * k;
+  {
+    constexpr int U = 16;  // independent loads in flight per thread
+    for (int i0 = tid; i0 < n; i0 += 256 * U) {
+      int hv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * 256;
+        hv[u] = i < n ? __ldg(a.hist + i) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * 256;
+        if (i < n) H[i] = hv[u];
+      }
+    }
+  }
+  for (int i = tid; i < na; i += 256) {
+    int e = a.topk_idx[(size_t)t0 * k + i];
+    if (e < 0 || e >= E) {
+      atomicOr(a.status, DEV_BADINDEX);
+      e = -1;
+    }
+    eidx[i] = e;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) {
+    int base = 0, tot = 0;
+    for (int bb = 0; bb < nb; ++bb) {
+      const int h = H[bb * E + e];
+      base += bb < b ? h : 0;
+      tot += h;
+    }
+    run[e] = base;
+    kp_s[e] = min(tot, a.cap);
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the kept counts over experts, 8 per lane
+    int v[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      v[i] = e < E ? kp_s[e] : 0;
+      sum += v[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int r = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < E) offs[e] = r;
+      r += v[i];
+    }
+    if (lane == 31) offs[E] = incl;
+  }
+  __syncthreads();
+  if (warp == 0) rank_block(eidx, na, run, offs, a.cap, rows);
+  __syncthreads();
+  for (int i = tid; i < na; i += 256) {
+    const int row = rows[i];
+    a.row_of[(size_t)t0 * k + i] = row;
+    if (row >= 0) a.tok_of[row] = t0 + i / k;
+  }
+  if (b == 0) {
+    for (int e = tid; e <= E; e += 256) a.offsets[e] = offs[e];
+    for (int e = tid; e < E; e += 256) a.kept[e] = kp_s[e];
+    if (tid == 0) *a.drops = a.T * k - offs[E];
+  }
+}
+
+// Counts and losses of a layer whose router left them to the dispatch: reduced by block 0 of the
+// row gather (thousands of blocks), off the critical path of the dispatch ranks.
+struct LossArgs {
+  const int32_t* hist;
+  const float* psum;
+  const float* lse2;
+  int nb, E, k, T;
+  float lb_coef, z_coef;
+  int32_t* counts;
+  float* losses;
+};
+
 // x_perm[r] = x[tok_of[r]] for r < n_rows (device count); one warp per row, 16-byte vectors, a
 // grid far larger than the SM count so that many loads are in flight.  The rows are written with
 // streaming (evict-first) stores so that they do not push x, which every one of its k rows
 // re-reads, out of L2.
+template <bool LOSSES>
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ tok_of,
                                                      const int32_t* __restrict__ n_rows_dev, int max_rows,
-                                                     int row_vecs, uint4* __restrict__ x_perm) {
+                                                     int row_vecs, uint4* __restrict__ x_perm, const LossArgs la) {
+  if constexpr (LOSSES) {
+    __shared__ LossScratch sc;
+    if (blockIdx.x == 0)
+      route_losses<true, true>(la.hist, la.psum, la.lse2, la.nb, la.E, la.k, la.T, la.lb_coef, la.z_coef, nullptr,
+                               la.counts, la.losses, sc);
+  }
   const int n_rows = min(*n_rows_dev, max_rows);
   const int warps = gridDim.x * 8;
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < n_rows; r += warps) {
@@ -180,6 +319,68 @@ cudaError_t launch_perm_scan(const int32_t* phist, int npb, const int32_t* count
   return cudaGetLastError();
 }
 
+bool dispatch_fuses_scan(int T, int E) {
+  return T > 0 && E >= 1 && E <= 256 && (long)perm_blocks(T) * E <= kDispatchScanInts;
+}
+
+namespace {
+template <int KMAX>
+cudaError_t launch_fused_k(const DispatchFusedArgs& a, int nb, cudaStream_t st) {
+  const size_t smem = sizeof(int) * (size_t)nb * a.E;
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(k_dispatch_fused<KMAX>), smem);
+  if (err != cudaSuccess) return err;
+  k_dispatch_fused<KMAX><<<nb, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(bool bf16, const void* x, int d, const int32_t* tok_of, const int32_t* n_rows, void* x_perm,
+                          int max_rows, cudaStream_t st, const LossArgs* la = nullptr) {
+  const size_t row_bytes = (size_t)d * (bf16 ? 2 : 4);
+  int blocks = (max_rows + 7) / 8;
+  if (blocks > 148 * 32) blocks = 148 * 32;
+  if (la && row_bytes % 16 != 0) return cudaErrorInvalidValue;
+  if (la)
+    k_gather_rows<true><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, n_rows, max_rows,
+                                                (int)(row_bytes / 16), static_cast<uint4*>(x_perm), *la);
+  else if (row_bytes % 16 == 0)
+    k_gather_rows<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, n_rows, max_rows,
+                                                 (int)(row_bytes / 16), static_cast<uint4*>(x_perm), LossArgs{});
+  else if (bf16)
+    k_gather_rows_scalar<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), tok_of, n_rows,
+                                                                max_rows, d, static_cast<__nv_bfloat16*>(x_perm));
+  else
+    k_gather_rows_scalar<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(x), tok_of, n_rows, max_rows, d,
+                                                        static_cast<float*>(x_perm));
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_dispatch_fused(bool bf16, const int32_t* topk_idx, const int32_t* hist, const float* psum,
+                                  const float* lse2, int T, int E, int k, int cap, float lb_coef, float z_coef,
+                                  const void* x, int d, int32_t* counts, float* losses, int32_t* offsets,
+                                  int32_t* kept, int32_t* drops, int32_t* row_of, int32_t* tok_of, void* x_perm,
+                                  int max_rows, uint32_t* status, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (!dispatch_fuses_scan(T, E) || k < 1 || k > 8 || !x_perm || ((size_t)d * (bf16 ? 2 : 4)) % 16 != 0)
+    return cudaErrorInvalidValue;
+  DispatchFusedArgs a;
+  a.topk_idx = topk_idx; a.hist = hist; a.psum = psum; a.lse2 = lse2;
+  a.T = T; a.E = E; a.k = k; a.cap = cap; a.lb_coef = lb_coef; a.z_coef = z_coef;
+  a.counts = counts; a.losses = losses; a.offsets = offsets; a.kept = kept; a.drops = drops;
+  a.row_of = row_of; a.tok_of = tok_of; a.status = status;
+  const int nb = perm_blocks(T);
+  cudaError_t e;
+  if (k <= 2) e = launch_fused_k<2>(a, nb, st);
+  else if (k <= 4) e = launch_fused_k<4>(a, nb, st);
+  else e = launch_fused_k<8>(a, nb, st);
+  if (e != cudaSuccess) return e;
+  LossArgs la;
+  la.hist = hist; la.psum = psum; la.lse2 = lse2; la.nb = nb; la.E = E; la.k = k; la.T = T;
+  la.lb_coef = lb_coef; la.z_coef = z_coef; la.counts = counts; la.losses = losses;
+  // the gather's block 0 reduces the losses, so it runs even when no row can be kept
+  return launch_gather(bf16, x, d, tok_of, offsets + E, x_perm, max_rows > 0 ? max_rows : 1, st, &la);
+}
+
 int dispatch_launches(bool with_rows, int d, int elt_bytes) {
   (void)d;
   (void)elt_bytes;
@@ -199,20 +400,7 @@ cudaError_t launch_dispatch(bool bf16, const int32_t* topk_idx, const int32_t* p
     k_dispatch<8><<<nb, 256, 0, st>>>(topk_idx, pbase, offsets, T, E, k, cap, row_of, tok_of, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !x_perm || max_rows <= 0) return e;
-  const size_t row_bytes = (size_t)d * (bf16 ? 2 : 4);
-  int blocks = (max_rows + 7) / 8;
-  if (blocks > 148 * 32) blocks = 148 * 32;
-  if (row_bytes % 16 == 0)
-    k_gather_rows<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, offsets + E, max_rows,
-                                          (int)(row_bytes / 16), static_cast<uint4*>(x_perm));
-  else if (bf16)
-    k_gather_rows_scalar<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), tok_of,
-                                                                offsets + E, max_rows, d,
-                                                                static_cast<__nv_bfloat16*>(x_perm));
-  else
-    k_gather_rows_scalar<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(x), tok_of, offsets + E, max_rows,
-                                                        d, static_cast<float*>(x_perm));
-  return cudaGetLastError();
+  return launch_gather(bf16, x, d, tok_of, offsets + E, x_perm, max_rows, st);
 }
 
 }  // namespace moe

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route_losses.cuh"
 
 namespace moe {
 
@@ -49,7 +50,7 @@ constexpr float kBandFloor = 2e-5f;
 constexpr float kBadLogit = -3.0e38f;
 
 enum : int { F_FEW = 2, F_ALL = 4, F_BAD = 8 };
-constexpr int PPARTS_LAST = 8;
+
 
 struct RouteCtl {
   uint64_t full[MAX_STAGES];
@@ -68,10 +69,7 @@ struct RouteCtl {
   int flags[RM];
   int ncand[RM];
   float lse2w[RWARPS];
-  float lbterm[256];
-  float red[RWARPS];
-  int lcnt[PPARTS_LAST][256];   // last CTA: per-slice counts and sums of P
-  float lps[PPARTS_LAST][256];
+  LossScratch ls;     // last CTA: slices of the per-block partials
 };
 
 // Epilogue scratch laid over the pipeline buffers once the main loop is done.
@@ -82,12 +80,11 @@ struct EpiScratch {
   int* tle;          // [2][RM][KLMAX]
   float* cexact;     // [RM][CMAX] recomputed logits of near-tie candidates
   float* ppart;      // [PPARTS][256] partial column sums
-  int* hpart;        // [PPARTS][256] partial counts (last CTA)
   uint16_t* pairs;   // [RM*CMAX] (row << 4) | candidate slot
   uint8_t* cand;     // [RM][CMAX] candidate experts, ascending
 };
 __host__ __device__ inline size_t epi_scratch_bytes(int E) {
-  return (size_t)RM * (E + 1) * 4 + 2 * (size_t)RM * KLMAX * 8 + (size_t)RM * CMAX * 4 + 2 * (size_t)PPARTS * 256 * 4 +
+  return (size_t)RM * (E + 1) * 4 + 2 * (size_t)RM * KLMAX * 8 + (size_t)RM * CMAX * 4 + (size_t)PPARTS * 256 * 4 +
          (size_t)RM * CMAX * (2 + 1);
 }
 __device__ inline EpiScratch epi_scratch(uint8_t* base, int E) {
@@ -97,8 +94,7 @@ __device__ inline EpiScratch epi_scratch(uint8_t* base, int E) {
   s.tle = reinterpret_cast<int*>(s.tlv + 2 * RM * KLMAX);
   s.cexact = reinterpret_cast<float*>(s.tle + 2 * RM * KLMAX);
   s.ppart = s.cexact + RM * CMAX;
-  s.hpart = reinterpret_cast<int*>(s.ppart + PPARTS * 256);
-  s.pairs = reinterpret_cast<uint16_t*>(s.hpart + PPARTS * 256);
+  s.pairs = reinterpret_cast<uint16_t*>(s.ppart + PPARTS * 256);
   s.cand = reinterpret_cast<uint8_t*>(s.pairs + RM * CMAX);
   return s;
 }
@@ -109,6 +105,7 @@ struct RouteArgs {
   const float* lbias;
   int T, d, E, k, npad, stages;
   int region;  // bytes before RouteCtl: the stages, or the epilogue scratch if that is larger
+  int finalize;  // 1: the last CTA computes counts and losses (and the dispatch scan with pbase)
   int xrows;  // rows of the x box: 128, or fewer (a multiple of 8) when the layer has fewer tokens
   int32_t* topk_idx;
   float* topk_w;
@@ -546,125 +543,49 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     a.hist[(size_t)blockIdx.x * E + e] = ctl->hist[e];
   }
   if (tid == 0) a.lse2[blockIdx.x] = ((ctl->lse2w[0] + ctl->lse2w[1]) + ctl->lse2w[2]) + ctl->lse2w[3];
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) ctl->is_last = (atomicAdd(a.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  if (a.finalize) {  // the last CTA to get here reduces every CTA's partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) ctl->is_last = (atomicAdd(a.done, 1u) == gridDim.x - 1) ? 1 : 0;
+  } else if (tid == 0) {
+    ctl->is_last = 0;  // the fused dispatch kernel reduces them
+  }
   __syncthreads();
 
   // ------------------------------------------------------------------ last CTA: counts and losses
   if (ctl->is_last) {
     __threadfence();
     const int nb = gridDim.x;
-    const int n = nb * E;
-    // Expert e's blocks are cut into `parts` slices with fixed boundaries; each slice is summed in
-    // block order and the slices in slice order, so the sums do not depend on scheduling.  When the
-    // per-block partials fit in the (now free) pipeline buffers they are first loaded there with
-    // many loads in flight, and the dispatch scan runs over the slices in parallel.
-    const bool staged = 8L * n <= (long)a.region;
-    int* H = reinterpret_cast<int*>(smem);             // [nb][E] per-block counts
-    float* PS = reinterpret_cast<float*>(smem) + n;    // [nb][E] per-block sums of P
-    float l = 0.f;
-    if (staged) {
-      constexpr int U = 16;  // independent loads in flight per thread
-      for (int i0 = tid; i0 < n; i0 += RTHREADS * U) {
-        int hv[U];
-        float pv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = i0 + u * RTHREADS;
-          hv[u] = i < n ? __ldcg(a.hist + i) : 0;
-          pv[u] = i < n ? __ldcg(a.psum + i) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = i0 + u * RTHREADS;
-          if (i < n) {
-            H[i] = hv[u];
-            PS[i] = pv[u];
-          }
-        }
-      }
-    }
-    if (warp == 1) {
-      for (int b = lane; b < nb; b += 32) l += __ldcg(a.lse2 + b);
-    }
-    __syncthreads();
-    {
-      const int e = tid % E, part = tid / E;
-      if (part < parts) {
-        const int b_lo = (int)((long)nb * part / parts), b_hi = (int)((long)nb * (part + 1) / parts);
-        int cnt = 0;
-        float ps = 0.f;
-        if (staged) {
-          for (int b = b_lo; b < b_hi; ++b) {
-            cnt += H[b * E + e];
-            ps += PS[b * E + e];
-          }
-        } else {
-          constexpr int U = 8;
-          for (int b0 = b_lo; b0 < b_hi; b0 += U) {
-            int hv[U];
-            float pv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const bool in = b0 + u < b_hi;
-              hv[u] = in ? __ldcg(a.hist + (size_t)(b0 + u) * E + e) : 0;
-              pv[u] = in ? __ldcg(a.psum + (size_t)(b0 + u) * E + e) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-              cnt += hv[u];
-              ps += pv[u];
-            }
-          }
-        }
-        ctl->lps[part][e] = ps;
-        ctl->lcnt[part][e] = cnt;
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += RTHREADS) {
-      int cnt = 0;
-      float ps = 0.f;
-      for (int part = 0; part < parts; ++part) {
-        cnt += ctl->lcnt[part][e];
-        ps += ctl->lps[part][e];
-      }
-      a.counts[e] = cnt;
-      ctl->lbterm[e] = (float)cnt * ps;
-      if (a.pbase) {  // capacity: the kept count of the expert
-        const int kp = min(cnt, a.cap);
-        a.kept[e] = kp;
-        ctl->hist[e] = kp;
-      }
-    }
-    if (warp == 1) {
-      float dl = l;
-#pragma unroll
-      for (int o = 16; o; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
-      if (lane == 0) ctl->red[1] = dl;
-    }
+    route_losses<true, true>(a.hist, a.psum, a.lse2, nb, E, k, a.T, a.lb_coef, a.z_coef, ctl->hist, a.counts,
+                             a.losses, ctl->ls);
     if (a.pbase) {
       // dispatch scan: each expert's exclusive scan over the blocks (the block's rank base), one
-      // slice per thread, starting from the sum of the earlier slices
+      // slice per thread starting from the earlier slices' counts; kept counts under the capacity;
+      // offsets over experts; drops
+      const int parts = loss_parts(E);
       const int e = tid % E, part = tid / E;
       if (part < parts) {
         const int b_lo = (int)((long)nb * part / parts), b_hi = (int)((long)nb * (part + 1) / parts);
         int run = 0;
-        for (int q = 0; q < part; ++q) run += ctl->lcnt[q][e];
-        for (int b = b_lo; b < b_hi; ++b) {
-          const int h = staged ? H[b * E + e] : __ldcg(a.hist + (size_t)b * E + e);
-          a.pbase[(size_t)b * E + e] = run;
+        for (int q = 0; q < part; ++q) run += ctl->ls.lcnt[q][e];
+        for (int bb = b_lo; bb < b_hi; ++bb) {
+          const int h = __ldcg(a.hist + (size_t)bb * E + e);
+          a.pbase[(size_t)bb * E + e] = run;
           run += h;
         }
+      }
+      for (int ee = tid; ee < E; ee += RTHREADS) {
+        const int kp = min(ctl->hist[ee], a.cap);
+        a.kept[ee] = kp;
+        ctl->hist[ee] = kp;
       }
       __syncthreads();
       if (warp == 2) {  // exclusive scan of the kept counts over experts, 8 per lane
         int v[8], sum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int e = lane * 8 + i;
-          v[i] = e < E ? ctl->hist[e] : 0;
+          const int ee = lane * 8 + i;
+          v[i] = ee < E ? ctl->hist[ee] : 0;
           sum += v[i];
         }
         int incl = sum;
@@ -676,32 +597,15 @@ __global__ void __launch_bounds__(RTHREADS, 1)
         int run = incl - sum;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int e = lane * 8 + i;
+          const int ee = lane * 8 + i;
           run += v[i];
-          if (e < E) a.offsets[e + 1] = run;
+          if (ee < E) a.offsets[ee + 1] = run;
         }
         if (lane == 0) a.offsets[0] = 0;
         if (lane == 31) *a.drops = a.T * k - incl;
       }
-    } else {
-      __syncthreads();
     }
-    if (warp == 0) {
-      float lb = 0.f;
-      for (int e = lane; e < E; e += 32) lb += ctl->lbterm[e];
-#pragma unroll
-      for (int o = 16; o; o >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
-      if (lane == 0) {
-        const float Tn = (float)a.T;
-        // lb = alpha E sum_e (c_e / (T k)) (psum_e / T);  zl = beta mean_t lse_t^2.  All in fp32:
-        // B300's FP64 pipe is narrow and slow enough that a few dependent FP64 operations cost
-        // microseconds here, and fp32 sums of <= 256 expert terms (and of the per-block z
-        // partials) stay within ~1e-5 relative
-        a.losses[0] = a.lb_coef * (float)E * (lb / (Tn * Tn * (float)k));
-        a.losses[1] = a.z_coef * (ctl->red[1] / Tn);
-        *a.done = 0;  // ready for the next call
-      }
-    }
+    if (tid == 0) *a.done = 0;  // ready for the next call
   }
 
   tc_fence_before();
@@ -740,7 +644,7 @@ bool route_tc_fuses_scan(int T, int E) {
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
-                            cudaStream_t st, const RouteScan* scan) {
+                            cudaStream_t st, const RouteScan* scan, bool finalize) {
   if (T <= 0) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (e != cudaSuccess) return e;
@@ -779,7 +683,8 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   a.counts = counts; a.losses = losses; a.lb_coef = lb_coef; a.z_coef = z_coef;
   a.band_scale = ldexpf((float)d / 16.f, -22);
   a.status = status;
-  const bool fuse = scan && route_tc_fuses_scan(T, E);
+  a.finalize = finalize ? 1 : 0;
+  const bool fuse = finalize && scan && route_tc_fuses_scan(T, E);
   a.cap = fuse ? scan->cap : 0;
   a.pbase = fuse ? scan->pbase : nullptr;
   a.kept = fuse ? scan->kept : nullptr;
