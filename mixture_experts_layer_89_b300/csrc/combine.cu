@@ -36,6 +36,8 @@ template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y_perm, const int32_t* __restrict__ row_of,
                                                  const float* __restrict__ topk_w, const float* __restrict__ y_shared,
                                                  T* __restrict__ y, int Tn, int d, int k) {
+  pdl_trigger();
+  pdl_wait();
   const int nch = (d + 255) / 256;
   const long items = (long)Tn * nch;
   const long warps = (long)gridDim.x * 8;
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(256) k_combine_scalar(const float* __restrict_
                                                         const float* __restrict__ topk_w,
                                                         const float* __restrict__ y_shared, T* __restrict__ y, int Tn,
                                                         int d, int k) {
+  pdl_trigger();
+  pdl_wait();
   const int warps = gridDim.x * 8;
   for (int t = blockIdx.x * 8 + (threadIdx.x >> 5); t < Tn; t += warps) {
     for (int c = threadIdx.x & 31; c < d; c += 32) {
@@ -102,16 +106,11 @@ cudaError_t launch_t(const float* y_perm, const int32_t* row_of, const float* to
   int blocks = (int)((items + 7) / 8);
   if (blocks > 148 * 32) blocks = 148 * 32;
   T* yo = static_cast<T*>(y);
-  if (d % 8 != 0) {
-    k_combine_scalar<T><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
-  } else if (k <= 2) {
-    k_combine<T, 2><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
-  } else if (k <= 4) {
-    k_combine<T, 4><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
-  } else {
-    k_combine<T, 8><<<blocks, 256, 0, st>>>(y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
-  }
-  return cudaGetLastError();
+  const dim3 g(blocks), b(256);
+  if (d % 8 != 0) return launch_pdl(k_combine_scalar<T>, g, b, 0, st, y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
+  if (k <= 2) return launch_pdl(k_combine<T, 2>, g, b, 0, st, y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
+  if (k <= 4) return launch_pdl(k_combine<T, 4>, g, b, 0, st, y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
+  return launch_pdl(k_combine<T, 8>, g, b, 0, st, y_perm, row_of, topk_w, y_shared, yo, Tn, d, k);
 }
 }  // namespace
 

@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
   const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const bool leader = crank == 0;  // PAIR: the even CTA issues the 2-SM MMAs
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -211,6 +212,9 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       tmem_relinquish();
     }
   }
+  // the set-up above overlaps the previous kernel's tail; the offsets, the A rows and every output
+  // buffer belong to earlier kernels from here on
+  pdl_wait();
   if (warp == 3) {
     // unit prefix over groups: lane owns groups [8 lane, 8 lane + 8)
     int cnt[8];
@@ -625,22 +629,21 @@ cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mA32, const CUten
   constexpr size_t smem = smem_total(OUTF32, EPIW);
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (!PAIR) {
-    kern<<<(unsigned)grid, threads, smem, st>>>(mA, mA32, mB0, mB1, mO, a);
-    return cudaGetLastError();
-  }
+  if (!PAIR) return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, st, mA, mA32, mB0, mB1, mO, a);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, mA, mA32, mB0, mB1, mO, a);
 }
 

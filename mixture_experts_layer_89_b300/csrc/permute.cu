@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(256) k_dispatch_fused(const DispatchFusedArgs 
   const int n = nb * E;
   const int t0 = b * PT;
   const int nt = min(PT, a.T - t0), na = nt * k;
+  pdl_trigger();
+  pdl_wait();
   {
     constexpr int U = 16;  // independent loads in flight per thread
     for (int i0 = tid; i0 < n; i0 += 256 * U) {
@@ -272,6 +274,8 @@ template <bool LOSSES>
 __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ x, const int32_t* __restrict__ tok_of,
                                                      const int32_t* __restrict__ n_rows_dev, int max_rows,
                                                      int row_vecs, uint4* __restrict__ x_perm, const LossArgs la) {
+  pdl_trigger();
+  pdl_wait();
   if constexpr (LOSSES) {
     __shared__ LossScratch sc;
     if (blockIdx.x == 0)
@@ -294,6 +298,8 @@ __global__ void __launch_bounds__(256) k_gather_rows_scalar(const T* __restrict_
                                                             const int32_t* __restrict__ tok_of,
                                                             const int32_t* __restrict__ n_rows_dev, int max_rows,
                                                             int d, T* __restrict__ x_perm) {
+  pdl_trigger();
+  pdl_wait();
   const int n_rows = min(*n_rows_dev, max_rows);
   const int warps = gridDim.x * 8;
   for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < n_rows; r += warps) {
@@ -329,8 +335,7 @@ cudaError_t launch_fused_k(const DispatchFusedArgs& a, int nb, cudaStream_t st) 
   const size_t smem = sizeof(int) * (size_t)nb * a.E;
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(k_dispatch_fused<KMAX>), smem);
   if (err != cudaSuccess) return err;
-  k_dispatch_fused<KMAX><<<nb, 256, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_dispatch_fused<KMAX>, dim3(nb), dim3(256), smem, st, a);
 }
 
 cudaError_t launch_gather(bool bf16, const void* x, int d, const int32_t* tok_of, const int32_t* n_rows, void* x_perm,
@@ -339,19 +344,18 @@ cudaError_t launch_gather(bool bf16, const void* x, int d, const int32_t* tok_of
   int blocks = (max_rows + 7) / 8;
   if (blocks > 148 * 32) blocks = 148 * 32;
   if (la && row_bytes % 16 != 0) return cudaErrorInvalidValue;
+  const dim3 g(blocks), b(256);
   if (la)
-    k_gather_rows<true><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, n_rows, max_rows,
-                                                (int)(row_bytes / 16), static_cast<uint4*>(x_perm), *la);
-  else if (row_bytes % 16 == 0)
-    k_gather_rows<false><<<blocks, 256, 0, st>>>(static_cast<const uint4*>(x), tok_of, n_rows, max_rows,
-                                                 (int)(row_bytes / 16), static_cast<uint4*>(x_perm), LossArgs{});
-  else if (bf16)
-    k_gather_rows_scalar<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(x), tok_of, n_rows,
-                                                                max_rows, d, static_cast<__nv_bfloat16*>(x_perm));
-  else
-    k_gather_rows_scalar<float><<<blocks, 256, 0, st>>>(static_cast<const float*>(x), tok_of, n_rows, max_rows, d,
-                                                        static_cast<float*>(x_perm));
-  return cudaGetLastError();
+    return launch_pdl(k_gather_rows<true>, g, b, 0, st, static_cast<const uint4*>(x), tok_of, n_rows, max_rows,
+                      (int)(row_bytes / 16), static_cast<uint4*>(x_perm), *la);
+  if (row_bytes % 16 == 0)
+    return launch_pdl(k_gather_rows<false>, g, b, 0, st, static_cast<const uint4*>(x), tok_of, n_rows, max_rows,
+                      (int)(row_bytes / 16), static_cast<uint4*>(x_perm), LossArgs{});
+  if (bf16)
+    return launch_pdl(k_gather_rows_scalar<__nv_bfloat16>, g, b, 0, st, static_cast<const __nv_bfloat16*>(x), tok_of,
+                      n_rows, max_rows, d, static_cast<__nv_bfloat16*>(x_perm));
+  return launch_pdl(k_gather_rows_scalar<float>, g, b, 0, st, static_cast<const float*>(x), tok_of, n_rows, max_rows,
+                    d, static_cast<float*>(x_perm));
 }
 }  // namespace
 

@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const int nvalid = min(RM, a.T - t0);  // rows of the tile that are tokens
   uint32_t tmem_cols = 32;
   while ((int)tmem_cols < a.npad) tmem_cols <<= 1;
+  pdl_trigger();
 
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -234,6 +235,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     tmem_alloc(smem_u32(&ctl->tmem_base), tmem_cols);
     tmem_relinquish();
   }
+  // the set-up above overlaps the previous kernel's tail; x, the logit bias and every output buffer
+  // belong to earlier kernels from here on
+  pdl_wait();
   if (warp == 3) {
     if (lane == 0) ctl->npairs = 0;
     for (int e = lane; e < 256; e += 32) {
@@ -621,8 +625,7 @@ cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, const RouteA
                       cudaStream_t st) {
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(k_route_tc<KL>), smem);
   if (err != cudaSuccess) return err;
-  k_route_tc<KL><<<nb, RTHREADS, smem, st>>>(mx, mw, a);
-  return cudaGetLastError();
+  return launch_pdl(k_route_tc<KL>, dim3(nb), dim3(RTHREADS), smem, st, mx, mw, a);
 }
 }  // namespace
 
