@@ -106,6 +106,8 @@ struct RouteArgs {
   int T, d, E, k, npad, stages;
   int region;  // bytes before RouteCtl: the stages, or the epilogue scratch if that is larger
   int finalize;  // 1: the last CTA computes counts and losses (and the dispatch scan with pbase)
+  int split;     // CTAs per tile (a cluster), each over a slice of the k-blocks
+  int pofs;      // split > 1: byte offset of the partial logits [128][E] in the pipeline buffers
   int xrows;  // rows of the x box: 128, or fewer (a multiple of 8) when the layer has fewer tokens
   int32_t* topk_idx;
   float* topk_w;
@@ -212,7 +214,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = a.E, k = a.k;
   const int kblocks = a.d / RBK;
-  const int t0 = blockIdx.x * RM;
+  // split > 1: a cluster of `split` CTAs shares one tile, each CTA accumulating its own slice of
+  // the k-blocks; the cluster's rank 0 sums the partial logits and does the rest alone
+  const int split = a.split;
+  const int crank = split > 1 ? (int)cluster_ctarank() : 0;
+  const int tile = (int)blockIdx.x / split;
+  const int ntiles = (int)gridDim.x / split;
+  const int kb_lo = kblocks * crank / split, kb_hi = kblocks * (crank + 1) / split;
+  const int t0 = tile * RM;
   const int nvalid = min(RM, a.T - t0);  // rows of the tile that are tokens
   uint32_t tmem_cols = 32;
   while ((int)tmem_cols < a.npad) tmem_cols <<= 1;
@@ -258,9 +267,10 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     bool aborted = false;
     // every CTA reads all of W_r: start each at a different k-block so that they do not all ask
     // the same L2 lines for the same tile at the same moment
-    const int kb0 = (int)(blockIdx.x % (unsigned)kblocks);
-    for (int i = 0; i < kblocks; ++i) {
-      const int kb = kb0 + i < kblocks ? kb0 + i : kb0 + i - kblocks;
+    const int nk = kb_hi - kb_lo;
+    const int kb0 = (int)(tile % (unsigned)nk);
+    for (int i = 0; i < nk; ++i) {
+      const int kb = kb_lo + (kb0 + i < nk ? kb0 + i : kb0 + i - nk);
       if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.status)) {
         aborted = true;
         break;
@@ -287,7 +297,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const uint32_t idesc = umma_idesc_bf16(RM, a.npad);
     int s = 0;
     uint32_t ph = 0;
-    for (int kb = 0; kb < kblocks; ++kb) {
+    for (int kb = 0; kb < kb_hi - kb_lo; ++kb) {
       if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, a.status)) break;
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
@@ -312,7 +322,73 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const int ZP = E + 1;                       // padded row pitch: conflict-free column accesses
 
   // ------------------------------------------------------------------ A: TMEM -> shared memory
-  {
+  if (split > 1) {
+    // raw partial logits of this CTA's k-blocks, rows [0, nvalid), pitch E, at the end of the
+    // pipeline buffers (after the epilogue scratch); rank 0 adds the others' (same offset in each
+    // CTA of the cluster) in rank order, 16 bytes at a time, then the bias
+    float* P = reinterpret_cast<float*>(smem + a.pofs);
+    {
+      const int q = warp & 3, r = q * 32 + lane;
+      const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+      for (int c0 = (warp >> 2) * 32; c0 < E; c0 += 64) {
+        uint32_t v[32];
+        tmem_ld32(trow + c0, v);
+        tmem_wait_ld();
+        if (r < nvalid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            if (c0 + i < E)
+              *reinterpret_cast<float4*>(P + r * E + c0 + i) =
+                  make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]), __uint_as_float(v[i + 2]),
+                              __uint_as_float(v[i + 3]));
+        }
+      }
+    }
+    tc_fence_before();
+    cluster_sync_all();  // every partial is in its CTA's shared memory
+    if (crank == 0) {
+      const int e4n = E >> 2;
+      for (int i = tid; i < nvalid * e4n; i += RTHREADS) {
+        const int r = i / e4n, e = (i - r * e4n) * 4;
+        const uint32_t off = smem_u32(P + r * E + e);
+        float4 z = *reinterpret_cast<const float4*>(P + r * E + e);
+        float4 rem[7];
+#pragma unroll
+        for (int c = 1; c < 8; ++c)
+          if (c < split) rem[c - 1] = ld_shared_cluster_f32x4(mapa_rank(off, (uint32_t)c));
+#pragma unroll
+        for (int c = 1; c < 8; ++c) {
+          if (c < split) {
+            z.x = __fadd_rn(z.x, rem[c - 1].x);
+            z.y = __fadd_rn(z.y, rem[c - 1].y);
+            z.z = __fadd_rn(z.z, rem[c - 1].z);
+            z.w = __fadd_rn(z.w, rem[c - 1].w);
+          }
+        }
+        const float zz[4] = {z.x, z.y, z.z, z.w};
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          float zj = __fadd_rn(zz[j], ctl->bias[e + j]);
+          if (!isfinite(zj)) {
+            zj = kBadLogit;
+            bad = true;
+          }
+          S.Z[r * ZP + e + j] = zj;
+        }
+        if (bad) atomicOr(&ctl->flags[r], F_BAD);
+      }
+    }
+    cluster_sync_all();  // rank 0 has read every partial: the other CTAs may leave
+    if (crank != 0) {
+      __syncthreads();
+      if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+      }
+      return;
+    }
+  } else {
     const int q = warp & 3, r = q * 32 + lane;
     const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
     bool bad = false;
@@ -543,14 +619,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   for (int e = tid; e < E; e += RTHREADS) {
     float ps = 0.f;
     for (int part = 0; part < parts; ++part) ps += S.ppart[part * 256 + e];
-    a.psum[(size_t)blockIdx.x * E + e] = ps;
-    a.hist[(size_t)blockIdx.x * E + e] = ctl->hist[e];
+    a.psum[(size_t)tile * E + e] = ps;
+    a.hist[(size_t)tile * E + e] = ctl->hist[e];
   }
-  if (tid == 0) a.lse2[blockIdx.x] = ((ctl->lse2w[0] + ctl->lse2w[1]) + ctl->lse2w[2]) + ctl->lse2w[3];
+  if (tid == 0) a.lse2[tile] = ((ctl->lse2w[0] + ctl->lse2w[1]) + ctl->lse2w[2]) + ctl->lse2w[3];
   if (a.finalize) {  // the last CTA to get here reduces every CTA's partials
     __threadfence();
     __syncthreads();
-    if (tid == 0) ctl->is_last = (atomicAdd(a.done, 1u) == gridDim.x - 1) ? 1 : 0;
+    if (tid == 0) ctl->is_last = (atomicAdd(a.done, 1u) == (unsigned)ntiles - 1) ? 1 : 0;
   } else if (tid == 0) {
     ctl->is_last = 0;  // the fused dispatch kernel reduces them
   }
@@ -559,7 +635,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   // ------------------------------------------------------------------ last CTA: counts and losses
   if (ctl->is_last) {
     __threadfence();
-    const int nb = gridDim.x;
+    const int nb = ntiles;
     route_losses<true, true>(a.hist, a.psum, a.lse2, nb, E, k, a.T, a.lb_coef, a.z_coef, ctl->hist, a.counts,
                              a.losses, ctl->ls);
     if (a.pbase) {
@@ -621,11 +697,51 @@ __global__ void __launch_bounds__(RTHREADS, 1)
 }
 
 template <int KL>
-cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, const RouteArgs& a, int nb, size_t smem,
+cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, RouteArgs a, int nb, size_t smem, int max_split,
                       cudaStream_t st) {
-  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(k_route_tc<KL>), smem);
+  auto kern = k_route_tc<KL>;
+  cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_route_tc<KL>, dim3(nb), dim3(RTHREADS), smem, st, mx, mw, a);
+  // Few tiles: split each tile's k-blocks over a cluster of up to 8 CTAs (one CTA per SM), so that
+  // more SMs pull x and W_r; the split shrinks until the clusters fit the GPU.
+  int nsm = 148;
+  {
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  }
+  int split = 1;
+  while (split < max_split && (long)nb * split * 2 <= nsm && split * 2 <= a.d / RBK) split <<= 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(RTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  for (; split > 1; split >>= 1) {
+    attr[1].val.clusterDim.x = split;
+    cfg.gridDim = dim3((unsigned)(nb * split), 1, 1);
+    cfg.numAttrs = 2;
+    int n_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n_clusters = 0;
+    }
+    if (n_clusters >= 1) break;
+  }
+  a.split = split;
+  cfg.gridDim = dim3((unsigned)(nb * split), 1, 1);
+  if (split > 1) {
+    attr[1].val.clusterDim.x = split;
+    cfg.numAttrs = 2;
+  } else {
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, mx, mw, a);
 }
 }  // namespace
 
@@ -695,9 +811,16 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   a.drops = fuse ? scan->drops : nullptr;
   const int nb = route_tc_blocks(T);
   cudaError_t err;
-  if (k + 1 <= 3) err = launch_kl<3>(mx, mw, a, nb, smem, st);
-  else if (k + 1 <= 5) err = launch_kl<5>(mx, mw, a, nb, smem, st);
-  else err = launch_kl<9>(mx, mw, a, nb, smem, st);
+  // split-K over a cluster needs E % 4 == 0 and room for the partials after the epilogue scratch;
+  // a partial tile (T < 128) takes up to 8 CTAs, full tiles up to 4 (rank 0 sums 128 rows)
+  const size_t pbytes = (size_t)RM * E * 4;
+  int max_split = (E % 4 == 0 && region >= pbytes && (region - pbytes) / 1024 * 1024 >= epi_scratch_bytes(E))
+                      ? (T < RM ? 8 : 4)
+                      : 1;
+  a.pofs = (int)((region - pbytes) / 1024 * 1024);
+  if (k + 1 <= 3) err = launch_kl<3>(mx, mw, a, nb, smem, max_split, st);
+  else if (k + 1 <= 5) err = launch_kl<5>(mx, mw, a, nb, smem, max_split, st);
+  else err = launch_kl<9>(mx, mw, a, nb, smem, max_split, st);
   return err;
 }
 
