@@ -338,7 +338,7 @@ def run_ours(args, wl, ws_n, rank, local):
     tokens_all = T * ws_n
     res = {
         "metric": "MoE-layer fwd tokens/s (expert-GEMM TFLOP/s alongside)",
-        "value": round(tokens_all / (ms_step * 1e-3), 1),
+        "value": round(job_tokens_per_s(T, ws_n, ms_step), 1),
         "unit": "tokens/s",
         "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 5),
@@ -439,11 +439,18 @@ def barrier():
 
 
 def max_over_ranks(v: float) -> float:
+    """The slowest rank's time (replicas are timed together; the job is as slow as its slowest)."""
     if not _PG:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput of `world` replicas: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_max * 1e-3)
 
 
 def main():
