@@ -27,6 +27,8 @@
 #include <float.h>
 #include <stdio.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "route_losses.cuh"
@@ -696,9 +698,47 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   }
 }
 
+// Whether at least one cluster of `split` CTAs of this kernel (with `smem` bytes each) can be
+// resident; asked once per (kernel, device, smem, split) and remembered.
+template <typename K>
+bool clusters_fit_query(K kern, const cudaLaunchConfig_t& cfg) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  return n >= 1;
+}
+struct FitEntry {
+  const void* k;
+  int dev;
+  size_t smem;
+  int split;
+  bool fit;
+};
+std::mutex g_fit_mu;
+FitEntry g_fit[64];
+int g_nfit = 0;
+
+template <int KL>
+bool clusters_fit_kl(size_t smem, int split, const cudaLaunchConfig_t& cfg) {
+  const void* key = reinterpret_cast<const void*>(k_route_tc<KL>);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(g_fit_mu);
+  for (int i = 0; i < g_nfit; ++i)
+    if (g_fit[i].k == key && g_fit[i].dev == dev && g_fit[i].smem == smem && g_fit[i].split == split) return g_fit[i].fit;
+  const bool fit = clusters_fit_query(k_route_tc<KL>, cfg);
+  if (g_nfit < 64) g_fit[g_nfit++] = FitEntry{key, dev, smem, split, fit};
+  return fit;
+}
+
 template <int KL>
 cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, RouteArgs a, int nb, size_t smem, int max_split,
                       cudaStream_t st) {
+  auto clusters_fit = [&](const void*, size_t sm, int sp, const cudaLaunchConfig_t& c) {
+    return clusters_fit_kl<KL>(sm, sp, c);
+  };
   auto kern = k_route_tc<KL>;
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
@@ -726,12 +766,7 @@ cudaError_t launch_kl(const CUtensorMap& mx, const CUtensorMap& mw, RouteArgs a,
     attr[1].val.clusterDim.x = split;
     cfg.gridDim = dim3((unsigned)(nb * split), 1, 1);
     cfg.numAttrs = 2;
-    int n_clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n_clusters = 0;
-    }
-    if (n_clusters >= 1) break;
+    if (clusters_fit(reinterpret_cast<const void*>(kern), smem, split, cfg)) break;
   }
   a.split = split;
   cfg.gridDim = dim3((unsigned)(nb * split), 1, 1);
