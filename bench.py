@@ -305,6 +305,32 @@ def run_ours(args, wl, ws_n, rank, local):
                      "frac_of_hbm": round(layer_gbs / hbm, 4)}
     expert_ms = stage_ms["up"] + stage_ms["down"] + stage_ms["shared"]
 
+    # ---- routing statistics of this workload (co-activation counts, imbalance, dropped share),
+    # from a standalone router call; timed alone, outside the layer's figures
+    topk_idx = torch.empty((T, wl.k), dtype=torch.int32, device=dev)
+    topk_w = torch.empty((T, wl.k), dtype=torch.float32, device=dev)
+    r_counts = torch.empty(wl.E, dtype=torch.int32, device=dev)
+    r_losses = torch.empty(2, dtype=torch.float32, device=dev)
+    moe.moe_route(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), topk_idx, topk_w, r_counts, r_losses,
+                  layer.ws, stream)
+    coact = torch.empty((wl.E, wl.E), dtype=torch.int32, device=dev)
+    rstats = torch.empty(2, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        moe.moe_route_stats(cfg, topk_idx, None, coact, rstats, layer.ws, stream)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(10):
+        moe.moe_route_stats(cfg, topk_idx, None, coact, rstats, layer.ws, stream)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    cm = coact.double().cpu()
+    diag = torch.diagonal(cm)
+    score = torch.where(diag[:, None] > 0, cm / diag.clamp(min=1)[:, None], torch.zeros_like(cm))
+    score.fill_diagonal_(0)
+    route_stats = {"ms": round(s0.elapsed_time(s1) / 10, 5), "load_imbalance": round(float(rstats[0].item()), 4),
+                   "dropped_fraction": round(int(drops.item()) / (T * wl.k), 5),
+                   "max_coactivation_score": round(float(score.max().item()), 4)}
+
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     x_host = inp["x"].cpu().pin_memory()
     y_host = torch.empty_like(x_host).pin_memory()
@@ -361,6 +387,7 @@ def run_ours(args, wl, ws_n, rank, local):
         "kept_rows": kept_rows, "drops": int(wl.T * wl.k - kept_rows),
         "roofline": roofline,
         "weight_stream": weight_stream,
+        "route_stats": route_stats,
         "e2e": {"value": round(tokens_all / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "moe_layer_forward with pinned host x/y"},

@@ -197,6 +197,21 @@ moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w
                              const float* logit_bias, int32_t* topk_idx, float* topk_w,
                              int32_t* counts, float* losses, void* stream);
 
+/* Routing statistics (beyond the layer itself): how the router spread the tokens over the
+ * experts.  Expert co-activation is discussed in the FLAME-MoE summary; load imbalance and
+ * capacity overflow in the Naive-N0.5-Flash article, sec. 4.
+ *   topk_idx [T,k] int32 from moe_route; offsets [E+1] from moe_permute, or NULL.
+ *   coact [E,E] int32, overwritten: coact[i][j] (i != j) = number of tokens whose k experts
+ *     include both i and j; coact[i][i] = number of tokens that chose i (moe_route's counts).
+ *     P(E_j | E_i) = coact[i][j] / coact[i][i].
+ *   stats [2] float, overwritten: [0] max_e coact[e][e] / (T k / E), the load of the busiest
+ *     expert relative to a uniform spread (1 = uniform); [1] dropped assignments / (T k) from
+ *     offsets[E] (0 when offsets is NULL).
+ *   ws: a workspace of this config (only its status word is used: an index outside [0, E) sets
+ *     MOE_ERR_DEVICE_STATUS and that token is skipped).  Deterministic (integer counts). */
+moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const int32_t* offsets,
+                           int32_t* coact, float* stats, void* ws, void* stream);
+
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -475,6 +475,16 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
                                     static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const int32_t* offsets, int32_t* coact,
+                           float* stats, void* ws, void* stream) {
+  MOE_TRY(validate(cfg));
+  if (!coact || !stats || !ws || (cfg->T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
+  if (cfg->k > 8) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = layout(cfg);
+  return cuda_status(launch_route_stats(topk_idx, offsets, cfg->T, cfg->E, cfg->k, coact, stats,
+                                        at<uint32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, float* losses,
                              int32_t* counts_out, int32_t* drops_out, void* ws, void* stream) {
   return layer_impl(cfg, w, x, y, losses, counts_out, drops_out, ws, static_cast<cudaStream_t>(stream), nullptr);

@@ -62,6 +62,11 @@ cudaError_t launch_dispatch_fused(bool bf16, const int32_t* topk_idx, const int3
                                   int32_t* kept, int32_t* drops, int32_t* row_of, int32_t* tok_of, void* x_perm,
                                   int max_rows, uint32_t* status, cudaStream_t st);
 
+// Routing statistics: co-activation counts coact [E][E] (zeroed here), stats [2] (load imbalance,
+// dropped fraction; offsets may be NULL).
+cudaError_t launch_route_stats(const int32_t* topk_idx, const int32_t* offsets, int T, int E, int k, int32_t* coact,
+                               float* stats, uint32_t* status, cudaStream_t st);
+
 // Kernels launch_dispatch launches (2 with the row copy, else 1).
 int dispatch_launches(bool with_rows, int d, int elt_bytes);
 

@@ -220,6 +220,42 @@ def expert_param_count(d: int, dff: int, act: str = "gelu", bias: bool = False) 
     return n + ((dff + d) if bias else 0)
 
 
+# ----------------------------------------------------------------------------- routing statistics
+def coactivation(idx: np.ndarray, E: int) -> np.ndarray:
+    """Expert co-activation counts.  C[i, j] (i != j) = number of tokens whose selected experts
+    include both i and j; C[i, i] = number of tokens that chose i.  The FLAME-MoE summary's
+    directed co-activation score from E_i to E_j (expert co-activation analysis, fig. 5) is the
+    conditional probability C[i, j] / C[i, i].  Plain loop over the tokens and their slot pairs."""
+    C = np.zeros((E, E), dtype=np.int64)
+    for row in np.asarray(idx):
+        for a in row:
+            for b in row:
+                C[int(a), int(b)] += 1
+    return C
+
+
+def coactivation_score(C: np.ndarray) -> np.ndarray:
+    """Directed score S[i, j] = P(j chosen | i chosen) = C[i, j] / C[i, i] (0 for unused i)."""
+    d = np.diag(C).astype(np.float64)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        S = np.where(d[:, None] > 0, C / d[:, None], 0.0)
+    return S
+
+
+def routing_stats(idx: np.ndarray, E: int, k: int, offsets=None):
+    """(load imbalance, dropped fraction).  Imbalance: the busiest expert's token count over the
+    uniform share T k / E that the load-balance loss of the OpenMythos article, sec. 3.1, pushes
+    towards (1 = uniform).  Dropped fraction: assignments past the capacity (same section) over
+    all T k, from offsets[E] = kept assignments; 0 without offsets."""
+    idx = np.asarray(idx)
+    tk = int(idx.shape[0]) * k
+    if tk == 0:
+        return 0.0, 0.0
+    counts = np.bincount(idx.ravel(), minlength=E)
+    dropped = 0.0 if offsets is None else (tk - int(offsets[E])) / tk
+    return float(counts.max()) * E / tk, dropped
+
+
 # ----------------------------------------------------------------------------- whole layer
 def moe_layer(inp: Dict, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
               lb_coef: float = 0.01, z_coef: float = 0.001,

@@ -209,6 +209,41 @@ def test_graph_replay_matches_eager():
             assert torch.equal(a, b)
 
 
+def _check_route_stats(wl, inp_gpu, got):
+    cfg = moe.config_from_workload(wl, inp_gpu["x"].shape[0])
+    ws = moe.alloc_workspace(cfg)
+    coact = torch.full((wl.E, wl.E), -7, dtype=torch.int32, device="cuda")
+    stats = torch.full((2,), -1.0, dtype=torch.float32, device="cuda")
+    moe.moe_route_stats(cfg, got["topk_idx"], got["offsets"], coact, stats, ws)
+    assert moe.moe_read_device_status(ws) == moe.MOE_OK
+    idx = got["topk_idx"].cpu().numpy()
+    assert np.array_equal(coact.cpu().numpy(), O.coactivation(idx, wl.E))      # integer counts: exact
+    imb, drop = O.routing_stats(idx, wl.E, wl.k, got["offsets"].cpu().numpy())
+    np.testing.assert_allclose(stats.cpu().numpy(), [imb, drop], rtol=1e-6)
+
+
+@pytest.mark.parametrize("case", ["bf16_swiglu_shared", "bf16_collapse_cap", "bf16_E256_k8", "fp32_E256_k8",
+                                  "bf16_one_token"])
+def test_route_stats_match_oracle(case):
+    """Co-activation counts (shared-memory path for E <= 128, global atomics above), load
+    imbalance and dropped fraction, from the library's own top-k indices and offsets."""
+    wl = CASES[case]
+    inp = _to(make_inputs(wl, "cpu"), "cuda")
+    got = run_steps(wl, inp)
+    assert got["status"] == moe.MOE_OK
+    _check_route_stats(wl, inp, got)
+
+
+def test_route_stats_empty_batch():
+    wl = CASES["bf16_swiglu_shared"].replace(T=0)
+    cfg = moe.config_from_workload(wl)
+    ws = moe.alloc_workspace(cfg)
+    coact = torch.full((wl.E, wl.E), -7, dtype=torch.int32, device="cuda")
+    stats = torch.full((2,), -1.0, dtype=torch.float32, device="cuda")
+    moe.moe_route_stats(cfg, None, None, coact, stats, ws)
+    assert coact.abs().sum().item() == 0 and stats.abs().sum().item() == 0
+
+
 # ------------------------------------------------------------------------------ full workloads
 def _full(name, n_sample, seed=0):
     wl = WORKLOADS[name]
@@ -224,6 +259,14 @@ def _full(name, n_sample, seed=0):
 
 def test_full_flash_bf16():
     _full("flash_bf16", None)
+
+
+def test_route_stats_full_finegrained():
+    wl = WORKLOADS["finegrained_bf16"]
+    inp = make_inputs(wl, "cuda")
+    got = run_steps(wl, inp)
+    assert got["status"] == moe.MOE_OK
+    _check_route_stats(wl, inp, got)
 
 
 def test_full_finegrained_bf16():

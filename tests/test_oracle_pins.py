@@ -211,9 +211,39 @@ def check_losses(o):
     assert o.aux_losses(np.zeros((0, 4)), np.zeros(0), np.zeros(4), 2, 0.01, 0.001) == (0.0, 0.0)
 
 
+def check_coactivation(o):
+    # hand-worked fixture (tests/golden/coactivation_small.json)
+    g = json.load(open(os.path.join(GOLDEN, "coactivation_small.json")))
+    idx = np.array(g["topk_idx"])
+    C = o.coactivation(idx, g["E"])
+    assert C.tolist() == g["coact"]
+    S = o.coactivation_score(C)
+    assert abs(S[0, 1] - g["score_0_to_1"]) < 1e-15 and abs(S[2, 1] - g["score_2_to_1"]) < 1e-15
+    offsets = np.array([0, 0, 0, 0, g["kept"]])
+    imb, drop = o.routing_stats(idx, g["E"], g["k"], offsets)
+    assert abs(imb - g["imbalance"]) < 1e-15 and abs(drop - g["dropped_fraction"]) < 1e-15
+    # invariants on random top-k selections: symmetric, diagonal = counts, each token choosing i
+    # has k - 1 other (distinct) experts, all pairs add up to T k (k - 1)
+    for T, E, k in [(50, 8, 2), (37, 6, 3), (20, 5, 5), (30, 4, 1)]:
+        idx = o.topk_select(RNG.standard_normal((T, E)), k)
+        C = o.coactivation(idx, E)
+        assert (C == C.T).all()
+        assert (np.diag(C) == np.bincount(idx.ravel(), minlength=E)).all()
+        off = C.sum(1) - np.diag(C)
+        assert (off == (k - 1) * np.diag(C)).all()
+        assert C.sum() - np.trace(C) == T * k * (k - 1)
+        if k == E:
+            assert (C == T).all()
+        if k == 1:
+            assert (C - np.diag(np.diag(C)) == 0).all()
+        imb, drop = o.routing_stats(idx, E, k)
+        assert imb >= 1.0 - 1e-12 and drop == 0.0
+    assert o.routing_stats(np.zeros((0, 2), dtype=int), 4, 2) == (0.0, 0.0)
+
+
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
               check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
-              check_losses]
+              check_losses, check_coactivation]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -303,6 +333,16 @@ def _mut_silu_sigmoid(u):
 O_combine = O.combine
 
 
+def _mut_coact_upper_only(idx, E):
+    C = np.zeros((E, E), dtype=np.int64)
+    for row in np.asarray(idx):
+        for a in row:
+            for b in row:
+                if a <= b:
+                    C[int(a), int(b)] += 1
+    return C
+
+
 @pytest.mark.parametrize("name,fn,check", [
     ("router_logits", _mut_router_transposed, check_router),
     ("topk_select", _mut_topk_high_index, check_topk),
@@ -314,6 +354,7 @@ O_combine = O.combine
     ("capacity", _mut_capacity_floor, check_capacity),
     ("combine", _mut_combine_unweighted, check_layer_reductions),
     ("silu", _mut_silu_sigmoid, check_expert_ffn),
+    ("coactivation", _mut_coact_upper_only, check_coactivation),
 ])
 def test_planted_mistakes_are_caught(name, fn, check, monkeypatch):
     """Plant one mistake in the oracle module itself (so its internal callers see it too)."""
