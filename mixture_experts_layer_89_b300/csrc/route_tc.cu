@@ -6,13 +6,14 @@
 // tutorial, sec. 3.1 (MoELayer) and the routing pseudo-code of the OpenMythos article, sec. 3.1;
 // the load-balance loss is that article's alpha E sum_e f_e P_e, the z-loss the one the FLAME-MoE
 // summary, sec. 2, names.  The logit GEMM is a dense contraction (T x d x E), so it runs on
-// tcgen05 with N = E (rounded up to 16) and the whole logit row of 128 tokens in TMEM; the main
-// loop then streams x from HBM once, at the HBM roofline.
+// tcgen05 with N = E (rounded up to 16) and the whole logit row of 128 tokens in TMEM.
 //
-// CTA = 128 tokens, 256 threads.  Main loop:
-//   warp 0     TMA producer: x tile [128 x 64] and W_r tile [Npad x 64] per stage
+// Tile = 128 tokens, 256 threads per CTA.  Main loop:
+//   warp 0     TMA producer: x tile [rows x 64] and W_r tile [Npad x 64] per stage
 //   warp 1     MMA issuer: 4 x tcgen05.mma (M=128, N=Npad, K=16) per stage
 //   warp 2     TMEM allocator;   warp 3   logit bias and counters
+// With few tiles, a cluster of up to 8 CTAs shares a tile, each over a slice of the k-blocks;
+// rank 0 adds the partial logits (distributed shared memory, rank order) and continues alone.
 // Epilogue, all 8 warps, the pipeline buffers reused as scratch:
 //   A  TMEM -> shared memory (warp w reads TMEM lane quarter w % 4)
 //   B  thread per (token, expert half): sorted top-(k+1) insertion lists, ties to the lower
@@ -21,9 +22,10 @@
 //      from a sequential sum, so a token whose leading k+1 logits lie closer than a bound on that
 //      accumulation error is re-decided from compensated fp32 (Neumaier) dot products of every
 //      expert within the band, shared out over the warps
-//   D  outputs per token; per-expert sums of P over the CTA's tokens in token order
-// The last CTA to finish (a counter in the workspace) reduces the per-CTA partials in block order
-// into counts and losses, so results do not depend on scheduling.
+//   D  outputs per token; per-tile expert histogram, sums of P and of lse^2
+// The per-tile partials are then reduced in tile order into counts and losses (route_losses.cuh):
+// by the last tile's CTA (a counter in the workspace) for a router call on its own, or, inside a
+// whole layer, by the dispatch and gather kernels.  Results do not depend on scheduling.
 #include <float.h>
 #include <stdio.h>
 
