@@ -1,8 +1,8 @@
 // Grouped expert projection on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
 //
-// The expert FFNs are dense contractions once tokens are grouped by expert (Naive-N0.5-Flash
-// article, sec. 4.2: "one big matmul per expert"), so they run here as one persistent grouped
-// GEMM per projection:
+// Once tokens are grouped by expert, each expert's FFN is a dense matrix product over that
+// expert's rows (the Naive-N0.5-Flash article, sec. 4.2, recommends exactly this grouping for
+// inference), so the experts run here as one persistent grouped GEMM per projection:
 //   up:   h = GELU(x_perm W_up^T + b_up)          or  h = SiLU(x_perm W_gate^T) * (x_perm W_up^T)
 //   down: y_perm = h W_down^T (+ b_down)
 // (expert forms: mini-moe tutorial, sec. 3.1; GPT-4 2% article, sec. 3.1).
@@ -11,13 +11,15 @@
 // SwiGLU the 256 columns are 128 gate columns followed by the same 128 up columns, so one MMA
 // (M=128, N=256, K=16) produces both halves and the epilogue multiplies them in registers.
 // Warp roles (one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: A tile (rows of one expert) + B tile (that expert's weights), 4 stages
+//   warp 0      TMA producer: A tile (rows of one expert; only its 32-row groups when the tile
+//               has few rows) + B tile (that expert's weights), 4 stages
 //   warp 1      MMA issuer (one thread): 4 x tcgen05.mma per stage into a TMEM accumulator
 //   warp 2      TMEM allocator (512 columns = two 256-column accumulators, double buffered)
 //   warp 3      builds the tile table from the device-side expert offsets (no count returns to
 //               the host)
-//   warps 4..   EPIW epilogue warps: tcgen05.ld (thread = row), bias/activation, stores.  Warp w
-//               reaches TMEM lanes 32 (w % 4)..; with 8 warps, w and w + 4 split the columns.
+//   warps 4..   EPIW epilogue warps: tcgen05.ld (thread = row), bias/activation, bf16 or fp32
+//               32x32 tiles staged in swizzled shared memory and written by TMA tile stores.
+//               Warp w reaches TMEM lanes 32 (w % 4)..; warps w, w + 4, ... split the columns.
 // Paired mode (PAIR): 2-SM MMAs.  CTAs run in clusters of two that take the two 128-row halves of a
 // 256-row tile of one expert; each holds its own 128 A rows and half of the 256 B rows in shared
 // memory (32 KB per stage instead of 48, so 6 stages), and the even CTA issues
@@ -25,7 +27,8 @@
 // Both CTAs' loads signal the leader's stage barriers; the leader's commits signal both CTAs'
 // "stage free" and "accumulator full" barriers; both epilogues signal the leader's "accumulator
 // free" barrier.  Per SM, operand traffic drops by a third for the same FLOPs.  Tiles are
-// enumerated m-tile-major with n fastest (measured faster than n-major here).
+// enumerated m-tile-major with n fastest (measured faster than n-major here).  Launched as a
+// programmatic dependent launch: the set-up overlaps the previous kernel's tail.
 #include <stdio.h>
 
 #include <mutex>

@@ -6,12 +6,13 @@
 // C = cf * tokens / E with overflow dropped are the OpenMythos article, sec. 3.1.
 //
 // Deterministic, atomics-free ordering over blocks of 128 tokens: (1) a per-block histogram of the
-// assignments per expert (for bf16 layers the router already writes it); (2) an exclusive scan of
-// each expert's histogram over blocks gives every block its rank base, the capacity gives the kept
-// counts and a scan over experts the offsets (for bf16 layers the router's last CTA does this);
-// (3) one kernel per block ranks its assignments in token order (one warp, equal experts inside a
+// assignments per expert; (2) an exclusive scan of each expert's histogram over blocks gives every
+// block its rank base, the capacity gives the kept counts and a scan over experts the offsets;
+// (3) one CTA per block ranks its assignments in token order (one warp, equal experts inside a
 // 32-wide chunk ranked with __match_any_sync) and writes row_of / tok_of; (4) a row-parallel copy
-// gathers x into x_perm.
+// gathers x into x_perm.  Inside a bf16 layer the router writes the per-block histograms (1) and
+// k_dispatch_fused derives (2) per CTA before ranking (3); moe_permute on its own and fp32 layers
+// run k_perm_hist, k_perm_scan and k_dispatch.
 #include "common.cuh"
 #include "kernels.h"
 #include "route_losses.cuh"
