@@ -43,6 +43,7 @@ NCU_TRAFFIC = {
 }
 
 
+METRIC = "MoE-layer fwd tokens/s and expert-GEMM TFLOP/s (% of bf16 peak) on 1 B300"
 L2_BYTES = 128 * 1024 * 1024  # B300 L2 is 126 MB; flush by writing twice this
 
 
@@ -163,6 +164,28 @@ class ClockSampler:
                 "source": "NVML (libnvidia-ml via ctypes), ~1 ms period, timed region only"}
 
 
+def weight_bytes_of(wl) -> int:
+    """Expert weights (routed and shared) one layer pass streams."""
+    elt = 2 if wl.dtype == "bf16" else 4
+    return (wl.E + wl.n_shared) * (3 if wl.act == "swiglu" else 2) * wl.d * wl.dff * elt
+
+
+def flushes_l2(wl) -> bool:
+    """Workloads whose weights are under twice the L2 get an L2 flush before every timed step."""
+    return weight_bytes_of(wl) < 2 * L2_BYTES
+
+
+def arm_config(wl, ws_n: int) -> dict:
+    """The workload the line is quoted on (both arms print the same one)."""
+    return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "experts": wl.E, "top_k": wl.k,
+            "d_ffn": wl.dff, "act": wl.act, "shared_experts": wl.n_shared,
+            "capacity_factor": wl.cf if wl.cf > 0 else None,
+            "parallelism": f"replicas x{ws_n} (no collective)",
+            "timing": "CUDA-graph replay of one moe_layer_forward per step",
+            "l2": ("L2 flushed before every timed step (256 MB write outside the events)" if flushes_l2(wl) else
+                   "inputs larger than L2 (expert weights %.0f MB per step)" % (weight_bytes_of(wl) / 1e6))}
+
+
 def expert_flops(wl, kept_rows: int, T: int):
     """Algorithmic expert FLOPs: 2 * rows * (matrices * d * dff) for the kept routed rows plus the
     shared experts on every token; (up, down) split."""
@@ -221,8 +244,7 @@ def run_ours(args, wl, ws_n, rank, local):
     # weights the step streams; below twice the L2 size the L2 is flushed (a 256 MB write outside
     # the timed events) before every timed step instead
     elt = 2 if wl.dtype == "bf16" else 4
-    weight_bytes = (wl.E + wl.n_shared) * (3 if wl.act == "swiglu" else 2) * wl.d * wl.dff * elt
-    flush_l2 = weight_bytes < 2 * L2_BYTES
+    flush_l2 = flushes_l2(wl)
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush_l2 else None
 
     def timed(fn, n):
@@ -390,7 +412,7 @@ def run_ours(args, wl, ws_n, rank, local):
 
     tokens_all = T * ws_n
     res = {
-        "metric": "MoE-layer fwd tokens/s (expert-GEMM TFLOP/s alongside)",
+        "metric": METRIC,
         "value": round(job_tokens_per_s(T, ws_n, ms_step), 1),
         "unit": "tokens/s",
         "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
@@ -400,13 +422,7 @@ def run_ours(args, wl, ws_n, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02^2) weights, random-init)",
-        "config": {"workload": wl.name, "T": wl.T, "d_model": wl.d, "experts": wl.E, "top_k": wl.k,
-                   "d_ffn": wl.dff, "act": wl.act, "shared_experts": wl.n_shared,
-                   "capacity_factor": wl.cf if wl.cf > 0 else None,
-                   "parallelism": f"replicas x{ws_n} (no collective)",
-                   "timing": "CUDA-graph replay of one moe_layer_forward per step",
-                   "l2": ("L2 flushed before every timed step (256 MB write outside the events)" if flush_l2 else
-                          "inputs larger than L2 (expert weights %.0f MB per step)" % (weight_bytes / 1e6))},
+        "config": arm_config(wl, ws_n),
         "expert_tflops": round(total_expert / (expert_ms * 1e-3) / 1e12, 2),
         "expert_frac_of_burst_peak": round(total_expert / (expert_ms * 1e-3) / 1e12 / peak_burst, 4),
         "expert_frac_of_sustained_peak": round(total_expert / (expert_ms * 1e-3) / 1e12 / peak_sus, 4),
@@ -464,10 +480,10 @@ def run_reference(args, wl):
     cores = oracle_threads()
     sample = f"first {n} of {wl.T} tokens of {wl.name}, full layer in fp64 per step"
     return {
-        "impl": "reference", "metric": "MoE-layer fwd tokens/s (expert-GEMM TFLOP/s alongside)",
+        "impl": "reference", "metric": METRIC,
         "value": round(value, 2), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": {"workload": wl.name, "T": n},
+        "dtype": "f64", "data": "synthetic", "config": arm_config(wl, dist_env()[0]),
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
