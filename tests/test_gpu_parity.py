@@ -41,6 +41,9 @@ CASES = {
                              seed=19, wseed=19),
     "bf16_gelu_shared3": Workload("bf16_gelu_shared3", T=260, d=192, E=5, k=2, dff=256, act="gelu",
                                   dtype="bf16", n_shared=3, seed=21, wseed=21),
+    # capacity 1: every expert keeps only its first assignment in token order
+    "bf16_cap1": Workload("bf16_cap1", T=300, d=128, E=8, k=2, dff=128, act="swiglu", dtype="bf16",
+                          n_shared=1, cf=0.01, seed=23, wseed=23),
     # enough rows per expert for the paired (2-SM) projections, with non-zero biases and drops
     "bf16_gelu_bias_pair": Workload("bf16_gelu_bias_pair", T=2100, d=256, E=4, k=2, dff=512, act="gelu",
                                     dtype="bf16", bias=True, bias_std=0.02, cf=1.05, seed=22, wseed=22),
