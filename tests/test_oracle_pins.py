@@ -241,9 +241,81 @@ def check_coactivation(o):
     assert o.routing_stats(np.zeros((0, 2), dtype=int), 4, 2) == (0.0, 0.0)
 
 
+def _bwd_case(rng, T, d, E, k, dff, act, bias, n_shared, wscale=0.7):
+    """Small layer whose top-k margins are far above a finite-difference step."""
+    while True:
+        inp = dict(x=rng.standard_normal((T, d)), w_router=rng.standard_normal((E, d)) * wscale,
+                   w_up=rng.standard_normal((E, dff, d)) * 0.5, w_down=rng.standard_normal((E, d, dff)) * 0.5)
+        if act == "swiglu":
+            inp["w_gate"] = rng.standard_normal((E, dff, d)) * 0.5
+        if bias:
+            inp["b_up"] = rng.standard_normal((E, dff)) * 0.3
+            inp["b_down"] = rng.standard_normal((E, d)) * 0.3
+        if n_shared:
+            inp["ws_up"] = rng.standard_normal((n_shared, dff, d)) * 0.5
+            inp["ws_down"] = rng.standard_normal((n_shared, d, dff)) * 0.5
+            if act == "swiglu":
+                inp["ws_gate"] = rng.standard_normal((n_shared, dff, d)) * 0.5
+        z = inp["x"] @ inp["w_router"].T
+        if k == E or np.min(O.topk_gap(z, k)) > 0.05:
+            return inp
+
+
+def check_backward(o, b=None):
+    """Finite differences of L = <dy, y> + dlb lb + dzl zl (forward oracle) against the analytic
+    gradients, for every tensor; k = E with identical experts leaves the router only the losses."""
+    if b is None:
+        from oracle import moe_backward as b
+    rng = np.random.default_rng(99)
+    cases = [dict(T=7, d=5, E=4, k=2, dff=3, act="gelu", bias=True, n_shared=0, cf=0.75),
+             dict(T=6, d=4, E=3, k=2, dff=3, act="swiglu", bias=False, n_shared=1, cf=0.0),
+             dict(T=5, d=4, E=4, k=1, dff=2, act="swiglu", bias=False, n_shared=0, cf=1.0)]
+    for c in cases:
+        cf = c.pop("cf")
+        inp = _bwd_case(rng, **c)
+        kw = dict(E=c["E"], k=c["k"], act=c["act"], n_shared=c["n_shared"], cf=cf, lb_coef=0.3, z_coef=0.2,
+                  dlb=1.0, dzl=1.0)
+        dy = rng.standard_normal((c["T"], c["d"]))
+        g = b.moe_layer_backward(inp, dy, **kw)
+        names = {"x": "dx", "w_router": "dw_router", "w_up": "dw_up", "w_down": "dw_down"}
+        if c["act"] == "swiglu":
+            names["w_gate"] = "dw_gate"
+        if c["bias"]:
+            names.update(b_up="db_up", b_down="db_down")
+        if c["n_shared"]:
+            names.update(ws_up="dws_up", ws_down="dws_down")
+            if c["act"] == "swiglu":
+                names["ws_gate"] = "dws_gate"
+        h = 1e-6
+        for tname, gname in names.items():
+            assert g[gname].shape == inp[tname].shape, (gname, g[gname].shape)
+            flat = inp[tname].reshape(-1)
+            for i in rng.choice(flat.size, size=min(8, flat.size), replace=False):
+                old = flat[i]
+                flat[i] = old + h
+                lp = b.objective(inp, dy, **kw)
+                flat[i] = old - h
+                lm = b.objective(inp, dy, **kw)
+                flat[i] = old
+                fd = (lp - lm) / (2 * h)
+                an = g[gname].reshape(-1)[i]
+                assert abs(an - fd) <= 1e-6 * (1.0 + abs(fd)), (c["act"], tname, int(i), an, fd)
+    # k = E, identical experts: y = FFN(x) whatever the routing, so without the losses the router
+    # gets no gradient, and with only the z-loss it gets 2 beta lse_t P_t / T through x
+    inp = _bwd_case(rng, 6, 4, 3, 3, 3, "gelu", False, 0)
+    for key in ("w_up", "w_down"):
+        inp[key] = np.repeat(inp[key][:1], 3, axis=0)
+    dy = rng.standard_normal((6, 4))
+    g = b.moe_layer_backward(inp, dy, E=3, k=3, act="gelu", dlb=0.0, dzl=0.0)
+    assert np.abs(g["dw_router"]).max() < 1e-12
+    g = b.moe_layer_backward(inp, np.zeros((6, 4)), E=3, k=3, act="gelu", z_coef=0.5, dlb=0.0, dzl=1.0)
+    P, lse = o.softmax_lse(inp["x"] @ inp["w_router"].T)
+    np.testing.assert_allclose(g["dw_router"], ((2 * 0.5 * lse / 6)[:, None] * P).T @ inp["x"], rtol=1e-12, atol=1e-14)
+
+
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
               check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
-              check_losses, check_coactivation]
+              check_losses, check_coactivation, check_backward]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -363,3 +435,31 @@ def test_planted_mistakes_are_caught(name, fn, check, monkeypatch):
     with pytest.raises((AssertionError, ValueError, IndexError)):
         check(O)
     monkeypatch.setattr(O, name, real)
+
+
+# planted mistakes in the backward oracle (patched in oracle.moe_backward itself)
+def _mut_gelu_grad_no_density(u):
+    return 0.5 * (1.0 + sps.erf(np.asarray(u) / math.sqrt(2.0)))
+
+
+def _mut_silu_grad_sigmoid(u):
+    return sps.expit(u)
+
+
+@pytest.mark.parametrize("name,fn", [
+    ("gelu_erf_grad", _mut_gelu_grad_no_density),
+    ("silu_grad", _mut_silu_grad_sigmoid),
+    ("expert_ffn_backward", "dx_halved"),
+])
+def test_planted_backward_mistakes_are_caught(name, fn, monkeypatch):
+    from oracle import moe_backward as B
+    real = getattr(B, name)
+    if fn == "dx_halved":
+        def fn(*a, **kw):
+            out = dict(real(*a, **kw))
+            out["dx"] = 0.5 * out["dx"]
+            return out
+    monkeypatch.setattr(B, name, fn)
+    with pytest.raises(AssertionError):
+        check_backward(O, B)
+
