@@ -256,6 +256,53 @@ def routing_stats(idx: np.ndarray, E: int, k: int, offsets=None):
     return float(counts.max()) * E / tk, dropped
 
 
+# ----------------------------------------------------------------------------- FP8 expert weights
+# Weight-only FP8 experts (a later row: the decode-shaped layer is bound by reading its expert
+# weights, so storing them in one byte halves the bytes).  Codes are OCP FP8 E4M3 ("fn": sign, 4
+# exponent bits with bias 7, 3 mantissa bits, no infinities, S.1111.111 is NaN, largest finite
+# 448), one fp32 scale per output row (nn.Linear row) = max |w| / 448.
+
+def e4m3_value(code: int) -> float:
+    """Value of an E4M3 code by its definition (NaN for S.1111.111)."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest E4M3 code (ties to the even mantissa), saturating at +-448."""
+    v = float(v)
+    if math.isnan(v):
+        raise ValueError("NaN has no E4M3 encoding here")
+    sign = 0x80 if (v < 0 or (v == 0 and math.copysign(1.0, v) < 0)) else 0
+    a = min(abs(v), 448.0)
+    best, best_err = 0, None
+    for c in range(0x7F):          # finite non-negative codes, 0x00 .. 0x7e
+        err = abs(e4m3_value(c) - a)
+        if best_err is None or err < best_err or (err == best_err and (c & 1) == 0 and (best & 1) == 1):
+            best, best_err = c, err
+    return sign | best
+
+
+def quantize_rows_e4m3(W) -> Dict[str, np.ndarray]:
+    """Per-row scaled E4M3 codes of a weight matrix W [rows, cols]: scale_r = max_c |W_rc| / 448
+    (1 for an all-zero row), codes_rc = e4m3(W_rc / scale_r); dequantised = value(code) * scale."""
+    W = np.asarray(W, np.float64)
+    amax = np.abs(W).max(axis=1)
+    scale = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32).astype(np.float64)
+    codes = np.zeros(W.shape, dtype=np.uint8)
+    for r in range(W.shape[0]):
+        for c in range(W.shape[1]):
+            codes[r, c] = e4m3_encode(W[r, c] / scale[r])
+    deq = np.vectorize(e4m3_value)(codes.astype(np.int64)) * scale[:, None]
+    return dict(codes=codes, scale=scale.astype(np.float32), dequantized=deq)
+
+
 # ----------------------------------------------------------------------------- whole layer
 def moe_layer(inp: Dict, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
               lb_coef: float = 0.01, z_coef: float = 0.001,

@@ -313,9 +313,35 @@ def check_backward(o, b=None):
     np.testing.assert_allclose(g["dw_router"], ((2 * 0.5 * lse / 6)[:, None] * P).T @ inp["x"], rtol=1e-12, atol=1e-14)
 
 
+def check_fp8(o):
+    # the definition against torch's float8_e4m3fn: every finite code decodes to the same value,
+    # and encoding agrees on random in-range values (ties to even included)
+    codes = torch.arange(256, dtype=torch.int64).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    for c in range(256):
+        v = o.e4m3_value(c)
+        assert (math.isnan(v) and math.isnan(ref[c])) or v == ref[c], (c, v, ref[c])
+    assert o.e4m3_value(0x7E) == 448.0 and o.e4m3_value(0x01) == 2.0 ** -9 and o.e4m3_value(0x38) == 1.0
+    vals = np.concatenate([RNG.standard_normal(300) * 40, [1.0625, 1.1875, -3.3, 2.0 ** -10, 0.0, 447.0]])
+    tq = torch.tensor(vals).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for v, c in zip(vals, tq):
+        assert o.e4m3_encode(v) == int(c) or (v == 0.0 and o.e4m3_value(o.e4m3_encode(v)) == 0.0), (v, c)
+    assert o.e4m3_encode(1000.0) == 0x7E and o.e4m3_encode(-1000.0) == 0xFE   # saturating
+    # per-row scaling: the row maximum maps to 448 exactly; relative error of normal values <= 2^-4
+    W = RNG.standard_normal((5, 40)) * 0.02
+    q = o.quantize_rows_e4m3(W)
+    assert q["codes"].dtype == np.uint8 and q["scale"].dtype == np.float32
+    amax = np.abs(W).max(axis=1)
+    np.testing.assert_allclose(np.abs(q["dequantized"]).max(axis=1), amax, rtol=1e-6)
+    normal = np.abs(W) / q["scale"].astype(np.float64)[:, None] >= 2.0 ** -6
+    rel = np.abs(q["dequantized"] - W)[normal] / np.abs(W)[normal]
+    assert rel.max() <= 2.0 ** -4 + 1e-7
+    assert (o.quantize_rows_e4m3(np.zeros((2, 3)))["dequantized"] == 0).all()
+
+
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
               check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
-              check_losses, check_coactivation, check_backward]
+              check_losses, check_coactivation, check_backward, check_fp8]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -405,6 +431,14 @@ def _mut_silu_sigmoid(u):
 O_combine = O.combine
 
 
+def _mut_e4m3_bias8(code):
+    v = _REAL_E4M3(code)
+    return v / 2.0 if v == v else v
+
+
+_REAL_E4M3 = O.e4m3_value
+
+
 def _mut_coact_upper_only(idx, E):
     C = np.zeros((E, E), dtype=np.int64)
     for row in np.asarray(idx):
@@ -427,6 +461,7 @@ def _mut_coact_upper_only(idx, E):
     ("combine", _mut_combine_unweighted, check_layer_reductions),
     ("silu", _mut_silu_sigmoid, check_expert_ffn),
     ("coactivation", _mut_coact_upper_only, check_coactivation),
+    ("e4m3_value", _mut_e4m3_bias8, check_fp8),
 ])
 def test_planted_mistakes_are_caught(name, fn, check, monkeypatch):
     """Plant one mistake in the oracle module itself (so its internal callers see it too)."""
