@@ -69,6 +69,16 @@ def router_logits(x, w_router, logit_bias=None) -> np.ndarray:
     return z
 
 
+def temper(z: np.ndarray, temperature: float = 1.0) -> np.ndarray:
+    """Router temperature (a routing variant): the logits divided by tau before the softmax, the
+    top-k and the losses, as the GPT-4 2%-parameters article's routing-collapse tips describe
+    (tau = 1 by default; a larger tau flattens the distribution).  The top-k choice is unchanged
+    for tau > 0; the renormalised weights become a softmax of z_selected / tau."""
+    if not temperature > 0:
+        raise ValueError("temperature must be positive")
+    return np.asarray(z, np.float64) / float(temperature)
+
+
 def softmax_lse(z: np.ndarray):
     """Row softmax P and log-sum-exp lse of the logits (max-subtracted)."""
     if z.shape[0] == 0:

@@ -339,9 +339,31 @@ def check_fp8(o):
     assert (o.quantize_rows_e4m3(np.zeros((2, 3)))["dequantized"] == 0).all()
 
 
+def check_temperature(o):
+    z = RNG.standard_normal((20, 6)) * 2
+    assert np.array_equal(o.temper(z, 1.0), z)
+    for tau in (0.5, 1.5, 4.0):
+        zt = o.temper(z, tau)
+        assert np.array_equal(o.topk_select(zt, 3), o.topk_select(z, 3))     # same experts chosen
+        P, _ = o.softmax_lse(zt)
+        idx = o.topk_select(zt, 2)
+        w = o.renormalise(P, idx)
+        # two selected experts: w_0 = sigmoid((z_a - z_b) / tau)
+        za = np.take_along_axis(z, idx, axis=1)
+        np.testing.assert_allclose(w[:, 0], sps.expit((za[:, 0] - za[:, 1]) / tau), rtol=1e-12)
+    # a very hot router spreads its weights evenly; a cold one puts all weight on the top expert
+    P, _ = o.softmax_lse(o.temper(z, 1e9))
+    np.testing.assert_allclose(o.renormalise(P, o.topk_select(z, 3)), 1.0 / 3, rtol=1e-6)
+    P, _ = o.softmax_lse(o.temper(z, 1e-6))
+    w = o.renormalise(P, o.topk_select(z, 3))
+    assert np.allclose(w[:, 0], 1.0) and np.allclose(w[:, 1:], 0.0)
+    with pytest.raises(ValueError):
+        o.temper(z, 0.0)
+
+
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
               check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
-              check_losses, check_coactivation, check_backward, check_fp8]
+              check_losses, check_coactivation, check_backward, check_fp8, check_temperature]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
