@@ -299,18 +299,57 @@ def e4m3_encode(v: float) -> int:
     return sign | best
 
 
-def quantize_rows_e4m3(W) -> Dict[str, np.ndarray]:
+def e4m3_table() -> np.ndarray:
+    """Values of all 256 E4M3 codes by e4m3_value (NaN at 0x7F and 0xFF)."""
+    return np.array([e4m3_value(c) for c in range(256)])
+
+
+def e4m3_encode_array(v) -> np.ndarray:
+    """e4m3_encode of every element of v (uint8 codes of the same shape): the nearest of the finite
+    non-negative values by a sorted search (they increase with the code), ties to the even code,
+    magnitudes above 448 saturating, the sign bit taken from v (so -0.0 gives 0x80)."""
+    v = np.asarray(v, np.float64)
+    if np.isnan(v).any():
+        raise ValueError("NaN has no E4M3 encoding here")
+    vals = e4m3_table()[:0x7F]
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.minimum(np.searchsorted(vals, a, side="left"), 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_rows_e4m3(W, division: str = "f64") -> Dict[str, np.ndarray]:
     """Per-row scaled E4M3 codes of a weight matrix W [rows, cols]: scale_r = max_c |W_rc| / 448
-    (1 for an all-zero row), codes_rc = e4m3(W_rc / scale_r); dequantised = value(code) * scale."""
+    (1 for an all-zero row), codes_rc = e4m3(W_rc / scale_r); dequantised = value(code) * scale.
+
+    division = "f64": the quotient W_rc / scale_r is taken in float64 and rounded once, to the
+    code.  division = "f32": scale and quotient are IEEE float32 divisions (for W exactly
+    representable in float32, such as bf16 weights), so a float32 implementation takes the same
+    rounding decisions; the scale is the same either way (max|w| / 448 rounded once to float32).
+    """
     W = np.asarray(W, np.float64)
-    amax = np.abs(W).max(axis=1)
-    scale = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32).astype(np.float64)
-    codes = np.zeros(W.shape, dtype=np.uint8)
-    for r in range(W.shape[0]):
-        for c in range(W.shape[1]):
-            codes[r, c] = e4m3_encode(W[r, c] / scale[r])
-    deq = np.vectorize(e4m3_value)(codes.astype(np.int64)) * scale[:, None]
-    return dict(codes=codes, scale=scale.astype(np.float32), dequantized=deq)
+    amax = np.abs(W).max(axis=1) if W.shape[1] else np.zeros(W.shape[0])
+    if division == "f32":
+        scale32 = np.where(amax > 0, amax.astype(np.float32) / np.float32(448.0), np.float32(1.0))
+        scale32 = scale32.astype(np.float32)
+        q = (W.astype(np.float32) / scale32[:, None]).astype(np.float64)
+        scale = scale32.astype(np.float64)
+    elif division == "f64":
+        scale = np.where(amax > 0, amax / 448.0, 1.0).astype(np.float32).astype(np.float64)
+        q = W / scale[:, None]
+    else:
+        raise ValueError(division)
+    codes = e4m3_encode_array(q)
+    return dict(codes=codes, scale=scale.astype(np.float32), dequantized=dequantize_rows_e4m3(codes, scale))
+
+
+def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
+    """value(codes[..., r, c]) * scale[..., r] in float64 (exact: a 4-bit significand times a
+    float32 scale)."""
+    codes = np.asarray(codes)
+    return e4m3_table()[codes.astype(np.int64)] * np.asarray(scale, np.float64)[..., None]
 
 
 # ----------------------------------------------------------------------------- whole layer

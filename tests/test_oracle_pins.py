@@ -337,6 +337,25 @@ def check_fp8(o):
     rel = np.abs(q["dequantized"] - W)[normal] / np.abs(W)[normal]
     assert rel.max() <= 2.0 ** -4 + 1e-7
     assert (o.quantize_rows_e4m3(np.zeros((2, 3)))["dequantized"] == 0).all()
+    # the vectorised encoder agrees with the scalar definition, exact midpoints (ties) included
+    tab = o.e4m3_table()
+    mids = np.array([(tab[c] + tab[c + 1]) / 2 for c in range(0x7E)])
+    vals = np.concatenate([RNG.standard_normal(600) * 40, RNG.standard_normal(200) * 0.01, mids, -mids,
+                           [0.0, -0.0, 448.0, 449.0, 464.0, 1e9, -1e9, 2.0 ** -10, -3 * 2.0 ** -10]])
+    arr = o.e4m3_encode_array(vals)
+    assert arr.dtype == np.uint8
+    assert all(int(a) == o.e4m3_encode(v) for a, v in zip(arr, vals))
+    # float32 division (the rounding a float32 quantiser takes): codes equal torch's float32 quotient
+    # converted by float8_e4m3fn, and the scale equals the float64 path's (one rounding either way)
+    Wb = torch.tensor(RNG.standard_normal((40, 192)) * 0.02, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    Wb[3] = 0.0
+    q32, q64 = o.quantize_rows_e4m3(Wb, "f32"), o.quantize_rows_e4m3(Wb)
+    assert np.array_equal(q32["scale"], q64["scale"]) and q32["scale"][3] == 1.0
+    t32 = torch.tensor(Wb, dtype=torch.float32) / torch.tensor(q32["scale"])[:, None]
+    assert np.array_equal(t32.to(torch.float8_e4m3fn).view(torch.uint8).numpy(), q32["codes"])
+    np.testing.assert_array_equal(o.dequantize_rows_e4m3(q32["codes"], q32["scale"]), q32["dequantized"])
+    with pytest.raises(ValueError):
+        o.quantize_rows_e4m3(Wb, "f16")
 
 
 def check_temperature(o):
@@ -461,6 +480,16 @@ def _mut_e4m3_bias8(code):
 _REAL_E4M3 = O.e4m3_value
 
 
+def _mut_e4m3_ties_away(v):
+    v = np.asarray(v, np.float64)
+    vals = O.e4m3_table()[:0x7F]
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.minimum(np.searchsorted(vals, a, side="left"), 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    code = np.where(a - vals[lo] < vals[hi] - a, lo, hi)
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
 def _mut_coact_upper_only(idx, E):
     C = np.zeros((E, E), dtype=np.int64)
     for row in np.asarray(idx):
@@ -484,6 +513,7 @@ def _mut_coact_upper_only(idx, E):
     ("silu", _mut_silu_sigmoid, check_expert_ffn),
     ("coactivation", _mut_coact_upper_only, check_coactivation),
     ("e4m3_value", _mut_e4m3_bias8, check_fp8),
+    ("e4m3_encode_array", _mut_e4m3_ties_away, check_fp8),
 ])
 def test_planted_mistakes_are_caught(name, fn, check, monkeypatch):
     """Plant one mistake in the oracle module itself (so its internal callers see it too)."""
