@@ -355,14 +355,18 @@ def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
 # ----------------------------------------------------------------------------- whole layer
 def moe_layer(inp: Dict, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
               lb_coef: float = 0.01, z_coef: float = 0.001,
-              tokens: Optional[Sequence[int]] = None) -> Dict:
+              tokens: Optional[Sequence[int]] = None, temperature: float = 1.0) -> Dict:
     """Forward pass of the layer on ``inp`` (the tensors of ``synth.make_inputs``).
 
     Routing, dispatch and losses are computed for every token; the FFNs and the combine only for
-    ``tokens`` (all tokens when None).  Returns routing, layout, losses and y [len(tokens), d]."""
+    ``tokens`` (all tokens when None).  With a router temperature the logits are divided by it
+    before everything that follows (``temper``).  Returns routing, layout, losses and
+    y [len(tokens), d]."""
     x = _f64(inp["x"])
     T = x.shape[0]
     z = router_logits(x, inp["w_router"], inp.get("logit_bias"))
+    if temperature != 1.0:
+        z = temper(z, temperature)
     P, lse = softmax_lse(z)
     idx = topk_select(z, k)
     w = renormalise(P, idx) if T else np.zeros((0, k))

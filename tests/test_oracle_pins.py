@@ -378,6 +378,21 @@ def check_temperature(o):
     assert np.allclose(w[:, 0], 1.0) and np.allclose(w[:, 1:], 0.0)
     with pytest.raises(ValueError):
         o.temper(z, 0.0)
+    # in the layer, tau acts on the logits before everything else: the same as a router (and logit
+    # bias) divided by tau, whatever the drops and shared experts
+    rng = np.random.default_rng(7)
+    inp = _bwd_case(rng, 12, 5, 4, 2, 6, "swiglu", False, 1)
+    inp["logit_bias"] = np.array([0.3, 0.0, -0.2, 0.1])
+    for tau in (0.5, 3.0):
+        a = o.moe_layer(inp, E=4, k=2, act="swiglu", n_shared=1, cf=0.8, temperature=tau)
+        scaled = dict(inp, w_router=inp["w_router"] / tau, logit_bias=inp["logit_bias"] / tau)
+        b = o.moe_layer(scaled, E=4, k=2, act="swiglu", n_shared=1, cf=0.8)
+        assert np.array_equal(a["idx"], b["idx"]) and np.array_equal(a["row_of"], b["row_of"])
+        np.testing.assert_allclose(a["y"], b["y"], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose([a["lb"], a["zl"]], [b["lb"], b["zl"]], rtol=1e-12)
+        # and the losses differ from the untempered layer's (the temperature is not ignored)
+        c = o.moe_layer(inp, E=4, k=2, act="swiglu", n_shared=1, cf=0.8)
+        assert abs(c["zl"] - a["zl"]) > 1e-6
 
 
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
