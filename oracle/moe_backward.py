@@ -81,10 +81,12 @@ def expert_ffn_backward(xr, act: str, dY, w_up, w_down, w_gate=None, b_up=None) 
 
 def moe_layer_backward(inp: Dict, dy, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
                        lb_coef: float = 0.01, z_coef: float = 0.001, dlb: float = 1.0,
-                       dzl: float = 1.0) -> Dict[str, np.ndarray]:
+                       dzl: float = 1.0, temperature: float = 1.0) -> Dict[str, np.ndarray]:
     """Gradients of L = sum_t <dy_t, y_t> + dlb lb + dzl zl with respect to x, the router weights,
-    every routed expert's weights (stacked [E, ...]) and every shared expert's (stacked [S, ...])."""
-    fwd = O.moe_layer(inp, E=E, k=k, act=act, n_shared=n_shared, cf=cf, lb_coef=lb_coef, z_coef=z_coef)
+    every routed expert's weights (stacked [E, ...]) and every shared expert's (stacked [S, ...]).
+    With a router temperature tau the layer sees z / tau, so the logits' gradient is divided by tau."""
+    fwd = O.moe_layer(inp, E=E, k=k, act=act, n_shared=n_shared, cf=cf, lb_coef=lb_coef, z_coef=z_coef,
+                      temperature=temperature)
     x = np.asarray(inp["x"], np.float64)
     dy = np.asarray(dy, np.float64)
     T, d = x.shape
@@ -118,6 +120,7 @@ def moe_layer_backward(inp: Dict, dy, *, E: int, k: int, act: str, n_shared: int
         dz += P * (gP[None, :] - (P @ gP)[:, None])
         dz += (dzl * 2.0 * z_coef * lse / T)[:, None] * P
 
+    dz = dz / float(temperature)  # through z / tau
     g: Dict[str, np.ndarray] = {"dw_router": dz.T @ x, "dx": dz @ Wr}
 
     # routed experts: row r of expert e carries w_tj dy_t
@@ -163,7 +166,9 @@ def moe_layer_backward(inp: Dict, dy, *, E: int, k: int, act: str, n_shared: int
 
 
 def objective(inp: Dict, dy, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
-              lb_coef: float = 0.01, z_coef: float = 0.001, dlb: float = 1.0, dzl: float = 1.0) -> float:
+              lb_coef: float = 0.01, z_coef: float = 0.001, dlb: float = 1.0, dzl: float = 1.0,
+              temperature: float = 1.0) -> float:
     """L = sum_t <dy_t, y_t> + dlb lb + dzl zl from the forward oracle (for finite differences)."""
-    fwd = O.moe_layer(inp, E=E, k=k, act=act, n_shared=n_shared, cf=cf, lb_coef=lb_coef, z_coef=z_coef)
+    fwd = O.moe_layer(inp, E=E, k=k, act=act, n_shared=n_shared, cf=cf, lb_coef=lb_coef, z_coef=z_coef,
+                      temperature=temperature)
     return float(np.sum(np.asarray(dy, np.float64) * fwd["y"])) + dlb * fwd["lb"] + dzl * fwd["zl"]

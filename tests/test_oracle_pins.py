@@ -267,14 +267,18 @@ def check_backward(o, b=None):
     if b is None:
         from oracle import moe_backward as b
     rng = np.random.default_rng(99)
-    cases = [dict(T=7, d=5, E=4, k=2, dff=3, act="gelu", bias=True, n_shared=0, cf=0.75),
-             dict(T=6, d=4, E=3, k=2, dff=3, act="swiglu", bias=False, n_shared=1, cf=0.0),
-             dict(T=5, d=4, E=4, k=1, dff=2, act="swiglu", bias=False, n_shared=0, cf=1.0)]
+    cases = [dict(T=7, d=5, E=4, k=2, dff=3, act="gelu", bias=True, n_shared=0, cf=0.75, tau=1.0),
+             dict(T=6, d=4, E=3, k=2, dff=3, act="swiglu", bias=False, n_shared=1, cf=0.0, tau=1.0),
+             dict(T=5, d=4, E=4, k=1, dff=2, act="swiglu", bias=False, n_shared=0, cf=1.0, tau=1.0),
+             # router temperatures: the logits' gradient through z / tau
+             dict(T=6, d=4, E=4, k=2, dff=3, act="gelu", bias=True, n_shared=1, cf=0.0, tau=0.6),
+             dict(T=6, d=4, E=3, k=2, dff=2, act="swiglu", bias=False, n_shared=0, cf=0.9, tau=2.5)]
     for c in cases:
         cf = c.pop("cf")
+        tau = c.pop("tau")
         inp = _bwd_case(rng, **c)
         kw = dict(E=c["E"], k=c["k"], act=c["act"], n_shared=c["n_shared"], cf=cf, lb_coef=0.3, z_coef=0.2,
-                  dlb=1.0, dzl=1.0)
+                  dlb=1.0, dzl=1.0, temperature=tau)
         dy = rng.standard_normal((c["T"], c["d"]))
         g = b.moe_layer_backward(inp, dy, **kw)
         names = {"x": "dx", "w_router": "dw_router", "w_up": "dw_up", "w_down": "dw_down"}
