@@ -252,6 +252,17 @@ def coactivation_score(C: np.ndarray) -> np.ndarray:
     return S
 
 
+def router_entropy(z: np.ndarray) -> float:
+    """Mean over tokens of the entropy of the router distribution, -sum_e P_te ln P_te (nats), from
+    the logits: H_t = lse_t - sum_e P_te z_te.  A low value means confident (or collapsed) routing,
+    ln E a uniform one -- the routing-collapse signal the GPT-4 2% article's tips watch."""
+    z = np.asarray(z, np.float64)
+    if z.shape[0] == 0:
+        return 0.0
+    P, lse = softmax_lse(z)
+    return float(np.mean(lse - np.sum(P * z, axis=1)))
+
+
 def routing_stats(idx: np.ndarray, E: int, k: int, offsets=None):
     """(load imbalance, dropped fraction).  Imbalance: the busiest expert's token count over the
     uniform share T k / E that the load-balance loss of the OpenMythos article, sec. 3.1, pushes

@@ -239,6 +239,19 @@ def check_coactivation(o):
         imb, drop = o.routing_stats(idx, E, k)
         assert imb >= 1.0 - 1e-12 and drop == 0.0
     assert o.routing_stats(np.zeros((0, 2), dtype=int), 4, 2) == (0.0, 0.0)
+    # router entropy: the definition -sum P ln P directly (scipy's entropy), uniform logits give
+    # ln E, a near one-hot router ~0, two experts the binary entropy of sigmoid(z_0 - z_1)
+    z = RNG.standard_normal((40, 7)) * 2
+    P, _ = o.softmax_lse(z)
+    assert abs(o.router_entropy(z) - float(np.mean(sps.entr(P).sum(axis=1)))) < 1e-12
+    assert abs(o.router_entropy(np.zeros((5, 6))) - math.log(6)) < 1e-14
+    hot = np.zeros((3, 4))
+    hot[:, 2] = 60.0
+    assert o.router_entropy(hot) < 1e-20
+    z2 = RNG.standard_normal((25, 2))
+    p = sps.expit(z2[:, 0] - z2[:, 1])
+    assert abs(o.router_entropy(z2) - float(np.mean(-p * np.log(p) - (1 - p) * np.log(1 - p)))) < 1e-12
+    assert o.router_entropy(np.zeros((0, 3))) == 0.0
 
 
 def _bwd_case(rng, T, d, E, k, dff, act, bias, n_shared, wscale=0.7):
