@@ -223,6 +223,21 @@ def lb_loss_squared_mean_form(P: np.ndarray, lb_coef: float) -> float:
     return lb_coef * E * float(np.sum(pbar * pbar))
 
 
+def lb_loss_kl_frequency_form(P: np.ndarray, counts: np.ndarray, lb_coef: float, eps: float = 1e-8) -> float:
+    """Variant from the GPT-4 2%-parameters article, sec. 4.2 (its load-balancing loss): alpha times
+    the KL divergence of the mean router probabilities Pbar from the uniform distribution,
+    sum_e (1/E)(ln(1/E) - ln(Pbar_e + eps)), plus the squared distance of the selection frequencies
+    f_e = counts_e / sum counts from 1/E.  eps is the article's smoothing inside the logarithm."""
+    P = np.asarray(P, np.float64)
+    E = P.shape[1]
+    pbar = P.mean(axis=0)
+    u = 1.0 / E
+    kl = float(np.sum(u * (math.log(u) - np.log(pbar + eps))))
+    c = np.asarray(counts, np.float64)
+    f = c / c.sum() if c.sum() > 0 else np.zeros(E)
+    return lb_coef * (kl + float(np.sum((f - u) ** 2)))
+
+
 def expert_param_count(d: int, dff: int, act: str = "gelu", bias: bool = False) -> int:
     """Weights of one expert: 2 d dff for the two-matrix form (Naive-N0.5-Flash article sec. 3.3),
     3 d dff for SwiGLU; biases add dff + d."""

@@ -252,6 +252,19 @@ def check_coactivation(o):
     p = sps.expit(z2[:, 0] - z2[:, 1])
     assert abs(o.router_entropy(z2) - float(np.mean(-p * np.log(p) - (1 - p) * np.log(1 - p)))) < 1e-12
     assert o.router_entropy(np.zeros((0, 3))) == 0.0
+    # the GPT-4 2% article's balance form: torch's kl_div (target uniform, log of the smoothed mean
+    # probabilities, summed) plus the squared frequency gap; zero at exactly uniform routing
+    z = RNG.standard_normal((30, 5))
+    P, _ = o.softmax_lse(z)
+    counts = np.array([20, 15, 10, 10, 5])
+    ref_kl = torch.nn.functional.kl_div(torch.log(torch.tensor(P.mean(axis=0)) + 1e-8),
+                                        torch.full((5,), 0.2, dtype=torch.float64), reduction="sum").item()
+    ref = 0.01 * (ref_kl + float(np.sum((counts / counts.sum() - 0.2) ** 2)))
+    assert abs(o.lb_loss_kl_frequency_form(P, counts, 0.01) - ref) < 1e-15
+    assert abs(o.lb_loss_kl_frequency_form(np.full((4, 5), 0.2), np.full(5, 3), 0.5, eps=0.0)) < 1e-15
+    # all tokens to one expert (k = 1): frequency term (E - 1) / E
+    assert abs(o.lb_loss_kl_frequency_form(np.full((4, 5), 0.2), np.array([4, 0, 0, 0, 0]), 1.0, eps=0.0)
+               - 0.8) < 1e-15
 
 
 def _bwd_case(rng, T, d, E, k, dff, act, bias, n_shared, wscale=0.7):
