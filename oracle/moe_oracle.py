@@ -238,6 +238,27 @@ def lb_loss_kl_frequency_form(P: np.ndarray, counts: np.ndarray, lb_coef: float,
     return lb_coef * (kl + float(np.sum((f - u) ** 2)))
 
 
+def moe_layer_backup_expert(inp: Dict, backup: Dict, *, E: int, k: int, act: str, n_shared: int = 0,
+                             cf: float = 0.0, lb_coef: float = 0.01, z_coef: float = 0.001) -> Dict:
+    """Routing variant with a backup expert: the mini-moe tutorial, sec. 6, says that tokens over an
+    expert's capacity are dropped or routed to a backup expert.  Here every assignment the capacity
+    drops goes to one extra expert (weights in ``backup``: w_up, w_down, and w_gate / b_up / b_down
+    as the layer's experts have them), keeping its routing weight:
+        y_t = (the layer's y_t) + sum over dropped slots j of w_tj FFN_backup(x_t).
+    Routing, counts and both losses are the layer's own."""
+    out = moe_layer(inp, E=E, k=k, act=act, n_shared=n_shared, cf=cf, lb_coef=lb_coef, z_coef=z_coef)
+    x = _f64(inp["x"])
+    T = x.shape[0]
+    y = out["y"].copy()
+    for t in range(T):
+        for j in range(k):
+            if int(out["row_of"][t, j]) < 0:
+                f = expert_ffn(x[t:t + 1], act, backup["w_up"], backup["w_down"], backup.get("w_gate"),
+                               backup.get("b_up"), backup.get("b_down"))
+                y[t] += out["w"][t, j] * f[0]
+    return dict(out, y=y, backup_rows=int(np.sum(np.asarray(out["row_of"]) < 0)))
+
+
 def expert_param_count(d: int, dff: int, act: str = "gelu", bias: bool = False) -> int:
     """Weights of one expert: 2 d dff for the two-matrix form (Naive-N0.5-Flash article sec. 3.3),
     3 d dff for SwiGLU; biases add dff + d."""

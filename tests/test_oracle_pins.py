@@ -388,6 +388,29 @@ def check_fp8(o):
         o.quantize_rows_e4m3(Wb, "f16")
 
 
+def check_backup_expert(o):
+    """A backup expert identical to every routed expert makes drops invisible (the dropless layer);
+    a zero backup expert gives the dropping layer; drops are counted."""
+    rng = np.random.default_rng(11)
+    T, d, E, k, f = 16, 5, 4, 2, 6
+    W1, W2 = rng.standard_normal((f, d)), rng.standard_normal((d, f))
+    b1, b2 = rng.standard_normal(f) * 0.1, rng.standard_normal(d) * 0.1
+    inp = dict(x=rng.standard_normal((T, d)), w_router=rng.standard_normal((E, d)),
+               w_up=np.repeat(W1[None], E, 0), w_down=np.repeat(W2[None], E, 0),
+               b_up=np.repeat(b1[None], E, 0), b_down=np.repeat(b2[None], E, 0))
+    same = dict(w_up=W1, w_down=W2, b_up=b1, b_down=b2)
+    a = o.moe_layer_backup_expert(inp, same, E=E, k=k, act="gelu", cf=0.5)
+    assert a["backup_rows"] > 0 and a["drops"] == a["backup_rows"]
+    full = o.moe_layer(inp, E=E, k=k, act="gelu", cf=0.0)
+    np.testing.assert_allclose(a["y"], full["y"], rtol=1e-12, atol=1e-12)
+    # with identical experts and renormalised weights the output is the dense FFN itself
+    np.testing.assert_allclose(a["y"], o.expert_ffn(inp["x"], "gelu", W1, W2, None, b1, b2), rtol=1e-12, atol=1e-12)
+    zero = dict(w_up=np.zeros((f, d)), w_down=np.zeros((d, f)), b_up=np.zeros(f), b_down=np.zeros(d))
+    b = o.moe_layer_backup_expert(inp, zero, E=E, k=k, act="gelu", cf=0.5)
+    np.testing.assert_array_equal(b["y"], o.moe_layer(inp, E=E, k=k, act="gelu", cf=0.5)["y"])
+    assert abs(a["lb"] - full["lb"]) < 1e-15 and abs(a["zl"] - full["zl"]) < 1e-15
+
+
 def check_temperature(o):
     z = RNG.standard_normal((20, 6)) * 2
     assert np.array_equal(o.temper(z, 1.0), z)
@@ -427,7 +450,7 @@ def check_temperature(o):
 
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
               check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
-              check_losses, check_coactivation, check_backward, check_fp8, check_temperature]
+              check_losses, check_coactivation, check_backward, check_fp8, check_temperature, check_backup_expert]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
