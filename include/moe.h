@@ -169,6 +169,15 @@ moe_status moe_layer_forward_timed(const moe_config* cfg, const moe_weights* w, 
  * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_STATUS) and clears it. */
 moe_status moe_read_device_status(void* ws, void* stream);
 
+/* Failure-detection test hook: sets, for every later call that uses the workspace `ws`, how long
+ * a bounded wait inside the tensor-core router (moe_route and the routing step of
+ * moe_layer_forward) may last before it gives up, in nanoseconds; 0 restores the default of one
+ * second.  A wait that gives up stops the CTA's pipeline, lets its copies and tensor-core work in
+ * flight finish, records MOE_ERR_TIMEOUT in the status word and returns (the results of that call
+ * are then meaningless).  The grouped expert GEMMs always keep the one-second limit.  Ordered on
+ * `stream` like the other calls.  MOE_ERR_INVALID_ARG for a NULL or misaligned ws. */
+moe_status moe_set_wait_limit(void* ws, uint64_t limit_ns, void* stream);
+
 /* Number of kernels moe_layer_forward launches for this config (for launch accounting). */
 int32_t moe_layer_forward_launches(const moe_config* cfg);
 
@@ -183,8 +192,9 @@ int32_t moe_layer_forward_launches(const moe_config* cfg);
  *   holds until the process exits.  This call allocates nothing.
  *   Limits: T <= MOE_ROUTE_NOALLOC_MAX_T and T * E <= MOE_ROUTE_NOALLOC_MAX_TE, else
  *   MOE_ERR_UNSUPPORTED (before any GPU work).
- *   The first call on a device looks up that array's device address (once per device, with that
- *   device current); make that first call outside any CUDA stream capture.
+ *   The first call on a device looks up that array's device address (once per device and CUDA
+ *   context, with that device current; again after a cudaDeviceReset replaced the context); make
+ *   that first call outside any CUDA stream capture.
  *   All calls share the one array and it keeps the previous call's contents: each call clears the
  *   status word itself, but two calls whose GPU work may overlap (different streams, or different
  *   host threads, without ordering between them) race on the array and must not be issued.

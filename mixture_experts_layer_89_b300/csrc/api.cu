@@ -7,6 +7,8 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -131,6 +133,16 @@ int num_sms_current() {
 }
 
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// NVTX range around one C-ABI call (host side: it brackets the argument checks and the launches,
+// which is what a profiler's timeline lines up with the kernels).  Costs nothing measurable when no
+// tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 #define MOE_TRY(expr)                      \
   do {                                     \
@@ -380,16 +392,39 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_route_scratch_mu;
 void* g_route_scratch_ptr[kMaxDevices] = {nullptr};
+CUcontext g_route_scratch_ctx[kMaxDevices] = {nullptr};
 
-// Device address of g_route_scratch on the current device (looked up on first use).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, looked up once.
+CtxGetCurrentFn ctx_get_current_fn() {
+  static const CtxGetCurrentFn fn = []() -> CtxGetCurrentFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return nullptr;
+  }();
+  return fn;
+}
+
+// Device address of g_route_scratch on the current device.  Looked up with cudaGetSymbolAddress
+// the first time a device is used, and again whenever that device's current context is no longer
+// the one the address was taken in (after a cudaDeviceReset the module is loaded afresh and the
+// array may move).
 moe_status route_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  const CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_route_scratch_mu);
-  if (!g_route_scratch_ptr[dev]) {
+  if (!g_route_scratch_ptr[dev] || g_route_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
     g_route_scratch_ptr[dev] = p;
+    g_route_scratch_ctx[dev] = ctx;
   }
   *out = g_route_scratch_ptr[dev];
   return MOE_OK;
@@ -418,6 +453,7 @@ moe_status moe_capacity(const moe_config* cfg, int32_t* cap, int32_t* a_max) {
 
 moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
                      int32_t* topk_idx, float* topk_w, int32_t* counts, float* losses, void* ws, void* stream) {
+  NvtxRange nvtx_range("moe_route");
   MOE_TRY(validate(cfg));
   if (!w_router || !counts || !losses || !ws) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!x || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
@@ -428,6 +464,7 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
 
 moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
                              int32_t* topk_idx, float* topk_w, int32_t* counts, float* losses, void* stream) {
+  NvtxRange nvtx_range("moe_route_noalloc");
   MOE_TRY(validate(cfg));
   if (!w_router || !counts || !losses) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!x || !topk_idx || !topk_w)) return MOE_ERR_INVALID_ARG;
@@ -439,13 +476,15 @@ moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w
   void* scratch = nullptr;
   MOE_TRY(route_scratch_address(&scratch));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_CUDA(cudaMemsetAsync(scratch, 0, 2 * sizeof(uint32_t), st));  // status word and CTA counter start at zero
+  // status word, CTA counter and wait-limit override (default) start at zero
+  MOE_CUDA(cudaMemsetAsync(scratch, 0, 4 * sizeof(uint32_t), st));
   return route_impl(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, losses, scratch, st);
 }
 
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx, const int32_t* counts,
                        int32_t* offsets, int32_t* kept, int32_t* row_of, int32_t* tok_of, void* x_perm, void* ws,
                        void* stream) {
+  NvtxRange nvtx_range("moe_permute");
   MOE_TRY(validate(cfg));
   if (!offsets || !kept || !ws) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!x || !topk_idx || !row_of || !tok_of || !x_perm)) return MOE_ERR_INVALID_ARG;
@@ -456,6 +495,7 @@ moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets, const moe_weights* w,
                           void* y_perm, const void* x, void* y_shared, void* ws, void* stream) {
+  NvtxRange nvtx_range("moe_expert_ffn");
   MOE_TRY(validate(cfg));
   MOE_TRY(check_weights(cfg, w));
   if (!offsets || !ws) return MOE_ERR_INVALID_ARG;
@@ -470,6 +510,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
 
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of, const float* topk_w,
                        const void* y_shared, void* y, void* stream) {
+  NvtxRange nvtx_range("moe_combine");
   MOE_TRY(validate(cfg));
   if (cfg->T > 0 && (!row_of || !topk_w || !y || (!y_perm && a_max_of(cfg) > 0))) return MOE_ERR_INVALID_ARG;
   if (misaligned(y_perm) || misaligned(y_shared) || misaligned(y)) return MOE_ERR_INVALID_ARG;
@@ -480,6 +521,7 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
 
 moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const int32_t* offsets, int32_t* coact,
                            float* stats, void* ws, void* stream) {
+  NvtxRange nvtx_range("moe_route_stats");
   MOE_TRY(validate(cfg));
   if (!coact || !stats || !ws || (cfg->T > 0 && !topk_idx)) return MOE_ERR_INVALID_ARG;
   if (cfg->k > 8) return MOE_ERR_UNSUPPORTED;
@@ -490,12 +532,14 @@ moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const
 
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, float* losses,
                              int32_t* counts_out, int32_t* drops_out, void* ws, void* stream) {
+  NvtxRange nvtx_range("moe_layer_forward");
   return layer_impl(cfg, w, x, y, losses, counts_out, drops_out, ws, static_cast<cudaStream_t>(stream), nullptr);
 }
 
 moe_status moe_layer_forward_timed(const moe_config* cfg, const moe_weights* w, const void* x, void* y,
                                    float* losses, int32_t* counts_out, int32_t* drops_out, void* ws, void* stream,
                                    void* const* events, int32_t n_events) {
+  NvtxRange nvtx_range("moe_layer_forward_timed");
   if (!events || n_events != 7) return MOE_ERR_INVALID_ARG;
   cudaEvent_t ev[7];
   for (int i = 0; i < 7; ++i) {
@@ -515,6 +559,14 @@ moe_status moe_read_device_status(void* ws, void* stream) {
   if (cudaMemset(ws, 0, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
   if (v & DEV_TIMEOUT) return MOE_ERR_TIMEOUT;
   return MOE_ERR_DEVICE_STATUS;
+}
+
+moe_status moe_set_wait_limit(void* ws, uint64_t limit_ns, void* stream) {
+  if (!ws || misaligned(ws)) return MOE_ERR_INVALID_ARG;
+  const uint32_t w[2] = {(uint32_t)limit_ns, (uint32_t)(limit_ns >> 32)};
+  // from pageable host memory: the source is staged before the call returns
+  return cuda_status(cudaMemcpyAsync(static_cast<uint32_t*>(ws) + 2, w, sizeof(w), cudaMemcpyHostToDevice,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 int32_t moe_layer_forward_launches(const moe_config* cfg) {

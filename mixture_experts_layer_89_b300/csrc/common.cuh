@@ -21,6 +21,16 @@ enum : uint32_t {
 // A bounded wait gives up after this long (the kernels here finish in milliseconds).
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
+// Words 2 and 3 of the workspace's status block hold an override of that limit in nanoseconds
+// (low word first; 0 = the default), which moe_set_wait_limit writes.  Kernels whose every wait
+// drains what is in flight on its own barriers read it once after their set-up.
+__device__ __forceinline__ unsigned long long wait_limit_ns(const uint32_t* status) {
+  if (!status) return kWaitLimitNs;
+  const volatile uint32_t* w = status;
+  const unsigned long long v = (unsigned long long)w[2] | ((unsigned long long)w[3] << 32);
+  return v ? v : kWaitLimitNs;
+}
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v);
@@ -95,17 +105,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up (returns false) when
-// the CTA-wide abort flag is set or after kWaitLimitNs; on a time-out it raises the abort flag
-// and records DEV_TIMEOUT in the status word, so every other waiter of the CTA also returns.
+// the CTA-wide abort flag is set or after limit_ns; on a time-out it raises the abort flag and
+// records DEV_TIMEOUT in the status word, so every other waiter of the CTA also returns.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  uint32_t* status) {
+                                                  uint32_t* status,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, DEV_TIMEOUT);
         return false;

@@ -265,6 +265,9 @@ __global__ void __launch_bounds__(RTHREADS, 1)
   const uint32_t tmem_base = ctl->tmem_base;
 
   // ------------------------------------------------------------------ main loop
+  // every wait below drains this CTA's own copies and MMAs when it gives up, so the limit may be
+  // shortened through the workspace (moe_set_wait_limit)
+  const unsigned long long wlimit = (warp < 2 && lane == 0) ? wait_limit_ns(a.status) : kWaitLimitNs;
   if (warp == 0 && lane == 0) {
     int s = 0;
     uint32_t ph = 0, armed = 0, armed_ph = 0;
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const int kb0 = (int)(tile % (unsigned)nk);
     for (int i = 0; i < nk; ++i) {
       const int kb = kb_lo + (kb0 + i < nk ? kb0 + i : kb0 + i - nk);
-      if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.status)) {
+      if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, a.status, wlimit)) {
         aborted = true;
         break;
       }
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     int s = 0;
     uint32_t ph = 0;
     for (int kb = 0; kb < kb_hi - kb_lo; ++kb) {
-      if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, a.status)) break;
+      if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, a.status, wlimit)) break;
       tc_fence_after();
       const uint32_t sa = smem_u32(smem + (size_t)s * stage_bytes);
       const uint32_t sb = sa + a_bytes;

@@ -65,12 +65,14 @@ def lib() -> ctypes.CDLL:
                                               P(_c_p), _c_i32]
         L.moe_read_device_status.argtypes = [_c_p, _c_p]
         L.moe_layer_forward_launches.argtypes = [cfgp]
+        L.moe_set_wait_limit.argtypes = [_c_p, ctypes.c_uint64, _c_p]
         L.moe_route_stats.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
         for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute",
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
-                     "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats"):
+                     "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
+                     "moe_set_wait_limit"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -78,7 +80,7 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
-            "moe_layer_forward_launches", "moe_route_stats", "moe_status_string")
+            "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_status_string")
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -195,6 +197,11 @@ def moe_read_device_status(ws, stream=None) -> int:
 def moe_route_stats(cfg, topk_idx, offsets, coact, stats, ws, stream=None):
     _check(lib().moe_route_stats(ctypes.byref(cfg), _p(topk_idx), _p(offsets), _p(coact), _p(stats), _p(ws),
                                  _s(stream)), "moe_route_stats")
+
+
+def moe_set_wait_limit(ws, limit_ns: int, stream=None):
+    """Shorten (or, with 0, restore) the router's bounded waits for calls that use ``ws``."""
+    _check(lib().moe_set_wait_limit(_p(ws), int(limit_ns), _s(stream)), "moe_set_wait_limit")
 
 
 def moe_layer_forward_launches(cfg) -> int:

@@ -118,3 +118,8 @@ def test_launch_count(L, name):
     router, dispatch = (1, 2) if wl.dtype == "bf16" else (2, 4)
     assert n == router + dispatch + 2 + (2 if wl.n_shared else 0) + 1
     assert moe.moe_layer_forward_launches(moe.config_from_workload(wl, T=0)) == router - 1 + 1
+
+
+def test_wait_limit_setter_rejects_bad_workspace_on_host(L):
+    assert L.moe_set_wait_limit(None, 5, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_set_wait_limit((1 << 12) + 8, 5, None) == moe.MOE_ERR_INVALID_ARG   # misaligned, never touched

@@ -193,6 +193,54 @@ def check_layer_reductions(o):
     np.testing.assert_allclose(sub["y"], full["y"][[3, 0, 14]], rtol=1e-13, atol=1e-13)
 
 
+def _frac(a):
+    a = np.asarray(a, dtype=np.float64)
+    return a[..., 0] / a[..., 1]
+
+
+def check_combine_fixture(o):
+    # hand-worked fixture (tests/golden/combine_distinct_experts.json): three experts with distinct
+    # constant outputs, k = 2, so the pairing of each slot's weight with its expert's row shows
+    g = json.load(open(os.path.join(GOLDEN, "combine_distinct_experts.json")))
+    E, k = g["E"], g["k"]
+    x = np.log(np.asarray(g["x_as_log"], np.float64))
+    c = np.asarray(g["c"], np.float64)
+    T, d = x.shape
+    inp = dict(x=x, w_router=np.eye(E, d), logit_bias=None,
+               w_up=np.zeros((E, 1, d)), b_up=np.zeros((E, 1)), w_down=np.zeros((E, d, 1)), b_down=c.copy())
+    out = o.moe_layer(inp, E=E, k=k, act="gelu", lb_coef=0.01)
+    assert out["idx"].tolist() == g["topk_idx"]
+    np.testing.assert_allclose(out["w"], _frac(g["topk_w"]), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(out["y"], _frac(g["y_dropless"]), rtol=1e-13, atol=1e-13)
+    assert abs(out["lb"] - 0.01 * g["lb_over_alpha"]) < 1e-15
+    cap = o.moe_layer(inp, E=E, k=k, act="gelu", cf=g["capacity_factor"])
+    assert cap["cap"] == g["capacity"]
+    assert cap["row_of"].tolist() == g["row_of_capped"]
+    assert cap["kept_counts"].tolist() == g["kept_capped"]
+    np.testing.assert_allclose(cap["y"], _frac(g["y_capped"]), rtol=1e-13, atol=1e-13)
+    # per-token brute force on random distinct experts (k = 3 of E = 5, SwiGLU, shared expert,
+    # capacity drops): y_t = sum over kept slots of w_tj FFN_{e_tj}(x_t) + FFN_shared(x_t),
+    # evaluated token by token without the expert-sorted layout
+    T, d, E, k, f = 23, 6, 5, 3, 8
+    inp = dict(x=RNG.standard_normal((T, d)), w_router=RNG.standard_normal((E, d)), logit_bias=None,
+               w_gate=RNG.standard_normal((E, f, d)), w_up=RNG.standard_normal((E, f, d)),
+               w_down=RNG.standard_normal((E, d, f)), ws_gate=RNG.standard_normal((1, f, d)),
+               ws_up=RNG.standard_normal((1, f, d)), ws_down=RNG.standard_normal((1, d, f)))
+    out = o.moe_layer(inp, E=E, k=k, act="swiglu", n_shared=1, cf=0.8)
+    assert out["drops"] > 0
+    z = inp["x"] @ inp["w_router"].T
+    for t in range(T):
+        sel = sorted(range(E), key=lambda e: (-z[t, e], e))[:k]
+        p = np.exp(z[t] - z[t].max())
+        p = p / p.sum()
+        yt = _torch_ffn(inp["x"][t:t + 1], "swiglu", inp["ws_up"][0], inp["ws_down"][0], inp["ws_gate"][0])[0]
+        for j, e in enumerate(sel):
+            if out["row_of"][t, j] >= 0:
+                yt = yt + p[e] / p[sel].sum() * _torch_ffn(inp["x"][t:t + 1], "swiglu", inp["w_up"][e],
+                                                            inp["w_down"][e], inp["w_gate"][e])[0]
+        np.testing.assert_allclose(out["y"][t], yt, rtol=1e-10, atol=1e-10)
+
+
 def check_losses(o):
     E, T, k = 8, 32, 2
     # zero router weights: every Pbar_e = 1/E exactly, so lb = alpha for any counts; zl = beta (ln E)^2
@@ -449,7 +497,7 @@ def check_temperature(o):
 
 
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
-              check_dispatch, check_activations, check_expert_ffn, check_layer_reductions,
+              check_dispatch, check_activations, check_expert_ffn, check_layer_reductions, check_combine_fixture,
               check_losses, check_coactivation, check_backward, check_fp8, check_temperature, check_backup_expert]
 
 
@@ -533,6 +581,11 @@ def _mut_combine_unweighted(idx, w, row_of, y_perm, tokens, y_shared=None):
     return O_combine(idx, np.ones_like(w), row_of, y_perm, tokens, y_shared)
 
 
+def _mut_combine_reversed_slots(idx, w, row_of, y_perm, tokens, y_shared=None):
+    # each slot's weight paired with the other slot's row (the weights reversed across the slots)
+    return O_combine(idx, np.ascontiguousarray(w[:, ::-1]), row_of, y_perm, tokens, y_shared)
+
+
 def _mut_silu_sigmoid(u):
     return sps.expit(u)
 
@@ -578,6 +631,8 @@ def _mut_coact_upper_only(idx, E):
     ("expert_ffn", _mut_ffn_no_bias, check_expert_ffn),
     ("capacity", _mut_capacity_floor, check_capacity),
     ("combine", _mut_combine_unweighted, check_layer_reductions),
+    ("combine", _mut_combine_unweighted, check_combine_fixture),
+    ("combine", _mut_combine_reversed_slots, check_combine_fixture),
     ("silu", _mut_silu_sigmoid, check_expert_ffn),
     ("coactivation", _mut_coact_upper_only, check_coactivation),
     ("e4m3_value", _mut_e4m3_bias8, check_fp8),
