@@ -171,8 +171,8 @@ moe_status moe_read_device_status(void* ws, void* stream);
 
 /* Failure-detection test hook: sets, for every later call that uses the workspace `ws`, how long
  * a bounded wait inside the tensor-core router (moe_route and the routing step of
- * moe_layer_forward) may last before it gives up, in nanoseconds; 0 restores the default of one
- * second.  A wait that gives up stops the CTA's pipeline, lets its copies and tensor-core work in
+ * moe_layer_forward) may last before it gives up, in nanoseconds (counted on the SM's cycle
+ * counter at a nominal 2 cycles per nanosecond); 0 restores the default of one second.  A wait that gives up stops the CTA's pipeline, lets its copies and tensor-core work in
  * flight finish, records MOE_ERR_TIMEOUT in the status word and returns (the results of that call
  * are then meaningless).  The grouped expert GEMMs always keep the one-second limit.  Ordered on
  * `stream` like the other calls.  MOE_ERR_INVALID_ARG for a NULL or misaligned ws. */

@@ -104,12 +104,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same phase (returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of `bar` with parity `parity` to complete.  Gives up (returns false) when
 // the CTA-wide abort flag is set or after limit_ns; on a time-out it raises the abort flag and
 // records DEV_TIMEOUT in the status word, so every other waiter of the CTA also returns.
+// The default limit is measured on the global timer between blocking polls.  A shortened limit
+// (the failure-detection test hook) is measured with non-blocking polls on the SM's cycle counter
+// at 2 cycles per nanosecond, because a blocking poll alone may outlast it and the global timer
+// ticks too coarsely for a limit of a few nanoseconds.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                   uint32_t* status,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns != kWaitLimitNs) {
+    const long long c0 = clock64();
+    const long long limit_cycles = (long long)(limit_ns < (1ull << 40) ? limit_ns : (1ull << 40)) * 2;
+    for (;;) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (clock64() - c0 > limit_cycles) {
+        *abort_flag = 1;
+        atomicOr(status, DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
