@@ -30,7 +30,8 @@
  *  - A_max = T*k (dropless) or min(T*k, E*C): the row capacity of the expert-sorted buffers.
  *  - Shape limits: 1 <= k <= min(E, 8), 1 <= E <= 256, T >= 0, d >= 1, dff >= 1.  bf16 layers
  *    also need d % 64 == 0 and dff % 64 == 0 (tensor-core tiles), and with n_shared > 1 also
- *    dff % 128 == 0 (SwiGLU) or dff % 256 == 0 (GELU).  Violations return MOE_ERR_UNSUPPORTED.
+ *    dff % 128 == 0 (SwiGLU) or dff % 256 == 0 (GELU); bf16 SwiGLU layers need distinct gate and
+ *    up weight tensors (w_gate != w_up, ws_gate != ws_up).  Violations return MOE_ERR_UNSUPPORTED.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -224,6 +225,11 @@ moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const
 
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);
+
+/* Text of the last host-side failure behind a MOE_ERR_CUDA on this host thread (a tensor-map
+ * encoding or a launch-configuration problem of the tensor-core kernels); "" if none.  Valid until
+ * the next call on this thread. */
+const char* moe_last_error(void);
 
 #ifdef __cplusplus
 }

@@ -117,21 +117,6 @@ inline P* at(void* ws, size_t off) {
 
 inline bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-// SM count of the current device, looked up once per device (atomics: callers may be on several
-// host threads).
-int num_sms_current() {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (dev < 0 || dev >= 64) return 148;
-  int n = cache[dev].load(std::memory_order_relaxed);
-  if (n <= 0) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cache[dev].store(n, std::memory_order_relaxed);
-  }
-  return n;
-}
-
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // NVTX range around one C-ABI call (host side: it brackets the argument checks and the launches,
@@ -190,71 +175,83 @@ moe_status permute_impl(const moe_config* c, const void* x, const int32_t* topk_
   return MOE_OK;
 }
 
-moe_status run_projection(const moe_config* c, const Projection& p, uint32_t* status, cudaStream_t st) {
-  cudaError_t e = is_bf16(c) ? launch_projection_tc(p, status, num_sms_current(), st)
-                             : launch_projection_simt(false, p, st);
-  return cuda_status(e);
+moe_status run_projection_simt(const Projection& p, cudaStream_t st) {
+  return cuda_status(launch_projection_simt(false, p, st));
 }
 
-moe_status ffn_routed_impl(const moe_config* c, const void* x_perm, const int32_t* offsets, const moe_weights* w,
-                           void* y_perm, void* ws, cudaStream_t st, cudaEvent_t ev_mid) {
+// The projections of the expert FFNs: routed experts over x_perm (groups from the device-side
+// offsets) and the shared experts over x, concatenated into one expert whose hidden layer is S dff
+// wide.  bf16 layers run both in one launch per projection (up, then down); fp32 layers run four
+// CUDA-core launches.  ev_up / ev_down (timed variant only) are recorded after the up and the down
+// projections of the routed experts.
+moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offsets, const moe_weights* w,
+                    void* y_perm, const void* x, void* y_shared, void* ws, cudaStream_t st, cudaEvent_t ev_up,
+                    cudaEvent_t ev_down) {
   const WsLayout L = layout(c);
   uint32_t* status = at<uint32_t>(ws, L.status);
   const int A = (int)a_max_of(c);
   const bool swiglu = c->act == MOE_ACT_SWIGLU;
+  const int S = c->n_shared;
+  const bool shared = S > 0 && c->T > 0;
   void* h = at<char>(ws, L.h);
+  void* hs = at<char>(ws, L.h_sh);
+  Projection up[2] = {}, dn[2] = {};
+  int nup = 0;
+  // a token picks an expert at most once, so no expert receives more than T rows (or C with a capacity)
+  const int64_t cap64 = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
+  const int routed_rows = (int)(cap64 >= 0 && cap64 < c->T ? cap64 : c->T);
   if (A > 0) {
-    Projection up{};
-    up.A = x_perm; up.lda = c->d; up.rows_alloc = A;
-    up.offsets = offsets; up.G = c->E; up.rows_static = 0;
-    up.B0 = swiglu ? w->w_gate : w->w_up; up.B1 = w->w_up;
-    up.bias = c->has_bias ? w->b_up : nullptr;
-    up.N = c->dff; up.K = c->d; up.N_w = c->dff; up.K_w = c->d; up.G_w = c->E;
-    up.act = swiglu ? ACT_SWIGLU : ACT_GELU;
-    up.out = h; up.ldc = c->dff;
-    MOE_TRY(run_projection(c, up, status, st));
+    Projection& p = up[nup++];
+    p.A = x_perm; p.lda = c->d; p.rows_alloc = A;
+    p.offsets = offsets; p.G = c->E; p.rows_static = 0;
+    p.B0 = swiglu ? w->w_gate : w->w_up; p.B1 = w->w_up;
+    p.bias = c->has_bias ? w->b_up : nullptr;
+    p.N = c->dff; p.K = c->d; p.N_w = c->dff; p.K_w = c->d; p.G_w = c->E;
+    p.act = swiglu ? ACT_SWIGLU : ACT_GELU;
+    p.out = h; p.ldc = c->dff; p.max_group_rows = routed_rows;
+    Projection& q = dn[nup - 1];
+    q.A = h; q.lda = c->dff; q.rows_alloc = A;
+    q.offsets = offsets; q.G = c->E; q.rows_static = 0;
+    q.B0 = w->w_down; q.B1 = nullptr;
+    q.bias = c->has_bias ? w->b_down : nullptr;
+    q.N = c->d; q.K = c->dff; q.N_w = c->d; q.K_w = c->dff; q.G_w = c->E;
+    q.act = ACT_NONE;
+    q.out = y_perm; q.ldc = c->d; q.out_f32 = true; q.max_group_rows = routed_rows;
   }
-  if (ev_mid) MOE_CUDA(cudaEventRecord(ev_mid, st));
-  if (A > 0) {
-    Projection dn{};
-    dn.A = h; dn.lda = c->dff; dn.rows_alloc = A;
-    dn.offsets = offsets; dn.G = c->E; dn.rows_static = 0;
-    dn.B0 = w->w_down; dn.B1 = nullptr;
-    dn.bias = c->has_bias ? w->b_down : nullptr;
-    dn.N = c->d; dn.K = c->dff; dn.N_w = c->d; dn.K_w = c->dff; dn.G_w = c->E;
-    dn.act = ACT_NONE;
-    dn.out = y_perm; dn.ldc = c->d; dn.out_f32 = true;
-    MOE_TRY(run_projection(c, dn, status, st));
+  if (shared) {
+    Projection& p = up[nup++];
+    p.A = x; p.lda = c->d; p.rows_alloc = c->T;
+    p.offsets = nullptr; p.G = 1; p.rows_static = c->T;
+    p.B0 = swiglu ? w->ws_gate : w->ws_up; p.B1 = w->ws_up;
+    p.bias = nullptr;
+    p.N = S * c->dff; p.K = c->d; p.N_w = c->dff; p.K_w = c->d; p.G_w = S;
+    p.act = swiglu ? ACT_SWIGLU : ACT_GELU;
+    p.out = hs; p.ldc = (int64_t)S * c->dff; p.max_group_rows = c->T;
+    Projection& q = dn[nup - 1];
+    q.A = hs; q.lda = (int64_t)S * c->dff; q.rows_alloc = c->T;
+    q.offsets = nullptr; q.G = 1; q.rows_static = c->T;
+    q.B0 = w->ws_down; q.B1 = nullptr; q.bias = nullptr;
+    q.N = c->d; q.K = S * c->dff; q.N_w = c->d; q.K_w = c->dff; q.G_w = S;
+    q.act = ACT_NONE;
+    q.out = y_shared; q.ldc = c->d; q.out_f32 = true; q.max_group_rows = c->T;
+  }
+  if (is_bf16(c)) {
+    if (nup) MOE_CUDA(launch_projection_tc(up, nup, status, st));
+    if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
+    if (nup) MOE_CUDA(launch_projection_tc(dn, nup, status, st));
+    if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
+    return MOE_OK;
+  }
+  const int nrouted = A > 0 ? 1 : 0;
+  if (nrouted) MOE_TRY(run_projection_simt(up[0], st));
+  if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
+  if (nrouted) MOE_TRY(run_projection_simt(dn[0], st));
+  if (ev_down) MOE_CUDA(cudaEventRecord(ev_down, st));
+  if (shared) {
+    MOE_TRY(run_projection_simt(up[nrouted], st));
+    MOE_TRY(run_projection_simt(dn[nrouted], st));
   }
   return MOE_OK;
-}
-
-// Shared experts, concatenated: the S hidden layers form one hidden layer of width S dff.
-moe_status ffn_shared_impl(const moe_config* c, const void* x, const moe_weights* w, void* y_shared, void* ws,
-                           cudaStream_t st) {
-  if (c->n_shared <= 0 || c->T <= 0) return MOE_OK;
-  const WsLayout L = layout(c);
-  uint32_t* status = at<uint32_t>(ws, L.status);
-  const bool swiglu = c->act == MOE_ACT_SWIGLU;
-  const int S = c->n_shared;
-  void* hs = at<char>(ws, L.h_sh);
-  Projection up{};
-  up.A = x; up.lda = c->d; up.rows_alloc = c->T;
-  up.offsets = nullptr; up.G = 1; up.rows_static = c->T;
-  up.B0 = swiglu ? w->ws_gate : w->ws_up; up.B1 = w->ws_up;
-  up.bias = nullptr;
-  up.N = S * c->dff; up.K = c->d; up.N_w = c->dff; up.K_w = c->d; up.G_w = S;
-  up.act = swiglu ? ACT_SWIGLU : ACT_GELU;
-  up.out = hs; up.ldc = (int64_t)S * c->dff;
-  MOE_TRY(run_projection(c, up, status, st));
-  Projection dn{};
-  dn.A = hs; dn.lda = (int64_t)S * c->dff; dn.rows_alloc = c->T;
-  dn.offsets = nullptr; dn.G = 1; dn.rows_static = c->T;
-  dn.B0 = w->ws_down; dn.B1 = nullptr; dn.bias = nullptr;
-  dn.N = c->d; dn.K = S * c->dff; dn.N_w = c->d; dn.K_w = c->dff; dn.G_w = S;
-  dn.act = ACT_NONE;
-  dn.out = y_shared; dn.ldc = c->d; dn.out_f32 = true;
-  return run_projection(c, dn, status, st);
 }
 
 moe_status check_weights(const moe_config* c, const moe_weights* w) {
@@ -263,54 +260,13 @@ moe_status check_weights(const moe_config* c, const moe_weights* w) {
   if (c->has_bias && (!w->b_up || !w->b_down)) return MOE_ERR_INVALID_ARG;
   if (c->n_shared > 0 && (!w->ws_up || !w->ws_down || (c->act == MOE_ACT_SWIGLU && !w->ws_gate)))
     return MOE_ERR_INVALID_ARG;
+  // bf16 SwiGLU experts read their gate and up rows through one tensor map spanning both tensors
+  if (is_bf16(c) && c->act == MOE_ACT_SWIGLU && (w->w_gate == w->w_up || (c->n_shared > 0 && w->ws_gate == w->ws_up)))
+    return MOE_ERR_UNSUPPORTED;
   const void* ps[] = {w->w_router, w->w_up, w->w_gate, w->w_down, w->b_up, w->b_down, w->ws_up, w->ws_gate, w->ws_down};
   for (const void* p : ps)
     if (p && misaligned(p)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
-}
-
-// A second stream per (host thread, device) on which the shared experts run beside the router,
-// the dispatch and the routed projections, forked from and joined back to the caller's stream
-// with events (which stream capture records as graph edges).  Created on first use; never
-// created while the caller's stream is being captured.
-struct SideStream {
-  cudaStream_t s = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-constexpr int kSideDevices = 64;
-thread_local SideStream t_side[kSideDevices];
-
-SideStream* side_stream(cudaStream_t st) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideDevices) return nullptr;
-  SideStream& ss = t_side[dev];
-  if (ss.s) return &ss;
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
-  cudaStream_t s = nullptr;
-  cudaEvent_t a = nullptr, b = nullptr;
-  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-  if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
-    if (a) cudaEventDestroy(a);
-    cudaStreamDestroy(s);
-    return nullptr;
-  }
-  ss.s = s;
-  ss.fork = a;
-  ss.join = b;
-  return &ss;
-}
-
-// The shared experts go to the side stream only when their two projections together occupy at
-// most a third of the SMs: then they run on otherwise idle SMs.  Larger ones fill the GPU by
-// themselves and stay on the caller's stream.
-bool shared_on_side_stream(const moe_config* c) {
-  if (c->n_shared <= 0 || c->T <= 0 || !is_bf16(c)) return false;
-  const int64_t mt = (c->T + 127) / 128;
-  const int64_t hid = (int64_t)c->n_shared * c->dff * (c->act == MOE_ACT_SWIGLU ? 2 : 1);
-  const int64_t tiles = mt * ((hid + 255) / 256) + mt * ((c->d + 255) / 256);
-  return tiles * 3 <= num_sms_current();
 }
 
 moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, void* y, float* losses,
@@ -343,14 +299,6 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
   // histograms fit its shared memory; else the router's last CTA does, scan included when it fits
   const bool dfused = is_bf16(c) && dispatch_fuses_scan(c->T, c->E);
   const bool scanned = !dfused && is_bf16(c) && route_tc_fuses_scan(c->T, c->E);
-  // stage timing (ev) keeps every step on the caller's stream so that each stage is timed alone
-  SideStream* side = (!ev && shared_on_side_stream(c)) ? side_stream(st) : nullptr;
-  if (side) {
-    MOE_CUDA(cudaEventRecord(side->fork, st));
-    MOE_CUDA(cudaStreamWaitEvent(side->s, side->fork, 0));
-    MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, side->s));
-    MOE_CUDA(cudaEventRecord(side->join, side->s));
-  }
   MOE_TRY(rec(0));
   MOE_TRY(route_impl(c, x, w->w_router, w->router_logit_bias, topk_idx, topk_w, counts, losses, ws, st,
                      dfused ? nullptr : &scan, !dfused));
@@ -366,12 +314,8 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
                          x_perm, drops, ws, st, scanned));
   }
   MOE_TRY(rec(2));
-  MOE_TRY(ffn_routed_impl(c, x_perm, offsets, w, y_perm, ws, st, ev ? ev[3] : nullptr));
-  MOE_TRY(rec(4));
-  if (side)
-    MOE_CUDA(cudaStreamWaitEvent(st, side->join, 0));
-  else
-    MOE_TRY(ffn_shared_impl(c, x, w, y_sh, ws, st));
+  // routed and shared experts (bf16: one launch per projection carries both)
+  MOE_TRY(ffn_impl(c, x_perm, offsets, w, y_perm, x, y_sh, ws, st, ev ? ev[3] : nullptr, ev ? ev[4] : nullptr));
   MOE_TRY(rec(5));
   MOE_CUDA(launch_combine(is_bf16(c), static_cast<const float*>(y_perm), row_of, topk_w,
                           static_cast<const float*>(y_sh), y, c->T, c->d, c->k, st));
@@ -503,9 +447,8 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32
   if (cfg->n_shared > 0 && cfg->T > 0 && (!x || !y_shared)) return MOE_ERR_INVALID_ARG;
   if (misaligned(ws) || misaligned(x_perm) || misaligned(y_perm) || misaligned(x) || misaligned(y_shared))
     return MOE_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  MOE_TRY(ffn_routed_impl(cfg, x_perm, offsets, w, y_perm, ws, st, nullptr));
-  return ffn_shared_impl(cfg, x, w, y_shared, ws, st);
+  return ffn_impl(cfg, x_perm, offsets, w, y_perm, x, y_shared, ws, static_cast<cudaStream_t>(stream), nullptr,
+                  nullptr);
 }
 
 moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of, const float* topk_w,
@@ -579,11 +522,14 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   const bool scanned = dfused || (is_bf16(cfg) && route_tc_fuses_scan(cfg->T, cfg->E));
   if (!tokens) n += 1;                        // scan (writes zero offsets)
   else n += (scanned ? 0 : 2) + dispatch_launches(true, cfg->d, is_bf16(cfg) ? 2 : 4);  // [hist, scan,] dispatch
-  if (a_max_of(cfg) > 0) n += 2;              // routed up + down projections
-  if (cfg->n_shared > 0 && tokens) n += 2;    // shared up + down projections
+  const bool routed = a_max_of(cfg) > 0, shared = cfg->n_shared > 0 && tokens;
+  if (is_bf16(cfg)) n += (routed || shared) ? 2 : 0;           // up + down, routed and shared together
+  else n += (routed ? 2 : 0) + (shared ? 2 : 0);                // routed up + down, shared up + down
   if (tokens) n += 1;                         // combine
   return n;
 }
+
+const char* moe_last_error(void) { return tc_last_error(); }
 
 const char* moe_status_string(moe_status s) {
   switch (s) {

@@ -1,35 +1,55 @@
-// Grouped expert projection on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+// Grouped expert projections on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
 //
 // Once tokens are grouped by expert, each expert's FFN is a dense matrix product over that
 // expert's rows (the Naive-N0.5-Flash article, sec. 4.2, recommends exactly this grouping for
-// inference), so the experts run here as one persistent grouped GEMM per projection:
+// inference), so the experts run as one persistent grouped GEMM per projection:
 //   up:   h = GELU(x_perm W_up^T + b_up)          or  h = SiLU(x_perm W_gate^T) * (x_perm W_up^T)
 //   down: y_perm = h W_down^T (+ b_down)
-// (expert forms: mini-moe tutorial, sec. 3.1; GPT-4 2% article, sec. 3.1).
+// (expert forms: mini-moe tutorial, sec. 3.1; GPT-4 2% article, sec. 3.1).  One launch may carry
+// two such problems -- the routed experts and the always-on shared experts (FLAME-MoE summary,
+// sec. 2) -- whose tiles share the persistent CTAs.
 //
-// Tile: 128 rows x 256 accumulator columns, K step 64 (one 128-byte swizzle row of bf16).  For
-// SwiGLU the 256 columns are 128 gate columns followed by the same 128 up columns, so one MMA
-// (M=128, N=256, K=16) produces both halves and the epilogue multiplies them in registers.
+// Orientation: the weights are the MMA's M side and the tokens its N side,
+//   D[feature, token] = sum_k W[feature, k] X[token, k],
+// so a tile always has 256 weight rows (the 2-SM MMA's M) and as many token rows as the expert
+// has left, rounded up to 16 (the MMA's N step), at most 256.  An expert with 225 tokens costs a
+// 240-column MMA instead of two 256-row tiles: each expert wastes at most 15 token rows.
+//
+// CTAs run in clusters of two (cta_group::2).  A tile is 256 weight rows x N token rows; CTA c of
+// the pair holds weight rows [128c, 128c + 128) and token rows [c N/2, (c + 1) N/2) of each K step
+// in its own shared memory, and the even CTA issues tcgen05.mma.cta_group::2 (M = 256) that reads
+// both CTAs' operands; CTA c's TMEM receives the 128 x N accumulator of its own weight rows.
+// SwiGLU: each CTA's 128 weight rows are the gate and the up rows of the same 64 features,
+// interleaved in blocks of 16 (16 gate rows, their 16 up rows, ...), loaded as ONE box through a
+// 5-D tensor map over (k, row in block, {gate, up}, block, expert) whose {gate, up} dimension
+// strides from one weight tensor to the other; each 32-lane TMEM quarter then holds the gate and
+// up accumulators of 16 features and one warp shuffle pairs them.  A pair tile covers 256 output
+// features (GELU, down) or 128 (SwiGLU).  TMA boxes stay large throughout: a box's issue cost is
+// nearly fixed, and splitting a stage into 8-row or 16-row boxes was measured 2-3x slower.
+// Calls whose every group has at most 32 token rows (decode-sized batches) use a variant with
+// 32-token tiles, whose small stages leave room for more weight bytes in flight.
+//
 // Warp roles (one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: A tile (rows of one expert; only its 32-row groups when the tile
-//               has few rows) + B tile (that expert's weights), 4 stages
-//   warp 1      MMA issuer (one thread): 4 x tcgen05.mma per stage into a TMEM accumulator
-//   warp 2      TMEM allocator (512 columns = two 256-column accumulators, double buffered)
-//   warp 3      builds the tile table from the device-side expert offsets (no count returns to
-//               the host)
-//   warps 4..   EPIW epilogue warps: tcgen05.ld (thread = row), bias/activation, bf16 or fp32
-//               32x32 tiles staged in swizzled shared memory and written by TMA tile stores.
-//               Warp w reaches TMEM lanes 32 (w % 4)..; warps w, w + 4, ... split the columns.
-// Paired mode (PAIR): 2-SM MMAs.  CTAs run in clusters of two that take the two 128-row halves of a
-// 256-row tile of one expert; each holds its own 128 A rows and half of the 256 B rows in shared
-// memory (32 KB per stage instead of 48, so 6 stages), and the even CTA issues
-// tcgen05.mma.cta_group::2 (M=256) that reads both CTAs' operands and writes both CTAs' TMEM.
-// Both CTAs' loads signal the leader's stage barriers; the leader's commits signal both CTAs'
-// "stage free" and "accumulator full" barriers; both epilogues signal the leader's "accumulator
-// free" barrier.  Per SM, operand traffic drops by a third for the same FLOPs.  Tiles are
-// enumerated m-tile-major with n fastest (measured faster than n-major here).  Launched as a
-// programmatic dependent launch: the set-up overlaps the previous kernel's tail.
+//   warp 0      TMA producer: this CTA's weight rows and token rows of a K step, one box each
+//               (6 stages of 32 KB; decode-sized 10 of 18 KB), all signalling the even CTA's
+//               stage barrier
+//   warp 1      MMA issuer (one thread of the even CTA): tcgen05.mma per 16-wide K step into one
+//               of two 256-column TMEM accumulators (double buffered: the epilogue of a tile
+//               overlaps the next tile's MMAs)
+//   warp 2      TMEM allocation (512 columns, both CTAs together)
+//   warp 3      tile table from the device-side expert offsets (no count returns to the host)
+//   warps 4..   EPIW epilogue warps: tcgen05.ld (thread = feature, registers = 32 tokens), bias,
+//               activation, then the transposed 32-token x 32-feature block through shared memory
+//               to a TMA tile store; blocks that reach past an expert's rows are stored directly
+//               instead (SwiGLU always stores directly: each half-warp writes 32 contiguous bytes
+//               of a token row).  Warp w reads TMEM lanes 32 (w % 4)..; warps w, w + 4, ... split
+//               the token columns.
+// Tiles are ordered problem, expert, feature tile, token tile (token tiles fastest), so the pairs
+// working at the same time share the weight tile in L2 and each weight tile is read from HBM once.
+// Launched as a programmatic dependent launch: the set-up overlaps the previous kernel's tail.
+// Every wait is bounded (one second); a CTA that gives up drains the copies and MMAs it started.
 #include <stdio.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -39,32 +59,57 @@
 namespace moe {
 
 namespace {
-constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int BNB = 256;  // B rows per tile (accumulator columns)
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BNB * BK * 2;
-constexpr int MAX_STAGES = 6;
-// single CTA: A + the whole B tile per stage, 4 stages; pair: A + half of B per CTA, 6 stages
-constexpr int stages_of(bool pair) { return pair ? 6 : 4; }
-constexpr int stage_bytes_of(bool pair) { return A_BYTES + (pair ? B_BYTES / 2 : B_BYTES); }
-constexpr int STAGE_REGION = 4 * (A_BYTES + B_BYTES);
-static_assert(6 * (A_BYTES + B_BYTES / 2) == STAGE_REGION, "both stage layouts fill the same region");
-constexpr int MAXG = 256;
+constexpr int BK = 64;                          // K per stage: one 128-byte swizzle row of bf16
+constexpr int AR = 128;                         // weight rows per CTA (the pair's M = 256)
+constexpr int WBOX = AR * BK * 2;               // 16 KB: one weight tile of a CTA
+constexpr int MAXP = 2;                         // problems per launch: routed and shared experts
+constexpr int MAXGT = 256 + 1;                  // groups over both problems
+constexpr int TBL_PER_LANE = (MAXGT + 31) / 32;
+constexpr int MAX_STAGES = 12;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = umma_idesc_bf16(BM, BNB);
-constexpr uint32_t IDESC_PAIR = umma_idesc_bf16(2 * BM, BNB);  // 2-SM MMA: M = 256 across the pair
 constexpr uint16_t PAIR_MASK = 0x3;
 
-struct TcArgs {
-  const int32_t* offsets;
-  int G;
-  int rows_static;
-  int N, K, N_w, K_w;
-  const __nv_bfloat16* bias;
-  void* out;  // bf16, or fp32 when the kernel's OUTF32 is set
+constexpr int SMEM_LIMIT = 232448;              // opt-in shared memory per CTA
+
+template <int ACT> constexpr int epi_warps() { return ACT == ACT_GELU ? 16 : 4; }  // the erf epilogue is ALU-bound
+template <int ACT> constexpr bool out_f32() { return ACT == ACT_NONE; }           // projections to the model width
+template <int ACT> constexpr int feat_per_tile() { return ACT == ACT_SWIGLU ? AR : 2 * AR; }  // output features per pair tile
+// token rows per tile: NTV (256, or 32 for decode-sized calls)
+template <int ACT, int NTV> constexpr int tile_tokens() { return NTV; }
+template <int ACT, int NTV> constexpr int a_bytes() { return WBOX; }
+template <int ACT, int NTV> constexpr int b_bytes() { return tile_tokens<ACT, NTV>() / 2 * BK * 2; }
+template <int ACT, int NTV> constexpr int stage_bytes() { return a_bytes<ACT, NTV>() + b_bytes<ACT, NTV>(); }
+// epilogue staging per warp: fp32 32 x 32 (128-byte rows) or bf16 32 x 32 (64-byte rows); two
+// buffers per warp except with 16 warps
+template <int ACT> constexpr int stg_bytes() { return ACT == ACT_NONE ? 4096 : 2048; }
+template <int ACT> constexpr int stg_bufs() { return epi_warps<ACT>() > 8 ? 1 : 2; }
+constexpr int CTL_BYTES = 2048;  // >= sizeof(SmemCtl), checked below
+template <int ACT, int NTV> constexpr int n_stages() {
+  return (SMEM_LIMIT - 1024 - CTL_BYTES - epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>()) /
+                     stage_bytes<ACT, NTV>() < MAX_STAGES
+             ? (SMEM_LIMIT - 1024 - CTL_BYTES - epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>()) /
+                   stage_bytes<ACT, NTV>()
+             : MAX_STAGES;
+}
+
+struct ProbArgs {
+  const int32_t* offsets;  // [G+1] device, or NULL: one group of rows [0, rows_static)
+  int G, rows_static;
+  int N, K, N_w, K_w;      // weight for feature n, reduction index kk of group g: matrix g + n / N_w + kk / K_w
+  const __nv_bfloat16* bias;  // [G_w][N_w] or NULL
+  void* out;
   int64_t ldc;
+  int gate_first;          // SwiGLU: the gate rows come first in each 32-row group (else the up rows)
+};
+struct TcArgs {
+  ProbArgs p[MAXP];
+  int nprob;
   uint32_t* status;
+};
+// Tensor maps of each problem: weights (SwiGLU: gate and up together), token rows in boxes of
+// NT/2 and 32 rows, and the output.
+struct TcMaps {
+  CUtensorMap w0[MAXP], x[MAXP], x32[MAXP], o[MAXP];
 };
 
 struct SmemCtl {
@@ -75,18 +120,21 @@ struct SmemCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  int u_pre[MAXG + 1];  // prefix over groups of row units (m-tiles, or m-tile pairs in PAIR mode)
+  int g0;               // groups of problem 0
+  int gt;               // groups over all problems
+  int u_pre[MAXGT + 1]; // prefix over groups of their tiles
 };
-// Epilogue staging for TMA tile stores: 32 x 32 tiles per warp (fp32 4 KB with the 128-byte
-// swizzle, bf16 2 KB with the 64-byte swizzle), two per warp (the store of one chunk overlaps the
-// staging of the next) except with 16 epilogue warps.  Shared memory: [alignment slack][stage
-// region][staging][control].
-constexpr int stg_bytes(bool outf32) { return outf32 ? 32 * 32 * 4 : 32 * 32 * 2; }
-constexpr int stg_bufs(int epiw) { return epiw > 8 ? 1 : 2; }
-constexpr size_t smem_total(bool outf32, int epiw) {
-  return 1024 + (size_t)STAGE_REGION + (size_t)epiw * stg_bufs(epiw) * stg_bytes(outf32) + sizeof(SmemCtl);
+static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block");
+template <int ACT, int NTV>
+constexpr size_t smem_total() {
+  return 1024 + (size_t)n_stages<ACT, NTV>() * stage_bytes<ACT, NTV>() +
+         (size_t)epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>() + CTL_BYTES;
 }
-static_assert(smem_total(true, 4) <= 232448 && smem_total(false, 16) <= 232448, "shared memory per CTA");
+static_assert(smem_total<ACT_NONE, 256>() <= SMEM_LIMIT && smem_total<ACT_GELU, 256>() <= SMEM_LIMIT &&
+                  smem_total<ACT_SWIGLU, 256>() <= SMEM_LIMIT && smem_total<ACT_SWIGLU, 32>() <= SMEM_LIMIT,
+              "shared memory per CTA");
+static_assert(n_stages<ACT_NONE, 256>() == 6 && n_stages<ACT_SWIGLU, 256>() == 6 && n_stages<ACT_NONE, 32>() >= 10,
+              "stage counts");
 
 // Wait that ignores the abort flag (used to drain in-flight async operations before exit).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -104,7 +152,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // Mathematical Functions, formula 7.1.26 (|error| <= 1.5e-7): for z >= 0,
 // erfc(z) = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2), t = 1 / (1 + p z).  With
 // z = |u| / sqrt 2 and g = |u| erfc(z) / 2:  u Phi(u) = u - g for u >= 0 and -g for u < 0, i.e.
-// max(u, 0) - g in both cases.  Two columns at a time with the packed fp32x2 multiply-adds
+// max(u, 0) - g in both cases.  Two values at a time with the packed fp32x2 multiply-adds
 // (the halved a_i fold the 1/2 into the polynomial); |u| is capped at 16 inside g, where
 // erfc(16 / sqrt 2) underflows, so that u = +-inf gives inf / 0 rather than inf * 0.
 __device__ __forceinline__ float rcp_approx(float x) {
@@ -136,55 +184,46 @@ __device__ __forceinline__ float2 gelu_erf2(float2 u) {
 }
 __device__ __forceinline__ float silu(float u) { return __fdividef(u, 1.f + __expf(-u)); }
 
-// One warp's 32 rows x 32 bf16 columns (16 packed words per lane, lane = row): a TMA tile store
-// through the warp's staging tile when all 32 rows are output rows (64-byte swizzle: 16-byte chunk
-// j of row r sits at chunk j ^ ((r / 2) % 4), conflict-free), else direct row stores.
-template <int NBUF>
-__device__ __forceinline__ void store_bf16_chunk(const uint32_t (&pk)[16], bool full_rows, uint8_t* stg,
-                                                 const CUtensorMap* tm, int col, int row0, __nv_bfloat16* dst_row,
-                                                 int lane) {
-  if (full_rows) {
-    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last used stg has read it
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-          make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) {
-      tma_store_2d(tm, smem_u32(stg), col, row0);
-      bulk_commit();
-    }
-  } else {
-    uint4* d = reinterpret_cast<uint4*>(dst_row);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-  }
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
 }
 
-template <int ACT, bool OUTF32, int EPIW, bool PAIR>
-__global__ void __launch_bounds__(128 + 32 * EPIW, 1)
-    k_proj_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA32,
-              const __grid_constant__ CUtensorMap tmB0,
-              const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmOut, const TcArgs args) {
-  constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
-  constexpr int CW = NOUT / (EPIW / 4);  // output columns per epilogue warp
-  constexpr int STAGES = stages_of(PAIR);
-  constexpr int STAGE_BYTES = stage_bytes_of(PAIR);
+struct Tile {
+  int p, g;        // problem, group (expert) within it
+  int m0, m_end;   // first token row of the tile, end of the group's rows
+  int n0;          // first output feature of the pair tile
+  int ntok, nmma;  // token rows of the tile, and that rounded up to the MMA's N step of 16
+  int kblocks;
+};
+
+template <int ACT, int NTV>
+__global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
+    k_proj_tc(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs args) {
+  constexpr int EPIW = epi_warps<ACT>();
+  constexpr int NBUF = stg_bufs<ACT>();
+  constexpr int STG = stg_bytes<ACT>();
+  constexpr int NT = tile_tokens<ACT, NTV>();
+  constexpr int FT = feat_per_tile<ACT>();
+  constexpr int A_BYTES = a_bytes<ACT, NTV>();
+  constexpr int STAGE_BYTES = stage_bytes<ACT, NTV>();
+  constexpr int STAGES = n_stages<ACT, NTV>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stg_base = smem + (size_t)STAGE_REGION;  // 1024-byte aligned (the swizzle atoms)
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * stg_bufs(EPIW) * stg_bytes(OUTF32));
+  uint8_t* stg_base = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned (the swizzle atoms)
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * NBUF * STG);
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = args.offsets ? args.G : 1;
-  const int n_tiles = (args.N + NOUT - 1) / NOUT;
-  const int kblocks = args.K / BK;
-  const int crank = PAIR ? (int)cluster_ctarank() : 0;
-  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int ustep = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  const bool leader = crank == 0;  // PAIR: the even CTA issues the 2-SM MMAs
+  const int crank = (int)cluster_ctarank();
+  const bool leader = crank == 0;  // the even CTA issues the 2-SM MMAs
+  const int unit0 = (int)(blockIdx.x >> 1);
+  const int ustep = (int)(gridDim.x >> 1);
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -194,43 +233,44 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
-      mbar_init(smem_u32(&ctl->tempty[a]), PAIR ? 2 * EPIW : EPIW);  // one arrive per epilogue warp of the pair
+      mbar_init(smem_u32(&ctl->tempty[a]), 2 * EPIW);  // one arrive per epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    if (!PAIR) tma_prefetch_desc(&tmA32);
-    tma_prefetch_desc(&tmB0);
-    if (ACT == ACT_SWIGLU) tma_prefetch_desc(&tmB1);
-  }
-  if (warp == 2) {
-    if (PAIR) {  // both CTAs of the pair allocate together and receive the same address
-      tmem_alloc_cg2(smem_u32(&ctl->tmem_base), TMEM_COLS);
-      tmem_relinquish_cg2();
-    } else {
-      tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-      tmem_relinquish();
+    for (int p = 0; p < args.nprob; ++p) {
+      tma_prefetch_desc(&maps.w0[p]);
+      tma_prefetch_desc(&maps.x[p]);
     }
   }
-  // the set-up above overlaps the previous kernel's tail; the offsets, the A rows and every output
-  // buffer belong to earlier kernels from here on
+  if (warp == 2) {  // both CTAs of the pair allocate together and receive the same address
+    tmem_alloc_cg2(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish_cg2();
+  }
+  // the set-up above overlaps the previous kernel's tail; the offsets, the token rows and every
+  // output buffer belong to earlier kernels from here on
   pdl_wait();
   if (warp == 3) {
-    // unit prefix over groups: lane owns groups [8 lane, 8 lane + 8)
-    int cnt[8];
+    // tiles of every group over both problems: lane owns groups [TBL_PER_LANE lane, + TBL_PER_LANE)
+    const int g0 = args.p[0].offsets ? args.p[0].G : 1;
+    const int g1 = args.nprob > 1 ? (args.p[1].offsets ? args.p[1].G : 1) : 0;
+    const int gt = g0 + g1;
+    int cnt[TBL_PER_LANE];
     int local = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int g = lane * 8 + i;
+    for (int i = 0; i < TBL_PER_LANE; ++i) {
+      const int g = lane * TBL_PER_LANE + i;
       cnt[i] = 0;
-      if (g < G) {
-        const int lo = args.offsets ? args.offsets[g] : 0;
-        const int hi = args.offsets ? args.offsets[g + 1] : args.rows_static;
-        const int mt = hi > lo ? (hi - lo + BM - 1) / BM : 0;
-        cnt[i] = PAIR ? (mt + 1) >> 1 : mt;
+      if (g < gt) {
+        const int p = g < g0 ? 0 : 1;
+        const ProbArgs& P = args.p[p];
+        const int gl = g - (p ? g0 : 0);
+        const int lo = P.offsets ? P.offsets[gl] : 0;
+        const int hi = P.offsets ? P.offsets[gl + 1] : P.rows_static;
+        const int tt = hi > lo ? (hi - lo + NT - 1) / NT : 0;
+        cnt[i] = tt * ((P.N + FT - 1) / FT);
         local += cnt[i];
       }
     }
@@ -242,36 +282,48 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
     }
     int run = incl - local;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int g = lane * 8 + i;
-      if (g < G) ctl->u_pre[g] = run;
+    for (int i = 0; i < TBL_PER_LANE; ++i) {
+      const int g = lane * TBL_PER_LANE + i;
+      if (g < gt) ctl->u_pre[g] = run;
       run += cnt[i];
     }
-    if (lane == 31) ctl->u_pre[G] = incl;
+    if (lane == 31) {
+      ctl->u_pre[gt] = incl;
+      ctl->g0 = g0;
+      ctl->gt = gt;
+    }
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync_all();  // the peer's barriers are initialised before any remote signal
+  cluster_sync_all();  // the peer's barriers are initialised before any remote signal
   tc_fence_after();
 
   const uint32_t tmem_base = ctl->tmem_base;
-  const int total_units = ctl->u_pre[G] * n_tiles;
+  const int n_groups = ctl->gt;
+  const int total_units = ctl->u_pre[n_groups];
 
-  // unit -> (group, first row, end of the group's rows, first output column); m-major, n fastest
-  auto decode = [&](int u, int& g, int& m0, int& m_end, int& n0) {
-    const int mu = u / n_tiles;
-    const int nt = u - mu * n_tiles;
-    int lo = 0, hi = G;
+  auto decode = [&](int u) {
+    int lo = 0, hi = n_groups;  // the largest group whose first tile is <= u
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (ctl->u_pre[mid] <= mu) lo = mid; else hi = mid;
+      if (ctl->u_pre[mid] <= u) lo = mid; else hi = mid;
     }
-    g = lo;
-    const int mt_local = PAIR ? 2 * (mu - ctl->u_pre[g]) + crank : mu - ctl->u_pre[g];
-    const int row_lo = args.offsets ? __ldg(args.offsets + g) : 0;
-    m0 = row_lo + mt_local * BM;   // may lie past m_end in PAIR mode: nothing is stored
-    m_end = args.offsets ? __ldg(args.offsets + g + 1) : args.rows_static;
-    n0 = nt * NOUT;
+    Tile t;
+    t.p = lo < ctl->g0 ? 0 : 1;
+    t.g = lo - (t.p ? ctl->g0 : 0);
+    const ProbArgs& P = args.p[t.p];
+    const int r0 = P.offsets ? __ldg(P.offsets + t.g) : 0;
+    t.m_end = P.offsets ? __ldg(P.offsets + t.g + 1) : P.rows_static;
+    const int tt = (t.m_end - r0 + NT - 1) / NT;
+    const int local = u - ctl->u_pre[lo];
+    const int fi = local / tt;
+    const int ti = local - fi * tt;
+    t.m0 = r0 + ti * NT;
+    t.ntok = min(NT, t.m_end - t.m0);
+    t.nmma = (t.ntok + 15) & ~15;
+    t.n0 = fi * FT;
+    t.kblocks = P.K / BK;
+    return t;
   };
 
   if (warp == 0) {
@@ -280,61 +332,49 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       uint32_t ph = 0, armed = 0, armed_ph = 0;
       bool aborted = false;
       for (int u = unit0; u < total_units && !aborted; u += ustep) {
-        int g, m0, m_end, n0;
-        decode(u, g, m0, m_end, n0);
-        const int nn = n0 % args.N_w;
-        // single CTA: a tile with few rows (an expert with few tokens) loads only its 32-row groups
-        // of A; the MMA rows past them read stale shared memory and give accumulator rows that are
-        // never stored
-        const int n32 = PAIR ? 4 : min(4, (max(m_end - m0, 1) + 31) >> 5);
-        const uint32_t tx_bytes = (uint32_t)(STAGE_BYTES - (4 - n32) * (A_BYTES / 4));
-        auto load_a = [&](uint8_t* sa, uint32_t fb, int k0) {
-          if (n32 == 4) {
-            tma_load_2d(smem_u32(sa), &tmA, fb, k0, m0);
-          } else {
-            for (int j = 0; j < n32; ++j) tma_load_2d(smem_u32(sa + j * (A_BYTES / 4)), &tmA32, fb, k0, m0 + 32 * j);
-          }
-        };
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const Tile t = decode(u);
+        const ProbArgs& P = args.p[t.p];
+        const int half = t.nmma >> 1;   // token rows of this CTA (a multiple of 8)
+        const int brow = t.m0 + crank * half;
+        // one token box per stage: 32 rows when this CTA's half fits, else the full NT/2 rows
+        const bool small_box = NT / 2 > 32 && half <= 32;
+        const uint32_t stage_tx = 2u * (uint32_t)(A_BYTES + (small_box ? 32 : NT / 2) * BK * 2);  // both CTAs' bytes
+        for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status)) {
             aborted = true;
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          const uint32_t lb = mapa_rank(fb, 0);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, stage_tx);
+            armed |= 1u << s;
+            armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          }
           const int k0 = kb * BK;
-          const int gw = g + n0 / args.N_w + k0 / args.K_w;
-          const int kk = k0 % args.K_w;
+          const int kk = k0 % P.K_w;
+          const int kq = k0 / P.K_w;
           uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
-          if (PAIR) {
-            // this CTA's 128 A rows and its half of the B tile (SwiGLU: the gate or the up half;
-            // else rows [128 crank, 128 crank + 128)), both signalling the leader's stage barrier
-            const uint32_t lb = mapa_rank(fb, 0);
-            if (leader) mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
-            tma_load_2d_cg2(smem_u32(sa), &tmA, lb, k0, m0);
-            if (ACT == ACT_SWIGLU)
-              tma_load_3d_cg2(smem_u32(sb), crank ? &tmB1 : &tmB0, lb, kk, nn, gw);
-            else
-              tma_load_3d_cg2(smem_u32(sb), &tmB0, lb, kk, nn + crank * (BNB / 2), gw);
-          } else if (ACT == ACT_SWIGLU) {
-            mbar_arrive_expect_tx(fb, tx_bytes);  // A (its existing rows) + the whole B tile
-            load_a(sa, fb, k0);
-            tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
-            tma_load_3d(smem_u32(sb + B_BYTES / 2), &tmB1, fb, kk, nn, gw);
+          if (ACT == ACT_SWIGLU) {
+            // this CTA's 64 features: gate and up rows interleaved in blocks of 16, one box
+            const int f = t.n0 + (AR / 2) * crank;
+            tma_load_5d_cg2(smem_u32(sa), &maps.w0[t.p], lb, kk, 0, 0, (f % P.N_w) / 16, t.g + f / P.N_w + kq);
           } else {
-            mbar_arrive_expect_tx(fb, tx_bytes);
-            load_a(sa, fb, k0);
-            tma_load_3d(smem_u32(sb), &tmB0, fb, kk, nn, gw);
+            const int f = t.n0 + AR * crank;
+            tma_load_3d_cg2(smem_u32(sa), &maps.w0[t.p], lb, kk, f % P.N_w, t.g + f / P.N_w + kq);
           }
+          if (small_box)
+            tma_load_2d_cg2(smem_u32(sb), &maps.x32[t.p], lb, k0, brow);
+          else
+            tma_load_2d_cg2(smem_u32(sb), &maps.x[t.p], lb, k0, brow);
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      if (aborted && leader) {  // let every armed copy (of both CTAs of a pair) land before leaving
+      if (aborted && leader) {  // let every armed copy (of both CTAs) land before leaving
         for (int i = 0; i < STAGES; ++i)
           if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
       }
@@ -345,12 +385,14 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       uint32_t ph = 0;
       bool aborted = false;
       for (int u = unit0; u < total_units && !aborted; u += ustep, ++it) {
+        const Tile t = decode(u);
         const int acc = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BNB);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        const uint32_t idesc = umma_idesc_bf16(2 * AR, t.nmma);
+        for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
             aborted = true;
             break;
@@ -359,45 +401,31 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
           const uint32_t sa = smem_u32(smem + (size_t)s * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            if (PAIR)
-              umma_bf16_cg2(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC_PAIR,
-                            (kb | kk) != 0 ? 1u : 0u);
-            else
-              umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), IDESC,
-                        (kb | kk) != 0 ? 1u : 0u);
-          }
-          if (PAIR)
-            umma_commit_cg2_mc(smem_u32(&ctl->empty[s]), PAIR_MASK);  // both CTAs' copies of the stage are free
-          else
-            umma_commit(smem_u32(&ctl->empty[s]));
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16_cg2(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+          umma_commit_cg2_mc(smem_u32(&ctl->empty[s]), PAIR_MASK);  // both CTAs' copies of the stage are free
           if (++s == STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (aborted) break;
-        if (PAIR)
-          umma_commit_cg2_mc(smem_u32(&ctl->tfull[acc]), PAIR_MASK);  // both CTAs' accumulators are full
-        else
-          umma_commit(smem_u32(&ctl->tfull[acc]));
+        umma_commit_cg2_mc(smem_u32(&ctl->tfull[acc]), PAIR_MASK);  // both CTAs' accumulators are full
       }
-      if (PAIR)
-        umma_commit_cg2_mc(smem_u32(&ctl->mma_done), PAIR_MASK);
-      else
-        umma_commit(smem_u32(&ctl->mma_done));
+      umma_commit_cg2_mc(smem_u32(&ctl->mma_done), PAIR_MASK);
       drain_wait(smem_u32(&ctl->mma_done), 0);
     }
   } else if (warp >= 4) {
-    const int q = warp & 3;                      // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
-    const int c_lo = ((warp - 4) >> 2) * CW;     // this warp's share of the output columns
-    constexpr int NBUF = stg_bufs(EPIW);
-    uint8_t* stg_w = stg_base + (size_t)(warp - 4) * NBUF * stg_bytes(OUTF32);
-    int chunk = 0;  // running chunk count of this warp: selects the staging buffer
+    const int q = warp & 3;                  // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
+    const int grp = (warp - 4) >> 2;         // this warp's share of the token columns
+    constexpr int NGRP = EPIW / 4;
+    uint8_t* stg_w = stg_base + (size_t)(warp - 4) * NBUF * STG;
+    int chunk = 0;                           // running count of staged blocks: selects the buffer
     int it = 0;
     for (int u = unit0; u < total_units; u += ustep, ++it) {
-      int g, m0, m_end, n0;
-      decode(u, g, m0, m_end, n0);
+      const Tile t = decode(u);
+      const ProbArgs& P = args.p[t.p];
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       // lane 0 waits, the warp follows its verdict (tcgen05.ld needs the whole warp converged)
@@ -406,101 +434,106 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int row = m0 + q * 32 + lane;
-      const bool valid = row < m_end;
-      const bool full_rows = m0 + q * 32 + 32 <= m_end;  // all 32 rows of this warp are output rows
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BNB);
-      const size_t orow = (size_t)(valid ? row : 0) * args.ldc;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
       if (ACT == ACT_SWIGLU) {
+        // lanes 0-15 and 16-31 hold the two matrices (gate, up) of features fl..fl+15; lane i < 16
+        // finishes tokens 0-15 of a 32-token block, lane i + 16 tokens 16-31
+        const int fl = t.n0 + (AR / 2) * crank + 16 * q;
+        const int f = fl + (lane & 15);
+        const bool upper = lane >= 16;
+        const bool gate_lo = P.gate_first != 0;  // lanes 0-15 hold the gate accumulators
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out);
 #pragma unroll 1
-        for (int c = c_lo; c < c_lo + CW; c += 32) {
-          uint32_t gv[32], uv[32];
-          tmem_ld32(tb + c, gv);
-          tmem_ld32(tb + 128 + c, uv);
+        for (int cb = grp; cb * 32 < t.ntok; cb += NGRP) {
+          uint32_t v[32];
+          tmem_ld32(tb + cb * 32, v);
           tmem_wait_ld();
-          if (valid && n0 + c < args.N) {
-            uint32_t pk[16];
+          const int tok0 = t.m0 + cb * 32;
+          const int nval = min(32, t.ntok - cb * 32);
+          const int tbase = upper ? 16 : 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h0 = silu(__uint_as_float(gv[2 * i])) * __uint_as_float(uv[2 * i]);
-              const float h1 = silu(__uint_as_float(gv[2 * i + 1])) * __uint_as_float(uv[2 * i + 1]);
-              pk[i] = pack_bf16x2(h0, h1);
-            }
-            store_bf16_chunk<NBUF>(pk, full_rows, stg_w + (chunk++ % NBUF) * stg_bytes(OUTF32), &tmOut, n0 + c,
-                                   m0 + q * 32, static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
+          for (int i = 0; i < 16; ++i) {
+            const float lo_v = __uint_as_float(v[i]), hi_v = __uint_as_float(v[16 + i]);
+            // lane < 16 keeps token i and receives the partner's value of it; lane >= 16 keeps 16 + i
+            const float got = __shfl_xor_sync(0xffffffffu, upper ? lo_v : hi_v, 16);
+            const float mine = upper ? hi_v : lo_v;
+            // `mine` belongs to this lane's matrix, `got` to the other one
+            const bool mine_is_gate = upper != gate_lo;
+            const float gate = mine_is_gate ? mine : got;
+            const float up = mine_is_gate ? got : mine;
+            if (f < P.N && tbase + i < nval)
+              out[(size_t)(tok0 + tbase + i) * P.ldc + f] = __float2bfloat16_rn(silu(gate) * up);
           }
         }
       } else {
+        const int fl = t.n0 + AR * crank + 32 * q;  // first feature of this warp
+        const int f = fl + lane;
+        float b = 0.f;
+        if (P.bias && f < P.N) {
+          const int gw = t.g + f / P.N_w;
+          b = __bfloat162float(P.bias[(size_t)gw * P.N_w + f % P.N_w]);
+        }
 #pragma unroll 1
-        for (int c = c_lo; c < c_lo + CW; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tb + c, v);
-          tmem_wait_ld();
-          if (valid && n0 + c < args.N) {
-            float f[32];
+        for (int cb = grp; cb * 32 < t.ntok; cb += NGRP) {
+          float h[32];
+          {
+            uint32_t v[32];
+            tmem_ld32(tb + cb * 32, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-            if (args.bias) {
-              const int col = n0 + c;
-              const int gw = g + col / args.N_w;
-              const uint4* bp = reinterpret_cast<const uint4*>(args.bias + (size_t)gw * args.N_w + col % args.N_w);
+            for (int i = 0; i < 32; ++i) h[i] = __uint_as_float(v[i]) + b;
+          }
+          if (ACT == ACT_GELU) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint4 bq = bp[i];
-                const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  f[8 * i + 2 * j] += __uint_as_float(bw[j] << 16);
-                  f[8 * i + 2 * j + 1] += __uint_as_float(bw[j] & 0xffff0000u);
-                }
-              }
+            for (int i = 0; i < 32; i += 2) {
+              const float2 g2 = gelu_erf2(make_float2(h[i], h[i + 1]));
+              h[i] = g2.x;
+              h[i + 1] = g2.y;
             }
-            if (ACT == ACT_GELU) {
+          }
+          const int tok0 = t.m0 + cb * 32;
+          const int nval = min(32, t.ntok - cb * 32);
+          if (nval == 32 && fl + 32 <= P.N) {
+            uint8_t* stg = stg_w + (chunk++ % NBUF) * STG;
+            if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last used stg has read it
+            __syncwarp();
+            const uint32_t sb = smem_u32(stg);
+            if (out_f32<ACT>()) {
+              // 128-byte rows, 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8)
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const float2 h2 = gelu_erf2(make_float2(f[i], f[i + 1]));
-                f[i] = h2.x;
-                f[i + 1] = h2.y;
-              }
-            }
-            if (OUTF32 && full_rows) {
-              // the warp's 32 rows x 32 columns go out as one TMA tile store through shared
-              // memory (128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r % 8))
-              uint8_t* stg = stg_w + (chunk++ % NBUF) * stg_bytes(OUTF32);
-              if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last used stg has read it
-              __syncwarp();
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                    make_float4(f[4 * j], f[4 * j + 1], f[4 * j + 2], f[4 * j + 3]);
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                tma_store_2d(&tmOut, smem_u32(stg), n0 + c, m0 + q * 32);
-                bulk_commit();
-              }
-            } else if (OUTF32) {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.out) + orow + n0 + c);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+              for (int i = 0; i < 32; ++i)
+                st_shared_f32(sb + i * 128 + ((((uint32_t)lane >> 2) ^ (uint32_t)(i & 7)) << 4) + (lane & 3) * 4, h[i]);
             } else {
-              uint32_t pk[16];
+              // 64-byte rows, 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r / 2) % 4)
 #pragma unroll
-              for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-              store_bf16_chunk<NBUF>(pk, full_rows, stg_w + (chunk++ % NBUF) * stg_bytes(OUTF32), &tmOut, n0 + c,
-                                     m0 + q * 32, static_cast<__nv_bfloat16*>(args.out) + orow + n0 + c, lane);
+              for (int i = 0; i < 32; ++i)
+                st_shared_u16(sb + i * 64 + ((((uint32_t)lane >> 3) ^ (uint32_t)((i >> 1) & 3)) << 4) + (lane & 7) * 2,
+                              bf16_bits(h[i]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&maps.o[t.p], sb, fl, tok0);
+              bulk_commit();
+            }
+          } else if (f < P.N) {
+            if (out_f32<ACT>()) {
+              float* out = static_cast<float*>(P.out);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nval) out[(size_t)(tok0 + i) * P.ldc + f] = h[i];
+            } else {
+              __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nval) out[(size_t)(tok0 + i) * P.ldc + f] = __float2bfloat16_rn(h[i]);
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if (PAIR)
-          mbar_arrive_cluster(mapa_rank(smem_u32(&ctl->tempty[acc]), 0));  // the leader reuses the accumulator
-        else
-          mbar_arrive(smem_u32(&ctl->tempty[acc]));
-      }
+      if (lane == 0) mbar_arrive_cluster(mapa_rank(smem_u32(&ctl->tempty[acc]), 0));  // the leader reuses the accumulator
     }
     if (lane == 0) bulk_wait_all();  // tile stores complete before the CTA leaves
     __syncwarp();
@@ -508,15 +541,12 @@ __global__ void __launch_bounds__(128 + 32 * EPIW, 1)
 
   tc_fence_before();
   __syncthreads();
-  // PAIR: no signal of the peer can still be in flight towards this CTA, and neither CTA's TMEM is
-  // in use, when the pair frees its TMEM together
-  if (PAIR) cluster_sync_all();
+  // no signal of the peer can still be in flight towards this CTA, and neither CTA's TMEM is in
+  // use, when the pair frees its TMEM together
+  cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
-    if (PAIR)
-      tmem_dealloc_cg2(tmem_base, TMEM_COLS);
-    else
-      tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_cg2(tmem_base, TMEM_COLS);
   }
 }
 
@@ -566,12 +596,16 @@ cudaError_t ensure_smem_attr(const void* kernel, size_t bytes) {
 static bool make_tmap(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int rank, const cuuint64_t* dims,
                       const cuuint64_t* strides, const cuuint32_t* box,
                       CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B) {
+  if (rank < 1 || rank > 5) {
+    snprintf(g_err, sizeof(g_err), "tensor map rank %d out of range", rank);
+    return false;
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) {
     snprintf(g_err, sizeof(g_err), "cuTensorMapEncodeTiled unavailable");
     return false;
   }
-  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -590,7 +624,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t*
 }
 
 namespace {
-// Largest number of co-resident 2-CTA clusters of a paired kernel (0 if none), per device.
+// Largest number of co-resident 2-CTA clusters of a kernel (0 if none), per device.
 template <typename K>
 int max_pair_clusters(K kernel, int threads, size_t smem) {
   struct Entry { const void* k; int dev; int n; };
@@ -626,16 +660,91 @@ int max_pair_clusters(K kernel, int threads, size_t smem) {
   return n;
 }
 
-template <int ACT, bool OUTF32, int EPIW, bool PAIR>
-cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mA32, const CUtensorMap& mB0, const CUtensorMap& mB1,
-                     const CUtensorMap& mO,
-                     const TcArgs& a, long grid, cudaStream_t st) {
-  auto kern = k_proj_tc<ACT, OUTF32, EPIW, PAIR>;
-  constexpr int threads = 128 + 32 * EPIW;
-  constexpr size_t smem = smem_total(OUTF32, EPIW);
+template <int ACT, int NTV>
+cudaError_t launch_t(const Projection* ps, int nprob, uint32_t* status, cudaStream_t st) {
+  constexpr int NT = tile_tokens<ACT, NTV>();
+  constexpr int FT = feat_per_tile<ACT>();
+  constexpr int threads = 128 + 32 * epi_warps<ACT>();
+  constexpr size_t smem = smem_total<ACT, NTV>();
+  auto kern = k_proj_tc<ACT, NTV>;
+  TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.status = status;
+  long units_bound = 0;
+  int np = 0;
+  for (int i = 0; i < nprob; ++i) {
+    const Projection& p = ps[i];
+    const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
+    if (rows_alloc <= 0 || p.N <= 0) continue;
+    if (p.offsets && p.G > MAXGT - 1) return cudaErrorInvalidValue;
+    {
+      const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)rows_alloc};
+      const cuuint64_t str[1] = {(cuuint64_t)p.lda * 2};
+      const cuuint32_t box[2] = {BK, NT / 2}, box32[2] = {BK, 32};
+      if (!make_tmap_bf16(&maps.x[np], p.A, 2, dims, str, box) || !make_tmap_bf16(&maps.x32[np], p.A, 2, dims, str, box32))
+        return cudaErrorInvalidValue;
+    }
+    int gate_first = 1;
+    if (ACT == ACT_SWIGLU) {
+      // gate (B0) and up (B1) as one 5-D tensor (k, row in block of 16, matrix, block, expert): the
+      // matrix dimension steps from the lower-addressed weight tensor to the other, so one box of
+      // {64, 16, 2, 4, 1} brings 16 rows of one matrix, the same 16 rows of the other, 4 times over
+      const char* g = static_cast<const char*>(p.B0);
+      const char* u = static_cast<const char*>(p.B1);
+      if (g == u || p.N_w % 16) {
+        snprintf(g_err, sizeof(g_err), "SwiGLU gate and up weights must be distinct tensors");
+        return cudaErrorInvalidValue;
+      }
+      gate_first = g < u ? 1 : 0;
+      const cuuint64_t dims[5] = {(cuuint64_t)p.K_w, 16, 2, (cuuint64_t)(p.N_w / 16), (cuuint64_t)p.G_w};
+      const cuuint64_t str[4] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)(gate_first ? u - g : g - u),
+                                 (cuuint64_t)p.K_w * 2 * 16, (cuuint64_t)p.N_w * p.K_w * 2};
+      const cuuint32_t box[5] = {BK, 16, 2, 4, 1};
+      if (!make_tmap_bf16(&maps.w0[np], gate_first ? g : u, 5, dims, str, box)) return cudaErrorInvalidValue;
+    } else {
+      const cuuint64_t dims[3] = {(cuuint64_t)p.K_w, (cuuint64_t)p.N_w, (cuuint64_t)p.G_w};
+      const cuuint64_t str[2] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)p.N_w * p.K_w * 2};
+      const cuuint32_t box[3] = {BK, AR, 1};
+      if (!make_tmap_bf16(&maps.w0[np], p.B0, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {  // output blocks of the epilogue's TMA stores: 32 tokens x 32 features
+      const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)rows_alloc};
+      const cuuint64_t str[1] = {(cuuint64_t)p.ldc * (out_f32<ACT>() ? 4 : 2)};
+      const cuuint32_t box[2] = {32, 32};
+      if (!make_tmap(&maps.o[np], out_f32<ACT>() ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     p.out, 2, dims, str, box, out_f32<ACT>() ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    }
+    ProbArgs& q = a.p[np];
+    q.offsets = p.offsets;
+    q.G = p.G;
+    q.rows_static = p.rows_static;
+    q.N = p.N;
+    q.K = p.K;
+    q.N_w = p.N_w;
+    q.K_w = p.K_w;
+    q.bias = static_cast<const __nv_bfloat16*>(p.bias);
+    q.out = p.out;
+    q.ldc = p.ldc;
+    q.gate_first = gate_first;
+    const long groups = p.offsets ? p.G : 1;
+    // each group adds at most one partial token tile
+    units_bound += ((rows_alloc + NT - 1) / NT + (p.offsets ? groups : 0)) * (long)((p.N + FT - 1) / FT);
+    ++np;
+  }
+  if (np == 0) return cudaSuccess;
+  a.nprob = np;
+  const int n_clusters = max_pair_clusters(kern, threads, smem);
+  if (n_clusters <= 0) {
+    snprintf(g_err, sizeof(g_err), "no co-resident pair of CTAs for the grouped GEMM");
+    return cudaErrorInvalidConfiguration;
+  }
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  if (!PAIR) return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, st, mA, mA32, mB0, mB1, mO, a);
+  long clusters = units_bound < n_clusters ? units_bound : n_clusters;
+  if (clusters < 1) clusters = 1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -644,95 +753,41 @@ cudaError_t launch_k(const CUtensorMap& mA, const CUtensorMap& mA32, const CUten
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.gridDim = dim3((unsigned)(2 * clusters), 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, mA, mA32, mB0, mB1, mO, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps, a);
+  if (e != cudaSuccess) snprintf(g_err, sizeof(g_err), "grouped GEMM launch: %s", cudaGetErrorString(e));
+  return e;
 }
 
-template <int ACT, bool OUTF32>
-cudaError_t launch_t(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
-  constexpr int NOUT = (ACT == ACT_SWIGLU) ? 128 : 256;
-  constexpr int EPIW = (ACT == ACT_GELU) ? 16 : 4;  // the erf epilogue is ALU-bound; the others are not
-  const int rows_alloc = p.offsets ? p.rows_alloc : p.rows_static;
-  if (rows_alloc <= 0 || p.N <= 0) return cudaSuccess;
-  const int G = p.offsets ? p.G : 1;
-  // Pairs pay off when groups average two or more row tiles (otherwise half the pair idles): a CTA
-  // then holds 6 stages of half a B tile instead of 4 of a whole one, so more MMA work is in
-  // flight per byte of shared memory while the tile loads are on their way.
-  int n_clusters = 0;
-  if ((long)rows_alloc >= 2L * BM * G)
-    n_clusters = max_pair_clusters(k_proj_tc<ACT, OUTF32, EPIW, true>, 128 + 32 * EPIW, smem_total(OUTF32, EPIW));
-  const bool pair = n_clusters > 0;
-  CUtensorMap mA, mA32, mB0, mB1;
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)rows_alloc};
-    const cuuint64_t str[1] = {(cuuint64_t)p.lda * 2};
-    const cuuint32_t box[2] = {BK, BM};
-    if (!make_tmap_bf16(&mA, p.A, 2, dims, str, box)) return cudaErrorInvalidValue;
-    const cuuint32_t box32[2] = {BK, 32};  // 32-row groups of A for tiles with few rows
-    if (!make_tmap_bf16(&mA32, p.A, 2, dims, str, box32)) return cudaErrorInvalidValue;
-  }
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)p.K_w, (cuuint64_t)p.N_w, (cuuint64_t)p.G_w};
-    const cuuint64_t str[2] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)p.N_w * p.K_w * 2};
-    const cuuint32_t box[3] = {BK, (cuuint32_t)((ACT == ACT_SWIGLU || pair) ? BNB / 2 : BNB), 1};
-    if (!make_tmap_bf16(&mB0, p.B0, 3, dims, str, box)) return cudaErrorInvalidValue;
-    if (ACT == ACT_SWIGLU) {
-      if (!make_tmap_bf16(&mB1, p.B1, 3, dims, str, box)) return cudaErrorInvalidValue;
-    } else {
-      mB1 = mB0;
-    }
-  }
-  CUtensorMap mO;
-  {  // output tile map for the TMA stores of the epilogue: 32 x 32 boxes (fp32: 128-byte rows, bf16: 64-byte)
-    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)rows_alloc};
-    const cuuint64_t str[1] = {(cuuint64_t)p.ldc * (OUTF32 ? 4 : 2)};
-    const cuuint32_t box[2] = {32, 32};
-    if (!make_tmap(&mO, OUTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.out, 2, dims,
-                   str, box, OUTF32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
-      return cudaErrorInvalidValue;
-  }
-  TcArgs a;
-  a.offsets = p.offsets;
-  a.G = p.G;
-  a.rows_static = p.rows_static;
-  a.N = p.N;
-  a.K = p.K;
-  a.N_w = p.N_w;
-  a.K_w = p.K_w;
-  a.bias = static_cast<const __nv_bfloat16*>(p.bias);
-  a.out = p.out;
-  a.ldc = p.ldc;
-  a.status = status;
-  const long n_tiles = (p.N + NOUT - 1) / NOUT;
-  const long ub_mt = (rows_alloc + BM - 1) / BM + (p.offsets ? G : 0);  // each group adds <= 1 partial tile
-  if (pair) {
-    long units = (ub_mt + G + 1) / 2 * n_tiles;
-    long clusters = units < n_clusters ? units : n_clusters;
-    if (clusters < 1) clusters = 1;
-    return launch_k<ACT, OUTF32, EPIW, true>(mA, mA32, mB0, mB1, mO, a, 2 * clusters, st);
-  }
-  long grid = ub_mt * n_tiles;
-  if (grid > num_sms) grid = num_sms;
-  if (grid < 1) grid = 1;
-  return launch_k<ACT, OUTF32, EPIW, false>(mA, mA32, mB0, mB1, mO, a, grid, st);
+template <int ACT>
+cudaError_t launch_a(const Projection* ps, int nprob, uint32_t* status, cudaStream_t st) {
+  // every group at most 32 token rows (decode-sized calls): 32-token tiles, more stages in flight
+  bool small = true;
+  for (int i = 0; i < nprob; ++i) small = small && ps[i].max_group_rows <= 32;
+  return small ? launch_t<ACT, 32>(ps, nprob, status, st) : launch_t<ACT, 256>(ps, nprob, status, st);
 }
 }  // namespace
 
 const char* tc_last_error() { return g_err; }
 
-cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st) {
+cudaError_t launch_projection_tc(const Projection* ps, int nprob, uint32_t* status, cudaStream_t st) {
+  if (nprob < 1 || nprob > MAXP) return cudaErrorInvalidValue;
+  const int act = ps[0].act;
+  for (int i = 1; i < nprob; ++i)
+    if (ps[i].act != act || ps[i].out_f32 != ps[0].out_f32) return cudaErrorInvalidValue;
   // hidden layers are bf16 (the next projection's MMA operand); projections to the model width
   // keep the fp32 accumulator so the layer output is rounded once
-  switch (p.act) {
-    case ACT_GELU: return launch_t<ACT_GELU, false>(p, status, num_sms, st);
-    case ACT_SWIGLU: return launch_t<ACT_SWIGLU, false>(p, status, num_sms, st);
-    default: return p.out_f32 ? launch_t<ACT_NONE, true>(p, status, num_sms, st)
-                              : launch_t<ACT_NONE, false>(p, status, num_sms, st);
+  switch (act) {
+    case ACT_GELU: return launch_a<ACT_GELU>(ps, nprob, status, st);
+    case ACT_SWIGLU: return launch_a<ACT_SWIGLU>(ps, nprob, status, st);
+    default:
+      if (!ps[0].out_f32) return cudaErrorInvalidValue;
+      return launch_a<ACT_NONE>(ps, nprob, status, st);
   }
 }
 

@@ -91,9 +91,12 @@ struct Projection {
   int act;
   void* out; int64_t ldc;
   bool out_f32;                                    // out is fp32 (else the layer dtype)
+  int max_group_rows;                              // bound on the rows of any one group (host-known)
 };
 cudaError_t launch_projection_simt(bool bf16, const Projection& p, cudaStream_t st);
-cudaError_t launch_projection_tc(const Projection& p, uint32_t* status, int num_sms, cudaStream_t st);
+// bf16 layers: nprob (1 or 2) projections with the same activation in one launch of the paired
+// tensor-core kernel (the routed and the shared experts share its persistent CTAs).
+cudaError_t launch_projection_tc(const Projection* ps, int nprob, uint32_t* status, cudaStream_t st);
 const char* tc_last_error();
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` (once per kernel and device).

@@ -36,7 +36,11 @@ class MoeWeights(ctypes.Structure):
 
 class MoeError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {moe_status_string(status)} ({status})")
+        detail = ""
+        if status == MOE_ERR_CUDA:
+            msg = lib().moe_last_error().decode()
+            detail = f" [{msg}]" if msg else ""
+        super().__init__(f"{where}: {moe_status_string(status)} ({status}){detail}")
         self.status = status
 
 
@@ -69,6 +73,8 @@ def lib() -> ctypes.CDLL:
         L.moe_route_stats.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_last_error.argtypes = []
+        L.moe_last_error.restype = ctypes.c_char_p
         for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute",
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
@@ -80,7 +86,8 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
-            "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_status_string")
+            "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_status_string",
+            "moe_last_error")
 
 
 # ----------------------------------------------------------------------------- marshalling

@@ -116,7 +116,10 @@ def test_launch_count(L, name):
     # bf16: one tensor-core router launch whose last CTA also scans the dispatch histograms, then the
     # rank kernel and the row gather; fp32: router + reduction, histogram + scan + rank + gather
     router, dispatch = (1, 2) if wl.dtype == "bf16" else (2, 4)
-    assert n == router + dispatch + 2 + (2 if wl.n_shared else 0) + 1
+    # bf16: the up and the down projection each carry the routed and the shared experts in one
+    # launch; fp32: routed up + down, then shared up + down
+    ffn = 2 if wl.dtype == "bf16" else 2 + (2 if wl.n_shared else 0)
+    assert n == router + dispatch + ffn + 1
     assert moe.moe_layer_forward_launches(moe.config_from_workload(wl, T=0)) == router - 1 + 1
 
 
