@@ -281,10 +281,13 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
         barrier()
         return max_over_ranks(sum(a.elapsed_time(b) for a, b in ev)) / n
 
+    # stage times first (right after the warm-up, so that they see the same clocks as the steps
+    # that follow on a power-limited part), then the graph-replayed steps, then the eager ones
+    with ClockSampler(local) as clk_stages:
+        timed(lambda i: step(i), n_stage_steps)
     with ClockSampler(local) as clk:
         ms_step = timed(lambda i: graph.replay(), args.steps)
     ms_eager = timed(lambda i: step(), args.steps) if full else None
-    timed(lambda i: step(i), n_stage_steps)
     st = moe.moe_read_device_status(layer.ws)
     if st != 0:
         raise RuntimeError(f"{wl.name}: device status after timing: {moe.moe_status_string(st)}")
@@ -355,6 +358,7 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
                           "frac_of_hbm": round(layer_gbs / hbm, 4)},
         "l2": arm_config(wl, ws_n)["l2"],
         "clocks": clocks,
+        "stage_clocks": {k: v for k, v in clk_stages.summary().items() if k in ("sm_mhz", "reasons", "samples")},
     }
     if full:
         res["eager"] = {"value": round(T * ws_n / (ms_eager * 1e-3), 1), "ms_per_step": round(ms_eager, 5),

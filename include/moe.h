@@ -3,13 +3,13 @@
  *
  * The layer (mini-moe tutorial, sec. 3.1 MoELayer; OpenMythos article, sec. 3.1; FLAME-MoE
  * summary, sec. 2) maps T tokens x[T,d] to y[T,d]:
- *   z = x W_r^T (+ fixed logit bias)        P = softmax(z)      S_t = top-k of z_t
+ *   z = x W_r^T (+ fixed logit bias)        P = softmax(z / tau) S_t = top-k of z_t
  *   w_tj = P_t[e_j] / sum_{e in S_t} P_t[e]
  *   per-expert capacity C = ceil(cf T k / E) (cf <= 0: dropless), assignments ranked in token
  *   order, rank >= C dropped (weight 0)
  *   y_t = sum_{kept j} w_tj FFN_{e_j}(x_t) + sum_s FFN^shared_s(x_t)
  *   lb = lb_coef E sum_e f_e Pbar_e  (f_e = counts_e/(T k), Pbar_e = mean_t P_te)
- *   zl = z_coef mean_t logsumexp(z_t)^2
+ *   zl = z_coef mean_t logsumexp(z_t / tau)^2        (tau: router temperature, 1 by default)
  * The residual add x + y is not part of the layer.
  *
  * Conventions shared by every call:
@@ -72,6 +72,12 @@ typedef struct {
   float capacity_factor;   /* <= 0: dropless                                                */
   float lb_coef;           /* load-balance loss coefficient (alpha)                         */
   float z_coef;            /* router z-loss coefficient (beta)                              */
+  float router_temperature;/* tau > 0 divides the logits before the softmax, the renormalised
+                              weights and both losses (the top-k choice is that of the raw
+                              logits); 0 means none (tau = 1).  Negative: MOE_ERR_INVALID_ARG */
+  int32_t backup_expert;   /* 1: assignments over the capacity go, with their routing weight, to
+                              one extra expert (weights wb_* / bb_*) instead of being dropped
+                              (mini-moe tutorial, sec. 6); A_max becomes T*k.  0: dropped      */
 } moe_config;
 
 typedef struct {
@@ -85,6 +91,11 @@ typedef struct {
   const void* ws_up;              /* shared [S,dff,d] or NULL when n_shared == 0             */
   const void* ws_gate;            /* shared [S,dff,d] (SwiGLU) or NULL                       */
   const void* ws_down;            /* shared [S,d,dff] or NULL                                */
+  const void* wb_up;              /* backup expert [dff,d] (backup_expert) or NULL           */
+  const void* wb_gate;            /* backup expert [dff,d] (SwiGLU) or NULL                  */
+  const void* wb_down;            /* backup expert [d,dff] or NULL                           */
+  const void* bb_up;              /* backup expert bias [dff] (has_bias) or NULL             */
+  const void* bb_down;            /* backup expert bias [d] (has_bias) or NULL               */
 } moe_weights;
 
 /* Workspace bytes needed by every call below for this config (host only, no GPU work).
@@ -117,7 +128,10 @@ moe_status moe_route(const moe_config* cfg, const void* x, const void* w_router,
  *   -> offsets [E+1] (expert e owns rows offsets[e]..offsets[e+1]-1 of the sorted layout),
  *      kept [E] = min(counts, C), row_of [T,k] (sorted row of slot j of token t, -1 if dropped),
  *      tok_of [A_max] (token of each sorted row), x_perm [A_max,d] = x[tok_of[r]].
- * Rows of an expert are in increasing token order; rows >= offsets[E] are left untouched.
+ * Rows of an expert are in increasing token order; rows >= offsets[E] are left untouched -- except
+ * with a backup expert, where the assignments over capacity take rows offsets[E] .. offsets[E] +
+ * drops - 1 in (token, slot) order (their row_of entries are then >= 0, and the row range is kept
+ * in ws for moe_expert_ffn).
  * A counts vector that disagrees with topk_idx sets MOE_ERR_DEVICE_STATUS in the status word. */
 moe_status moe_permute(const moe_config* cfg, const void* x, const int32_t* topk_idx,
                        const int32_t* counts, int32_t* offsets, int32_t* kept,
@@ -222,6 +236,25 @@ moe_status moe_route_noalloc(const moe_config* cfg, const void* x, const void* w
  *     MOE_ERR_DEVICE_STATUS and that token is skipped).  Deterministic (integer counts). */
 moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const int32_t* offsets,
                            int32_t* coact, float* stats, void* ws, void* stream);
+
+/* Routing diagnostics (beyond the layer itself): the router entropy that the Naive-N0.5-Flash
+ * article (sec. 4, monitoring) and the GPT-4 2% article (routing-collapse tips) watch, and the two
+ * other balance-loss forms the pages give, beside the layer's own (OpenMythos article, sec. 3.1).
+ *   x [T,d], w_router [E,d], logit_bias [E] or NULL, with cfg's router temperature tau
+ *   -> diag [4] fp32, overwritten:
+ *      [0] mean over tokens of -sum_e P_te ln P_te (nats; P = softmax(z / tau))
+ *      [1] lb_coef E sum_e Pbar_e^2                             (mini-moe tutorial, sec. 3.1)
+ *      [2] lb_coef (sum_e (1/E)(ln(1/E) - ln(Pbar_e + 1e-8)) + sum_e (f_e - 1/E)^2)
+ *                                                               (GPT-4 2% article, sec. 4.2)
+ *      [3] lb_coef E sum_e f_e Pbar_e, the layer's load-balance loss
+ *      with Pbar_e = mean_t P_te and f_e = counts_e / (T k) from the top-k of the raw logits;
+ *   entropy_tok [T] fp32 or NULL: each token's entropy.
+ * The logits are recomputed in fp32 on CUDA cores in a fixed order; the per-block partials are
+ * reduced in block order (deterministic).  ws: a workspace of this config; the call overwrites
+ * the router's scratch in it (not the status word, where non-finite logits are reported). */
+moe_status moe_route_diagnostics(const moe_config* cfg, const void* x, const void* w_router,
+                                 const float* logit_bias, float* diag, float* entropy_tok, void* ws,
+                                 void* stream);
 
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);

@@ -18,7 +18,7 @@ using namespace moe;
 namespace {
 
 struct WsLayout {
-  size_t status, r_hist, r_psum, r_lse2, p_hist, p_base, drops;
+  size_t status, r_hist, r_psum, r_lse2, p_hist, p_base, drops, b_count, b_offs;
   size_t topk_idx, topk_w, counts, offsets, kept, row_of, tok_of;
   size_t x_perm, h, y_perm, h_sh, y_sh;
   size_t total;
@@ -27,6 +27,8 @@ struct WsLayout {
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 inline size_t elt(const moe_config* c) { return c->dtype == MOE_BF16 ? 2 : 4; }
 inline bool is_bf16(const moe_config* c) { return c->dtype == MOE_BF16; }
+// 1 / router temperature (0 in the config means no temperature)
+inline float inv_tau_of(const moe_config* c) { return c->router_temperature > 0.f ? 1.f / c->router_temperature : 1.f; }
 
 // cap = ceil(cf T k / E) computed exactly from the binary value of the float32 cf; -1 = dropless.
 int64_t capacity_exact(float cf, int64_t T, int64_t k, int64_t E) {
@@ -52,6 +54,7 @@ int64_t capacity_exact(float cf, int64_t T, int64_t k, int64_t E) {
 
 int64_t a_max_of(const moe_config* c) {
   const int64_t tk = (int64_t)c->T * c->k;
+  if (c->backup_expert) return tk;  // every assignment gets a row: kept ones, then the backup expert's
   const int64_t cap = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
   if (cap < 0) return tk;
   const int64_t ec = cap * c->E;
@@ -64,8 +67,10 @@ moe_status validate(const moe_config* c) {
   if (c->act != MOE_ACT_GELU_ERF && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (isnan(c->capacity_factor)) return MOE_ERR_INVALID_ARG;
+  if (!(c->router_temperature >= 0.f) || isinf(c->router_temperature)) return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->k > 8 || c->k > c->E || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
   if (c->has_bias && c->act != MOE_ACT_GELU_ERF) return MOE_ERR_UNSUPPORTED;
+  if (c->backup_expert != 0 && c->backup_expert != 1) return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->T * c->k > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->n_shared * c->dff > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if (is_bf16(c)) {
@@ -94,6 +99,8 @@ WsLayout layout(const moe_config* c) {
   L.p_hist = take(npb * E * 4);
   L.p_base = take(npb * E * 4);
   L.drops = take(4);
+  L.b_count = take(c->backup_expert ? npb * 4 : 0);
+  L.b_offs = take(c->backup_expert ? 8 : 0);
   L.topk_idx = take(T * k * 4);
   L.topk_w = take(T * k * 4);
   L.counts = take(E * 4);
@@ -147,13 +154,23 @@ moe_status route_impl(const moe_config* c, const void* x, const void* wr, const 
     return cuda_status(launch_route_tc(x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w,
                                        at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
                                        status + 1, counts, losses, c->lb_coef, c->z_coef, status, st, scan,
-                                       finalize));
+                                       finalize, inv_tau_of(c)));
   }
   MOE_CUDA(launch_route(false, x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w, at<int32_t>(ws, L.r_hist),
-                        at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2), status, st));
+                        at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2), status, st, inv_tau_of(c)));
   MOE_CUDA(launch_route_finalize(at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
                                  route_blocks(c->T), c->T, c->E, c->k, c->lb_coef, c->z_coef, counts, losses, st));
   return MOE_OK;
+}
+
+// Backup expert: the assignments the capacity dropped take the rows after the kept ones, in token
+// order (row range kept in the workspace for the projections).
+moe_status backup_impl(const moe_config* c, const void* x, const int32_t* offsets, int32_t* row_of, int32_t* tok_of,
+                       void* x_perm, void* ws, cudaStream_t st) {
+  if (!c->backup_expert || c->T <= 0) return MOE_OK;
+  const WsLayout L = layout(c);
+  return cuda_status(launch_backup_dispatch(is_bf16(c), offsets + c->E, c->T, c->k, c->d, x, row_of, tok_of, x_perm,
+                                            at<int32_t>(ws, L.b_count), at<int32_t>(ws, L.b_offs), st));
 }
 
 // scanned: the router already wrote the rank bases (p_base), kept, offsets and drops.
@@ -172,7 +189,7 @@ moe_status permute_impl(const moe_config* c, const void* x, const int32_t* topk_
   }
   MOE_CUDA(launch_dispatch(is_bf16(c), topk_idx, at<int32_t>(ws, L.p_base), offsets, c->T, c->E, c->k, cap, x, c->d,
                            row_of, tok_of, x_perm, (int)a_max_of(c), status, st));
-  return MOE_OK;
+  return backup_impl(c, x, offsets, row_of, tok_of, x_perm, ws, st);
 }
 
 moe_status run_projection_simt(const Projection& p, cudaStream_t st) {
@@ -195,7 +212,7 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
   const bool shared = S > 0 && c->T > 0;
   void* h = at<char>(ws, L.h);
   void* hs = at<char>(ws, L.h_sh);
-  Projection up[2] = {}, dn[2] = {};
+  Projection up[3] = {}, dn[3] = {};
   int nup = 0;
   // a token picks an expert at most once, so no expert receives more than T rows (or C with a capacity)
   const int64_t cap64 = capacity_exact(c->capacity_factor, c->T, c->k, c->E);
@@ -235,6 +252,27 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     q.act = ACT_NONE;
     q.out = y_shared; q.ldc = c->d; q.out_f32 = true; q.max_group_rows = c->T;
   }
+  int nbk = -1;  // index of the backup expert's problem
+  if (c->backup_expert && A > 0) {
+    nbk = nup;
+    const int32_t* boffs = at<int32_t>(ws, L.b_offs);  // {first backup row, end}, written by the dispatch
+    Projection& p = up[nup++];
+    p.A = x_perm; p.lda = c->d; p.rows_alloc = A;
+    p.offsets = boffs; p.G = 1; p.rows_static = 0;
+    p.B0 = swiglu ? w->wb_gate : w->wb_up; p.B1 = w->wb_up;
+    p.bias = c->has_bias ? w->bb_up : nullptr;
+    p.N = c->dff; p.K = c->d; p.N_w = c->dff; p.K_w = c->d; p.G_w = 1;
+    p.act = swiglu ? ACT_SWIGLU : ACT_GELU;
+    p.out = h; p.ldc = c->dff; p.max_group_rows = A;
+    Projection& q = dn[nup - 1];
+    q.A = h; q.lda = c->dff; q.rows_alloc = A;
+    q.offsets = boffs; q.G = 1; q.rows_static = 0;
+    q.B0 = w->wb_down; q.B1 = nullptr;
+    q.bias = c->has_bias ? w->bb_down : nullptr;
+    q.N = c->d; q.K = c->dff; q.N_w = c->d; q.K_w = c->dff; q.G_w = 1;
+    q.act = ACT_NONE;
+    q.out = y_perm; q.ldc = c->d; q.out_f32 = true; q.max_group_rows = A;
+  }
   if (is_bf16(c)) {
     if (nup) MOE_CUDA(launch_projection_tc(up, nup, status, st));
     if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
@@ -251,6 +289,10 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     MOE_TRY(run_projection_simt(up[nrouted], st));
     MOE_TRY(run_projection_simt(dn[nrouted], st));
   }
+  if (nbk >= 0) {
+    MOE_TRY(run_projection_simt(up[nbk], st));
+    MOE_TRY(run_projection_simt(dn[nbk], st));
+  }
   return MOE_OK;
 }
 
@@ -260,10 +302,15 @@ moe_status check_weights(const moe_config* c, const moe_weights* w) {
   if (c->has_bias && (!w->b_up || !w->b_down)) return MOE_ERR_INVALID_ARG;
   if (c->n_shared > 0 && (!w->ws_up || !w->ws_down || (c->act == MOE_ACT_SWIGLU && !w->ws_gate)))
     return MOE_ERR_INVALID_ARG;
+  if (c->backup_expert && (!w->wb_up || !w->wb_down || (c->act == MOE_ACT_SWIGLU && !w->wb_gate) ||
+                           (c->has_bias && (!w->bb_up || !w->bb_down))))
+    return MOE_ERR_INVALID_ARG;
+  if (is_bf16(c) && c->act == MOE_ACT_SWIGLU && c->backup_expert && w->wb_gate == w->wb_up) return MOE_ERR_UNSUPPORTED;
   // bf16 SwiGLU experts read their gate and up rows through one tensor map spanning both tensors
   if (is_bf16(c) && c->act == MOE_ACT_SWIGLU && (w->w_gate == w->w_up || (c->n_shared > 0 && w->ws_gate == w->ws_up)))
     return MOE_ERR_UNSUPPORTED;
-  const void* ps[] = {w->w_router, w->w_up, w->w_gate, w->w_down, w->b_up, w->b_down, w->ws_up, w->ws_gate, w->ws_down};
+  const void* ps[] = {w->w_router, w->w_up, w->w_gate, w->w_down, w->b_up, w->b_down, w->ws_up, w->ws_gate, w->ws_down,
+                      w->wb_up, w->wb_gate, w->wb_down, w->bb_up, w->bb_down};
   for (const void* p : ps)
     if (p && misaligned(p)) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -309,6 +356,7 @@ moe_status layer_impl(const moe_config* c, const moe_weights* w, const void* x, 
                                    counts, losses, offsets, at<int32_t>(ws, L.kept), drops, row_of,
                                    at<int32_t>(ws, L.tok_of), x_perm, (int)a_max_of(c), at<uint32_t>(ws, L.status),
                                    st));
+    MOE_TRY(backup_impl(c, x, offsets, row_of, at<int32_t>(ws, L.tok_of), x_perm, ws, st));
   } else {
     MOE_TRY(permute_impl(c, x, topk_idx, counts, offsets, at<int32_t>(ws, L.kept), row_of, at<int32_t>(ws, L.tok_of),
                          x_perm, drops, ws, st, scanned));
@@ -473,6 +521,21 @@ moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const
                                         at<uint32_t>(ws, L.status), static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_route_diagnostics(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
+                                 float* diag, float* entropy_tok, void* ws, void* stream) {
+  NvtxRange nvtx_range("moe_route_diagnostics");
+  MOE_TRY(validate(cfg));
+  if (!w_router || !diag || !ws || (cfg->T > 0 && !x)) return MOE_ERR_INVALID_ARG;
+  if (misaligned(ws) || misaligned(x) || misaligned(w_router)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(cfg);
+  static_assert(kRouteTokens == 32, "the diagnostics reuse the router's 32-token block scratch");
+  if (route_diag_blocks(cfg->T) > route_blocks(cfg->T)) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_route_diag(is_bf16(cfg), x, w_router, logit_bias, cfg->T, cfg->d, cfg->E, cfg->k,
+                                       inv_tau_of(cfg), cfg->lb_coef, diag, entropy_tok, at<float>(ws, L.r_psum),
+                                       at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_lse2), at<uint32_t>(ws, L.status),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x, void* y, float* losses,
                              int32_t* counts_out, int32_t* drops_out, void* ws, void* stream) {
   NvtxRange nvtx_range("moe_layer_forward");
@@ -522,9 +585,10 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   const bool scanned = dfused || (is_bf16(cfg) && route_tc_fuses_scan(cfg->T, cfg->E));
   if (!tokens) n += 1;                        // scan (writes zero offsets)
   else n += (scanned ? 0 : 2) + dispatch_launches(true, cfg->d, is_bf16(cfg) ? 2 : 4);  // [hist, scan,] dispatch
+  if (tokens && cfg->backup_expert) n += 2;   // backup rows: count, place
   const bool routed = a_max_of(cfg) > 0, shared = cfg->n_shared > 0 && tokens;
   if (is_bf16(cfg)) n += (routed || shared) ? 2 : 0;           // up + down, routed and shared together
-  else n += (routed ? 2 : 0) + (shared ? 2 : 0);                // routed up + down, shared up + down
+  else n += (routed ? 2 : 0) + (shared ? 2 : 0) + (routed && cfg->backup_expert ? 2 : 0);  // routed, shared, backup
   if (tokens) n += 1;                         // combine
   return n;
 }

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) k_proj_simt(const T* __restrict__ A, int6
   if (n >= N) return;
   int g = 0;
   if (offsets) {
-    if (row >= offsets[G]) return;
+    if (row < offsets[0] || row >= offsets[G]) return;  // a problem's rows need not start at row 0
     int lo = 0, hi = G;  // largest g with offsets[g] <= row
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;

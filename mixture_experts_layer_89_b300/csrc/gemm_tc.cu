@@ -6,8 +6,9 @@
 //   up:   h = GELU(x_perm W_up^T + b_up)          or  h = SiLU(x_perm W_gate^T) * (x_perm W_up^T)
 //   down: y_perm = h W_down^T (+ b_down)
 // (expert forms: mini-moe tutorial, sec. 3.1; GPT-4 2% article, sec. 3.1).  One launch may carry
-// two such problems -- the routed experts and the always-on shared experts (FLAME-MoE summary,
-// sec. 2) -- whose tiles share the persistent CTAs.
+// up to three such problems -- the routed experts, the always-on shared experts (FLAME-MoE
+// summary, sec. 2) and a backup expert for assignments over capacity (mini-moe tutorial, sec. 6)
+// -- whose tiles share the persistent CTAs.
 //
 // Orientation: the weights are the MMA's M side and the tokens its N side,
 //   D[feature, token] = sum_k W[feature, k] X[token, k],
@@ -31,8 +32,8 @@
 //
 // Warp roles (one CTA per SM, persistent over tiles):
 //   warp 0      TMA producer: this CTA's weight rows and token rows of a K step, one box each
-//               (6 stages of 32 KB; decode-sized 10 of 18 KB), all signalling the even CTA's
-//               stage barrier
+//               (6 stages of 32 KB, SwiGLU 7; decode-sized 10 of 18 KB), all signalling the even
+//               CTA's stage barrier
 //   warp 1      MMA issuer (one thread of the even CTA): tcgen05.mma per 16-wide K step into one
 //               of two 256-column TMEM accumulators (double buffered: the epilogue of a tile
 //               overlaps the next tile's MMAs)
@@ -62,8 +63,8 @@ namespace {
 constexpr int BK = 64;                          // K per stage: one 128-byte swizzle row of bf16
 constexpr int AR = 128;                         // weight rows per CTA (the pair's M = 256)
 constexpr int WBOX = AR * BK * 2;               // 16 KB: one weight tile of a CTA
-constexpr int MAXP = 2;                         // problems per launch: routed and shared experts
-constexpr int MAXGT = 256 + 1;                  // groups over both problems
+constexpr int MAXP = 3;                         // problems per launch: routed, shared and backup experts
+constexpr int MAXGT = 256 + 2;                  // groups over all problems
 constexpr int TBL_PER_LANE = (MAXGT + 31) / 32;
 constexpr int MAX_STAGES = 12;
 constexpr uint32_t TMEM_COLS = 512;
@@ -80,9 +81,9 @@ template <int ACT, int NTV> constexpr int a_bytes() { return WBOX; }
 template <int ACT, int NTV> constexpr int b_bytes() { return tile_tokens<ACT, NTV>() / 2 * BK * 2; }
 template <int ACT, int NTV> constexpr int stage_bytes() { return a_bytes<ACT, NTV>() + b_bytes<ACT, NTV>(); }
 // epilogue staging per warp: fp32 32 x 32 (128-byte rows) or bf16 32 x 32 (64-byte rows); two
-// buffers per warp except with 16 warps
+// buffers per warp except with 16 warps; none for SwiGLU, which stores straight from registers
 template <int ACT> constexpr int stg_bytes() { return ACT == ACT_NONE ? 4096 : 2048; }
-template <int ACT> constexpr int stg_bufs() { return epi_warps<ACT>() > 8 ? 1 : 2; }
+template <int ACT> constexpr int stg_bufs() { return ACT == ACT_SWIGLU ? 0 : (epi_warps<ACT>() > 8 ? 1 : 2); }
 constexpr int CTL_BYTES = 2048;  // >= sizeof(SmemCtl), checked below
 template <int ACT, int NTV> constexpr int n_stages() {
   return (SMEM_LIMIT - 1024 - CTL_BYTES - epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>()) /
@@ -120,7 +121,7 @@ struct SmemCtl {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
-  int g0;               // groups of problem 0
+  int g0, g01;          // groups of problem 0, of problems 0 and 1
   int gt;               // groups over all problems
   int u_pre[MAXGT + 1]; // prefix over groups of their tiles
 };
@@ -133,7 +134,7 @@ constexpr size_t smem_total() {
 static_assert(smem_total<ACT_NONE, 256>() <= SMEM_LIMIT && smem_total<ACT_GELU, 256>() <= SMEM_LIMIT &&
                   smem_total<ACT_SWIGLU, 256>() <= SMEM_LIMIT && smem_total<ACT_SWIGLU, 32>() <= SMEM_LIMIT,
               "shared memory per CTA");
-static_assert(n_stages<ACT_NONE, 256>() == 6 && n_stages<ACT_SWIGLU, 256>() == 6 && n_stages<ACT_NONE, 32>() >= 10,
+static_assert(n_stages<ACT_NONE, 256>() == 6 && n_stages<ACT_SWIGLU, 256>() == 7 && n_stages<ACT_NONE, 32>() >= 10,
               "stage counts");
 
 // Wait that ignores the abort flag (used to drain in-flight async operations before exit).
@@ -207,7 +208,7 @@ template <int ACT, int NTV>
 __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
     k_proj_tc(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs args) {
   constexpr int EPIW = epi_warps<ACT>();
-  constexpr int NBUF = stg_bufs<ACT>();
+  constexpr int NBUF = stg_bufs<ACT>() > 0 ? stg_bufs<ACT>() : 1;  // (SwiGLU stages nothing)
   constexpr int STG = stg_bytes<ACT>();
   constexpr int NT = tile_tokens<ACT, NTV>();
   constexpr int FT = feat_per_tile<ACT>();
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stg_base = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned (the swizzle atoms)
-  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * NBUF * STG);
+  SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * stg_bufs<ACT>() * STG);
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int crank = (int)cluster_ctarank();
@@ -256,7 +257,8 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
     // tiles of every group over both problems: lane owns groups [TBL_PER_LANE lane, + TBL_PER_LANE)
     const int g0 = args.p[0].offsets ? args.p[0].G : 1;
     const int g1 = args.nprob > 1 ? (args.p[1].offsets ? args.p[1].G : 1) : 0;
-    const int gt = g0 + g1;
+    const int g2 = args.nprob > 2 ? (args.p[2].offsets ? args.p[2].G : 1) : 0;
+    const int gt = g0 + g1 + g2;
     int cnt[TBL_PER_LANE];
     int local = 0;
 #pragma unroll
@@ -264,9 +266,9 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
       const int g = lane * TBL_PER_LANE + i;
       cnt[i] = 0;
       if (g < gt) {
-        const int p = g < g0 ? 0 : 1;
+        const int p = g < g0 ? 0 : (g < g0 + g1 ? 1 : 2);
         const ProbArgs& P = args.p[p];
-        const int gl = g - (p ? g0 : 0);
+        const int gl = g - (p == 0 ? 0 : (p == 1 ? g0 : g0 + g1));
         const int lo = P.offsets ? P.offsets[gl] : 0;
         const int hi = P.offsets ? P.offsets[gl + 1] : P.rows_static;
         const int tt = hi > lo ? (hi - lo + NT - 1) / NT : 0;
@@ -290,6 +292,7 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
     if (lane == 31) {
       ctl->u_pre[gt] = incl;
       ctl->g0 = g0;
+      ctl->g01 = g0 + g1;
       ctl->gt = gt;
     }
   }
@@ -309,8 +312,8 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
       if (ctl->u_pre[mid] <= u) lo = mid; else hi = mid;
     }
     Tile t;
-    t.p = lo < ctl->g0 ? 0 : 1;
-    t.g = lo - (t.p ? ctl->g0 : 0);
+    t.p = lo < ctl->g0 ? 0 : (lo < ctl->g01 ? 1 : 2);
+    t.g = lo - (t.p == 0 ? 0 : (t.p == 1 ? ctl->g0 : ctl->g01));
     const ProbArgs& P = args.p[t.p];
     const int r0 = P.offsets ? __ldg(P.offsets + t.g) : 0;
     t.m_end = P.offsets ? __ldg(P.offsets + t.g + 1) : P.rows_static;

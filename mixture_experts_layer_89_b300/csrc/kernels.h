@@ -13,9 +13,10 @@ constexpr int kRouteTokens = 32;  // tokens per router CTA
 int route_blocks(int T);
 // x [T,d] and w_router [E,d] of type `bf16` (else fp32).  Writes top-k, per-CTA histograms,
 // per-CTA softmax column sums and per-CTA sums of lse^2.
+// inv_tau: 1 / router temperature (the softmax, the weights and lse use z / tau; the top-k uses z)
 cudaError_t launch_route(bool bf16, const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                          int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2,
-                         uint32_t* status, cudaStream_t st);
+                         uint32_t* status, cudaStream_t st, float inv_tau = 1.f);
 // Tensor-core router of bf16 layers (one launch, 128 tokens per CTA): writes top-k, and through
 // the last CTA to finish, counts [E] and losses [2].  hist/psum/lse2 hold route_tc_blocks(T) rows
 // of partials; *done must be zero before the launch and is zero again after it.
@@ -33,7 +34,7 @@ bool route_tc_fuses_scan(int T, int E);
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
-                            cudaStream_t st, const RouteScan* scan, bool finalize = true);
+                            cudaStream_t st, const RouteScan* scan, bool finalize = true, float inv_tau = 1.f);
 // Reduces the per-CTA partials: counts [E] and losses [2].
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,
                                   int k, float lb_coef, float z_coef, int32_t* counts, float* losses,
@@ -66,6 +67,21 @@ cudaError_t launch_dispatch_fused(bool bf16, const int32_t* topk_idx, const int3
 // dropped fraction; offsets may be NULL).
 cudaError_t launch_route_stats(const int32_t* topk_idx, const int32_t* offsets, int T, int E, int k, int32_t* coact,
                                float* stats, uint32_t* status, cudaStream_t st);
+
+// Routing diagnostics (route_diag.cu): diag [4] = {mean router entropy, lb_coef E sum Pbar^2,
+// lb_coef (KL(uniform || Pbar + 1e-8) + sum (f - 1/E)^2), lb_coef E sum f Pbar}; ent_tok [T] or NULL.
+// psum/cnt [route_diag_blocks(T)][E] and hsum [route_diag_blocks(T)] are scratch.
+int route_diag_blocks(int T);
+cudaError_t launch_route_diag(bool bf16, const void* x, const void* wr, const float* lbias, int T, int d, int E,
+                              int k, float inv_tau, float lb_coef, float* diag, float* ent_tok, float* psum,
+                              int32_t* cnt, float* hsum, uint32_t* status, cudaStream_t st);
+
+// Backup expert: after a dispatch with capacity drops, the dropped assignments take rows
+// kept_rows[0] .. (in token order) of row_of / tok_of / x_perm; backup_offs [2] = that row range.
+// bcount [perm_blocks(T)] is scratch.  Two launches.
+cudaError_t launch_backup_dispatch(bool bf16, const int32_t* kept_rows, int T, int k, int d, const void* x,
+                                   int32_t* row_of, int32_t* tok_of, void* x_perm, int32_t* bcount,
+                                   int32_t* backup_offs, cudaStream_t st);
 
 // Kernels launch_dispatch launches (2 with the row copy, else 1).
 int dispatch_launches(bool with_rows, int d, int elt_bytes);

@@ -308,9 +308,114 @@ __global__ void __launch_bounds__(256) k_gather_rows_scalar(const T* __restrict_
     for (int c = threadIdx.x & 31; c < d; c += 32) x_perm[(size_t)r * d + c] = x[(size_t)t * d + c];
   }
 }
+
+// Backup expert (a routing variant: the mini-moe tutorial, sec. 6, routes tokens over an expert's
+// capacity to a backup expert instead of dropping them).  The assignments the capacity drops take
+// rows offsets[E] .. offsets[E] + drops - 1 of the expert-sorted layout, in (token, slot) order, and
+// keep their routing weight.  k_backup_count: dropped assignments per block of PT tokens.
+__global__ void __launch_bounds__(256) k_backup_count(const int32_t* __restrict__ row_of, int Tn, int k,
+                                                      int32_t* __restrict__ bcount) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int c;
+  if (threadIdx.x == 0) c = 0;
+  __syncthreads();
+  const long a0 = (long)blockIdx.x * PT * k;
+  const long a1 = min(a0 + (long)PT * k, (long)Tn * k);
+  int local = 0;
+  for (long a = a0 + threadIdx.x; a < a1; a += 256) local += row_of[a] < 0 ? 1 : 0;
+  atomicAdd(&c, local);  // integers: the total does not depend on the order
+  __syncthreads();
+  if (threadIdx.x == 0) bcount[blockIdx.x] = c;
+}
+
+// One CTA per block: its base (the earlier blocks' counts), the ranks of its dropped assignments in
+// (token, slot) order (warp 0, ballots over 32-wide chunks), row_of / tok_of, and the token rows
+// copied into x_perm.  CTA 0 also writes the backup expert's row range {offsets[E], offsets[E] + all}.
+template <typename T>
+__global__ void __launch_bounds__(256) k_backup_place(const int32_t* __restrict__ bcount, int nb,
+                                                      const int32_t* __restrict__ kept_rows, int Tn, int k, int d,
+                                                      const T* __restrict__ x, int32_t* __restrict__ row_of,
+                                                      int32_t* __restrict__ tok_of, T* __restrict__ x_perm,
+                                                      int32_t* __restrict__ backup_offs) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ int red[256];
+  __shared__ int rows[PT * 8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int a_kept = *kept_rows;
+  int before = 0, all = 0;
+  for (int b = tid; b < nb; b += 256) {
+    const int c = bcount[b];
+    all += c;
+    if (b < (int)blockIdx.x) before += c;
+  }
+  red[tid] = before;
+  __syncthreads();
+  for (int sh = 128; sh; sh >>= 1) {
+    if (tid < sh) red[tid] += red[tid + sh];
+    __syncthreads();
+  }
+  const int base = a_kept + red[0];
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    red[tid] = all;
+    __syncthreads();
+    for (int sh = 128; sh; sh >>= 1) {
+      if (tid < sh) red[tid] += red[tid + sh];
+      __syncthreads();
+    }
+    if (tid == 0) {
+      backup_offs[0] = a_kept;
+      backup_offs[1] = a_kept + red[0];
+    }
+  }
+  const long a0 = (long)blockIdx.x * PT * k;
+  const int na = (int)(min(a0 + (long)PT * k, (long)Tn * k) - a0);
+  if (warp == 0) {
+    int run = 0;
+    for (int c0 = 0; c0 < na; c0 += 32) {
+      const int a = c0 + lane;
+      const bool dropped = a < na && row_of[a0 + a] < 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, dropped);
+      const int row = dropped ? base + run + __popc(bal & ((1u << lane) - 1u)) : -1;
+      run += __popc(bal);
+      if (a < na) rows[a] = row;
+      if (dropped) {
+        row_of[a0 + a] = row;
+        tok_of[row] = (int)((a0 + a) / k);
+      }
+    }
+  }
+  __syncthreads();
+  for (int a = warp; a < na; a += 8) {  // one warp per backup row
+    const int row = rows[a];
+    if (row < 0) continue;
+    const T* src = x + (size_t)((a0 + a) / k) * d;
+    T* dst = x_perm + (size_t)row * d;
+    for (int c = lane; c < d; c += 32) dst[c] = src[c];
+  }
+}
 }  // namespace
 
 int perm_blocks(int T) { return (T + PT - 1) / PT; }
+
+cudaError_t launch_backup_dispatch(bool bf16, const int32_t* kept_rows, int T, int k, int d, const void* x,
+                                   int32_t* row_of, int32_t* tok_of, void* x_perm, int32_t* bcount,
+                                   int32_t* backup_offs, cudaStream_t st) {
+  if (T <= 0 || k > 8) return T <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+  const int nb = perm_blocks(T);
+  cudaError_t e = launch_pdl(k_backup_count, dim3(nb), dim3(256), 0, st, static_cast<const int32_t*>(row_of), T, k,
+                             bcount);
+  if (e != cudaSuccess) return e;
+  if (bf16)
+    return launch_pdl(k_backup_place<__nv_bfloat16>, dim3(nb), dim3(256), 0, st, static_cast<const int32_t*>(bcount),
+                      nb, kept_rows, T, k, d, static_cast<const __nv_bfloat16*>(x), row_of, tok_of,
+                      static_cast<__nv_bfloat16*>(x_perm), backup_offs);
+  return launch_pdl(k_backup_place<float>, dim3(nb), dim3(256), 0, st, static_cast<const int32_t*>(bcount), nb,
+                    kept_rows, T, k, d, static_cast<const float*>(x), row_of, tok_of, static_cast<float*>(x_perm),
+                    backup_offs);
+}
 
 cudaError_t launch_perm_hist(const int32_t* topk_idx, int T, int E, int k, int32_t* phist, uint32_t* status,
                              cudaStream_t st) {

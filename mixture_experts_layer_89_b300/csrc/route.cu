@@ -27,7 +27,7 @@ template <typename T, int NI>
 __global__ void __launch_bounds__(RTHREADS)
     k_route(const T* __restrict__ x, const T* __restrict__ wr, const float* __restrict__ lbias, int Tn, int d, int E,
             int k, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ hist,
-            float* __restrict__ psum, float* __restrict__ lse2, uint32_t* status) {
+            float* __restrict__ psum, float* __restrict__ lse2, uint32_t* status, float inv_tau) {
   extern __shared__ float sm[];
   float* xs = sm;                      // [RT][RDC+1]
   float* wsm = xs + RT * (RDC + 1);    // [E][RDC+1]
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(RTHREADS)
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (lane + 32 * i < E) s += expf(v[i] - m);
+      if (lane + 32 * i < E) s += expf((v[i] - m) * inv_tau);
 #pragma unroll
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     const float inv_s = 1.f / s;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(RTHREADS)
         }
       }
       if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      const float p = expf(bv - m);
+      const float p = expf((bv - m) * inv_tau);
       selsum += p;
       if (lane == j) {
         my_e = be;
@@ -150,10 +150,10 @@ __global__ void __launch_bounds__(RTHREADS)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      if (e < E) lg[r * (E + 1) + e] = expf(v[i] - m) * inv_s;
+      if (e < E) lg[r * (E + 1) + e] = expf((v[i] - m) * inv_tau) * inv_s;
     }
     if (lane == 0) {
-      lse_s[r] = m + logf(s);
+      lse_s[r] = m * inv_tau + logf(s);
       if (bad) atomicOr(status, DEV_NONFINITE);
     }
   }
@@ -218,25 +218,26 @@ __global__ void __launch_bounds__(256) k_route_finalize(const int32_t* __restric
 template <typename T, int NI>
 cudaError_t launch_route_t(const void* x, const void* wr, const float* lbias, int Tn, int d, int E, int k,
                            int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, float inv_tau) {
   const size_t smem = sizeof(float) * ((size_t)RT * (RDC + 1) + (size_t)E * (RDC + 1) + (size_t)RT * (E + 1) + RT) +
                       sizeof(int) * (size_t)E;
   cudaError_t err = ensure_smem_attr(reinterpret_cast<const void*>(k_route<T, NI>), smem);
   if (err != cudaSuccess) return err;
   k_route<T, NI><<<route_blocks(Tn), RTHREADS, smem, st>>>(static_cast<const T*>(x), static_cast<const T*>(wr), lbias,
-                                                            Tn, d, E, k, topk_idx, topk_w, hist, psum, lse2, status);
+                                                            Tn, d, E, k, topk_idx, topk_w, hist, psum, lse2, status,
+                                                            inv_tau);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_route_dispatch_ni(const void* x, const void* wr, const float* lbias, int Tn, int d, int E, int k,
                                      int32_t* ti, float* tw, int32_t* hist, float* psum, float* lse2, uint32_t* status,
-                                     cudaStream_t st) {
-  if (E <= 16) return launch_route_t<T, 1>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st);
-  if (E <= 32) return launch_route_t<T, 2>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st);
-  if (E <= 64) return launch_route_t<T, 4>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st);
-  if (E <= 128) return launch_route_t<T, 8>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st);
-  return launch_route_t<T, 16>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st);
+                                     cudaStream_t st, float inv_tau) {
+  if (E <= 16) return launch_route_t<T, 1>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st, inv_tau);
+  if (E <= 32) return launch_route_t<T, 2>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st, inv_tau);
+  if (E <= 64) return launch_route_t<T, 4>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st, inv_tau);
+  if (E <= 128) return launch_route_t<T, 8>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st, inv_tau);
+  return launch_route_t<T, 16>(x, wr, lbias, Tn, d, E, k, ti, tw, hist, psum, lse2, status, st, inv_tau);
 }
 }  // namespace
 
@@ -244,12 +245,13 @@ int route_blocks(int T) { return (T + RT - 1) / RT; }
 
 cudaError_t launch_route(bool bf16, const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                          int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* status,
-                         cudaStream_t st) {
+                         cudaStream_t st, float inv_tau) {
   if (T <= 0) return cudaSuccess;
   if (bf16)
     return launch_route_dispatch_ni<__nv_bfloat16>(x, wr, lbias, T, d, E, k, topk_idx, topk_w, hist, psum, lse2,
-                                                   status, st);
-  return launch_route_dispatch_ni<float>(x, wr, lbias, T, d, E, k, topk_idx, topk_w, hist, psum, lse2, status, st);
+                                                   status, st, inv_tau);
+  return launch_route_dispatch_ni<float>(x, wr, lbias, T, d, E, k, topk_idx, topk_w, hist, psum, lse2, status, st,
+                                         inv_tau);
 }
 
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,

@@ -123,6 +123,7 @@ struct RouteArgs {
   float* losses;
   float lb_coef, z_coef;
   float band_scale;   // 2^-22 * d / 16
+  float inv_tau;      // 1 / router temperature (softmax, weights and lse of z / tau; top-k on z)
   // dispatch scan fused into the last CTA (pbase == NULL: not done here): per-block rank bases
   // [nb][E], kept counts [E], offsets [E+1], dropped assignments; cap = capacity (INT_MAX dropless)
   int cap;
@@ -507,14 +508,14 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     } else {
     int e = e_lo;
     for (; e + 1 < e_hi; e += 2) {
-      const float p0 = __expf(S.Z[r * ZP + e] - m), p1 = __expf(S.Z[r * ZP + e + 1] - m);
+      const float p0 = __expf((S.Z[r * ZP + e] - m) * a.inv_tau), p1 = __expf((S.Z[r * ZP + e + 1] - m) * a.inv_tau);
       S.Z[r * ZP + e] = p0;
       S.Z[r * ZP + e + 1] = p1;
       s0 += p0;
       s1 += p1;
     }
     if (e < e_hi) {
-      const float p0 = __expf(S.Z[r * ZP + e] - m);
+      const float p0 = __expf((S.Z[r * ZP + e] - m) * a.inv_tau);
       S.Z[r * ZP + e] = p0;
       s0 += p0;
     }
@@ -527,7 +528,7 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     const float s = ctl->spart[0][r] + ctl->spart[1][r];
     const bool valid = t0 + r < a.T;
     ctl->sinv[r] = valid ? 1.f / s : 0.f;
-    ctl->lse[r] = valid ? ctl->mx[r] + __logf(s) : 0.f;
+    ctl->lse[r] = valid ? ctl->mx[r] * a.inv_tau + __logf(s) : 0.f;
   }
 
   // ------------------------------------------------------------------ C: exact re-decision of near ties
@@ -591,13 +592,13 @@ __global__ void __launch_bounds__(RTHREADS, 1)
     if (t < a.T) {
       float wsum = 0.f;
 #pragma unroll
-      for (int j = 0; j < KL; ++j) wsum += (j < k) ? __expf(lv[j] - lv[0]) : 0.f;
+      for (int j = 0; j < KL; ++j) wsum += (j < k) ? __expf((lv[j] - lv[0]) * a.inv_tau) : 0.f;
       const float inv_w = 1.f / wsum;
 #pragma unroll
       for (int j = 0; j < KL; ++j) {
         if (j < k) {
           a.topk_idx[(size_t)t * k + j] = le[j];
-          a.topk_w[(size_t)t * k + j] = __expf(lv[j] - lv[0]) * inv_w;
+          a.topk_w[(size_t)t * k + j] = __expf((lv[j] - lv[0]) * a.inv_tau) * inv_w;
           atomicAdd(&ctl->hist[le[j]], 1);
         }
       }
@@ -803,7 +804,7 @@ bool route_tc_fuses_scan(int T, int E) {
 cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
-                            cudaStream_t st, const RouteScan* scan, bool finalize) {
+                            cudaStream_t st, const RouteScan* scan, bool finalize, float inv_tau) {
   if (T <= 0) {
     cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (e != cudaSuccess) return e;
@@ -841,6 +842,7 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
   a.hist = hist; a.psum = psum; a.lse2 = lse2; a.done = done;
   a.counts = counts; a.losses = losses; a.lb_coef = lb_coef; a.z_coef = z_coef;
   a.band_scale = ldexpf((float)d / 16.f, -22);
+  a.inv_tau = inv_tau;
   a.status = status;
   a.finalize = finalize ? 1 : 0;
   const bool fuse = finalize && scan && route_tc_fuses_scan(T, E);

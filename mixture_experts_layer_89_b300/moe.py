@@ -25,13 +25,15 @@ _c_p = ctypes.c_void_p
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", _c_i32), ("d", _c_i32), ("E", _c_i32), ("k", _c_i32), ("dff", _c_i32),
                 ("n_shared", _c_i32), ("act", _c_i32), ("dtype", _c_i32), ("has_bias", _c_i32),
-                ("capacity_factor", ctypes.c_float), ("lb_coef", ctypes.c_float), ("z_coef", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_float), ("lb_coef", ctypes.c_float), ("z_coef", ctypes.c_float),
+                ("router_temperature", ctypes.c_float), ("backup_expert", _c_i32)]
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [("w_router", _c_p), ("router_logit_bias", _c_p), ("w_up", _c_p), ("w_gate", _c_p),
                 ("w_down", _c_p), ("b_up", _c_p), ("b_down", _c_p), ("ws_up", _c_p), ("ws_gate", _c_p),
-                ("ws_down", _c_p)]
+                ("ws_down", _c_p), ("wb_up", _c_p), ("wb_gate", _c_p), ("wb_down", _c_p), ("bb_up", _c_p),
+                ("bb_down", _c_p)]
 
 
 class MoeError(RuntimeError):
@@ -70,6 +72,7 @@ def lib() -> ctypes.CDLL:
         L.moe_read_device_status.argtypes = [_c_p, _c_p]
         L.moe_layer_forward_launches.argtypes = [cfgp]
         L.moe_set_wait_limit.argtypes = [_c_p, ctypes.c_uint64, _c_p]
+        L.moe_route_diagnostics.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_route_stats.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -78,7 +81,7 @@ def lib() -> ctypes.CDLL:
         for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute",
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
-                     "moe_set_wait_limit"):
+                     "moe_set_wait_limit", "moe_route_diagnostics"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -86,8 +89,8 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
-            "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_status_string",
-            "moe_last_error")
+            "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_route_diagnostics",
+            "moe_status_string", "moe_last_error")
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -118,21 +121,24 @@ def _check(status: int, where: str):
 
 def make_config(T: int, d: int, E: int, k: int, dff: int, act: str = "gelu", dtype: str = "bf16",
                 n_shared: int = 0, has_bias: bool = False, capacity_factor: float = 0.0,
-                lb_coef: float = 0.01, z_coef: float = 0.001) -> MoeConfig:
+                lb_coef: float = 0.01, z_coef: float = 0.001, temperature: float = 1.0,
+                backup_expert: bool = False) -> MoeConfig:
     return MoeConfig(T, d, E, k, dff, n_shared, MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_GELU_ERF,
                      MOE_BF16 if dtype == "bf16" else MOE_F32, int(bool(has_bias)), float(capacity_factor),
-                     float(lb_coef), float(z_coef))
+                     float(lb_coef), float(z_coef), float(temperature), int(bool(backup_expert)))
 
 
 def config_from_workload(wl, T: Optional[int] = None) -> MoeConfig:
     return make_config(wl.T if T is None else T, wl.d, wl.E, wl.k, wl.dff, wl.act, wl.dtype, wl.n_shared,
-                       wl.bias, wl.cf, wl.lb_coef, wl.z_coef)
+                       wl.bias, wl.cf, wl.lb_coef, wl.z_coef, getattr(wl, "temperature", 1.0),
+                       getattr(wl, "backup", False))
 
 
 def make_weights(t: Dict[str, Optional[torch.Tensor]]) -> MoeWeights:
     """MoeWeights over the tensors of ``t`` (keys as produced by ``synth.make_inputs``)."""
     w = MoeWeights(*[_p(t.get(n)) for n in ("w_router", "logit_bias", "w_up", "w_gate", "w_down", "b_up", "b_down",
-                                            "ws_up", "ws_gate", "ws_down")])
+                                            "ws_up", "ws_gate", "ws_down", "wb_up", "wb_gate", "wb_down", "bb_up",
+                                            "bb_down")])
     w._keep = t  # keep the tensors alive as long as the struct
     return w
 
@@ -209,6 +215,11 @@ def moe_route_stats(cfg, topk_idx, offsets, coact, stats, ws, stream=None):
 def moe_set_wait_limit(ws, limit_ns: int, stream=None):
     """Shorten (or, with 0, restore) the router's bounded waits for calls that use ``ws``."""
     _check(lib().moe_set_wait_limit(_p(ws), int(limit_ns), _s(stream)), "moe_set_wait_limit")
+
+
+def moe_route_diagnostics(cfg, x, w_router, logit_bias, diag, entropy_tok, ws, stream=None):
+    _check(lib().moe_route_diagnostics(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(diag),
+                                       _p(entropy_tok), _p(ws), _s(stream)), "moe_route_diagnostics")
 
 
 def moe_layer_forward_launches(cfg) -> int:

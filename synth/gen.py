@@ -9,7 +9,9 @@ so a test always hands the *same* drawn tensors to both sides):
   ``w_router [E,d]``; then for each routed expert e = 0..E-1 either
   ``w_up[e] [dff,d]`` (+ ``b_up[e]``), ``w_down[e] [d,dff]`` (+ ``b_down[e]``)   (GELU experts) or
   ``w_gate[e] [dff,d]``, ``w_up[e] [dff,d]``, ``w_down[e] [d,dff]``              (SwiGLU experts);
-  then for each shared expert s the same matrices into ``ws_gate/ws_up/ws_down``.
+  then for each shared expert s the same matrices into ``ws_gate/ws_up/ws_down``; then, for a
+  layer with a backup expert, its matrices into ``wb_gate/wb_up/wb_down`` (biases ``bb_up``,
+  ``bb_down`` as the routed experts have them).
   Each draw is ``randn * std`` (std 0.02) in fp32, then cast to the layer dtype;
 * biases are zero unless ``bias_std > 0`` (only synthetic test shapes use that);
 * an optional fixed router logit bias (fp32 ``[E]``) is ``(logit_bias0, 0, ..., 0)``.
@@ -46,6 +48,8 @@ class Workload:
     z_coef: float = 0.001
     w_std: float = 0.02
     bias_std: float = 0.0
+    temperature: float = 1.0 # router temperature (a routing variant; 1 = none)
+    backup: bool = False     # one backup expert takes the assignments over capacity (a routing variant)
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -134,4 +138,15 @@ def make_inputs(wl: Workload, device: str = "cpu", T: Optional[int] = None) -> D
         out.update(ws_gate=ws_gate, ws_up=ws_up, ws_down=ws_down)
     else:
         out.update(ws_gate=None, ws_up=None, ws_down=None)
+    if wl.backup:
+        wb_gate = _draw(gw, (f, d), wl.w_std, dt, dev) if swiglu else None
+        wb_up = _draw(gw, (f, d), wl.w_std, dt, dev)
+        bb_up = (_draw(gw, (f,), wl.bias_std, dt, dev) if wl.bias_std > 0 else torch.zeros(f, dtype=dt, device=dev)) \
+            if wl.bias else None
+        wb_down = _draw(gw, (d, f), wl.w_std, dt, dev)
+        bb_down = (_draw(gw, (d,), wl.bias_std, dt, dev) if wl.bias_std > 0 else torch.zeros(d, dtype=dt, device=dev)) \
+            if wl.bias else None
+        out.update(wb_gate=wb_gate, wb_up=wb_up, wb_down=wb_down, bb_up=bb_up, bb_down=bb_down)
+    else:
+        out.update(wb_gate=None, wb_up=None, wb_down=None, bb_up=None, bb_down=None)
     return out

@@ -71,7 +71,7 @@ def run_layer(wl, inp):
 
 def oracle(wl, inp, tokens=None):
     return O.moe_layer(inp, E=wl.E, k=wl.k, act=wl.act, n_shared=wl.n_shared, cf=wl.cf, lb_coef=wl.lb_coef,
-                       z_coef=wl.z_coef, tokens=tokens)
+                       z_coef=wl.z_coef, tokens=tokens, temperature=wl.temperature)
 
 
 def check_output(got: np.ndarray, ref: np.ndarray, dtype: str, what: str):

@@ -47,6 +47,11 @@ CASES = {
     # enough rows per expert for the paired (2-SM) projections, with non-zero biases and drops
     "bf16_gelu_bias_pair": Workload("bf16_gelu_bias_pair", T=2100, d=256, E=4, k=2, dff=512, act="gelu",
                                     dtype="bf16", bias=True, bias_std=0.02, cf=1.05, seed=22, wseed=22),
+    # router temperature (a routing variant): softmax, weights and losses of z / tau
+    "bf16_swiglu_temp2": Workload("bf16_swiglu_temp2", T=700, d=512, E=16, k=4, dff=256, act="swiglu",
+                                  dtype="bf16", n_shared=2, cf=1.25, seed=24, wseed=24, temperature=2.0),
+    "fp32_gelu_temp_half": Workload("fp32_gelu_temp_half", T=150, d=64, E=8, k=2, dff=128, act="gelu",
+                                    dtype="f32", bias=True, seed=25, wseed=25, temperature=0.5),
 }
 
 
@@ -323,3 +328,106 @@ def test_full_skewed_bf16():
 def test_full_skewed_cf1_bf16():
     got, ref = _full("skewed_cf1_bf16", 1024, seed=1)
     assert ref["drops"] > 0
+
+
+# ------------------------------------------------------------------------------ routing diagnostics
+def _check_diagnostics(wl, inp_gpu, inp_cpu=None):
+    inp_cpu = inp_gpu if inp_cpu is None else inp_cpu
+    T = inp_gpu["x"].shape[0]
+    cfg = moe.config_from_workload(wl, T)
+    ws = moe.alloc_workspace(cfg)
+    diag = torch.full((4,), -1.0, dtype=torch.float32, device="cuda")
+    ent = torch.full((max(T, 1),), -1.0, dtype=torch.float32, device="cuda")
+    moe.moe_route_diagnostics(cfg, inp_gpu["x"], inp_gpu["w_router"], inp_gpu.get("logit_bias"), diag, ent, ws)
+    assert moe.moe_read_device_status(ws) == moe.MOE_OK
+    z = O.temper(O.router_logits(inp_cpu["x"], inp_cpu["w_router"], inp_cpu.get("logit_bias")), wl.temperature)
+    P, lse = O.softmax_lse(z)
+    h_tok = lse - np.sum(P * z, axis=1) if T else np.zeros(0)
+    got = diag.cpu().numpy().astype(np.float64)
+    if T == 0:
+        assert np.all(got == 0)
+        return
+    idx = O.topk_select(z, wl.k)
+    counts = np.bincount(idx.ravel(), minlength=wl.E)
+    ref = [float(np.mean(h_tok)), O.lb_loss_squared_mean_form(P, wl.lb_coef),
+           O.lb_loss_kl_frequency_form(P, counts, wl.lb_coef), O.aux_losses(P, lse, counts, wl.k, wl.lb_coef, 0.0)[0]]
+    np.testing.assert_allclose(ent[:T].cpu().numpy(), h_tok, rtol=1e-4, atol=2e-5)
+    # near-tie tokens (oracle gap < 1e-5) may fall on either side of the top-k boundary: each moves
+    # one count, 1 / (T k) of f
+    n_exempt = int((O.topk_gap(z, wl.k) < 1e-5).sum())
+    np.testing.assert_allclose(got[:2], ref[:2], rtol=1e-4, atol=1e-7)
+    tol = 1e-4 + 4.0 * n_exempt / (T * wl.k)
+    np.testing.assert_allclose(got[2:], ref[2:], rtol=tol, atol=1e-7)
+    print(f"  diagnostics {wl.name}: {got.tolist()} vs {ref}; near ties {n_exempt}")
+
+
+@pytest.mark.parametrize("case", ["bf16_swiglu_shared", "bf16_E256_k8", "fp32_E256_k8", "bf16_collapse_cap",
+                                  "bf16_swiglu_temp2", "fp32_gelu_temp_half", "bf16_one_token", "tiny_fp32"])
+def test_route_diagnostics_match_oracle(case):
+    """Router entropy (per token and mean) and the three balance-loss forms, against the oracle's
+    router_entropy, lb_loss_squared_mean_form, lb_loss_kl_frequency_form and aux_losses."""
+    wl = CASES[case]
+    inp_cpu = make_inputs(wl, "cpu")
+    _check_diagnostics(wl, _to(inp_cpu, "cuda"), inp_cpu)
+
+
+def test_route_diagnostics_empty_batch():
+    wl = CASES["bf16_swiglu_shared"].replace(T=0)
+    _check_diagnostics(wl, _to(make_inputs(wl, "cpu"), "cuda"))
+
+
+def test_route_diagnostics_full_finegrained():
+    wl = WORKLOADS["finegrained_bf16"]
+    _check_diagnostics(wl, make_inputs(wl, "cuda"))
+
+
+# ------------------------------------------------------------------------------ backup expert
+BACKUP_CASES = {
+    "bf16_swiglu_backup": Workload("bf16_swiglu_backup", T=700, d=512, E=16, k=4, dff=256, act="swiglu",
+                                   dtype="bf16", n_shared=2, cf=0.6, seed=26, wseed=26, backup=True),
+    "bf16_gelu_bias_backup": Workload("bf16_gelu_bias_backup", T=1000, d=256, E=8, k=2, dff=512, act="gelu",
+                                      dtype="bf16", bias=True, bias_std=0.02, cf=0.7, seed=27, wseed=27,
+                                      backup=True),
+    "bf16_collapse_backup": Workload("bf16_collapse_backup", T=300, d=128, E=8, k=2, dff=128, act="swiglu",
+                                     dtype="bf16", cf=1.0, logit_bias0=50.0, seed=28, wseed=28, backup=True),
+    "fp32_gelu_backup": Workload("fp32_gelu_backup", T=333, d=96, E=6, k=3, dff=160, act="gelu", dtype="f32",
+                                 bias=True, bias_std=0.02, cf=0.5, seed=29, wseed=29, backup=True),
+    "bf16_decode_backup": Workload("bf16_decode_backup", T=32, d=256, E=8, k=2, dff=256, act="swiglu",
+                                   dtype="bf16", n_shared=1, cf=0.5, seed=30, wseed=30, backup=True),
+}
+
+
+@pytest.mark.parametrize("case", list(BACKUP_CASES))
+def test_backup_expert_matches_oracle(case):
+    """Assignments over capacity go, with their routing weight, to one extra expert: the dispatch
+    places them after the kept rows in (token, slot) order, the projections run the backup expert on
+    them in the same launches, and the combine adds them -- against the oracle's
+    moe_layer_backup_expert on the same tensors."""
+    wl = BACKUP_CASES[case]
+    inp_cpu = make_inputs(wl, "cpu")
+    inp_gpu = _to(inp_cpu, "cuda")
+    backup = {n: inp_cpu[m] for n, m in (("w_up", "wb_up"), ("w_gate", "wb_gate"), ("w_down", "wb_down"),
+                                         ("b_up", "bb_up"), ("b_down", "bb_down"))}
+    ref = O.moe_layer_backup_expert(inp_cpu, backup, E=wl.E, k=wl.k, act=wl.act, n_shared=wl.n_shared, cf=wl.cf,
+                                    lb_coef=wl.lb_coef, z_coef=wl.z_coef)
+    assert ref["backup_rows"] > 0 and (ref["gap"] >= 1e-5).all()
+    got = run_steps(wl, inp_gpu)
+    assert got["status"] == moe.MOE_OK, moe.moe_status_string(got["status"])
+    T, k, E = wl.T, wl.k, wl.E
+    A = int(ref["offsets"][E])
+    assert np.array_equal(got["offsets"].cpu().numpy(), ref["offsets"])
+    # kept rows as without the backup; the dropped slots, in (token, slot) order, at A, A + 1, ...
+    row_of = got["row_of"].cpu().numpy()
+    exp_rows = ref["row_of"].copy()
+    dropped = exp_rows < 0
+    exp_rows[dropped] = A + np.arange(int(dropped.sum()))
+    assert np.array_equal(row_of, exp_rows)
+    tok_of = got["tok_of"].cpu().numpy()
+    assert np.array_equal(tok_of[A:T * k], np.nonzero(dropped)[0])
+    assert torch.equal(got["x_perm"][:T * k], inp_gpu["x"][got["tok_of"][:T * k].long()])
+    check_losses(got["losses"], ref["lb"], ref["zl"])
+    check_output(to_np(got["y"]), ref["y"], wl.dtype, "y")
+    lay = run_layer(wl, inp_gpu)
+    assert lay["status"] == moe.MOE_OK
+    assert torch.equal(lay["y"], got["y"])
+    assert int(lay["drops"].item()) == ref["drops"]
