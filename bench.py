@@ -33,15 +33,16 @@ DEFAULT_WORKLOAD = "skewed_bf16"
 SUB_WORKLOADS = ("tiny_fp32", "flash_bf16", "finegrained_bf16", "decode_bf16", "skewed_bf16", "skewed_cf1_bf16")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM bytes per launch of the routed up-projection kernel, from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload; valid only while the kernel
-# source hash matches the one the capture was taken with.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the up-projection
+# kernel, from ncu captures (profiles/k_proj_tc_skewed_e16_bf16.md), keyed by workload; valid only
+# while gemm_tc.cu and common.cuh hash to src_sha1.  skewed_e16_bf16 is measured; skewed_bf16 is
+# too large to capture under a full metric set, so its figure is the stand-in's traffic per
+# algorithmic byte (1.0142) times the full launch's algorithmic bytes (weights of 128 experts,
+# token rows in, hidden rows out).
 NCU_TRAFFIC = {
-    # dram__bytes_read.sum + dram__bytes_write.sum of the routed up-projection, one ncu --set full
-    # capture per workload; valid while gemm_tc.cu and common.cuh hash to src_sha1
-    "flash_bf16": {"bytes": 168053504 + 101091840, "src_sha1": "169092f3a46a9d3545c9d3efe75e3b74e4d79992"},
-    "finegrained_bf16": {"bytes": 940263936 + 191008512, "src_sha1": "169092f3a46a9d3545c9d3efe75e3b74e4d79992"},
-    "decode_bf16": {"bytes": 512903680 + 3441152, "src_sha1": "169092f3a46a9d3545c9d3efe75e3b74e4d79992"},
+    "skewed_e16_bf16": {"bytes": 1668925000 + 49719040, "src_sha1": "108ba47307cbefe169e5494a6dcd1ee851add9e3"},
+    "skewed_bf16": {"bytes": 13749152320, "src_sha1": "108ba47307cbefe169e5494a6dcd1ee851add9e3",
+                    "scaled_from": "skewed_e16_bf16"},
 }
 
 
@@ -302,14 +303,18 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     clocks = clk.summary()
-    # the burst peak for a kernel in a short step; the sustained (power-capped) one once the timed
-    # region ran under the power cap
-    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    stage_clk = clk_stages.summary()
+    # the burst peak for a kernel in a short step; the sustained (power-capped) one when the region
+    # the stage times come from ran under the power cap with the SM clock held below its maximum
+    smax = stage_clk.get("sm_max_mhz") or 0
+    capped = ("sw_power_cap" in (stage_clk.get("reasons") or []) and smax > 0
+              and (stage_clk.get("sm_mhz") or smax) < 0.95 * smax)
     peak, peak_name = (peak_sus, "bf16_tflops_sustained") if capped else (peak_burst, "bf16_tflops")
-    traffic = None
+    traffic, traffic_note = None, None
     rec = NCU_TRAFFIC.get(wl.name)
     if rec and rec.get("src_sha1") == kernel_src_sha1():
         traffic = rec["bytes"]
+        traffic_note = ("scaled from the ncu capture of " + rec["scaled_from"]) if rec.get("scaled_from") else "ncu capture"
     touched = int((counts > 0).sum().item())
     m_up = 2 if wl.act == "swiglu" else 1
     expert_ms = stage_ms["up"] + stage_ms["down"] + stage_ms["shared"]
@@ -321,7 +326,7 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
                     "achieved": round(up_tflops, 2), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(up_tflops / peak, 4), "frac_of_burst_peak": round(up_tflops / peak_burst, 4),
                     "frac_of_sustained_peak": round(up_tflops / peak_sus, 4),
-                    "peak_source": f"{peak_src} {peak_name}", "traffic": traffic,
+                    "peak_source": f"{peak_src} {peak_name}", "traffic": traffic, "traffic_source": traffic_note,
                     "algorithmic_flops_per_launch": up_all}
         up_bytes = ((touched + wl.n_shared) * m_up * wl.d * wl.dff * elt
                     + (kept_rows + (T if wl.n_shared else 0)) * wl.d * elt
@@ -331,7 +336,7 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
             up_gbs = up_bytes / (stage_ms["up"] * 1e-3) / 1e9
             roofline = {"bound": "hbm", "kernel": "k_proj_tc up-projection (weight streaming)",
                         "achieved": round(up_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(up_gbs / hbm, 4),
-                        "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic,
+                        "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic, "traffic_source": traffic_note,
                         "algorithmic_bytes_per_launch": up_bytes,
                         "units": f"{touched} routed + {wl.n_shared} shared experts' up weights, token rows read, "
                                  "hidden rows written"}
@@ -358,7 +363,7 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
                           "frac_of_hbm": round(layer_gbs / hbm, 4)},
         "l2": arm_config(wl, ws_n)["l2"],
         "clocks": clocks,
-        "stage_clocks": {k: v for k, v in clk_stages.summary().items() if k in ("sm_mhz", "reasons", "samples")},
+        "stage_clocks": {k: v for k, v in stage_clk.items() if k in ("sm_mhz", "reasons", "samples")},
     }
     if full:
         res["eager"] = {"value": round(T * ws_n / (ms_eager * 1e-3), 1), "ms_per_step": round(ms_eager, 5),
@@ -489,7 +494,7 @@ def run_ours(args, wl, ws_n, rank, local):
     }
     for key in ("expert_tflops", "expert_frac_of_burst_peak", "expert_frac_of_sustained_peak", "stage_ms",
                 "kept_rows", "drops", "roofline", "weight_stream", "route_stats", "e2e", "gpu_launches", "clocks",
-                "cpu_baseline"):
+                "stage_clocks", "cpu_baseline"):
         if key in head:
             res[key] = head[key]
     if ws_n == 1 and not args.no_per_config:

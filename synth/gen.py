@@ -78,6 +78,10 @@ WORKLOADS: Dict[str, Workload] = {
     "skewed_cf1_bf16": Workload("skewed_cf1_bf16", T=16384, d=4096, E=128, k=2, dff=6144,
                                 act="swiglu", dtype="bf16", cf=1.0, seed=4, wseed=4,
                                 logit_bias0=2.0),
+    # Profiling stand-in for the skewed layer (kernel counters on a few GB of device memory): the
+    # same expert shape and about the same rows per expert (~256), 16 experts instead of 128.
+    "skewed_e16_bf16": Workload("skewed_e16_bf16", T=2048, d=4096, E=16, k=2, dff=6144, act="swiglu",
+                                dtype="bf16", seed=5, wseed=5, logit_bias0=2.0),
 }
 
 
