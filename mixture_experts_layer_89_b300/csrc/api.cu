@@ -18,7 +18,7 @@ using namespace moe;
 namespace {
 
 struct WsLayout {
-  size_t status, r_hist, r_psum, r_lse2, p_hist, p_base, drops, b_count, b_offs;
+  size_t status, r_hist, r_psum, r_lse2, r_z, p_hist, p_base, drops, b_count, b_offs;
   size_t topk_idx, topk_w, counts, offsets, kept, row_of, tok_of;
   size_t x_perm, h, y_perm, h_sh, y_sh;
   size_t total;
@@ -96,6 +96,9 @@ WsLayout layout(const moe_config* c) {
   L.r_hist = take(nrb * E * 4);
   L.r_psum = take(nrb * E * 4);
   L.r_lse2 = take(nrb * 4);
+  // per-token probabilities and lse^2 of the small-batch router (part of the router's scratch,
+  // before the dispatch's buffers)
+  L.r_z = take(is_bf16(c) && T <= (size_t)kSmallRouteTokens ? T * (E + 1) * 4 : 0);
   L.p_hist = take(npb * E * 4);
   L.p_base = take(npb * E * 4);
   L.drops = take(4);
@@ -150,6 +153,13 @@ moe_status route_impl(const moe_config* c, const void* x, const void* wr, const 
                       const RouteScan* scan = nullptr, bool finalize = true) {
   const WsLayout L = layout(c);
   uint32_t* status = at<uint32_t>(ws, L.status);
+  if (is_bf16(c) && c->T > 0 && c->T <= kSmallRouteTokens && !scan) {  // decode-sized batches
+    float* ptok = at<float>(ws, L.r_z);
+    return cuda_status(launch_route_small(x, wr, lbias, c->T, c->d, c->E, c->k, inv_tau_of(c), ptok,
+                                          ptok + (size_t)c->T * c->E, status + 1, topk_idx, topk_w,
+                                          at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
+                                          finalize, counts, losses, c->lb_coef, c->z_coef, status, st));
+  }
   if (is_bf16(c)) {  // tensor-core router; the last CTA reduces the partials (counter: status block word 1)
     return cuda_status(launch_route_tc(x, wr, lbias, c->T, c->d, c->E, c->k, topk_idx, topk_w,
                                        at<int32_t>(ws, L.r_hist), at<float>(ws, L.r_psum), at<float>(ws, L.r_lse2),
@@ -579,7 +589,7 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   if (validate(cfg) != MOE_OK) return -1;
   int n = 0;
   const bool tokens = cfg->T > 0;
-  if (is_bf16(cfg)) n += tokens ? 1 : 0;      // tensor-core router (finalize fused; T = 0: memsets only)
+  if (is_bf16(cfg)) n += tokens ? 1 : 0;      // tensor-core or small-batch router (finalize fused; T = 0: memsets)
   else n += tokens ? 2 : 1;                   // router + finalize
   const bool dfused = is_bf16(cfg) && dispatch_fuses_scan(cfg->T, cfg->E);
   const bool scanned = dfused || (is_bf16(cfg) && route_tc_fuses_scan(cfg->T, cfg->E));

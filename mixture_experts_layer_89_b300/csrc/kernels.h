@@ -35,6 +35,15 @@ cudaError_t launch_route_tc(const void* x, const void* wr, const float* lbias, i
                             int32_t* topk_idx, float* topk_w, int32_t* hist, float* psum, float* lse2, uint32_t* done,
                             int32_t* counts, float* losses, float lb_coef, float z_coef, uint32_t* status,
                             cudaStream_t st, const RouteScan* scan, bool finalize = true, float inv_tau = 1.f);
+// Router of bf16 layers for T <= kSmallRouteTokens (route_small.cu): one CTA per token
+// (compensated fp32 logits, top-k, weights, softmax), per-token probabilities ptok [T][E] and
+// lse^2 l2tok [T] in the workspace; the last CTA (counter *done, zero between calls) writes the
+// router's partials of one block (hist, psum [E], lse2 [1]) and, with finalize, counts and losses.
+constexpr int kSmallRouteTokens = 64;
+cudaError_t launch_route_small(const void* x, const void* wr, const float* lbias, int T, int d, int E, int k,
+                               float inv_tau, float* ptok, float* l2tok, uint32_t* done, int32_t* topk_idx,
+                               float* topk_w, int32_t* hist, float* psum, float* lse2, bool finalize, int32_t* counts,
+                               float* losses, float lb_coef, float z_coef, uint32_t* status, cudaStream_t st);
 // Reduces the per-CTA partials: counts [E] and losses [2].
 cudaError_t launch_route_finalize(const int32_t* hist, const float* psum, const float* lse2, int nb, int T, int E,
                                   int k, float lb_coef, float z_coef, int32_t* counts, float* losses,

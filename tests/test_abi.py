@@ -120,7 +120,7 @@ def test_launch_count(L, name):
     # launch; fp32: routed up + down, then shared up + down
     ffn = 2 if wl.dtype == "bf16" else 2 + (2 if wl.n_shared else 0)
     assert n == router + dispatch + ffn + 1
-    assert moe.moe_layer_forward_launches(moe.config_from_workload(wl, T=0)) == router - 1 + 1
+    assert moe.moe_layer_forward_launches(moe.config_from_workload(wl, T=0)) == (1 if wl.dtype == "bf16" else 2)
 
 
 def test_wait_limit_setter_rejects_bad_workspace_on_host(L):
