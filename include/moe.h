@@ -160,12 +160,11 @@ moe_status moe_combine(const moe_config* cfg, const void* y_perm, const int32_t*
  *   x [T,d] -> y [T,d]; losses [2]; counts_out [E] (nullable); drops_out [1] (nullable,
  *   number of dropped assignments).  Intermediates live in ws.
  * Ordering: everything is ordered after the work already queued on `stream`, and the work queued
- * on `stream` afterwards is ordered after the whole layer.  Internally, bf16 layers whose shared
- * experts are small run those on a second stream (per host thread and device, created on first
- * use outside stream capture) forked from and joined back to `stream` with events; the kernels
- * use programmatic dependent launch, so a kernel's set-up may overlap the previous kernel on
- * `stream` (each waits for it before touching memory).  Both are captured faithfully by CUDA
- * graph capture of `stream`.  Calls that share a workspace must not overlap on the GPU. */
+ * on `stream` afterwards is ordered after the whole layer.  Every kernel runs on `stream` (the
+ * shared and backup experts ride in the routed experts' GEMM launches); the kernels use
+ * programmatic dependent launch, so a kernel's set-up may overlap the previous kernel on `stream`
+ * (each waits for it before touching memory), which CUDA graph capture of `stream` keeps.
+ * Calls that share a workspace must not overlap on the GPU. */
 moe_status moe_layer_forward(const moe_config* cfg, const moe_weights* w, const void* x,
                              void* y, float* losses, int32_t* counts_out, int32_t* drops_out,
                              void* ws, void* stream);

@@ -399,6 +399,53 @@ def dequantize_rows_e4m3(codes, scale) -> np.ndarray:
     return e4m3_table()[codes.astype(np.int64)] * np.asarray(scale, np.float64)[..., None]
 
 
+# ----------------------------------------------------------------------------- INT8 expert weights
+# The mini-moe tutorial's deployment advice (model compression: quantise every expert to INT8 to
+# cut what must be stored and loaded).  The pages give no scheme; the reading used is symmetric
+# per-output-row scaling: scale_r = max_c |W_rc| / 127 (1 for an all-zero row) and
+# q_rc = the integer nearest to W_rc / scale_r (ties to even), in [-127, 127].
+
+def quantize_rows_int8(W) -> Dict[str, np.ndarray]:
+    """Per-row symmetric INT8 codes of W [rows, cols].  The scale and the quotient are IEEE
+    float32 divisions of the float32 values of W (exact for bf16 or fp32 weights), so a float32
+    implementation takes the same rounding decisions; the quotient is rounded to the nearest
+    integer, ties to even.  Returns codes (int8), scale (float32 [rows]) and the dequantised
+    matrix codes * scale in float64."""
+    W32 = np.asarray(W, np.float64).astype(np.float32)
+    rows = W32.shape[0]
+    amax = np.abs(W32).max(axis=1) if W32.shape[1] else np.zeros(rows, np.float32)
+    scale = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+    q = (W32 / scale[:, None]).astype(np.float32)
+    codes = np.clip(np.rint(q), -127, 127).astype(np.int8)
+    return dict(codes=codes, scale=scale, dequantized=dequantize_rows_int8(codes, scale))
+
+
+def dequantize_rows_int8(codes, scale) -> np.ndarray:
+    """codes[..., r, c] * scale[..., r] in float64 (exact)."""
+    return np.asarray(codes, np.float64) * np.asarray(scale, np.float64)[..., None]
+
+
+def quantize_experts(W, fmt: str, joint_blocks: bool = False) -> Dict[str, np.ndarray]:
+    """Quantise a stack of expert matrices W [B, rows, cols] (fmt "int8" or "e4m3", float32
+    division).  joint_blocks=False: every row of every block gets its own scale (scale [B, rows]).
+    joint_blocks=True: row r of all B blocks together is one row of the [rows, B cols] matrix the
+    blocks form side by side (the shared experts' down projections, which act as one wide expert),
+    with one scale per r (scale [rows]).  Returns codes [B, rows, cols], scale and dequantized
+    [B, rows, cols]."""
+    W = np.asarray(W, np.float64)
+    B, R, C = W.shape
+    flat = np.concatenate(list(W), axis=1) if joint_blocks else W.reshape(B * R, C)
+    q = quantize_rows_int8(flat) if fmt == "int8" else quantize_rows_e4m3(flat, "f32")
+    if fmt not in ("int8", "e4m3"):
+        raise ValueError(fmt)
+    if joint_blocks:
+        codes = np.stack([q["codes"][:, b * C:(b + 1) * C] for b in range(B)])
+        deq = np.stack([q["dequantized"][:, b * C:(b + 1) * C] for b in range(B)])
+        return dict(codes=codes, scale=q["scale"], dequantized=deq)
+    return dict(codes=q["codes"].reshape(B, R, C), scale=q["scale"].reshape(B, R),
+                dequantized=q["dequantized"].reshape(B, R, C))
+
+
 # ----------------------------------------------------------------------------- whole layer
 def moe_layer(inp: Dict, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
               lb_coef: float = 0.01, z_coef: float = 0.001,

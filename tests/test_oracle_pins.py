@@ -5,6 +5,7 @@ one planted mistake: ``test_planted_mistakes_are_caught`` shows that a dropped t
 index, a transposed operand or a wrong rounding rule fails a pin.
 """
 import json
+from fractions import Fraction
 import math
 import os
 
@@ -436,6 +437,54 @@ def check_fp8(o):
         o.quantize_rows_e4m3(Wb, "f16")
 
 
+def check_int8(o):
+    """INT8 per-row codes against brute force on exact rationals: the code is the integer of
+    [-127, 127] nearest to the IEEE float32 quotient (torch's float32 division), ties to even;
+    the row maximum maps to +-127; dequantised values lie within half a step of W."""
+    rng = np.random.default_rng(21)
+    W = torch.tensor(rng.standard_normal((12, 40)) * 0.02, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    W[5] = 0.0
+    W[7, 3] = -np.abs(W[7]).max() * 1.5          # the row maximum on a negative entry
+    q = o.quantize_rows_int8(W)
+    assert q["codes"].dtype == np.int8 and q["scale"].dtype == np.float32
+    W32 = torch.tensor(W, dtype=torch.float32)
+    amax = W32.abs().amax(dim=1)
+    scale = torch.where(amax > 0, amax / torch.tensor(127.0), torch.tensor(1.0))
+    assert np.array_equal(scale.numpy(), q["scale"])
+    quot = (W32 / scale[:, None]).numpy()
+    for r in range(W.shape[0]):
+        for c in range(W.shape[1]):
+            x = Fraction(float(quot[r, c]))
+            best = min(range(-127, 128), key=lambda n: (abs(x - n), n % 2))
+            assert int(q["codes"][r, c]) == best, (r, c, float(x), best)
+    assert q["scale"][5] == 1.0 and (q["codes"][5] == 0).all()
+    for r in range(W.shape[0]):
+        if r != 5:
+            assert np.abs(q["codes"][r].astype(int)).max() == 127
+    assert q["codes"][7, 3] == -127
+    step = q["scale"].astype(np.float64)[:, None]
+    assert (np.abs(q["dequantized"] - W) <= step / 2 * (1 + 1e-6)).all()
+    # exact halves round to the even integer: rows scaled so that W / s = n + 1/2 exactly
+    s = np.float32(2.0 ** -7)
+    Wt = np.array([[127 * s, 0.5 * s, 1.5 * s, 2.5 * s, -2.5 * s, -0.5 * s, 126.5 * s]], np.float64)
+    qt = o.quantize_rows_int8(Wt)
+    assert qt["scale"][0] == s
+    assert qt["codes"][0].tolist() == [127, 0, 2, 2, -2, 0, 126]
+    # stacks of experts: separate rows, or one scale per row over blocks placed side by side
+    Ws = rng.standard_normal((3, 4, 8)) * 0.02
+    Ws[1, 2, 5] = 0.5
+    sep = o.quantize_experts(Ws, "int8")
+    assert sep["scale"].shape == (3, 4) and np.isclose(sep["scale"][1, 2], np.float32(0.5) / np.float32(127))
+    joint = o.quantize_experts(Ws, "int8", joint_blocks=True)
+    assert joint["scale"].shape == (4,) and joint["codes"].shape == (3, 4, 8)
+    for r in range(4):
+        assert joint["scale"][r] == np.float32(np.float32(np.abs(Ws[:, r, :]).max()) / np.float32(127))
+    assert joint["codes"][1, 2, 5] == 127 and np.abs(joint["codes"][0, 2].astype(int)).max() < 127
+    np.testing.assert_array_equal(joint["dequantized"][2], o.dequantize_rows_int8(joint["codes"][2], joint["scale"]))
+    e = o.quantize_experts(Ws, "e4m3", joint_blocks=True)
+    assert e["scale"][2] == np.float32(np.float32(0.5) / np.float32(448))
+
+
 def check_backup_expert(o):
     """A backup expert identical to every routed expert makes drops invisible (the dropless layer);
     a zero backup expert gives the dropping layer; drops are counted."""
@@ -498,7 +547,8 @@ def check_temperature(o):
 
 ALL_CHECKS = [check_router, check_softmax, check_topk, check_renormalise, check_capacity,
               check_dispatch, check_activations, check_expert_ffn, check_layer_reductions, check_combine_fixture,
-              check_losses, check_coactivation, check_backward, check_fp8, check_temperature, check_backup_expert]
+              check_losses, check_coactivation, check_backward, check_fp8, check_int8, check_temperature,
+              check_backup_expert]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -611,6 +661,33 @@ def _mut_e4m3_ties_away(v):
     return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
 
 
+def _mut_int8_ties_away(W):
+    W32 = np.asarray(W, np.float64).astype(np.float32)
+    amax = np.abs(W32).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+    q = (W32 / scale[:, None]).astype(np.float64)
+    codes = np.clip(np.sign(q) * np.floor(np.abs(q) + 0.5), -127, 127).astype(np.int8)
+    return dict(codes=codes, scale=scale, dequantized=codes * scale.astype(np.float64)[:, None])
+
+
+def _mut_int8_scale_128(W):
+    W32 = np.asarray(W, np.float64).astype(np.float32)
+    amax = np.abs(W32).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(128.0), np.float32(1.0)).astype(np.float32)
+    codes = np.clip(np.rint(W32 / scale[:, None]), -127, 127).astype(np.int8)
+    return dict(codes=codes, scale=scale, dequantized=codes * scale.astype(np.float64)[:, None])
+
+
+_REAL_QUANT_EXPERTS = O.quantize_experts
+
+
+def _mut_quant_experts_no_joint(W, fmt, joint_blocks=False):
+    r = _REAL_QUANT_EXPERTS(W, fmt, False)
+    if joint_blocks:
+        r = dict(r, scale=r["scale"][0])
+    return r
+
+
 def _mut_coact_upper_only(idx, E):
     C = np.zeros((E, E), dtype=np.int64)
     for row in np.asarray(idx):
@@ -637,6 +714,9 @@ def _mut_coact_upper_only(idx, E):
     ("coactivation", _mut_coact_upper_only, check_coactivation),
     ("e4m3_value", _mut_e4m3_bias8, check_fp8),
     ("e4m3_encode_array", _mut_e4m3_ties_away, check_fp8),
+    ("quantize_rows_int8", _mut_int8_ties_away, check_int8),
+    ("quantize_rows_int8", _mut_int8_scale_128, check_int8),
+    ("quantize_experts", _mut_quant_experts_no_joint, check_int8),
 ])
 def test_planted_mistakes_are_caught(name, fn, check, monkeypatch):
     """Plant one mistake in the oracle module itself (so its internal callers see it too)."""
