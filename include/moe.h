@@ -59,6 +59,18 @@ typedef enum {
   MOE_ACT_SWIGLU = 1     /* W_down (silu(W_gate x) * W_up x)      (GPT-4 2% article, sec. 3.1)  */
 } moe_act;
 
+/* Storage of the expert FFN weights (routed, shared and backup experts; the router keeps the
+ * layer dtype).  The mini-moe tutorial (deployment optimisation) suggests quantising every expert
+ * to INT8 to cut what is stored and loaded; the 8-bit formats hold one code per weight and one
+ * fp32 scale per output row (see moe_quantize_experts), need a bf16 layer, and multiply the codes
+ * by the bf16 activations on the tensor cores (codes widened to bf16 exactly in shared memory)
+ * with the scale applied to the fp32 accumulator. */
+typedef enum {
+  MOE_EXPERT_WEIGHTS_DTYPE = 0,  /* the layer dtype                                              */
+  MOE_EXPERT_WEIGHTS_INT8 = 1,   /* int8 codes q, weight = q * scale_row, |q| <= 127              */
+  MOE_EXPERT_WEIGHTS_E4M3 = 2    /* OCP FP8 E4M3 codes, weight = value(code) * scale_row          */
+} moe_expert_weights;
+
 typedef struct {
   int32_t T;               /* tokens                                                        */
   int32_t d;               /* model width                                                   */
@@ -78,6 +90,8 @@ typedef struct {
   int32_t backup_expert;   /* 1: assignments over the capacity go, with their routing weight, to
                               one extra expert (weights wb_* / bb_*) instead of being dropped
                               (mini-moe tutorial, sec. 6); A_max becomes T*k.  0: dropped      */
+  int32_t expert_weights;  /* moe_expert_weights; 8-bit formats need dtype == MOE_BF16, else
+                              MOE_ERR_UNSUPPORTED                                              */
 } moe_config;
 
 typedef struct {
@@ -96,6 +110,18 @@ typedef struct {
   const void* wb_down;            /* backup expert [d,dff] or NULL                           */
   const void* bb_up;              /* backup expert bias [dff] (has_bias) or NULL             */
   const void* bb_down;            /* backup expert bias [d] (has_bias) or NULL               */
+  /* 8-bit expert weights only (else ignored): the tensors above hold codes (same shapes, one
+   * byte each; biases stay bf16) and these hold the fp32 scale of every output row.          */
+  const float* s_up;              /* [E,dff]                                                */
+  const float* s_gate;            /* [E,dff] (SwiGLU)                                       */
+  const float* s_down;            /* [E,d]                                                  */
+  const float* ss_up;             /* [S,dff]                                                */
+  const float* ss_gate;           /* [S,dff] (SwiGLU)                                       */
+  const float* ss_down;           /* [d]: one scale per row of the [d, S*dff] matrix that the
+                                     shared experts' down projections form side by side    */
+  const float* sb_up;             /* [dff] backup expert                                    */
+  const float* sb_gate;           /* [dff] backup expert (SwiGLU)                           */
+  const float* sb_down;           /* [d]   backup expert                                    */
 } moe_weights;
 
 /* Workspace bytes needed by every call below for this config (host only, no GPU work).
@@ -254,6 +280,22 @@ moe_status moe_route_stats(const moe_config* cfg, const int32_t* topk_idx, const
 moe_status moe_route_diagnostics(const moe_config* cfg, const void* x, const void* w_router,
                                  const float* logit_bias, float* diag, float* entropy_tok, void* ws,
                                  void* stream);
+
+/* 8-bit expert weights (mini-moe tutorial, deployment optimisation: quantise each expert).
+ *   w [blocks, rows, cols] of dtype (moe_dtype) -> codes [blocks, rows, cols] (one byte each),
+ *   scale [rows] fp32, where logical row r is row r of every block placed side by side:
+ *     scale_r = max |w[:, r, :]| / qmax  (an IEEE fp32 division; 1 for an all-zero row),
+ *     codes   = the code nearest to w / scale_r (an IEEE fp32 division), ties to even;
+ *   format MOE_EXPERT_WEIGHTS_INT8: qmax 127, int8 codes in [-127, 127];
+ *   format MOE_EXPERT_WEIGHTS_E4M3: qmax 448, E4M3 codes (saturating at +-448).
+ *   For per-row scales of an expert stack [E, rows, cols] pass blocks = 1, rows = E * rows; for
+ *   the shared experts' down projections [S, d, dff] (one wide matrix) pass blocks = S, rows = d.
+ *   nonfinite: NULL, or a device int32 the call adds the number of non-finite weights to (their
+ *   codes are meaningless).  Deterministic; blocks * rows * cols < 2^40, cols <= 2^20.
+ *   MOE_ERR_INVALID_ARG for bad sizes or pointers, MOE_ERR_UNSUPPORTED for another format. */
+moe_status moe_quantize_experts(const void* w, int32_t dtype, int32_t format, int32_t blocks,
+                                int32_t rows, int32_t cols, void* codes, float* scale,
+                                int32_t* nonfinite, void* stream);
 
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);

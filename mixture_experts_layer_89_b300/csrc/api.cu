@@ -71,6 +71,9 @@ moe_status validate(const moe_config* c) {
   if (c->E > 256 || c->k > 8 || c->k > c->E || c->n_shared > 64) return MOE_ERR_UNSUPPORTED;
   if (c->has_bias && c->act != MOE_ACT_GELU_ERF) return MOE_ERR_UNSUPPORTED;
   if (c->backup_expert != 0 && c->backup_expert != 1) return MOE_ERR_INVALID_ARG;
+  if (c->expert_weights < MOE_EXPERT_WEIGHTS_DTYPE || c->expert_weights > MOE_EXPERT_WEIGHTS_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  if (c->expert_weights != MOE_EXPERT_WEIGHTS_DTYPE && !is_bf16(c)) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->n_shared * c->dff > INT_MAX / 2) return MOE_ERR_UNSUPPORTED;
   if (is_bf16(c)) {
@@ -236,10 +239,11 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     p.N = c->dff; p.K = c->d; p.N_w = c->dff; p.K_w = c->d; p.G_w = c->E;
     p.act = swiglu ? ACT_SWIGLU : ACT_GELU;
     p.out = h; p.ldc = c->dff; p.max_group_rows = routed_rows;
+    p.scale0 = swiglu ? w->s_gate : w->s_up; p.scale1 = w->s_up;
     Projection& q = dn[nup - 1];
     q.A = h; q.lda = c->dff; q.rows_alloc = A;
     q.offsets = offsets; q.G = c->E; q.rows_static = 0;
-    q.B0 = w->w_down; q.B1 = nullptr;
+    q.B0 = w->w_down; q.B1 = nullptr; q.scale0 = w->s_down;
     q.bias = c->has_bias ? w->b_down : nullptr;
     q.N = c->d; q.K = c->dff; q.N_w = c->d; q.K_w = c->dff; q.G_w = c->E;
     q.act = ACT_NONE;
@@ -254,10 +258,12 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     p.N = S * c->dff; p.K = c->d; p.N_w = c->dff; p.K_w = c->d; p.G_w = S;
     p.act = swiglu ? ACT_SWIGLU : ACT_GELU;
     p.out = hs; p.ldc = (int64_t)S * c->dff; p.max_group_rows = c->T;
+    p.scale0 = swiglu ? w->ss_gate : w->ss_up; p.scale1 = w->ss_up;
     Projection& q = dn[nup - 1];
     q.A = hs; q.lda = (int64_t)S * c->dff; q.rows_alloc = c->T;
     q.offsets = nullptr; q.G = 1; q.rows_static = c->T;
     q.B0 = w->ws_down; q.B1 = nullptr; q.bias = nullptr;
+    q.scale0 = w->ss_down;  // one scale per row of the S down matrices side by side
     q.N = c->d; q.K = S * c->dff; q.N_w = c->d; q.K_w = c->dff; q.G_w = S;
     q.act = ACT_NONE;
     q.out = y_shared; q.ldc = c->d; q.out_f32 = true; q.max_group_rows = c->T;
@@ -274,15 +280,17 @@ moe_status ffn_impl(const moe_config* c, const void* x_perm, const int32_t* offs
     p.N = c->dff; p.K = c->d; p.N_w = c->dff; p.K_w = c->d; p.G_w = 1;
     p.act = swiglu ? ACT_SWIGLU : ACT_GELU;
     p.out = h; p.ldc = c->dff; p.max_group_rows = A;
+    p.scale0 = swiglu ? w->sb_gate : w->sb_up; p.scale1 = w->sb_up;
     Projection& q = dn[nup - 1];
     q.A = h; q.lda = c->dff; q.rows_alloc = A;
     q.offsets = boffs; q.G = 1; q.rows_static = 0;
-    q.B0 = w->wb_down; q.B1 = nullptr;
+    q.B0 = w->wb_down; q.B1 = nullptr; q.scale0 = w->sb_down;
     q.bias = c->has_bias ? w->bb_down : nullptr;
     q.N = c->d; q.K = c->dff; q.N_w = c->d; q.K_w = c->dff; q.G_w = 1;
     q.act = ACT_NONE;
     q.out = y_perm; q.ldc = c->d; q.out_f32 = true; q.max_group_rows = A;
   }
+  for (int i = 0; i < nup; ++i) up[i].wfmt = dn[i].wfmt = c->expert_weights;
   if (is_bf16(c)) {
     if (nup) MOE_CUDA(launch_projection_tc(up, nup, status, st));
     if (ev_up) MOE_CUDA(cudaEventRecord(ev_up, st));
@@ -319,6 +327,12 @@ moe_status check_weights(const moe_config* c, const moe_weights* w) {
   // bf16 SwiGLU experts read their gate and up rows through one tensor map spanning both tensors
   if (is_bf16(c) && c->act == MOE_ACT_SWIGLU && (w->w_gate == w->w_up || (c->n_shared > 0 && w->ws_gate == w->ws_up)))
     return MOE_ERR_UNSUPPORTED;
+  if (c->expert_weights != MOE_EXPERT_WEIGHTS_DTYPE) {  // row scales of every 8-bit matrix
+    const bool sw = c->act == MOE_ACT_SWIGLU;
+    if (!w->s_up || !w->s_down || (sw && !w->s_gate)) return MOE_ERR_INVALID_ARG;
+    if (c->n_shared > 0 && (!w->ss_up || !w->ss_down || (sw && !w->ss_gate))) return MOE_ERR_INVALID_ARG;
+    if (c->backup_expert && (!w->sb_up || !w->sb_down || (sw && !w->sb_gate))) return MOE_ERR_INVALID_ARG;
+  }
   const void* ps[] = {w->w_router, w->w_up, w->w_gate, w->w_down, w->b_up, w->b_down, w->ws_up, w->ws_gate, w->ws_down,
                       w->wb_up, w->wb_gate, w->wb_down, w->bb_up, w->bb_down};
   for (const void* p : ps)
@@ -601,6 +615,22 @@ int32_t moe_layer_forward_launches(const moe_config* cfg) {
   else n += (routed ? 2 : 0) + (shared ? 2 : 0) + (routed && cfg->backup_expert ? 2 : 0);  // routed, shared, backup
   if (tokens) n += 1;                         // combine
   return n;
+}
+
+moe_status moe_quantize_experts(const void* w, int32_t dtype, int32_t format, int32_t blocks, int32_t rows,
+                                int32_t cols, void* codes, float* scale, int32_t* nonfinite, void* stream) {
+  NvtxRange nvtx_range("moe_quantize_experts");
+  if (dtype != MOE_F32 && dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (format != MOE_EXPERT_WEIGHTS_INT8 && format != MOE_EXPERT_WEIGHTS_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (blocks < 0 || rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)blocks * rows * cols >= (int64_t)1 << 40 || cols > (1 << 20)) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)blocks * rows * cols == 0) return MOE_OK;
+  if (!w || !codes || !scale) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scale) & 3u) || (reinterpret_cast<uintptr_t>(nonfinite) & 3u) ||
+      (reinterpret_cast<uintptr_t>(w) & (dtype == MOE_BF16 ? 1u : 3u)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize(dtype == MOE_BF16, format, w, blocks, rows, cols, static_cast<uint8_t*>(codes),
+                                     scale, nonfinite, static_cast<cudaStream_t>(stream)));
 }
 
 const char* moe_last_error(void) { return tc_last_error(); }

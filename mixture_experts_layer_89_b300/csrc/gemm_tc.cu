@@ -72,7 +72,14 @@ constexpr uint16_t PAIR_MASK = 0x3;
 
 constexpr int SMEM_LIMIT = 232448;              // opt-in shared memory per CTA
 
+// 8-bit expert weights (W8): the weight box of a K step arrives as one byte per weight in a ring
+// of its own, and CONVW converter warps widen it to bf16 into the stage's swizzled operand tile
+constexpr int CONVW = 4;
+constexpr int RAW_BYTES = AR * BK;              // 8 KB: one CTA's 8-bit weight tile of a K step
+constexpr int MAX_RAW = 24;
+
 template <int ACT> constexpr int epi_warps() { return ACT == ACT_GELU ? 16 : 4; }  // the erf epilogue is ALU-bound
+template <int ACT, bool W8> constexpr int n_threads() { return 128 + 32 * (epi_warps<ACT>() + (W8 ? CONVW : 0)); }
 template <int ACT> constexpr bool out_f32() { return ACT == ACT_NONE; }           // projections to the model width
 template <int ACT> constexpr int feat_per_tile() { return ACT == ACT_SWIGLU ? AR : 2 * AR; }  // output features per pair tile
 // token rows per tile: NTV (256, or 32 for decode-sized calls)
@@ -85,12 +92,22 @@ template <int ACT, int NTV> constexpr int stage_bytes() { return a_bytes<ACT, NT
 template <int ACT> constexpr int stg_bytes() { return ACT == ACT_NONE ? 4096 : 2048; }
 template <int ACT> constexpr int stg_bufs() { return ACT == ACT_SWIGLU ? 0 : (epi_warps<ACT>() > 8 ? 1 : 2); }
 constexpr int CTL_BYTES = 2048;  // >= sizeof(SmemCtl), checked below
-template <int ACT, int NTV> constexpr int n_stages() {
-  return (SMEM_LIMIT - 1024 - CTL_BYTES - epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>()) /
-                     stage_bytes<ACT, NTV>() < MAX_STAGES
-             ? (SMEM_LIMIT - 1024 - CTL_BYTES - epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>()) /
-                   stage_bytes<ACT, NTV>()
-             : MAX_STAGES;
+template <int ACT> constexpr int stg_total() { return epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>(); }
+// bf16 operand stages: as many as fit (at most MAX_STAGES); with 8-bit weights a few, the bytes in
+// flight from HBM being the raw ring's
+template <int ACT, int NTV, bool W8 = false> constexpr int n_stages() {
+  return W8 ? (NTV <= 32 ? 4 : 3)
+             : ((SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>()) / stage_bytes<ACT, NTV>() < MAX_STAGES
+                    ? (SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>()) / stage_bytes<ACT, NTV>()
+                    : MAX_STAGES);
+}
+template <int ACT, int NTV, bool W8> constexpr int raw_stages() {
+  return !W8 ? 0
+             : ((SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>() - n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>()) /
+                        RAW_BYTES < MAX_RAW
+                    ? (SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>() - n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>()) /
+                          RAW_BYTES
+                    : MAX_RAW);
 }
 
 struct ProbArgs {
@@ -101,10 +118,13 @@ struct ProbArgs {
   void* out;
   int64_t ldc;
   int gate_first;          // SwiGLU: the gate rows come first in each 32-row group (else the up rows)
+  const float* scale0;     // 8-bit weights: fp32 scale of each row of B0 (SwiGLU: the gate) and of
+  const float* scale1;     // B1 (SwiGLU: the up rows), indexed like the bias
 };
 struct TcArgs {
   ProbArgs p[MAXP];
   int nprob;
+  int wfmt;                // 8-bit weights: 1 int8, 2 E4M3 (0 otherwise)
   uint32_t* status;
 };
 // Tensor maps of each problem: weights (SwiGLU: gate and up together), token rows in boxes of
@@ -116,6 +136,8 @@ struct TcMaps {
 struct SmemCtl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
+  uint64_t raw_full[MAX_RAW];   // 8-bit weight ring: loaded / widened
+  uint64_t raw_empty[MAX_RAW];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -126,14 +148,21 @@ struct SmemCtl {
   int u_pre[MAXGT + 1]; // prefix over groups of their tiles
 };
 static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block");
-template <int ACT, int NTV>
+template <int ACT, int NTV, bool W8 = false>
 constexpr size_t smem_total() {
-  return 1024 + (size_t)n_stages<ACT, NTV>() * stage_bytes<ACT, NTV>() +
-         (size_t)epi_warps<ACT>() * stg_bufs<ACT>() * stg_bytes<ACT>() + CTL_BYTES;
+  return 1024 + (size_t)n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>() +
+         (size_t)raw_stages<ACT, NTV, W8>() * RAW_BYTES + (size_t)stg_total<ACT>() + CTL_BYTES;
 }
 static_assert(smem_total<ACT_NONE, 256>() <= SMEM_LIMIT && smem_total<ACT_GELU, 256>() <= SMEM_LIMIT &&
                   smem_total<ACT_SWIGLU, 256>() <= SMEM_LIMIT && smem_total<ACT_SWIGLU, 32>() <= SMEM_LIMIT,
               "shared memory per CTA");
+static_assert(smem_total<ACT_NONE, 256, true>() <= SMEM_LIMIT && smem_total<ACT_GELU, 256, true>() <= SMEM_LIMIT &&
+                  smem_total<ACT_SWIGLU, 256, true>() <= SMEM_LIMIT && smem_total<ACT_SWIGLU, 32, true>() <= SMEM_LIMIT &&
+                  smem_total<ACT_NONE, 32, true>() <= SMEM_LIMIT && smem_total<ACT_GELU, 32, true>() <= SMEM_LIMIT,
+              "shared memory per CTA (8-bit weights)");
+static_assert(raw_stages<ACT_SWIGLU, 32, true>() >= 16 && raw_stages<ACT_NONE, 32, true>() >= 12 &&
+                  raw_stages<ACT_NONE, 256, true>() >= 8 && raw_stages<ACT_GELU, 256, true>() >= 8,
+              "8-bit weight bytes in flight");
 static_assert(n_stages<ACT_NONE, 256>() == 6 && n_stages<ACT_SWIGLU, 256>() == 7 && n_stages<ACT_NONE, 32>() >= 10,
               "stage counts");
 
@@ -196,6 +225,65 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
+// ------------------------------------------------------------- 8-bit weights widened to bf16
+// int8: q + 128 (the byte with its top bit flipped) placed in the low mantissa byte of 2^23 gives
+// the float 2^23 + q + 128 exactly; subtracting 2^23 + 128 leaves q, which bf16 holds exactly.
+__device__ __forceinline__ void int8x4_to_bf16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  const float2 a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
+                              make_float2(-8388736.f, -8388736.f));
+  const float2 b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                                          __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
+                              make_float2(-8388736.f, -8388736.f));
+  lo = pack_bf16x2(a.x, a.y);
+  hi = pack_bf16x2(b.x, b.y);
+}
+// E4M3: the hardware conversion to f16 is exact (every E4M3 value is a normal f16 or zero); moving
+// the f16 exponent and mantissa fields down by 3 bits (the sign stays) gives the bf16 whose value
+// is the f16's times 2^-112 (the two formats' exponent biases differ by 112), and one bf16x2
+// multiply by 2^112 restores it -- exactly, zero included.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)pair));
+  const uint32_t t = ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x77807780u));  // 0x7780 = 2^112
+  return r;
+}
+// One CTA's 8-bit weight tile (AR rows of BK bytes, row-major) -> the bf16 operand tile (AR rows
+// of 128 bytes, 16-byte chunk j of row i at chunk j ^ (i % 8), the layout TMA's 128-byte swizzle
+// writes).  Thread ct of the CONVW converter warps widens 16 weights per step; a warp's loads cover
+// 512 contiguous bytes and its stores hit every bank once per quarter warp.
+__device__ __forceinline__ void widen_tile(uint32_t raw, uint32_t dst, int ct, int fmt) {
+#pragma unroll
+  for (int it = 0; it < AR * (BK / 16) / (CONVW * 32); ++it) {
+    const int item = it * CONVW * 32 + ct;
+    const int row = item >> 2, piece = item & 3;
+    const uint4 v = ld_shared_v4(raw + row * BK + piece * 16);
+    uint32_t o[8];
+    if (fmt == 1) {
+      int8x4_to_bf16(v.x, o[0], o[1]);
+      int8x4_to_bf16(v.y, o[2], o[3]);
+      int8x4_to_bf16(v.z, o[4], o[5]);
+      int8x4_to_bf16(v.w, o[6], o[7]);
+    } else {
+      o[0] = e4m3x2_to_bf16x2(v.x & 0xFFFFu);
+      o[1] = e4m3x2_to_bf16x2(v.x >> 16);
+      o[2] = e4m3x2_to_bf16x2(v.y & 0xFFFFu);
+      o[3] = e4m3x2_to_bf16x2(v.y >> 16);
+      o[4] = e4m3x2_to_bf16x2(v.z & 0xFFFFu);
+      o[5] = e4m3x2_to_bf16x2(v.z >> 16);
+      o[6] = e4m3x2_to_bf16x2(v.w & 0xFFFFu);
+      o[7] = e4m3x2_to_bf16x2(v.w >> 16);
+    }
+    const uint32_t base = dst + row * 128;
+    const uint32_t sw = (uint32_t)(row & 7);
+    st_shared_v4(base + (((uint32_t)(2 * piece) ^ sw) << 4), o[0], o[1], o[2], o[3]);
+    st_shared_v4(base + (((uint32_t)(2 * piece + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+  }
+}
+
 struct Tile {
   int p, g;        // problem, group (expert) within it
   int m0, m_end;   // first token row of the tile, end of the group's rows
@@ -204,8 +292,8 @@ struct Tile {
   int kblocks;
 };
 
-template <int ACT, int NTV>
-__global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
+template <int ACT, int NTV, bool W8>
+__global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
     k_proj_tc(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs args) {
   constexpr int EPIW = epi_warps<ACT>();
   constexpr int NBUF = stg_bufs<ACT>() > 0 ? stg_bufs<ACT>() : 1;  // (SwiGLU stages nothing)
@@ -214,10 +302,12 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
   constexpr int FT = feat_per_tile<ACT>();
   constexpr int A_BYTES = a_bytes<ACT, NTV>();
   constexpr int STAGE_BYTES = stage_bytes<ACT, NTV>();
-  constexpr int STAGES = n_stages<ACT, NTV>();
+  constexpr int STAGES = n_stages<ACT, NTV, W8>();
+  constexpr int RAWST = raw_stages<ACT, NTV, W8>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stg_base = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned (the swizzle atoms)
+  uint8_t* raw_base = smem + (size_t)STAGES * STAGE_BYTES;   // 8-bit weight ring (W8)
+  uint8_t* stg_base = raw_base + (size_t)RAWST * RAW_BYTES;  // 1024-byte aligned (the swizzle atoms)
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * stg_bufs<ACT>() * STG);
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -229,8 +319,14 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
+      // W8: every converter warp of the pair arrives once the stage's weights are widened (the
+      // leader's first one also arms the token rows' bytes)
+      mbar_init(smem_u32(&ctl->full[s]), W8 ? 2 * CONVW : 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int r = 0; r < RAWST; ++r) {
+      mbar_init(smem_u32(&ctl->raw_full[r]), 1);
+      mbar_init(smem_u32(&ctl->raw_empty[r]), CONVW);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&ctl->tfull[a]), 1);
@@ -329,7 +425,47 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
     return t;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && W8) {
+    // 8-bit weights: this CTA's weight box of each K step into the raw ring (its own barrier)
+    if (lane == 0) {
+      int r = 0;
+      uint32_t rph = 0, armed = 0, armed_ph = 0;
+      bool aborted = false;
+      for (int u = unit0; u < total_units && !aborted; u += ustep) {
+        const Tile t = decode(u);
+        const ProbArgs& P = args.p[t.p];
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->raw_empty[r]), rph ^ 1u, abort_flag, args.status)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->raw_full[r]);
+          mbar_arrive_expect_tx(fb, RAW_BYTES);
+          armed |= 1u << r;
+          armed_ph = (armed_ph & ~(1u << r)) | (rph << r);
+          const int k0 = kb * BK;
+          const int kk = k0 % P.K_w;
+          const int kq = k0 / P.K_w;
+          const uint32_t dst = smem_u32(raw_base + (size_t)r * RAW_BYTES);
+          if (ACT == ACT_SWIGLU) {
+            const int f = t.n0 + (AR / 2) * crank;
+            tma_load_5d(dst, &maps.w0[t.p], fb, kk, 0, 0, (f % P.N_w) / 16, t.g + f / P.N_w + kq);
+          } else {
+            const int f = t.n0 + AR * crank;
+            tma_load_3d(dst, &maps.w0[t.p], fb, kk, f % P.N_w, t.g + f / P.N_w + kq);
+          }
+          if (++r == RAWST) {
+            r = 0;
+            rph ^= 1u;
+          }
+        }
+      }
+      if (aborted) {  // this CTA's own copies land before it leaves
+        for (int i = 0; i < RAWST; ++i)
+          if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->raw_full[i]), (armed_ph >> i) & 1u);
+      }
+    }
+  } else if (warp == 0) {
     if (lane == 0) {
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
@@ -396,7 +532,7 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
         const uint32_t idesc = umma_idesc_bf16(2 * AR, t.nmma);
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
+          if (!mbar_wait_bounded<W8>(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
             aborted = true;
             break;
           }
@@ -419,7 +555,73 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
       umma_commit_cg2_mc(smem_u32(&ctl->mma_done), PAIR_MASK);
       drain_wait(smem_u32(&ctl->mma_done), 0);
     }
-  } else if (warp >= 4) {
+  } else if (W8 && warp >= 4 + EPIW) {
+    // converter warps (8-bit weights): per K step, wait for the bf16 stage to be free, load this
+    // CTA's token rows into it, widen the raw weight box into its operand tile, then arrive on the
+    // leader's stage barrier (the leader's first warp also arms the two CTAs' token-row bytes)
+    const int cw = warp - 4 - EPIW;
+    const int ct = cw * 32 + lane;
+    int s = 0, r = 0;
+    uint32_t ph = 0, rph = 0, armed = 0, armed_ph = 0;
+    bool aborted = false;
+    for (int u = unit0; u < total_units && !aborted; u += ustep) {
+      const Tile t = decode(u);
+      const int half = t.nmma >> 1;
+      const int brow = t.m0 + crank * half;
+      const bool small_box = NT / 2 > 32 && half <= 32;
+      const uint32_t b_tx = 2u * (uint32_t)((small_box ? 32 : NT / 2) * BK * 2);  // both CTAs' token rows
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) {
+          aborted = true;
+          break;
+        }
+        uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
+        const uint32_t fb = smem_u32(&ctl->full[s]);
+        const uint32_t lb = mapa_rank(fb, 0);
+        if (ct == 0) {
+          if (small_box)
+            tma_load_2d_cg2(smem_u32(sa + A_BYTES), &maps.x32[t.p], lb, kb * BK, brow);
+          else
+            tma_load_2d_cg2(smem_u32(sa + A_BYTES), &maps.x[t.p], lb, kb * BK, brow);
+        }
+        if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->raw_full[r]), rph, abort_flag, args.status) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) widen_tile(smem_u32(raw_base + (size_t)r * RAW_BYTES), smem_u32(sa), ct, args.wfmt);
+        fence_proxy_async_smem();  // the widened tile is read by the tensor cores (async proxy)
+        __syncwarp();
+        if (lane == 0) {
+          // arrive even after a failed wait, so that the stage's token-row copies can be drained
+          mbar_arrive(smem_u32(&ctl->raw_empty[r]));
+          if (leader && cw == 0) {
+            mbar_arrive_expect_tx(fb, b_tx);
+            armed |= 1u << s;
+            armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          } else {
+            mbar_arrive_cluster(lb);
+          }
+        }
+        if (!ok) {
+          aborted = true;
+          break;
+        }
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (++r == RAWST) {
+          r = 0;
+          rph ^= 1u;
+        }
+      }
+    }
+    if (aborted && leader && ct == 0) {  // let the armed token-row copies (of both CTAs) land
+      for (int i = 0; i < STAGES; ++i)
+        if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
+    }
+  } else if (warp >= 4 && warp < 4 + EPIW) {
     const int q = warp & 3;                  // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
     const int grp = (warp - 4) >> 2;         // this warp's share of the token columns
     constexpr int NGRP = EPIW / 4;
@@ -445,6 +647,11 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
         const int f = fl + (lane & 15);
         const bool upper = lane >= 16;
         const bool gate_lo = P.gate_first != 0;  // lanes 0-15 hold the gate accumulators
+        // `mine` below belongs to this lane's matrix, `got` to the other one
+        const bool mine_is_gate = upper != gate_lo;
+        float sc = 1.f;  // 8-bit weights: the scale of this lane's weight row
+        if (W8 && f < P.N)
+          sc = __ldg((mine_is_gate ? P.scale0 : P.scale1) + (size_t)(t.g + f / P.N_w) * P.N_w + f % P.N_w);
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(P.out);
 #pragma unroll 1
         for (int cb = grp; cb * 32 < t.ntok; cb += NGRP) {
@@ -456,12 +663,11 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
           const int tbase = upper ? 16 : 0;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float lo_v = __uint_as_float(v[i]), hi_v = __uint_as_float(v[16 + i]);
+            const float lo_v = W8 ? __uint_as_float(v[i]) * sc : __uint_as_float(v[i]);
+            const float hi_v = W8 ? __uint_as_float(v[16 + i]) * sc : __uint_as_float(v[16 + i]);
             // lane < 16 keeps token i and receives the partner's value of it; lane >= 16 keeps 16 + i
             const float got = __shfl_xor_sync(0xffffffffu, upper ? lo_v : hi_v, 16);
             const float mine = upper ? hi_v : lo_v;
-            // `mine` belongs to this lane's matrix, `got` to the other one
-            const bool mine_is_gate = upper != gate_lo;
             const float gate = mine_is_gate ? mine : got;
             const float up = mine_is_gate ? got : mine;
             if (f < P.N && tbase + i < nval)
@@ -471,11 +677,12 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
       } else {
         const int fl = t.n0 + AR * crank + 32 * q;  // first feature of this warp
         const int f = fl + lane;
-        float b = 0.f;
+        float b = 0.f, sc = 1.f;  // bias; 8-bit weights: the scale of this thread's weight row
         if (P.bias && f < P.N) {
           const int gw = t.g + f / P.N_w;
           b = __bfloat162float(P.bias[(size_t)gw * P.N_w + f % P.N_w]);
         }
+        if (W8 && f < P.N) sc = __ldg(P.scale0 + (size_t)(t.g + f / P.N_w) * P.N_w + f % P.N_w);
 #pragma unroll 1
         for (int cb = grp; cb * 32 < t.ntok; cb += NGRP) {
           float h[32];
@@ -484,7 +691,7 @@ __global__ void __launch_bounds__(128 + 32 * epi_warps<ACT>(), 1)
             tmem_ld32(tb + cb * 32, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) h[i] = __uint_as_float(v[i]) + b;
+            for (int i = 0; i < 32; ++i) h[i] = W8 ? fmaf(__uint_as_float(v[i]), sc, b) : __uint_as_float(v[i]) + b;
           }
           if (ACT == ACT_GELU) {
 #pragma unroll
@@ -663,18 +870,23 @@ int max_pair_clusters(K kernel, int threads, size_t smem) {
   return n;
 }
 
-template <int ACT, int NTV>
+template <int ACT, int NTV, bool W8>
 cudaError_t launch_t(const Projection* ps, int nprob, uint32_t* status, cudaStream_t st) {
   constexpr int NT = tile_tokens<ACT, NTV>();
   constexpr int FT = feat_per_tile<ACT>();
-  constexpr int threads = 128 + 32 * epi_warps<ACT>();
-  constexpr size_t smem = smem_total<ACT, NTV>();
-  auto kern = k_proj_tc<ACT, NTV>;
+  constexpr int threads = n_threads<ACT, W8>();
+  constexpr size_t smem = smem_total<ACT, NTV, W8>();
+  // weights: bf16 through the 128-byte swizzle, or 8-bit codes as plain 64-byte rows
+  constexpr int wel = W8 ? 1 : 2;
+  const CUtensorMapDataType wdt = W8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle wsw = W8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  auto kern = k_proj_tc<ACT, NTV, W8>;
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
   TcArgs a;
   memset(&a, 0, sizeof(a));
   a.status = status;
+  a.wfmt = W8 ? ps[0].wfmt : 0;
   long units_bound = 0;
   int np = 0;
   for (int i = 0; i < nprob; ++i) {
@@ -702,15 +914,19 @@ cudaError_t launch_t(const Projection* ps, int nprob, uint32_t* status, cudaStre
       }
       gate_first = g < u ? 1 : 0;
       const cuuint64_t dims[5] = {(cuuint64_t)p.K_w, 16, 2, (cuuint64_t)(p.N_w / 16), (cuuint64_t)p.G_w};
-      const cuuint64_t str[4] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)(gate_first ? u - g : g - u),
-                                 (cuuint64_t)p.K_w * 2 * 16, (cuuint64_t)p.N_w * p.K_w * 2};
+      const cuuint64_t str[4] = {(cuuint64_t)p.K_w * wel, (cuuint64_t)(gate_first ? u - g : g - u),
+                                 (cuuint64_t)p.K_w * wel * 16, (cuuint64_t)p.N_w * p.K_w * wel};
       const cuuint32_t box[5] = {BK, 16, 2, 4, 1};
-      if (!make_tmap_bf16(&maps.w0[np], gate_first ? g : u, 5, dims, str, box)) return cudaErrorInvalidValue;
+      if (!make_tmap(&maps.w0[np], wdt, gate_first ? g : u, 5, dims, str, box, wsw)) return cudaErrorInvalidValue;
     } else {
       const cuuint64_t dims[3] = {(cuuint64_t)p.K_w, (cuuint64_t)p.N_w, (cuuint64_t)p.G_w};
-      const cuuint64_t str[2] = {(cuuint64_t)p.K_w * 2, (cuuint64_t)p.N_w * p.K_w * 2};
+      const cuuint64_t str[2] = {(cuuint64_t)p.K_w * wel, (cuuint64_t)p.N_w * p.K_w * wel};
       const cuuint32_t box[3] = {BK, AR, 1};
-      if (!make_tmap_bf16(&maps.w0[np], p.B0, 3, dims, str, box)) return cudaErrorInvalidValue;
+      if (!make_tmap(&maps.w0[np], wdt, p.B0, 3, dims, str, box, wsw)) return cudaErrorInvalidValue;
+    }
+    if (W8 && (p.wfmt != a.wfmt || !p.scale0 || (ACT == ACT_SWIGLU && !p.scale1))) {
+      snprintf(g_err, sizeof(g_err), "8-bit weights need one format and row scales for every matrix");
+      return cudaErrorInvalidValue;
     }
     {  // output blocks of the epilogue's TMA stores: 32 tokens x 32 features
       const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)rows_alloc};
@@ -732,6 +948,8 @@ cudaError_t launch_t(const Projection* ps, int nprob, uint32_t* status, cudaStre
     q.out = p.out;
     q.ldc = p.ldc;
     q.gate_first = gate_first;
+    q.scale0 = W8 ? p.scale0 : nullptr;
+    q.scale1 = W8 ? p.scale1 : nullptr;
     const long groups = p.offsets ? p.G : 1;
     // each group adds at most one partial token tile
     units_bound += ((rows_alloc + NT - 1) / NT + (p.offsets ? groups : 0)) * (long)((p.N + FT - 1) / FT);
@@ -772,7 +990,9 @@ cudaError_t launch_a(const Projection* ps, int nprob, uint32_t* status, cudaStre
   // every group at most 32 token rows (decode-sized calls): 32-token tiles, more stages in flight
   bool small = true;
   for (int i = 0; i < nprob; ++i) small = small && ps[i].max_group_rows <= 32;
-  return small ? launch_t<ACT, 32>(ps, nprob, status, st) : launch_t<ACT, 256>(ps, nprob, status, st);
+  if (ps[0].wfmt != 0)
+    return small ? launch_t<ACT, 32, true>(ps, nprob, status, st) : launch_t<ACT, 256, true>(ps, nprob, status, st);
+  return small ? launch_t<ACT, 32, false>(ps, nprob, status, st) : launch_t<ACT, 256, false>(ps, nprob, status, st);
 }
 }  // namespace
 
@@ -782,7 +1002,8 @@ cudaError_t launch_projection_tc(const Projection* ps, int nprob, uint32_t* stat
   if (nprob < 1 || nprob > MAXP) return cudaErrorInvalidValue;
   const int act = ps[0].act;
   for (int i = 1; i < nprob; ++i)
-    if (ps[i].act != act || ps[i].out_f32 != ps[0].out_f32) return cudaErrorInvalidValue;
+    if (ps[i].act != act || ps[i].out_f32 != ps[0].out_f32 || ps[i].wfmt != ps[0].wfmt) return cudaErrorInvalidValue;
+  if (ps[0].wfmt < 0 || ps[0].wfmt > 2) return cudaErrorInvalidValue;
   // hidden layers are bf16 (the next projection's MMA operand); projections to the model width
   // keep the fp32 accumulator so the layer output is rounded once
   switch (act) {

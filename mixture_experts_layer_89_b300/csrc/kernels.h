@@ -117,7 +117,12 @@ struct Projection {
   void* out; int64_t ldc;
   bool out_f32;                                    // out is fp32 (else the layer dtype)
   int max_group_rows;                              // bound on the rows of any one group (host-known)
+  int wfmt;                                        // weights: 0 layer dtype, 1 int8, 2 E4M3 codes
+  const float* scale0; const float* scale1;        // 8-bit weights: fp32 row scales of B0, B1
 };
+// Per-row scaled 8-bit codes of w [blocks][rows][cols] (fmt 1 int8, 2 E4M3), one CTA per row.
+cudaError_t launch_quantize(bool bf16, int fmt, const void* w, int blocks, int rows, int cols, uint8_t* codes,
+                            float* scale, int32_t* nonfinite, cudaStream_t st);
 cudaError_t launch_projection_simt(bool bf16, const Projection& p, cudaStream_t st);
 // bf16 layers: nprob (1 or 2) projections with the same activation in one launch of the paired
 // tensor-core kernel (the routed and the shared experts share its persistent CTAs).

@@ -26,14 +26,18 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [("T", _c_i32), ("d", _c_i32), ("E", _c_i32), ("k", _c_i32), ("dff", _c_i32),
                 ("n_shared", _c_i32), ("act", _c_i32), ("dtype", _c_i32), ("has_bias", _c_i32),
                 ("capacity_factor", ctypes.c_float), ("lb_coef", ctypes.c_float), ("z_coef", ctypes.c_float),
-                ("router_temperature", ctypes.c_float), ("backup_expert", _c_i32)]
+                ("router_temperature", ctypes.c_float), ("backup_expert", _c_i32), ("expert_weights", _c_i32)]
 
 
 class MoeWeights(ctypes.Structure):
     _fields_ = [("w_router", _c_p), ("router_logit_bias", _c_p), ("w_up", _c_p), ("w_gate", _c_p),
                 ("w_down", _c_p), ("b_up", _c_p), ("b_down", _c_p), ("ws_up", _c_p), ("ws_gate", _c_p),
                 ("ws_down", _c_p), ("wb_up", _c_p), ("wb_gate", _c_p), ("wb_down", _c_p), ("bb_up", _c_p),
-                ("bb_down", _c_p)]
+                ("bb_down", _c_p), ("s_up", _c_p), ("s_gate", _c_p), ("s_down", _c_p), ("ss_up", _c_p),
+                ("ss_gate", _c_p), ("ss_down", _c_p), ("sb_up", _c_p), ("sb_gate", _c_p), ("sb_down", _c_p)]
+
+# expert weight storage (moe_expert_weights)
+EXPERT_WEIGHTS = {"dtype": 0, "int8": 1, "e4m3": 2}
 
 
 class MoeError(RuntimeError):
@@ -74,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.moe_set_wait_limit.argtypes = [_c_p, ctypes.c_uint64, _c_p]
         L.moe_route_diagnostics.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_route_stats.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_quantize_experts.argtypes = [_c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_last_error.argtypes = []
@@ -81,7 +86,7 @@ def lib() -> ctypes.CDLL:
         for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute",
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
-                     "moe_set_wait_limit", "moe_route_diagnostics"):
+                     "moe_set_wait_limit", "moe_route_diagnostics", "moe_quantize_experts"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -90,7 +95,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
             "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_route_diagnostics",
-            "moe_status_string", "moe_last_error")
+            "moe_quantize_experts", "moe_status_string", "moe_last_error")
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -122,23 +127,25 @@ def _check(status: int, where: str):
 def make_config(T: int, d: int, E: int, k: int, dff: int, act: str = "gelu", dtype: str = "bf16",
                 n_shared: int = 0, has_bias: bool = False, capacity_factor: float = 0.0,
                 lb_coef: float = 0.01, z_coef: float = 0.001, temperature: float = 1.0,
-                backup_expert: bool = False) -> MoeConfig:
+                backup_expert: bool = False, expert_weights: str = "dtype") -> MoeConfig:
     return MoeConfig(T, d, E, k, dff, n_shared, MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_GELU_ERF,
                      MOE_BF16 if dtype == "bf16" else MOE_F32, int(bool(has_bias)), float(capacity_factor),
-                     float(lb_coef), float(z_coef), float(temperature), int(bool(backup_expert)))
+                     float(lb_coef), float(z_coef), float(temperature), int(bool(backup_expert)),
+                     EXPERT_WEIGHTS[expert_weights])
 
 
 def config_from_workload(wl, T: Optional[int] = None) -> MoeConfig:
     return make_config(wl.T if T is None else T, wl.d, wl.E, wl.k, wl.dff, wl.act, wl.dtype, wl.n_shared,
                        wl.bias, wl.cf, wl.lb_coef, wl.z_coef, getattr(wl, "temperature", 1.0),
-                       getattr(wl, "backup", False))
+                       getattr(wl, "backup", False), getattr(wl, "weights8", "dtype"))
 
 
 def make_weights(t: Dict[str, Optional[torch.Tensor]]) -> MoeWeights:
     """MoeWeights over the tensors of ``t`` (keys as produced by ``synth.make_inputs``)."""
     w = MoeWeights(*[_p(t.get(n)) for n in ("w_router", "logit_bias", "w_up", "w_gate", "w_down", "b_up", "b_down",
                                             "ws_up", "ws_gate", "ws_down", "wb_up", "wb_gate", "wb_down", "bb_up",
-                                            "bb_down")])
+                                            "bb_down", "s_up", "s_gate", "s_down", "ss_up", "ss_gate", "ss_down",
+                                            "sb_up", "sb_gate", "sb_down")])
     w._keep = t  # keep the tensors alive as long as the struct
     return w
 
@@ -226,7 +233,42 @@ def moe_layer_forward_launches(cfg) -> int:
     return int(lib().moe_layer_forward_launches(ctypes.byref(cfg)))
 
 
+def moe_quantize_experts(w, fmt: str, blocks: int, rows: int, cols: int, codes, scale, nonfinite=None,
+                         stream=None):
+    """Per-row scaled 8-bit codes of ``w`` [blocks, rows, cols] (``fmt`` "int8" or "e4m3")."""
+    dtype = MOE_BF16 if w.dtype == torch.bfloat16 else MOE_F32
+    _check(lib().moe_quantize_experts(_p(w), dtype, EXPERT_WEIGHTS[fmt], int(blocks), int(rows), int(cols),
+                                      _p(codes), _p(scale), _p(nonfinite), _s(stream)), "moe_quantize_experts")
+
+
 # ----------------------------------------------------------------------------- convenience
+_QUANT_KEYS = (("w_up", "s_up", False), ("w_gate", "s_gate", False), ("w_down", "s_down", False),
+               ("ws_up", "ss_up", False), ("ws_gate", "ss_gate", False), ("ws_down", "ss_down", True),
+               ("wb_up", "sb_up", False), ("wb_gate", "sb_gate", False), ("wb_down", "sb_down", False))
+
+
+def quantize_expert_tensors(t: Dict[str, Optional[torch.Tensor]], fmt: str, stream=None):
+    """A copy of the layer tensors ``t`` whose expert matrices are replaced by 8-bit codes (int8 or
+    uint8 E4M3 tensors of the same shapes) with their row scales under the s_* / ss_* / sb_* keys,
+    quantised on the GPU by moe_quantize_experts (the shared experts' down matrices share one scale
+    per row).  Raises if a weight is not finite."""
+    out = dict(t)
+    bad = torch.zeros(1, dtype=torch.int32, device=next(v for v in t.values() if v is not None).device)
+    for wk, sk, joint in _QUANT_KEYS:
+        w = t.get(wk)
+        if w is None:
+            continue
+        w3 = w.reshape(1, *w.shape) if w.dim() == 2 else w
+        B, R, C = w3.shape
+        codes = torch.empty(w3.shape, dtype=torch.int8 if fmt == "int8" else torch.uint8, device=w.device)
+        blocks, rows = (B, R) if joint else (1, B * R)
+        scale = torch.empty(rows, dtype=torch.float32, device=w.device)
+        moe_quantize_experts(w3, fmt, blocks, rows, C, codes, scale, bad, stream)
+        out[wk] = codes.reshape(w.shape)
+        out[sk] = scale if joint else scale.reshape(w.shape[:-1])
+    if int(bad.item()):
+        raise ValueError(f"{int(bad.item())} non-finite expert weights")
+    return out
 def alloc_workspace(cfg: MoeConfig, device="cuda") -> torch.Tensor:
     """Zero-filled workspace (the status word must start at zero)."""
     return torch.zeros(max(moe_workspace_size(cfg), 256), dtype=torch.uint8, device=device)

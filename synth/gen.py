@@ -50,6 +50,8 @@ class Workload:
     bias_std: float = 0.0
     temperature: float = 1.0 # router temperature (a routing variant; 1 = none)
     backup: bool = False     # one backup expert takes the assignments over capacity (a routing variant)
+    weights8: str = "dtype"  # expert weights stored as "int8" or "e4m3" codes with row scales (quantised
+                             # from the drawn weights by the library), or in the layer dtype
 
     def replace(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -78,6 +80,9 @@ WORKLOADS: Dict[str, Workload] = {
     "skewed_cf1_bf16": Workload("skewed_cf1_bf16", T=16384, d=4096, E=128, k=2, dff=6144,
                                 act="swiglu", dtype="bf16", cf=1.0, seed=4, wseed=4,
                                 logit_bias0=2.0),
+    # The decode-shaped call with its experts stored as per-row scaled INT8 codes.
+    "decode_int8_bf16": Workload("decode_int8_bf16", T=32, d=2048, E=64, k=6, dff=1024, act="swiglu",
+                                 dtype="bf16", n_shared=2, seed=3, wseed=2, weights8="int8"),
     # Profiling stand-in for the skewed layer (kernel counters on a few GB of device memory): the
     # same expert shape and about the same rows per expert (~256), 16 experts instead of 128.
     "skewed_e16_bf16": Workload("skewed_e16_bf16", T=2048, d=4096, E=16, k=2, dff=6144, act="swiglu",
