@@ -30,7 +30,8 @@ from synth import WORKLOADS, make_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "skewed_bf16"
 # the other workloads, each measured as a sub-record of the single-GPU line
-SUB_WORKLOADS = ("tiny_fp32", "flash_bf16", "finegrained_bf16", "decode_bf16", "skewed_bf16", "skewed_cf1_bf16")
+SUB_WORKLOADS = ("tiny_fp32", "flash_bf16", "finegrained_bf16", "decode_bf16", "decode_int8_bf16", "skewed_bf16",
+                 "skewed_cf1_bf16")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the up-projection
@@ -167,10 +168,14 @@ class ClockSampler:
                 "source": "NVML (libnvidia-ml via ctypes), ~1 ms period, timed region only"}
 
 
+def weight_elt(wl) -> int:
+    """Bytes per expert weight: 1 for 8-bit codes, else the layer dtype's."""
+    return 1 if getattr(wl, "weights8", "dtype") != "dtype" else (2 if wl.dtype == "bf16" else 4)
+
+
 def weight_bytes_of(wl) -> int:
     """Expert weights (routed and shared) one layer pass streams."""
-    elt = 2 if wl.dtype == "bf16" else 4
-    return (wl.E + wl.n_shared) * (3 if wl.act == "swiglu" else 2) * wl.d * wl.dff * elt
+    return (wl.E + wl.n_shared) * (3 if wl.act == "swiglu" else 2) * wl.d * wl.dff * weight_elt(wl)
 
 
 def flushes_l2(wl) -> bool:
@@ -180,7 +185,9 @@ def flushes_l2(wl) -> bool:
 
 def arm_config(wl, ws_n: int) -> dict:
     """The workload the line is quoted on (both arms print the same one)."""
-    return {"workload": wl.name, "T": wl.T, "d_model": wl.d, "experts": wl.E, "top_k": wl.k,
+    w8 = {} if getattr(wl, "weights8", "dtype") == "dtype" else {
+        "expert_weights": f"{wl.weights8} codes + fp32 row scales (quantised once, before timing)"}
+    return {**w8, "workload": wl.name, "T": wl.T, "d_model": wl.d, "experts": wl.E, "top_k": wl.k,
             "d_ffn": wl.dff, "act": wl.act, "shared_experts": wl.n_shared,
             "capacity_factor": wl.cf if wl.cf > 0 else None,
             "parallelism": f"replicas x{ws_n} (no collective)",
@@ -211,6 +218,8 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = make_inputs(wl, str(dev))
+    if getattr(wl, "weights8", "dtype") != "dtype":  # 8-bit experts: quantised once, by the library
+        inp = moe.quantize_expert_tensors(inp, wl.weights8)
     cfg = moe.config_from_workload(wl)
     layer = moe.MoELayer(cfg, inp, device=dev)
     T, d = wl.T, wl.d
@@ -251,6 +260,10 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
     # weights the step streams; below twice the L2 size the L2 is flushed (a 256 MB write outside
     # the timed events) before every timed step instead
     elt = 2 if wl.dtype == "bf16" else 4
+    welt = weight_elt(wl)
+    # 8-bit experts also read one fp32 scale per weight row
+    srow = 4.0 / wl.d if welt == 1 else 0.0
+    srow_dn = 4.0 / wl.dff if welt == 1 else 0.0
     flush_l2 = flushes_l2(wl)
     flush_buf = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev) if flush_l2 else None
 
@@ -328,7 +341,7 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
                     "frac_of_sustained_peak": round(up_tflops / peak_sus, 4),
                     "peak_source": f"{peak_src} {peak_name}", "traffic": traffic, "traffic_source": traffic_note,
                     "algorithmic_flops_per_launch": up_all}
-        up_bytes = ((touched + wl.n_shared) * m_up * wl.d * wl.dff * elt
+        up_bytes = int((touched + wl.n_shared) * m_up * wl.d * wl.dff * (welt + srow)
                     + (kept_rows + (T if wl.n_shared else 0)) * wl.d * elt
                     + (kept_rows + T * wl.n_shared) * wl.dff * elt)
         if up_all / up_bytes < peak * 1e12 / (hbm * 1e9):
@@ -338,16 +351,17 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
                         "achieved": round(up_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(up_gbs / hbm, 4),
                         "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic, "traffic_source": traffic_note,
                         "algorithmic_bytes_per_launch": up_bytes,
-                        "units": f"{touched} routed + {wl.n_shared} shared experts' up weights, token rows read, "
-                                 "hidden rows written"}
+                        "units": f"{touched} routed + {wl.n_shared} shared experts' up weights"
+                                 + (f" ({welt}-byte codes + row scales)" if welt == 1 else "")
+                                 + ", token rows read, hidden rows written"}
     else:
         roofline = {"bound": "latency", "kernel": "whole fp32 layer (CUDA cores; the fp32 parity bound rules "
                     "out the tensor cores)", "achieved": round(ms_step * 1e3, 2), "unit": "us per layer",
                     "peak": None, "frac": None, "traffic": None}
     # bytes the step must move: the weights of every expert that received a token, the shared
     # experts, the router weights, x in and y out
-    layer_bytes = ((touched + wl.n_shared) * (m_up + 1) * wl.d * wl.dff * elt + wl.E * wl.d * elt
-                   + 2 * T * wl.d * elt)
+    layer_bytes = int((touched + wl.n_shared) * wl.d * wl.dff * (m_up * (welt + srow) + welt + srow_dn)
+                      + wl.E * wl.d * elt + 2 * T * wl.d * elt)
     layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
     res = {
         "workload": wl.name,
@@ -561,6 +575,15 @@ def cpu_leg(wl, host_inp, n: int):
     host memory): the median of up to three passes (one when a pass takes over 3 s)."""
     from oracle import moe_oracle as O
 
+    if getattr(wl, "weights8", "dtype") != "dtype":  # the oracle takes the dequantised weights
+        deq = O.dequantize_rows_int8 if wl.weights8 == "int8" else O.dequantize_rows_e4m3
+        host_inp = dict(host_inp)
+        for wk, sk in (("w_up", "s_up"), ("w_gate", "s_gate"), ("w_down", "s_down"), ("ws_up", "ss_up"),
+                       ("ws_gate", "ss_gate"), ("wb_up", "sb_up"), ("wb_gate", "sb_gate"), ("wb_down", "sb_down")):
+            if host_inp.get(wk) is not None:
+                host_inp[wk] = deq(host_inp[wk].numpy(), host_inp[sk].numpy())
+        if host_inp.get("ws_down") is not None:  # one scale per row over the S matrices
+            host_inp["ws_down"] = deq(host_inp["ws_down"].numpy(), host_inp["ss_down"].numpy()[None, :])
     times = []
     for _ in range(3):
         t = time.perf_counter()

@@ -92,21 +92,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// CL: acquire at cluster scope, for a phase completed by arrivals (release, cluster scope) of
-// threads of the peer CTA whose shared-memory writes the waiter's tensor-core work then reads.
-template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  if (CL)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  else
-    asm volatile(
+  asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
@@ -136,7 +124,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // (the failure-detection test hook) is measured with non-blocking polls on the SM's cycle counter
 // at 2 cycles per nanosecond, because a blocking poll alone may outlast it and the global timer
 // ticks too coarsely for a limit of a few nanoseconds.
-template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                   uint32_t* status,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
@@ -153,10 +140,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
       }
     }
   }
-  if (mbar_try_wait<CL>(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait<CL>(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > limit_ns) {
@@ -190,14 +177,6 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
       "[%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
-}
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 // Tile loads of a 2-SM (cta_group::2) MMA pair: the data lands in this CTA's shared memory and the
 // completion is signalled on the mbarrier at `bar`, a shared::cluster address that may lie in the
@@ -240,6 +219,13 @@ __device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t cluster_addr)
   return v;
 }
 // Arrive once on an mbarrier given by a shared::cluster address (possibly in another CTA).
+// Arrive on an mbarrier that may lie in another CTA of the cluster, with the default (CTA-scope)
+// release: used after fence.proxy.async by threads whose shared-memory writes the leader's
+// tensor-core work reads (the arrive needs no cluster-wide memory barrier, which costs ~0.5 us
+// under a full memory system).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }

@@ -74,12 +74,13 @@ constexpr int SMEM_LIMIT = 232448;              // opt-in shared memory per CTA
 
 // 8-bit expert weights (W8): the weight box of a K step arrives as one byte per weight in a ring
 // of its own, and CONVW converter warps widen it to bf16 into the stage's swizzled operand tile
-constexpr int CONVW = 4;
+template <int ACT> constexpr int conv_warps();  // 8, or 4 beside the 16-warp GELU epilogue
 constexpr int RAW_BYTES = AR * BK;              // 8 KB: one CTA's 8-bit weight tile of a K step
 constexpr int MAX_RAW = 24;
 
 template <int ACT> constexpr int epi_warps() { return ACT == ACT_GELU ? 16 : 4; }  // the erf epilogue is ALU-bound
-template <int ACT, bool W8> constexpr int n_threads() { return 128 + 32 * (epi_warps<ACT>() + (W8 ? CONVW : 0)); }
+template <int ACT> constexpr int conv_warps() { return epi_warps<ACT>() > 8 ? 4 : 8; }
+template <int ACT, bool W8> constexpr int n_threads() { return 128 + 32 * (epi_warps<ACT>() + (W8 ? conv_warps<ACT>() : 0)); }
 template <int ACT> constexpr bool out_f32() { return ACT == ACT_NONE; }           // projections to the model width
 template <int ACT> constexpr int feat_per_tile() { return ACT == ACT_SWIGLU ? AR : 2 * AR; }  // output features per pair tile
 // token rows per tile: NTV (256, or 32 for decode-sized calls)
@@ -87,6 +88,8 @@ template <int ACT, int NTV> constexpr int tile_tokens() { return NTV; }
 template <int ACT, int NTV> constexpr int a_bytes() { return WBOX; }
 template <int ACT, int NTV> constexpr int b_bytes() { return tile_tokens<ACT, NTV>() / 2 * BK * 2; }
 template <int ACT, int NTV> constexpr int stage_bytes() { return a_bytes<ACT, NTV>() + b_bytes<ACT, NTV>(); }
+// 8-bit weights: a ring of raw weight boxes (as deep as shared memory allows: the bytes in flight
+// from HBM) feeds the stage ring, whose stages hold the widened bf16 weight tile and the token rows
 // epilogue staging per warp: fp32 32 x 32 (128-byte rows) or bf16 32 x 32 (64-byte rows); two
 // buffers per warp except with 16 warps; none for SwiGLU, which stores straight from registers
 template <int ACT> constexpr int stg_bytes() { return ACT == ACT_NONE ? 4096 : 2048; }
@@ -96,17 +99,18 @@ template <int ACT> constexpr int stg_total() { return epi_warps<ACT>() * stg_buf
 // bf16 operand stages: as many as fit (at most MAX_STAGES); with 8-bit weights a few, the bytes in
 // flight from HBM being the raw ring's
 template <int ACT, int NTV, bool W8 = false> constexpr int n_stages() {
-  return W8 ? (NTV <= 32 ? 4 : 3)
+  return W8 ? (NTV <= 32 ? 5 : 3)
              : ((SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>()) / stage_bytes<ACT, NTV>() < MAX_STAGES
                     ? (SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>()) / stage_bytes<ACT, NTV>()
                     : MAX_STAGES);
 }
+template <int ACT, int NTV, bool W8> constexpr int w8_fixed_bytes() {
+  return n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>();
+}
 template <int ACT, int NTV, bool W8> constexpr int raw_stages() {
   return !W8 ? 0
-             : ((SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>() - n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>()) /
-                        RAW_BYTES < MAX_RAW
-                    ? (SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>() - n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>()) /
-                          RAW_BYTES
+             : ((SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>() - w8_fixed_bytes<ACT, NTV, W8>()) / RAW_BYTES < MAX_RAW
+                    ? (SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>() - w8_fixed_bytes<ACT, NTV, W8>()) / RAW_BYTES
                     : MAX_RAW);
 }
 
@@ -136,7 +140,7 @@ struct TcMaps {
 struct SmemCtl {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
-  uint64_t raw_full[MAX_RAW];   // 8-bit weight ring: loaded / widened
+  uint64_t raw_full[MAX_RAW];   // 8-bit weights, slot ring: raw box loaded / widened
   uint64_t raw_empty[MAX_RAW];
   uint64_t tfull[2];
   uint64_t tempty[2];
@@ -161,7 +165,8 @@ static_assert(smem_total<ACT_NONE, 256, true>() <= SMEM_LIMIT && smem_total<ACT_
                   smem_total<ACT_NONE, 32, true>() <= SMEM_LIMIT && smem_total<ACT_GELU, 32, true>() <= SMEM_LIMIT,
               "shared memory per CTA (8-bit weights)");
 static_assert(raw_stages<ACT_SWIGLU, 32, true>() >= 16 && raw_stages<ACT_NONE, 32, true>() >= 12 &&
-                  raw_stages<ACT_NONE, 256, true>() >= 8 && raw_stages<ACT_GELU, 256, true>() >= 8,
+                  raw_stages<ACT_NONE, 256, true>() >= 8 && raw_stages<ACT_GELU, 256, true>() >= 8 &&
+                  raw_stages<ACT_SWIGLU, 256, true>() >= 12,
               "8-bit weight bytes in flight");
 static_assert(n_stages<ACT_NONE, 256>() == 6 && n_stages<ACT_SWIGLU, 256>() == 7 && n_stages<ACT_NONE, 32>() >= 10,
               "stage counts");
@@ -253,34 +258,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t pair) {
 }
 // One CTA's 8-bit weight tile (AR rows of BK bytes, row-major) -> the bf16 operand tile (AR rows
 // of 128 bytes, 16-byte chunk j of row i at chunk j ^ (i % 8), the layout TMA's 128-byte swizzle
-// writes).  Thread ct of the CONVW converter warps widens 16 weights per step; a warp's loads cover
-// 512 contiguous bytes and its stores hit every bank once per quarter warp.
-__device__ __forceinline__ void widen_tile(uint32_t raw, uint32_t dst, int ct, int fmt) {
+// writes).  Thread ct of the CONVW converter warps widens 16 weights per item; a warp's loads cover
+// 512 contiguous bytes and its stores hit every bank once per quarter warp.  All loads of a thread
+// are issued before its first conversion (plain shared-memory accesses, so the compiler may
+// overlap them).
+template <int CONVW>
+__device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int ct, int fmt) {
+  constexpr int ITEMS = AR * (BK / 16) / (CONVW * 32);
+  uint4 v[ITEMS];
 #pragma unroll
-  for (int it = 0; it < AR * (BK / 16) / (CONVW * 32); ++it) {
+  for (int it = 0; it < ITEMS; ++it) {
+    const int item = it * CONVW * 32 + ct;
+    v[it] = *reinterpret_cast<const uint4*>(raw + (item >> 2) * BK + (item & 3) * 16);
+  }
+#pragma unroll
+  for (int it = 0; it < ITEMS; ++it) {
     const int item = it * CONVW * 32 + ct;
     const int row = item >> 2, piece = item & 3;
-    const uint4 v = ld_shared_v4(raw + row * BK + piece * 16);
     uint32_t o[8];
     if (fmt == 1) {
-      int8x4_to_bf16(v.x, o[0], o[1]);
-      int8x4_to_bf16(v.y, o[2], o[3]);
-      int8x4_to_bf16(v.z, o[4], o[5]);
-      int8x4_to_bf16(v.w, o[6], o[7]);
+      int8x4_to_bf16(v[it].x, o[0], o[1]);
+      int8x4_to_bf16(v[it].y, o[2], o[3]);
+      int8x4_to_bf16(v[it].z, o[4], o[5]);
+      int8x4_to_bf16(v[it].w, o[6], o[7]);
     } else {
-      o[0] = e4m3x2_to_bf16x2(v.x & 0xFFFFu);
-      o[1] = e4m3x2_to_bf16x2(v.x >> 16);
-      o[2] = e4m3x2_to_bf16x2(v.y & 0xFFFFu);
-      o[3] = e4m3x2_to_bf16x2(v.y >> 16);
-      o[4] = e4m3x2_to_bf16x2(v.z & 0xFFFFu);
-      o[5] = e4m3x2_to_bf16x2(v.z >> 16);
-      o[6] = e4m3x2_to_bf16x2(v.w & 0xFFFFu);
-      o[7] = e4m3x2_to_bf16x2(v.w >> 16);
+      o[0] = e4m3x2_to_bf16x2(v[it].x & 0xFFFFu);
+      o[1] = e4m3x2_to_bf16x2(v[it].x >> 16);
+      o[2] = e4m3x2_to_bf16x2(v[it].y & 0xFFFFu);
+      o[3] = e4m3x2_to_bf16x2(v[it].y >> 16);
+      o[4] = e4m3x2_to_bf16x2(v[it].z & 0xFFFFu);
+      o[5] = e4m3x2_to_bf16x2(v[it].z >> 16);
+      o[6] = e4m3x2_to_bf16x2(v[it].w & 0xFFFFu);
+      o[7] = e4m3x2_to_bf16x2(v[it].w >> 16);
     }
-    const uint32_t base = dst + row * 128;
-    const uint32_t sw = (uint32_t)(row & 7);
-    st_shared_v4(base + (((uint32_t)(2 * piece) ^ sw) << 4), o[0], o[1], o[2], o[3]);
-    st_shared_v4(base + (((uint32_t)(2 * piece + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+    uint8_t* base = dst + row * 128;
+    const int sw = row & 7;
+    *reinterpret_cast<uint4*>(base + (((2 * piece) ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(base + (((2 * piece + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -296,6 +310,7 @@ template <int ACT, int NTV, bool W8>
 __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
     k_proj_tc(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs args) {
   constexpr int EPIW = epi_warps<ACT>();
+  constexpr int CONVW = conv_warps<ACT>();
   constexpr int NBUF = stg_bufs<ACT>() > 0 ? stg_bufs<ACT>() : 1;  // (SwiGLU stages nothing)
   constexpr int STG = stg_bytes<ACT>();
   constexpr int NT = tile_tokens<ACT, NTV>();
@@ -306,8 +321,8 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
   constexpr int RAWST = raw_stages<ACT, NTV, W8>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* raw_base = smem + (size_t)STAGES * STAGE_BYTES;   // 8-bit weight ring (W8)
-  uint8_t* stg_base = raw_base + (size_t)RAWST * RAW_BYTES;  // 1024-byte aligned (the swizzle atoms)
+  uint8_t* raw_base = smem + (size_t)STAGES * STAGE_BYTES;  // W8: the raw weight ring
+  uint8_t* stg_base = raw_base + (size_t)RAWST * RAW_BYTES; // 1024-byte aligned (the swizzle atoms)
   SmemCtl* ctl = reinterpret_cast<SmemCtl*>(stg_base + (size_t)EPIW * stg_bufs<ACT>() * STG);
   volatile int* abort_flag = &ctl->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -319,9 +334,9 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      // W8: every converter warp of the pair arrives once the stage's weights are widened (the
-      // leader's first one also arms the token rows' bytes)
-      mbar_init(smem_u32(&ctl->full[s]), W8 ? 2 * CONVW : 1);
+      // W8: every converter warp of the pair arrives once the stage's weights are widened, and the
+      // leader's token-row thread once it has armed both CTAs' token-row bytes
+      mbar_init(smem_u32(&ctl->full[s]), W8 ? 2 * CONVW + 1 : 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     for (int r = 0; r < RAWST; ++r) {
@@ -425,8 +440,9 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
     return t;
   };
 
-  if (warp == 0 && W8) {
-    // 8-bit weights: this CTA's weight box of each K step into the raw ring (its own barrier)
+  if (W8 && warp == 0) {
+    // 8-bit weights: this CTA's raw weight box of every K step (own barrier), as soon as the
+    // converters have widened the slot's previous box
     if (lane == 0) {
       int r = 0;
       uint32_t rph = 0, armed = 0, armed_ph = 0;
@@ -463,6 +479,46 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
       if (aborted) {  // this CTA's own copies land before it leaves
         for (int i = 0; i < RAWST; ++i)
           if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->raw_full[i]), (armed_ph >> i) & 1u);
+      }
+    }
+  } else if (W8 && warp == 3) {
+    // 8-bit weights: this CTA's token rows of every K step into the stage, once the MMAs have
+    // read it (the leader arms its stage barrier with both CTAs' bytes)
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      bool aborted = false;
+      for (int u = unit0; u < total_units && !aborted; u += ustep) {
+        const Tile t = decode(u);
+        const int half = t.nmma >> 1;
+        const int brow = t.m0 + crank * half;
+        const bool small_box = NT / 2 > 32 && half <= 32;
+        const uint32_t b_tx = 2u * (uint32_t)((small_box ? 32 : NT / 2) * BK * 2);  // both CTAs' token rows
+        for (int kb = 0; kb < t.kblocks; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, b_tx);
+            armed |= 1u << s;
+            armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          }
+          const uint32_t dst = smem_u32(smem + (size_t)s * STAGE_BYTES + A_BYTES);
+          if (small_box)
+            tma_load_2d_cg2(dst, &maps.x32[t.p], mapa_rank(fb, 0), kb * BK, brow);
+          else
+            tma_load_2d_cg2(dst, &maps.x[t.p], mapa_rank(fb, 0), kb * BK, brow);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted && leader) {  // both CTAs' armed token-row copies land (or the wait runs out)
+        for (int i = 0; i < STAGES; ++i)
+          if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
       }
     }
   } else if (warp == 0) {
@@ -532,7 +588,7 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
         const uint32_t idesc = umma_idesc_bf16(2 * AR, t.nmma);
         for (int kb = 0; kb < t.kblocks; ++kb) {
-          if (!mbar_wait_bounded<W8>(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
+          if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
             aborted = true;
             break;
           }
@@ -556,56 +612,33 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
       drain_wait(smem_u32(&ctl->mma_done), 0);
     }
   } else if (W8 && warp >= 4 + EPIW) {
-    // converter warps (8-bit weights): per K step, wait for the bf16 stage to be free, load this
-    // CTA's token rows into it, widen the raw weight box into its operand tile, then arrive on the
-    // leader's stage barrier (the leader's first warp also arms the two CTAs' token-row bytes)
+    // converter warps (8-bit weights): per K step, once the bf16 tile of the stage is free and the
+    // slot's raw box has landed, widen the box into it and arrive on the leader's stage barrier
     const int cw = warp - 4 - EPIW;
     const int ct = cw * 32 + lane;
     int s = 0, r = 0;
-    uint32_t ph = 0, rph = 0, armed = 0, armed_ph = 0;
+    uint32_t ph = 0, rph = 0;
     bool aborted = false;
     for (int u = unit0; u < total_units && !aborted; u += ustep) {
       const Tile t = decode(u);
-      const int half = t.nmma >> 1;
-      const int brow = t.m0 + crank * half;
-      const bool small_box = NT / 2 > 32 && half <= 32;
-      const uint32_t b_tx = 2u * (uint32_t)((small_box ? 32 : NT / 2) * BK * 2);  // both CTAs' token rows
       for (int kb = 0; kb < t.kblocks; ++kb) {
         int ok = 1;
-        if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status) ? 1 : 0;
+        if (lane == 0)
+          ok = (mbar_wait_bounded(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, args.status) &&
+                mbar_wait_bounded(smem_u32(&ctl->raw_full[r]), rph, abort_flag, args.status))
+                   ? 1
+                   : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) {
           aborted = true;
           break;
         }
-        uint8_t* sa = smem + (size_t)s * STAGE_BYTES;
-        const uint32_t fb = smem_u32(&ctl->full[s]);
-        const uint32_t lb = mapa_rank(fb, 0);
-        if (ct == 0) {
-          if (small_box)
-            tma_load_2d_cg2(smem_u32(sa + A_BYTES), &maps.x32[t.p], lb, kb * BK, brow);
-          else
-            tma_load_2d_cg2(smem_u32(sa + A_BYTES), &maps.x[t.p], lb, kb * BK, brow);
-        }
-        if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl->raw_full[r]), rph, abort_flag, args.status) ? 1 : 0;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) widen_tile(smem_u32(raw_base + (size_t)r * RAW_BYTES), smem_u32(sa), ct, args.wfmt);
+        widen_tile<CONVW>(raw_base + (size_t)r * RAW_BYTES, smem + (size_t)s * STAGE_BYTES, ct, args.wfmt);
         fence_proxy_async_smem();  // the widened tile is read by the tensor cores (async proxy)
         __syncwarp();
         if (lane == 0) {
-          // arrive even after a failed wait, so that the stage's token-row copies can be drained
           mbar_arrive(smem_u32(&ctl->raw_empty[r]));
-          if (leader && cw == 0) {
-            mbar_arrive_expect_tx(fb, b_tx);
-            armed |= 1u << s;
-            armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          } else {
-            mbar_arrive_cluster(lb);
-          }
-        }
-        if (!ok) {
-          aborted = true;
-          break;
+          mbar_arrive_remote(mapa_rank(smem_u32(&ctl->full[s]), 0));
         }
         if (++s == STAGES) {
           s = 0;
@@ -616,10 +649,6 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
           rph ^= 1u;
         }
       }
-    }
-    if (aborted && leader && ct == 0) {  // let the armed token-row copies (of both CTAs) land
-      for (int i = 0; i < STAGES; ++i)
-        if ((armed >> i) & 1u) drain_wait(smem_u32(&ctl->full[i]), (armed_ph >> i) & 1u);
     }
   } else if (warp >= 4 && warp < 4 + EPIW) {
     const int q = warp & 3;                  // TMEM lanes 32q..32q+31 (a warp reaches only its quarter)
