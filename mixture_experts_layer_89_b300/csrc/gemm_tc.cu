@@ -45,6 +45,14 @@
 //               instead (SwiGLU always stores directly: each half-warp writes 32 contiguous bytes
 //               of a token row).  Warp w reads TMEM lanes 32 (w % 4)..; warps w, w + 4, ... split
 //               the token columns.
+// 8-bit expert weights (INT8 or E4M3 codes with one fp32 scale per weight row; the mini-moe
+// tutorial's deployment advice): warp 0 streams this CTA's raw weight boxes (one byte per weight)
+// into a ring of its own, as deep as shared memory allows; warp 3 loads the token rows into the
+// stage; converter warps (after the epilogue warps) widen each raw box exactly to bf16 -- into the
+// swizzled shared-memory operand tile, or, for 32-token tiles, whose accumulators leave most of the
+// tensor memory free, straight into tensor memory, from where the MMA reads its A operand -- and
+// arrive on the pair leader's stage barrier; the epilogue multiplies each accumulator row by its
+// weight row's scale.
 // Tiles are ordered problem, expert, feature tile, token tile (token tiles fastest), so the pairs
 // working at the same time share the weight tile in L2 and each weight tile is read from HBM once.
 // Launched as a programmatic dependent launch: the set-up overlaps the previous kernel's tail.
@@ -74,13 +82,17 @@ constexpr int SMEM_LIMIT = 232448;              // opt-in shared memory per CTA
 
 // 8-bit expert weights (W8): the weight box of a K step arrives as one byte per weight in a ring
 // of its own, and CONVW converter warps widen it to bf16 into the stage's swizzled operand tile
-template <int ACT> constexpr int conv_warps();  // 8, or 4 beside the 16-warp GELU epilogue
+template <int ACT, int NTV> constexpr int conv_warps();
 constexpr int RAW_BYTES = AR * BK;              // 8 KB: one CTA's 8-bit weight tile of a K step
 constexpr int MAX_RAW = 24;
 
 template <int ACT> constexpr int epi_warps() { return ACT == ACT_GELU ? 16 : 4; }  // the erf epilogue is ALU-bound
-template <int ACT> constexpr int conv_warps() { return epi_warps<ACT>() > 8 ? 4 : 8; }
-template <int ACT, bool W8> constexpr int n_threads() { return 128 + 32 * (epi_warps<ACT>() + (W8 ? conv_warps<ACT>() : 0)); }
+// converter warps: 8 (two per TMEM quarter when they widen into tensor memory), 4 beside the
+// 16-warp GELU epilogue; measured, 16 warps were slower on both paths
+template <int ACT, int NTV> constexpr int conv_warps() { return epi_warps<ACT>() > 8 ? 4 : 8; }
+template <int ACT, int NTV, bool W8> constexpr int n_threads() {
+  return 128 + 32 * (epi_warps<ACT>() + (W8 ? conv_warps<ACT, NTV>() : 0));
+}
 template <int ACT> constexpr bool out_f32() { return ACT == ACT_NONE; }           // projections to the model width
 template <int ACT> constexpr int feat_per_tile() { return ACT == ACT_SWIGLU ? AR : 2 * AR; }  // output features per pair tile
 // token rows per tile: NTV (256, or 32 for decode-sized calls)
@@ -89,7 +101,15 @@ template <int ACT, int NTV> constexpr int a_bytes() { return WBOX; }
 template <int ACT, int NTV> constexpr int b_bytes() { return tile_tokens<ACT, NTV>() / 2 * BK * 2; }
 template <int ACT, int NTV> constexpr int stage_bytes() { return a_bytes<ACT, NTV>() + b_bytes<ACT, NTV>(); }
 // 8-bit weights: a ring of raw weight boxes (as deep as shared memory allows: the bytes in flight
-// from HBM) feeds the stage ring, whose stages hold the widened bf16 weight tile and the token rows
+// from HBM) feeds the stage ring, whose stages hold the widened bf16 weight tile and the token rows.
+// Decode-sized calls (32-token tiles, whose accumulators need 32 TMEM columns each) widen the weights
+// into tensor memory instead, which the MMA reads as its A operand: the stages then hold only the
+// token rows, and widening adds no shared-memory traffic beside the tensor cores' operand reads.
+template <int NTV, bool W8> constexpr bool a_in_tmem() { return W8 && NTV <= 32; }
+template <int NTV, bool W8> constexpr int acc_cols() { return a_in_tmem<NTV, W8>() ? 32 : 256; }
+template <int ACT, int NTV, bool W8> constexpr int stage_bytes_of() {
+  return a_in_tmem<NTV, W8>() ? b_bytes<ACT, NTV>() : stage_bytes<ACT, NTV>();
+}
 // epilogue staging per warp: fp32 32 x 32 (128-byte rows) or bf16 32 x 32 (64-byte rows); two
 // buffers per warp except with 16 warps; none for SwiGLU, which stores straight from registers
 template <int ACT> constexpr int stg_bytes() { return ACT == ACT_NONE ? 4096 : 2048; }
@@ -99,13 +119,13 @@ template <int ACT> constexpr int stg_total() { return epi_warps<ACT>() * stg_buf
 // bf16 operand stages: as many as fit (at most MAX_STAGES); with 8-bit weights a few, the bytes in
 // flight from HBM being the raw ring's
 template <int ACT, int NTV, bool W8 = false> constexpr int n_stages() {
-  return W8 ? (NTV <= 32 ? 5 : 3)
+  return W8 ? (NTV <= 32 ? 12 : 3)
              : ((SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>()) / stage_bytes<ACT, NTV>() < MAX_STAGES
                     ? (SMEM_LIMIT - 1024 - CTL_BYTES - stg_total<ACT>()) / stage_bytes<ACT, NTV>()
                     : MAX_STAGES);
 }
 template <int ACT, int NTV, bool W8> constexpr int w8_fixed_bytes() {
-  return n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>();
+  return n_stages<ACT, NTV, W8>() * stage_bytes_of<ACT, NTV, W8>();
 }
 template <int ACT, int NTV, bool W8> constexpr int raw_stages() {
   return !W8 ? 0
@@ -154,8 +174,12 @@ struct SmemCtl {
 static_assert(sizeof(SmemCtl) <= CTL_BYTES, "control block");
 template <int ACT, int NTV, bool W8 = false>
 constexpr size_t smem_total() {
-  return 1024 + (size_t)n_stages<ACT, NTV, W8>() * stage_bytes<ACT, NTV>() +
+  return 1024 + (size_t)n_stages<ACT, NTV, W8>() * stage_bytes_of<ACT, NTV, W8>() +
          (size_t)raw_stages<ACT, NTV, W8>() * RAW_BYTES + (size_t)stg_total<ACT>() + CTL_BYTES;
+}
+// TMEM columns: two accumulators, then (A in TMEM) one 32-column bf16 weight tile per stage
+template <int ACT, int NTV, bool W8> constexpr int tmem_cols_used() {
+  return 2 * acc_cols<NTV, W8>() + (a_in_tmem<NTV, W8>() ? n_stages<ACT, NTV, W8>() * (BK / 2) : 0);
 }
 static_assert(smem_total<ACT_NONE, 256>() <= SMEM_LIMIT && smem_total<ACT_GELU, 256>() <= SMEM_LIMIT &&
                   smem_total<ACT_SWIGLU, 256>() <= SMEM_LIMIT && smem_total<ACT_SWIGLU, 32>() <= SMEM_LIMIT,
@@ -164,6 +188,9 @@ static_assert(smem_total<ACT_NONE, 256, true>() <= SMEM_LIMIT && smem_total<ACT_
                   smem_total<ACT_SWIGLU, 256, true>() <= SMEM_LIMIT && smem_total<ACT_SWIGLU, 32, true>() <= SMEM_LIMIT &&
                   smem_total<ACT_NONE, 32, true>() <= SMEM_LIMIT && smem_total<ACT_GELU, 32, true>() <= SMEM_LIMIT,
               "shared memory per CTA (8-bit weights)");
+static_assert(tmem_cols_used<ACT_SWIGLU, 32, true>() <= (int)TMEM_COLS && tmem_cols_used<ACT_NONE, 32, true>() <= (int)TMEM_COLS &&
+                  tmem_cols_used<ACT_SWIGLU, 256, false>() <= (int)TMEM_COLS,
+              "tensor memory columns");
 static_assert(raw_stages<ACT_SWIGLU, 32, true>() >= 16 && raw_stages<ACT_NONE, 32, true>() >= 12 &&
                   raw_stages<ACT_NONE, 256, true>() >= 8 && raw_stages<ACT_GELU, 256, true>() >= 8 &&
                   raw_stages<ACT_SWIGLU, 256, true>() >= 12,
@@ -298,6 +325,46 @@ __device__ __forceinline__ void widen_tile(const uint8_t* raw, uint8_t* dst, int
   }
 }
 
+// (A in TMEM) Thread `lane` of a converter warp in TMEM quarter q widens its row 32q + lane of the
+// CTA's raw weight box -- the KPW weights [k0, k0 + KPW) -- into 32-bit TMEM columns (two weights
+// each) starting at taddr.  The raw box is laid out by TMA's 64-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ ((r / 2) % 4)), so the quarter warp's loads of one chunk hit distinct banks.
+template <int KPW>
+__device__ __forceinline__ void widen_to_tmem(const uint8_t* raw, int row, int k0, uint32_t taddr, int fmt) {
+  constexpr int CH = KPW / 16;  // 16-byte chunks of the thread's row
+  uint4 v[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int chunk = (k0 / 16 + c) ^ ((row >> 1) & 3);
+    v[c] = *reinterpret_cast<const uint4*>(raw + row * BK + chunk * 16);
+  }
+  uint32_t o[CH * 8];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    {
+      const uint4 w = v[c];
+      uint32_t* d = o + 8 * c;
+      if (fmt == 1) {
+        int8x4_to_bf16(w.x, d[0], d[1]);
+        int8x4_to_bf16(w.y, d[2], d[3]);
+        int8x4_to_bf16(w.z, d[4], d[5]);
+        int8x4_to_bf16(w.w, d[6], d[7]);
+      } else {
+        d[0] = e4m3x2_to_bf16x2(w.x & 0xFFFFu);
+        d[1] = e4m3x2_to_bf16x2(w.x >> 16);
+        d[2] = e4m3x2_to_bf16x2(w.y & 0xFFFFu);
+        d[3] = e4m3x2_to_bf16x2(w.y >> 16);
+        d[4] = e4m3x2_to_bf16x2(w.z & 0xFFFFu);
+        d[5] = e4m3x2_to_bf16x2(w.z >> 16);
+        d[6] = e4m3x2_to_bf16x2(w.w & 0xFFFFu);
+        d[7] = e4m3x2_to_bf16x2(w.w >> 16);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CH; ++c) tmem_st8(taddr + 8 * c, o + 8 * c);
+}
+
 struct Tile {
   int p, g;        // problem, group (expert) within it
   int m0, m_end;   // first token row of the tile, end of the group's rows
@@ -307,16 +374,20 @@ struct Tile {
 };
 
 template <int ACT, int NTV, bool W8>
-__global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
+__global__ void __launch_bounds__(n_threads<ACT, NTV, W8>(), 1)
     k_proj_tc(const __grid_constant__ TcMaps maps, const __grid_constant__ TcArgs args) {
   constexpr int EPIW = epi_warps<ACT>();
-  constexpr int CONVW = conv_warps<ACT>();
+  constexpr int CONVW = conv_warps<ACT, NTV>();
   constexpr int NBUF = stg_bufs<ACT>() > 0 ? stg_bufs<ACT>() : 1;  // (SwiGLU stages nothing)
   constexpr int STG = stg_bytes<ACT>();
   constexpr int NT = tile_tokens<ACT, NTV>();
   constexpr int FT = feat_per_tile<ACT>();
   constexpr int A_BYTES = a_bytes<ACT, NTV>();
-  constexpr int STAGE_BYTES = stage_bytes<ACT, NTV>();
+  constexpr bool TA = a_in_tmem<NTV, W8>();    // A operand widened into tensor memory
+  constexpr int ACC_COLS = acc_cols<NTV, W8>();
+  constexpr uint32_t A_COL0 = 2 * ACC_COLS;      // (TA) first column of the stages' weight tiles
+  constexpr int STAGE_BYTES = stage_bytes_of<ACT, NTV, W8>();
+  constexpr int B_OFF = TA ? 0 : A_BYTES;        // token rows within a stage
   constexpr int STAGES = n_stages<ACT, NTV, W8>();
   constexpr int RAWST = raw_stages<ACT, NTV, W8>();
   extern __shared__ uint8_t smem_raw[];
@@ -505,7 +576,7 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
             armed |= 1u << s;
             armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           }
-          const uint32_t dst = smem_u32(smem + (size_t)s * STAGE_BYTES + A_BYTES);
+          const uint32_t dst = smem_u32(smem + (size_t)s * STAGE_BYTES + B_OFF);
           if (small_box)
             tma_load_2d_cg2(dst, &maps.x32[t.p], mapa_rank(fb, 0), kb * BK, brow);
           else
@@ -585,7 +656,7 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), aph ^ 1u, abort_flag, args.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 256);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * ACC_COLS);
         const uint32_t idesc = umma_idesc_bf16(2 * AR, t.nmma);
         for (int kb = 0; kb < t.kblocks; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl->full[s]), ph, abort_flag, args.status)) {
@@ -594,11 +665,18 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)s * STAGE_BYTES);
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + B_OFF;
+          if (TA) {
+            const uint32_t a_tmem = tmem_base + A_COL0 + (uint32_t)(s * (BK / 2));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16_cg2(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16_cg2_ta(d_tmem, a_tmem + kk * 8, sdesc_k_sw128(sb + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              umma_bf16_cg2(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc,
+                            (kb | kk) != 0 ? 1u : 0u);
+          }
           umma_commit_cg2_mc(smem_u32(&ctl->empty[s]), PAIR_MASK);  // both CTAs' copies of the stage are free
           if (++s == STAGES) {
             s = 0;
@@ -633,8 +711,21 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
           aborted = true;
           break;
         }
-        widen_tile<CONVW>(raw_base + (size_t)r * RAW_BYTES, smem + (size_t)s * STAGE_BYTES, ct, args.wfmt);
-        fence_proxy_async_smem();  // the widened tile is read by the tensor cores (async proxy)
+        if (TA) {
+          // this warp: TMEM quarter q (its rows 32q..32q+31) and the weights [k0, k0 + KPW) of them
+          constexpr int KPW = BK / (CONVW / 4);
+          const int q = warp & 3;
+          const int k0 = (cw >> 2) * KPW;
+          tc_fence_after();  // the MMAs that read this stage's tile before have completed
+          widen_to_tmem<KPW>(raw_base + (size_t)r * RAW_BYTES, 32 * q + lane, k0,
+                             tmem_base + ((uint32_t)(32 * q) << 16) + A_COL0 + (uint32_t)(s * (BK / 2) + k0 / 2),
+                             args.wfmt);
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          widen_tile<CONVW>(raw_base + (size_t)r * RAW_BYTES, smem + (size_t)s * STAGE_BYTES, ct, args.wfmt);
+          fence_proxy_async_smem();  // the widened tile is read by the tensor cores (async proxy)
+        }
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(smem_u32(&ctl->raw_empty[r]));
@@ -668,7 +759,7 @@ __global__ void __launch_bounds__(n_threads<ACT, W8>(), 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * 256);
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * ACC_COLS);
       if (ACT == ACT_SWIGLU) {
         // lanes 0-15 and 16-31 hold the two matrices (gate, up) of features fl..fl+15; lane i < 16
         // finishes tokens 0-15 of a 32-token block, lane i + 16 tokens 16-31
@@ -903,12 +994,13 @@ template <int ACT, int NTV, bool W8>
 cudaError_t launch_t(const Projection* ps, int nprob, uint32_t* status, cudaStream_t st) {
   constexpr int NT = tile_tokens<ACT, NTV>();
   constexpr int FT = feat_per_tile<ACT>();
-  constexpr int threads = n_threads<ACT, W8>();
+  constexpr int threads = n_threads<ACT, NTV, W8>();
   constexpr size_t smem = smem_total<ACT, NTV, W8>();
   // weights: bf16 through the 128-byte swizzle, or 8-bit codes as plain 64-byte rows
   constexpr int wel = W8 ? 1 : 2;
   const CUtensorMapDataType wdt = W8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapSwizzle wsw = W8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle wsw = !W8 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                     : (a_in_tmem<NTV, W8>() ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE);
   auto kern = k_proj_tc<ACT, NTV, W8>;
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
