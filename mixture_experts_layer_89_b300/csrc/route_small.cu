@@ -6,10 +6,13 @@
 // The router is the bias-free Linear -> softmax -> top-k -> renormalise of the mini-moe tutorial,
 // sec. 3.1 (MoELayer), with the losses of the OpenMythos article, sec. 3.1, and the FLAME-MoE
 // summary, sec. 2.  A 128-token tile holding a few tokens leaves the tensor-core router one CTA
-// (or one cluster) and a serial epilogue; here every (token, expert) logit is its own warp's
-// compensated (Neumaier) fp32 dot product of two bf16 rows -- bf16 x bf16 products are exact in
-// fp32, so the logits are within a few ulp of the exact sums and the top-k choice needs no
-// re-decision.  One CTA per token computes its logits and selects; the last CTA to finish reduces.
+// (or one cluster) and a serial epilogue; here every (token, expert) logit is its own warp's fp32
+// dot product of two bf16 rows (the products are exact in fp32), with a rigorous bound on its
+// rounding error.  Where two of a token's leading k + 1 logits lie within their bounds of each
+// other, that token's logits are recomputed with compensated (Neumaier) sums, within a few ulp of
+// the exact values, before selecting: the choice and order of the k experts are those of the exact
+// logits up to ties closer than that.  One CTA per token computes its logits and selects; the last
+// CTA to finish reduces.
 #include <float.h>
 
 #include <algorithm>
@@ -23,52 +26,16 @@ namespace moe {
 namespace {
 constexpr float kBad = -3.0e38f;
 
-// Compensated fp32 dot product of two bf16 rows of length d (a multiple of 8), one warp; every lane
-// returns the same value.
+// One step of Neumaier's compensated summation: s + c carries the running sum.
 __device__ __forceinline__ void neumaier(float& s, float& c, float p) {
   const float t = __fadd_rn(s, p);
   c = __fadd_rn(c, fabsf(s) >= fabsf(p) ? __fadd_rn(__fsub_rn(s, t), p) : __fadd_rn(__fsub_rn(p, t), s));
   s = t;
 }
 
-__device__ __forceinline__ float comp_dot(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ b,
-                                          int d, int lane) {
-  constexpr int U = 4;
-  float s = 0.f, c = 0.f;
-  for (int base = lane * 8; base < d; base += 256 * U) {
-    uint4 av[U], bv[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = base + u * 256;
-      av[u] = i < d ? __ldg(reinterpret_cast<const uint4*>(a + i)) : make_uint4(0, 0, 0, 0);
-      bv[u] = i < d ? __ldg(reinterpret_cast<const uint4*>(b + i)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t aw[4] = {av[u].x, av[u].y, av[u].z, av[u].w};
-      const uint32_t bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        neumaier(s, c, __fmul_rn(__uint_as_float(aw[j] << 16), __uint_as_float(bw[j] << 16)));
-        neumaier(s, c, __fmul_rn(__uint_as_float(aw[j] & 0xffff0000u), __uint_as_float(bw[j] & 0xffff0000u)));
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {  // pairwise, carrying each side's compensation
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
-    const float t = __fadd_rn(s, s2);
-    const float bp = __fsub_rn(t, s);
-    const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(s2, bp));
-    c = __fadd_rn(__fadd_rn(c, c2), err);
-    s = t;
-  }
-  return __fadd_rn(s, c);
-}
-
-// The same compensated dot product with the token's row already in shared memory (d <= 4096 per
-// round of eight 16-byte loads per lane of the weight row, all in flight together).
+// Compensated fp32 dot product of the token's row (shared memory) and a weight row (length d, a
+// multiple of 8), one warp; every lane returns the same value.  Eight 16-byte loads per lane of the
+// weight row are in flight together.
 __device__ __forceinline__ float comp_dot_sx(const uint4* __restrict__ xs, const __nv_bfloat16* __restrict__ b, int d,
                                              int lane) {
   constexpr int U = 8;
@@ -106,6 +73,47 @@ __device__ __forceinline__ float comp_dot_sx(const uint4* __restrict__ xs, const
   return __fadd_rn(s, c);
 }
 
+// Plain fp32 dot product of the token's row (shared memory) and a weight row, and the squared norm
+// of the weight row; one warp, every lane returns both.  Each lane sums its d/32 exact bf16 x bf16
+// products in order and five shuffle levels add the lanes, so the rounding error is at most
+// (d/32 + 6) 2^-24 sum_i |x_i w_i| <= (d/32 + 6) 2^-24 ||x|| ||w|| (recursive summation, then
+// Cauchy-Schwarz).
+__device__ __forceinline__ float fast_dot_sx(const uint4* __restrict__ xs, const __nv_bfloat16* __restrict__ b, int d,
+                                             int lane, float& nw2) {
+  constexpr int U = 8;
+  float s = 0.f, n = 0.f;
+  for (int base = lane * 8; base < d; base += 256 * U) {
+    uint4 bv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * 256;
+      bv[u] = i < d ? __ldg(reinterpret_cast<const uint4*>(b + i)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * 256;
+      const uint4 av = i < d ? xs[i >> 3] : make_uint4(0, 0, 0, 0);
+      const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
+      const uint32_t bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float b0 = __uint_as_float(bw[j] << 16), b1 = __uint_as_float(bw[j] & 0xffff0000u);
+        s = fmaf(__uint_as_float(aw[j] << 16), b0, s);
+        s = fmaf(__uint_as_float(aw[j] & 0xffff0000u), b1, s);
+        n = fmaf(b0, b0, n);
+        n = fmaf(b1, b1, n);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    n += __shfl_xor_sync(0xffffffffu, n, o);
+  }
+  nw2 = n;
+  return s;
+}
+
 // One CTA per token, 1024 threads: warp w computes the logits of experts w, w + 32, ...; warp 0
 // selects the top k (ties to the lower index), normalises the weights and the softmax of z / tau,
 // and writes the token's probabilities and lse^2 to the workspace.  The last CTA to finish (a
@@ -125,6 +133,9 @@ __global__ void __launch_bounds__(1024, 1) k_route_small(const __nv_bfloat16* __
   pdl_trigger();
   pdl_wait();
   __shared__ float zs[256];
+  __shared__ float zb[256];  // squared weight-row norms, then the logits' error bounds
+  __shared__ float nx2_s;
+  __shared__ int redo;
   __shared__ int h[256];
   __shared__ int is_last;
   __shared__ LossScratch sc;
@@ -135,87 +146,141 @@ __global__ void __launch_bounds__(1024, 1) k_route_small(const __nv_bfloat16* __
   uint4* xs = reinterpret_cast<uint4*>(pst);  // the token's row (d bf16) before pst holds anything else
   for (int i = tid; i < d / 8; i += 1024) xs[i] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d) + i);
   __syncthreads();
-  for (int e = warp; e < E; e += 32) {
-    const float v = comp_dot_sx(xs, wr + (size_t)e * d, d, lane);
-    if (lane == 0) zs[e] = __fadd_rn(v, lbias ? lbias[e] : 0.f);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float v[8];
-    float m = kBad;
-    bool bad = false;
+  if (warp == 0) {  // |x|^2 of the token's row, for the logits' error bounds
+    float nx = 0.f;
+    for (int i = lane; i < d / 8; i += 32) {
+      const uint4 a = xs[i];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      float zz = -FLT_MAX;
-      if (e < E) {
-        zz = zs[e];
-        if (!isfinite(zz)) {
-          bad = true;
-          zz = kBad;
-        }
+      for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(aw[j] << 16), hi = __uint_as_float(aw[j] & 0xffff0000u);
+        nx = fmaf(lo, lo, fmaf(hi, hi, nx));
       }
-      v[i] = zz;
-      m = fmaxf(m, zz);
     }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, DEV_NONFINITE);
-    // top-k: k rounds of argmax, ties to the lower expert index
-    uint32_t taken = 0;
-    int my_e = 0;
-    float my_v = 0.f, top = 0.f;
-    for (int j = 0; j < k; ++j) {
-      float bv = -FLT_MAX;
-      int be = 0x7fffffff;
+    for (int o = 16; o; o >>= 1) nx += __shfl_xor_sync(0xffffffffu, nx, o);
+    if (lane == 0) {
+      nx2_s = nx;
+      redo = 0;
+    }
+  }
+  for (int e = warp; e < E; e += 32) {
+    float nw2;
+    const float v = fast_dot_sx(xs, wr + (size_t)e * d, d, lane, nw2);
+    if (lane == 0) {
+      zs[e] = __fadd_rn(v, lbias ? lbias[e] : 0.f);
+      zb[e] = nw2;  // becomes the bound below
+    }
+  }
+  __syncthreads();
+  // error bound of each fp32 logit: (d/32 + 8) 2^-24 (||x|| ||w_e|| + |z_e|) (the last term covers
+  // the bias addition), with 1 % slack for the rounding of the norms themselves
+  const float gamma = (float)(d / 32 + 8) * 5.9604645e-8f * 1.01f;
+  for (int e = tid; e < E; e += 1024) zb[e] = gamma * (sqrtf(nx2_s * zb[e]) + fabsf(zs[e]));
+  __syncthreads();
+  for (int pass = 0; pass < 2; ++pass) {
+    if (warp == 0) do {
+      float v[8];
+      float m = kBad;
+      bool bad = false;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-          bv = v[i];
-          be = e;
+        float zz = -FLT_MAX;
+        if (e < E) {
+          zz = zs[e];
+          if (!isfinite(zz)) {
+            bad = true;
+            zz = kBad;
+          }
+        }
+        v[i] = zz;
+        m = fmaxf(m, zz);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (any_bad && lane == 0) atomicOr(status, DEV_NONFINITE);
+      // top-k: k rounds of argmax, ties to the lower expert index
+      uint32_t taken = 0;
+      int my_e = 0;
+      float my_v = 0.f, top = 0.f;
+      float lead_v[9];  // the leading k + 1 logits in selection order, and their experts
+      int lead_e[9];
+      for (int j = 0; j < k + (k < E ? 1 : 0); ++j) {
+        float bv = -FLT_MAX;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = lane + 32 * i;
+          if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
+            bv = v[i];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        lead_v[j] = bv;
+        lead_e[j] = be;
+        if (j == k) break;  // the (k+1)-th: only for the near-tie check
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (j == 0) top = bv;
+        if (lane == j) {
+          my_e = be;
+          my_v = bv;
         }
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
+      if (pass == 0 && !any_bad) {
+        // the fp32 logits decide the order of the leading k + 1 only where neighbours lie further
+        // apart than their two error bounds; else the token's logits are recomputed compensated
+        bool near = false;
+        for (int j = 0; j + 1 < k + (k < E ? 1 : 0); ++j)
+          near = near || (lead_v[j] - lead_v[j + 1] <= zb[lead_e[j]] + zb[lead_e[j + 1]]);
+        if (near) {
+          if (lane == 0) redo = 1;
+          continue;  // (warp-uniform) the exact pass decides
         }
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (j == 0) top = bv;
-      if (lane == j) {
-        my_e = be;
-        my_v = bv;
+      // renormalised weights of the k (the softmax over the selected logits / tau)
+      float wsum = 0.f;
+      for (int j = 0; j < k; ++j) wsum += __expf((__shfl_sync(0xffffffffu, my_v, j) - top) * inv_tau);
+      if (lane < k) {
+        topk_idx[(size_t)t * k + lane] = my_e;
+        topk_w[(size_t)t * k + lane] = __expf((my_v - top) * inv_tau) * (1.f / wsum);
       }
-    }
-    // renormalised weights of the k (the softmax over the selected logits / tau)
-    float wsum = 0.f;
-    for (int j = 0; j < k; ++j) wsum += __expf((__shfl_sync(0xffffffffu, my_v, j) - top) * inv_tau);
-    if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = my_e;
-      topk_w[(size_t)t * k + lane] = __expf((my_v - top) * inv_tau) * (1.f / wsum);
-    }
-    // softmax over all E and lse, of z / tau
-    float s = 0.f, p[8];
+      // softmax over all E and lse, of z / tau
+      float s = 0.f, p[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      p[i] = lane + 32 * i < E ? __expf((v[i] - m) * inv_tau) : 0.f;
-      s += p[i];
-    }
+      for (int i = 0; i < 8; ++i) {
+        p[i] = lane + 32 * i < E ? __expf((v[i] - m) * inv_tau) : 0.f;
+        s += p[i];
+      }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float inv_s = 1.f / s;
+      for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      const float inv_s = 1.f / s;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (lane + 32 * i < E) ptok[(size_t)t * E + lane + 32 * i] = p[i] * inv_s;
-    if (lane == 0) {
-      const float l = m * inv_tau + __logf(s);
-      l2tok[t] = l * l;
+      for (int i = 0; i < 8; ++i)
+        if (lane + 32 * i < E) ptok[(size_t)t * E + lane + 32 * i] = p[i] * inv_s;
+      if (lane == 0) {
+        const float l = m * inv_tau + __logf(s);
+        l2tok[t] = l * l;
+      }
+    } while (false);
+    __syncthreads();
+    if (!redo) break;
+    for (int e = warp; e < E; e += 32) {  // near ties: the compensated logits decide
+      const float v = comp_dot_sx(xs, wr + (size_t)e * d, d, lane);
+      if (lane == 0) zs[e] = __fadd_rn(v, lbias ? lbias[e] : 0.f);
     }
+    if (tid == 0) redo = 0;
+    __syncthreads();
   }
   __threadfence();
   __syncthreads();

@@ -149,6 +149,39 @@ def test_all_ties_pick_lowest_indices():
     check_all_steps(wl, inp_cpu, _to(inp_cpu, "cuda"))
 
 
+def test_small_router_near_ties_decided_exactly():
+    """Decode-sized calls route on fp32 logits with an error bound and recompute a token's logits
+    with compensated sums when its leading logits lie within the bounds.  Experts 0 and 1 differ by
+    one bf16 step in one weight and carry the same large logit bias, so every token's top two are
+    {0, 1} with a gap of |x_tj| * 2^-13 -- mostly above the 1e-5 exemption yet below the fp32
+    bound (~2e-4 here): the order must be the exact one."""
+    wl = Workload("bf16_near_ties", T=48, d=2048, E=16, k=2, dff=128, act="swiglu", dtype="bf16", seed=31, wseed=31)
+    inp_cpu = make_inputs(wl, "cpu")
+    w = inp_cpu["w_router"].float()
+    j = 5
+    w[1] = w[0]
+    w[0, j] = 0.02
+    w[1, j] = 0.02 + 2.0 ** -13          # one bf16 step above 0.02 (spacing 2^-13 in [2^-6, 2^-5))
+    inp_cpu["w_router"] = w.to(torch.bfloat16)
+    assert float(inp_cpu["w_router"][1, j]) - float(inp_cpu["w_router"][0, j]) == 2.0 ** -13
+    lb = torch.zeros(wl.E)
+    lb[:2] = 5.0
+    inp_cpu["logit_bias"] = lb
+    ref = oracle(wl, inp_cpu)
+    gap = np.abs(O._f64(inp_cpu["x"])[:, j]) * 2.0 ** -13
+    assert (gap > 1e-5).sum() >= 40 and ((gap > 1e-5) & (gap < 1e-4)).sum() >= 25  # most below the fp32 bound
+    assert all(sorted(ref["idx"][t].tolist()) == [0, 1] for t in range(wl.T))
+    got = run_steps(wl, _to(inp_cpu, "cuda"))
+    assert got["status"] == moe.MOE_OK
+    idx = got["topk_idx"].cpu().numpy()
+    assert all(sorted(idx[t].tolist()) == [0, 1] for t in range(wl.T))
+    decided = gap > 1e-5               # the exemption applies to the rest: either order is acceptable
+    bad = np.nonzero((idx != ref["idx"]).any(axis=1) & decided)[0]
+    assert bad.size == 0, [(int(t), idx[t].tolist(), ref["idx"][t].tolist(), float(gap[t])) for t in bad]
+    check_topk_weights(idx, got["topk_w"].cpu().numpy().astype(np.float64), ref, np.zeros(wl.T, bool))
+    check_losses(got["losses"], ref["lb"], ref["zl"])
+
+
 def test_empty_batch():
     wl = CASES["bf16_swiglu_shared"].replace(T=0)
     inp_gpu = _to(make_inputs(wl, "cpu"), "cuda")
