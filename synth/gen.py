@@ -83,6 +83,9 @@ WORKLOADS: Dict[str, Workload] = {
     # The decode-shaped call with its experts stored as per-row scaled INT8 codes.
     "decode_int8_bf16": Workload("decode_int8_bf16", T=32, d=2048, E=64, k=6, dff=1024, act="swiglu",
                                  dtype="bf16", n_shared=2, seed=3, wseed=2, weights8="int8"),
+    # The skewed layer with its experts stored as INT8 codes (9.7 GB instead of 19.3 GB).
+    "skewed_int8_bf16": Workload("skewed_int8_bf16", T=16384, d=4096, E=128, k=2, dff=6144, act="swiglu",
+                                 dtype="bf16", seed=4, wseed=4, logit_bias0=2.0, weights8="int8"),
     # Profiling stand-in for the skewed layer (kernel counters on a few GB of device memory): the
     # same expert shape and about the same rows per expert (~256), 16 experts instead of 128.
     "skewed_e16_bf16": Workload("skewed_e16_bf16", T=2048, d=4096, E=16, k=2, dff=6144, act="swiglu",

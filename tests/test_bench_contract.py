@@ -41,3 +41,13 @@ def test_expert_flops_counts_shared_experts():
     up, down, sh_up, sh_down = bench.expert_flops(wl, wl.T * wl.k, wl.T)
     assert up == 2.0 * wl.T * wl.k * 2 * wl.d * wl.dff and down == up / 2
     assert sh_up == 2.0 * wl.T * wl.n_shared * 2 * wl.d * wl.dff and sh_down == sh_up / 2
+
+
+def test_eight_bit_workloads_count_one_byte_per_weight():
+    # 8-bit experts stream one byte per weight; the roofline adds their fp32 row scales
+    for name in ("decode_int8_bf16", "skewed_int8_bf16"):
+        wl8 = WORKLOADS[name]
+        assert bench.weight_elt(wl8) == 1
+        wl16 = wl8.replace(weights8="dtype")
+        assert bench.weight_bytes_of(wl16) == 2 * bench.weight_bytes_of(wl8)
+        assert "expert_weights" in bench.arm_config(wl8, 1) and "expert_weights" not in bench.arm_config(wl16, 1)
