@@ -177,3 +177,34 @@ def test_weights8_argument_checks():
     bad = moe.config_from_workload(wl)
     bad.expert_weights = 3
     assert L.moe_workspace_size(ctypes.byref(bad), ctypes.byref(ctypes.c_size_t())) == moe.MOE_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_weights8_deterministic_and_graph_replay(fmt):
+    """Repeat calls give the same bits, and a CUDA-graph replay of the layer equals the eager call
+    (the converter warps and the stage barriers do not depend on scheduling)."""
+    wl = LAYER_CASES["swiglu_decode_shared3"].replace(weights8=fmt)
+    inp = make_inputs(wl, "cuda")
+    q = moe.quantize_expert_tensors(inp, fmt)
+    layer = moe.MoELayer(moe.config_from_workload(wl), q)
+    y0, l0, c0, d0 = layer.forward(inp["x"])
+    y1, l1, c1, d1 = layer.forward(inp["x"])
+    assert torch.equal(y0, y1) and torch.equal(l0, l1) and torch.equal(c0, c1)
+    cfg = layer.cfg
+    y = torch.empty_like(inp["x"])
+    losses = torch.empty(2, dtype=torch.float32, device="cuda")
+    counts = torch.empty(cfg.E, dtype=torch.int32, device="cuda")
+    drops = torch.empty(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe.moe_layer_forward(cfg, layer.weights, inp["x"], y, losses, counts, drops, layer.ws, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.moe_layer_forward(cfg, layer.weights, inp["x"], y, losses, counts, drops, layer.ws,
+                              torch.cuda.current_stream())
+    y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0) and torch.equal(losses, l0)
+    assert moe.moe_read_device_status(layer.ws) == moe.MOE_OK
