@@ -79,6 +79,54 @@ def expert_ffn_backward(xr, act: str, dY, w_up, w_down, w_gate=None, b_up=None) 
     return out
 
 
+def combine_backward(dy, y_perm, row_of, w) -> Dict[str, np.ndarray]:
+    """Backward of the combine y_t = sum over kept slots j of w_tj y_perm[row_of[t, j]] (+ shared):
+    dw [T, k] = <dy_t, y_perm[row]> (0 for a dropped slot) and dy_perm [rows, d], the upstream
+    gradient of each kept row, w_tj dy_t."""
+    dy = np.asarray(dy, np.float64)
+    y_perm = np.asarray(y_perm, np.float64)
+    row_of = np.asarray(row_of)
+    T, k = row_of.shape
+    dw = np.zeros((T, k))
+    dy_perm = np.zeros_like(y_perm)
+    for t in range(T):
+        for j in range(k):
+            r = int(row_of[t, j])
+            if r >= 0:
+                dw[t, j] = float(dy[t] @ y_perm[r])
+                dy_perm[r] = w[t, j] * dy[t]
+    return dict(dw=dw, dy_perm=dy_perm)
+
+
+def router_backward(x, w_router, P, lse, idx, w, dw, counts, *, E: int, k: int, lb_coef: float = 0.01,
+                    z_coef: float = 0.001, dlb: float = 1.0, dzl: float = 1.0,
+                    temperature: float = 1.0) -> Dict[str, np.ndarray]:
+    """Backward of the router given dL/dw_tj (dw [T, k]) and the weights of the two losses:
+    the renormalised top-k weights are a softmax over the k selected logits, so
+    dz_e = w_e (dw_e - sum_i w_i dw_i) for the selected e (top-k selection itself passes no
+    gradient); the load-balance loss alpha E sum_e f_e Pbar_e adds, through the full softmax,
+    P_te (g_e - sum_e' P_te' g_e') with g_e = dlb alpha E f_e / T (f_e = counts_e / (T k), counts
+    pass no gradient); the z-loss beta mean_t lse_t^2 adds dzl 2 beta lse_t P_te / T; a router
+    temperature divides the whole by tau.  Returns dz [T, E], dw_router = dz^T x [E, d] and
+    dx = dz W_r [T, d]."""
+    x = np.asarray(x, np.float64)
+    Wr = np.asarray(w_router, np.float64)
+    P = np.asarray(P, np.float64)
+    T = x.shape[0]
+    dz = np.zeros((T, E))
+    for t in range(T):
+        s = float(w[t] @ dw[t])
+        for j in range(k):
+            dz[t, int(idx[t, j])] += w[t, j] * (dw[t, j] - s)
+    if T > 0:
+        f = np.asarray(counts, np.float64) / float(T * k)
+        gP = dlb * lb_coef * E * f / T
+        dz += P * (gP[None, :] - (P @ gP)[:, None])
+        dz += (dzl * 2.0 * z_coef * np.asarray(lse, np.float64) / T)[:, None] * P
+    dz = dz / float(temperature)
+    return dict(dz=dz, dw_router=dz.T @ x, dx=dz @ Wr)
+
+
 def moe_layer_backward(inp: Dict, dy, *, E: int, k: int, act: str, n_shared: int = 0, cf: float = 0.0,
                        lb_coef: float = 0.01, z_coef: float = 0.001, dlb: float = 1.0,
                        dzl: float = 1.0, temperature: float = 1.0) -> Dict[str, np.ndarray]:
@@ -95,33 +143,17 @@ def moe_layer_backward(inp: Dict, dy, *, E: int, k: int, act: str, n_shared: int
     row_of, tok_of, y_perm = fwd["row_of"], fwd["tok_of"], fwd["y_perm"]
 
     # combine: y_t = sum over kept slots of w_tj F_tj  ->  dL/dw_tj = <dy_t, F_tj>, 0 if dropped
-    dw = np.zeros((T, k))
+    cb = combine_backward(dy, y_perm, row_of, w)
+    dw = cb["dw"]
     slot_of_row = {}
     for t in range(T):
         for j in range(k):
             r = int(row_of[t, j])
             if r >= 0:
-                dw[t, j] = float(dy[t] @ y_perm[r])
                 slot_of_row[r] = (t, j)
-
-    # the weights are a softmax over the k selected logits (renormalised top-k probabilities):
-    # dz_e = w_e (dw_e - sum_i w_i dw_i) for the selected e, 0 elsewhere
-    dz = np.zeros((T, E))
-    for t in range(T):
-        s = float(w[t] @ dw[t])
-        for j in range(k):
-            dz[t, int(idx[t, j])] += w[t, j] * (dw[t, j] - s)
-
-    if T > 0:
-        # load-balance loss lb = alpha E sum_e f_e Pbar_e: dlb/dP_te = alpha E f_e / T, through the
-        # full softmax; z-loss zl = beta mean_t lse_t^2: dzl/dz_te = 2 beta lse_t P_te / T
-        f = fwd["counts"] / float(T * k)
-        gP = dlb * lb_coef * E * f / T
-        dz += P * (gP[None, :] - (P @ gP)[:, None])
-        dz += (dzl * 2.0 * z_coef * lse / T)[:, None] * P
-
-    dz = dz / float(temperature)  # through z / tau
-    g: Dict[str, np.ndarray] = {"dw_router": dz.T @ x, "dx": dz @ Wr}
+    rb = router_backward(x, Wr, P, lse, idx, w, dw, fwd["counts"], E=E, k=k, lb_coef=lb_coef, z_coef=z_coef,
+                         dlb=dlb, dzl=dzl, temperature=temperature)
+    g: Dict[str, np.ndarray] = {"dw_router": rb["dw_router"], "dx": rb["dx"].copy()}
 
     # routed experts: row r of expert e carries w_tj dy_t
     has_bias = inp.get("b_up") is not None

@@ -485,6 +485,53 @@ def check_int8(o):
     assert e["scale"][2] == np.float32(np.float32(0.5) / np.float32(448))
 
 
+def check_routing_backward(b):
+    """combine_backward and router_backward against torch autograd of the same composite: the
+    combine y_t = sum_j w_tj y_perm[row_of[t, j]] (dropped slots excluded), and the router from x and
+    W_r through z = x W_r^T, the renormalised softmax of the selected logits / tau, the load-balance
+    loss with fixed counts and the z-loss."""
+    rng = np.random.default_rng(51)
+    T, d, E, k, tau = 7, 6, 5, 2, 1.7
+    lb_coef, z_coef, dlb, dzl = 0.01, 0.001, 1.3, 0.7
+    x = rng.standard_normal((T, d))
+    Wr = rng.standard_normal((E, d))
+    z = x @ Wr.T
+    idx = O.topk_select(z, k)
+    P, lse = O.softmax_lse(O.temper(z, tau))
+    w = O.renormalise(P, idx)
+    counts = np.bincount(idx.ravel(), minlength=E)
+    dw = rng.standard_normal((T, k))
+    rb = b.router_backward(x, Wr, P, lse, idx, w, dw, counts, E=E, k=k, lb_coef=lb_coef, z_coef=z_coef,
+                           dlb=dlb, dzl=dzl, temperature=tau)
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(Wr, requires_grad=True)
+    zt = (xt @ wt.T) / tau
+    sel = torch.gather(zt, 1, torch.tensor(idx))
+    L = (torch.softmax(sel, dim=1) * torch.tensor(dw)).sum()
+    Pt = torch.softmax(zt, dim=1)
+    f = torch.tensor(counts / (T * k))
+    L = L + dlb * lb_coef * E * (f * Pt.mean(dim=0)).sum()
+    L = L + dzl * z_coef * (torch.logsumexp(zt, dim=1) ** 2).mean()
+    L.backward()
+    np.testing.assert_allclose(rb["dx"], xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(rb["dw_router"], wt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    # combine: a dropped slot (row -1) gets no gradient
+    row_of = np.array([[0, 3], [1, -1], [2, 4], [5, 6], [7, -1], [8, 9], [10, 11]])
+    y_perm = rng.standard_normal((12, d))
+    dy = rng.standard_normal((T, d))
+    cb = b.combine_backward(dy, y_perm, row_of, w)
+    wv = torch.tensor(w, requires_grad=True)
+    yv = torch.tensor(y_perm, requires_grad=True)
+    y = torch.zeros((T, d), dtype=torch.float64)
+    for t in range(T):
+        for j in range(k):
+            if row_of[t, j] >= 0:
+                y[t] = y[t] + wv[t, j] * yv[row_of[t, j]]
+    (y * torch.tensor(dy)).sum().backward()
+    np.testing.assert_allclose(cb["dw"], wv.grad.numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(cb["dy_perm"], yv.grad.numpy(), rtol=1e-12, atol=1e-14)
+
+
 def check_backup_expert(o):
     """A backup expert identical to every routed expert makes drops invisible (the dropless layer);
     a zero backup expert gives the dropping layer; drops are counted."""
@@ -753,3 +800,31 @@ def test_planted_backward_mistakes_are_caught(name, fn, monkeypatch):
     with pytest.raises(AssertionError):
         check_backward(O, B)
 
+
+
+def test_routing_backward_pin():
+    from oracle import moe_backward as B
+    check_routing_backward(B)
+
+
+@pytest.mark.parametrize("name,mistake", [
+    ("router_backward", "no_temperature"),
+    ("router_backward", "z_loss_dropped"),
+    ("combine_backward", "row_scale_wrong"),
+])
+def test_planted_routing_backward_mistakes_are_caught(name, mistake, monkeypatch):
+    from oracle import moe_backward as B
+    real = getattr(B, name)
+
+    def fn(*a, **kw):
+        if mistake == "no_temperature":
+            kw = dict(kw, temperature=1.0)
+        if mistake == "z_loss_dropped":
+            kw = dict(kw, dzl=0.0)
+        out = dict(real(*a, **kw))
+        if mistake == "row_scale_wrong":
+            out["dy_perm"] = np.where(out["dy_perm"] != 0, out["dy_perm"] * 1.5, 0.0)
+        return out
+    monkeypatch.setattr(B, name, fn)
+    with pytest.raises(AssertionError):
+        check_routing_backward(B)
