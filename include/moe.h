@@ -1,5 +1,6 @@
 /*
- * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN layer, forward pass.
+ * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN layer: the forward pass,
+ * and the backward of its routing half.
  *
  * The layer (mini-moe tutorial, sec. 3.1 MoELayer; OpenMythos article, sec. 3.1; FLAME-MoE
  * summary, sec. 2) maps T tokens x[T,d] to y[T,d]:
@@ -63,8 +64,8 @@ typedef enum {
  * layer dtype).  The mini-moe tutorial (deployment optimisation) suggests quantising every expert
  * to INT8 to cut what is stored and loaded; the 8-bit formats hold one code per weight and one
  * fp32 scale per output row (see moe_quantize_experts), need a bf16 layer, and multiply the codes
- * by the bf16 activations on the tensor cores (codes widened to bf16 exactly in shared memory)
- * with the scale applied to the fp32 accumulator. */
+ * by the bf16 activations on the tensor cores (codes widened exactly to bf16 on the SM, into shared
+ * or tensor memory) with the scale applied to the fp32 accumulator. */
 typedef enum {
   MOE_EXPERT_WEIGHTS_DTYPE = 0,  /* the layer dtype                                              */
   MOE_EXPERT_WEIGHTS_INT8 = 1,   /* int8 codes q, weight = q * scale_row, |q| <= 127              */
@@ -296,6 +297,34 @@ moe_status moe_route_diagnostics(const moe_config* cfg, const void* x, const voi
 moe_status moe_quantize_experts(const void* w, int32_t dtype, int32_t format, int32_t blocks,
                                 int32_t rows, int32_t cols, void* codes, float* scale,
                                 int32_t* nonfinite, void* stream);
+
+/* Backward of the routing half of the layer (a first part of the backward pass; the expert FFNs'
+ * gradients are not provided).  The objective is L = sum_t <dy_t, y_t> + dlb lb + dzl zl (the pages
+ * train with the load-balance loss and the router z-loss added: mini-moe tutorial, training loop;
+ * FLAME-MoE summary, sec. 2).  Top-k selection, capacity drops and the expert counts pass no
+ * gradient.  All sums in a fixed order; fp32 on CUDA cores.
+ *
+ * moe_combine_backward (FLAME-MoE summary sec. 2: y = routing-weighted sum of the experts):
+ *   dy [T,d] (layer dtype), y_perm [A_max,d] fp32, row_of [T,k], topk_w [T,k] as the forward
+ *   steps left them -> dw [T,k] fp32 = <dy_t, y_perm[row_of[t,j]]> (0 for a dropped slot) and
+ *   dy_perm [A_max,d] (layer dtype): row row_of[t,j] = topk_w[t,j] dy_t, the upstream gradient of
+ *   the expert FFN of that row (rows of no kept slot are left untouched).
+ *
+ * moe_route_backward (the router of moe_route, with cfg's temperature, lb_coef and z_coef):
+ *   x [T,d], w_router [E,d], logit_bias [E] or NULL, topk_idx / topk_w [T,k] and counts [E] as
+ *   moe_route returned them, dw [T,k] from moe_combine_backward, dlb / dzl the weights of the two
+ *   losses in the objective
+ *   -> dz [T,E] fp32, the gradient of the logits (z recomputed in fp32); dw_router [E,d] fp32 =
+ *      dz^T x; dx [T,d] fp32 = dz W_r, the router's part of the input gradient (overwritten).
+ * MOE_ERR_INVALID_ARG for NULL or misaligned pointers, MOE_ERR_UNSUPPORTED outside the shape
+ * limits of the forward. */
+moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const float* y_perm,
+                                const int32_t* row_of, const float* topk_w, float* dw, void* dy_perm,
+                                void* stream);
+moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* w_router,
+                              const float* logit_bias, const int32_t* topk_idx, const float* topk_w,
+                              const int32_t* counts, const float* dw, float dlb, float dzl, float* dz,
+                              float* dw_router, float* dx, void* stream);
 
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);

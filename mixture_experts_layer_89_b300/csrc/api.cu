@@ -633,6 +633,36 @@ moe_status moe_quantize_experts(const void* w, int32_t dtype, int32_t format, in
                                      scale, nonfinite, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const float* y_perm, const int32_t* row_of,
+                                const float* topk_w, float* dw, void* dy_perm, void* stream) {
+  NvtxRange nvtx_range("moe_combine_backward");
+  MOE_TRY(validate(cfg));
+  if (cfg->T > 0 && (!dy || !row_of || !topk_w || !dw || (a_max_of(cfg) > 0 && (!y_perm || !dy_perm))))
+    return MOE_ERR_INVALID_ARG;
+  if (misaligned(dy) || misaligned(y_perm) || misaligned(row_of) || misaligned(topk_w) || misaligned(dw) ||
+      misaligned(dy_perm))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_backward(is_bf16(cfg), dy, y_perm, row_of, topk_w, cfg->T, cfg->d, cfg->k, dw,
+                                             dy_perm, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
+                              const int32_t* topk_idx, const float* topk_w, const int32_t* counts, const float* dw,
+                              float dlb, float dzl, float* dz, float* dw_router, float* dx, void* stream) {
+  NvtxRange nvtx_range("moe_route_backward");
+  MOE_TRY(validate(cfg));
+  if (!w_router || !counts || !dw_router) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!x || !topk_idx || !topk_w || !dw || !dz || !dx)) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(dlb) || !isfinite(dzl)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {x, w_router, logit_bias, topk_idx, topk_w, counts, dw, dz, dw_router, dx};
+  for (const void* p : ps)
+    if (misaligned(p)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_router_backward(is_bf16(cfg), x, w_router, logit_bias, topk_idx, topk_w, counts, dw,
+                                            cfg->T, cfg->d, cfg->E, cfg->k, inv_tau_of(cfg), cfg->lb_coef,
+                                            cfg->z_coef, dlb, dzl, dz, dw_router, dx,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 const char* moe_last_error(void) { return tc_last_error(); }
 
 const char* moe_status_string(moe_status s) {

@@ -120,6 +120,15 @@ struct Projection {
   int wfmt;                                        // weights: 0 layer dtype, 1 int8, 2 E4M3 codes
   const float* scale0; const float* scale1;        // 8-bit weights: fp32 row scales of B0, B1
 };
+// Backward of the routing half: dw [T,k] and dy_perm (rows of kept slots) from dy and y_perm; the
+// router's dz [T,E], dW_r [E,d] and dx [T,d] from dw (see backward.cu).
+cudaError_t launch_combine_backward(bool bf16, const void* dy, const float* y_perm, const int32_t* row_of,
+                                    const float* topk_w, int T, int d, int k, float* dw, void* dy_perm,
+                                    cudaStream_t st);
+cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, const float* lbias, const int32_t* idx,
+                                   const float* tw, const int32_t* counts, const float* dw, int T, int d, int E, int k,
+                                   float inv_tau, float lb_coef, float z_coef, float dlb, float dzl, float* dz,
+                                   float* dwr, float* dx, cudaStream_t st);
 // Per-row scaled 8-bit codes of w [blocks][rows][cols] (fmt 1 int8, 2 E4M3), one CTA per row.
 cudaError_t launch_quantize(bool bf16, int fmt, const void* w, int blocks, int rows, int cols, uint8_t* codes,
                             float* scale, int32_t* nonfinite, cudaStream_t st);

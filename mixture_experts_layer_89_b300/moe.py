@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
         L.moe_route_diagnostics.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_route_stats.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_quantize_experts.argtypes = [_c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p]
+        L.moe_combine_backward.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_route_backward.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float,
+                                         ctypes.c_float, _c_p, _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_last_error.argtypes = []
@@ -86,7 +89,8 @@ def lib() -> ctypes.CDLL:
         for name in ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute",
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
-                     "moe_set_wait_limit", "moe_route_diagnostics", "moe_quantize_experts"):
+                     "moe_set_wait_limit", "moe_route_diagnostics", "moe_quantize_experts", "moe_combine_backward",
+                     "moe_route_backward"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -95,7 +99,8 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
             "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_route_diagnostics",
-            "moe_quantize_experts", "moe_status_string", "moe_last_error")
+            "moe_quantize_experts", "moe_combine_backward", "moe_route_backward", "moe_status_string",
+            "moe_last_error")
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -239,6 +244,18 @@ def moe_quantize_experts(w, fmt: str, blocks: int, rows: int, cols: int, codes, 
     dtype = MOE_BF16 if w.dtype == torch.bfloat16 else MOE_F32
     _check(lib().moe_quantize_experts(_p(w), dtype, EXPERT_WEIGHTS[fmt], int(blocks), int(rows), int(cols),
                                       _p(codes), _p(scale), _p(nonfinite), _s(stream)), "moe_quantize_experts")
+
+
+def moe_combine_backward(cfg, dy, y_perm, row_of, topk_w, dw, dy_perm, stream=None):
+    _check(lib().moe_combine_backward(ctypes.byref(cfg), _p(dy), _p(y_perm), _p(row_of), _p(topk_w), _p(dw),
+                                      _p(dy_perm), _s(stream)), "moe_combine_backward")
+
+
+def moe_route_backward(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, dw, dlb, dzl, dz, dw_router, dx,
+                       stream=None):
+    _check(lib().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx),
+                                    _p(topk_w), _p(counts), _p(dw), float(dlb), float(dzl), _p(dz), _p(dw_router),
+                                    _p(dx), _s(stream)), "moe_route_backward")
 
 
 # ----------------------------------------------------------------------------- convenience
