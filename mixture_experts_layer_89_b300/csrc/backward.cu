@@ -12,7 +12,9 @@
 //             beta mean_t lse_t^2 adds dzl 2 beta lse_t P_te / T; everything is divided by tau;
 //             then dW_r = dz^T x and dx = dz W_r.
 // Every sum runs in a fixed order (results do not depend on scheduling).  fp32 arithmetic on CUDA
-// cores: these are small contractions next to the expert GEMMs (E <= 256 columns).
+// cores (the three contractions -- logits, dz^T x, dz W_r -- through one register-tiled SGEMM):
+// they are small next to the expert GEMMs (E <= 256 columns), and fp32 keeps the gradients within
+// ~1e-6 of the exact ones.
 #include <float.h>
 
 #include "common.cuh"
@@ -54,170 +56,144 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const T* __restrict__ dy, c
   if (lane == 0) dw[warp_g] = s;
 }
 
-// Router gradient of the logits, 32 tokens per CTA: the fp32 logits (K in chunks of 64 columns
-// through shared memory, every logit accumulated in column order), then one warp per token.
-constexpr int BT = 32, BC = 64, BTHREADS = 256;
-constexpr int BMAXO = BT * 256 / BTHREADS;
-
-template <typename T>
-__global__ void __launch_bounds__(BTHREADS) k_router_dz(const T* __restrict__ x, const T* __restrict__ wr,
-                                                        const float* __restrict__ lbias, const int32_t* __restrict__ idx,
-                                                        const float* __restrict__ tw, const int32_t* __restrict__ counts,
-                                                        const float* __restrict__ dw, int Tn, int d, int E, int k,
-                                                        float inv_tau, float lb_coef, float z_coef, float dlb, float dzl,
-                                                        float* __restrict__ dz) {
-  extern __shared__ float sm[];
-  float* xs = sm;                   // [BT][BC+1]
-  float* wsm = xs + BT * (BC + 1);  // [E][BC+1]
-  float* zs = wsm + E * (BC + 1);   // [BT][E+1]
-  float* gp = zs + BT * (E + 1);    // [E]: dlb alpha E f_e / T
+// C [M, N] fp32 (row-major, ldc) = sum_k A(m, k) B(k, n), on CUDA cores: 128 x 128 output tiles,
+// 256 threads with 8 x 8 register tiles (two 4 x 4 quadrants 64 rows / columns apart, so the
+// shared-memory reads are conflict-free float4s), K in steps of 8 through shared memory.  Every
+// output is accumulated in k order.  A(m, k) = A[m lda + k] (AK: K contiguous) or A[k lda + m];
+// B(k, n) = B[k ldb + n] (BN: N contiguous) or B[n ldb + k].
+template <typename TA, typename TB, bool AK, bool BN>
+__global__ void __launch_bounds__(256) k_sgemm(const TA* __restrict__ A, int64_t lda, const TB* __restrict__ B,
+                                               int64_t ldb, float* __restrict__ C, int64_t ldc, int M, int N,
+                                               int K) {
+  __shared__ __align__(16) float As[8][128];
+  __shared__ __align__(16) float Bs[8][128];
   const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * BT;
-  const int nvalid = min(BT, Tn - t0);
-  for (int e = tid; e < E; e += BTHREADS)
+  const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  const int ty = tid >> 4, tx = tid & 15;
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < K; k0 += 8) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 1024 elements of each operand tile, 4 per thread
+      const int i = tid + q * 256;
+      // A tile [128 m][8 k], B tile [8 k][128 n]: index so that consecutive threads read
+      // consecutive addresses of the operand's contiguous dimension
+      const int am = AK ? (i >> 3) : (i & 127), ak = AK ? (i & 7) : (i >> 7);
+      const int gm = m0 + am, gk = k0 + ak;
+      As[ak][am] = (gm < M && gk < K) ? to_f(AK ? A[(size_t)gm * lda + gk] : A[(size_t)gk * lda + gm]) : 0.f;
+      const int bn = BN ? (i & 127) : (i >> 3), bk = BN ? (i >> 7) : (i & 7);
+      const int gn = n0 + bn, gk2 = k0 + bk;
+      Bs[bk][bn] = (gn < N && gk2 < K) ? to_f(BN ? B[(size_t)gk2 * ldb + gn] : B[(size_t)gn * ldb + gk2]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int gm = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    if (gm >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+      if (gn < N) C[(size_t)gm * ldc + gn] = acc[i][j];
+    }
+  }
+}
+
+template <typename TA, typename TB, bool AK, bool BN>
+cudaError_t sgemm(const TA* A, int64_t lda, const TB* B, int64_t ldb, float* C, int64_t ldc, int M, int N, int K,
+                  cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  k_sgemm<TA, TB, AK, BN><<<dim3((N + 127) / 128, (M + 127) / 128), 256, 0, st>>>(A, lda, B, ldb, C, ldc, M, N, K);
+  return cudaGetLastError();
+}
+
+// out[i] = sum over the S slices of part[s][i], in slice order (the split-K partials of dW_r).
+__global__ void __launch_bounds__(256) k_sum_slices(const float* __restrict__ part, int S, size_t n,
+                                                    float* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int q = 0; q < S; ++q) v += part[(size_t)q * n + i];
+    out[i] = v;
+  }
+}
+
+// Router gradient of the logits from the fp32 logits z [T, E] (without the logit bias; recomputed
+// by the SGEMM above, each in column order): one warp per token.
+template <typename T>
+__global__ void __launch_bounds__(256) k_router_dz2(const float* zin, const float* __restrict__ lbias,
+                                                    const int32_t* __restrict__ idx, const float* __restrict__ tw,
+                                                    const int32_t* __restrict__ counts, const float* __restrict__ dw,
+                                                    int Tn, int E, int k, float inv_tau, float lb_coef, float z_coef,
+                                                    float dlb, float dzl, float* dz) {
+  // zin and dz may be the same buffer: each warp reads its token's row before writing it
+  __shared__ float gp[256];  // dlb alpha E f_e / T
+  for (int e = threadIdx.x; e < E; e += 256)
     gp[e] = dlb * lb_coef * (float)E * ((float)counts[e] / ((float)Tn * (float)k)) / (float)Tn;
-  const int nout = BT * E;
-  float acc[BMAXO];
-#pragma unroll
-  for (int j = 0; j < BMAXO; ++j) acc[j] = 0.f;
-  for (int c0 = 0; c0 < d; c0 += BC) {
-    const int cw = min(BC, d - c0);
-    for (int i = tid; i < BT * BC; i += BTHREADS) {
-      const int r = i / BC, c = i - r * BC;
-      xs[r * (BC + 1) + c] = (r < nvalid && c < cw) ? to_f(x[(size_t)(t0 + r) * d + c0 + c]) : 0.f;
-    }
-    for (int i = tid; i < E * BC; i += BTHREADS) {
-      const int e = i / BC, c = i - e * BC;
-      wsm[e * (BC + 1) + c] = c < cw ? to_f(wr[(size_t)e * d + c0 + c]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < BMAXO; ++j) {
-      const int o = tid + j * BTHREADS;
-      if (o < nout) {
-        const int r = o / E, e = o - r * E;
-        const float* xr = xs + r * (BC + 1);
-        const float* we = wsm + e * (BC + 1);
-        float a = acc[j];
-#pragma unroll 8
-        for (int c = 0; c < BC; ++c) a = fmaf(xr[c], we[c], a);
-        acc[j] = a;
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int j = 0; j < BMAXO; ++j) {
-    const int o = tid + j * BTHREADS;
-    if (o < nout) {
-      const int r = o / E, e = o - r * E;
-      const float z = acc[j] + (lbias ? lbias[e] : 0.f);
-      zs[r * (E + 1) + e] = isfinite(z) ? z : kBad;
-    }
-  }
   __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int r = warp; r < nvalid; r += BTHREADS / 32) {
-    const int t = t0 + r;
-    const float* zr = zs + r * (E + 1);
-    float m = kBad;
-    for (int e = lane; e < E; e += 32) m = fmaxf(m, zr[e]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= Tn) return;
+  float zr[8];
+  float m = kBad;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float s = 0.f;
-    for (int e = lane; e < E; e += 32) s += __expf((zr[e] - m) * inv_tau);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float inv_s = 1.f / s;
-    const float lse = m * inv_tau + __logf(s);
-    // sum_e P_e g_e (load-balance term) and sum_j w_j dw_j (renormalised top-k)
-    float pg = 0.f;
-    for (int e = lane; e < E; e += 32) pg = fmaf(__expf((zr[e] - m) * inv_tau) * inv_s, gp[e], pg);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) pg += __shfl_xor_sync(0xffffffffu, pg, o);
-    float wd = 0.f;
-    for (int j = 0; j < k; ++j) wd = fmaf(tw[(size_t)t * k + j], dw[(size_t)t * k + j], wd);
-    const float zc = dzl * 2.f * z_coef * lse / (float)Tn;
-    for (int e = lane; e < E; e += 32) {
-      const float p = __expf((zr[e] - m) * inv_tau) * inv_s;
-      float g = p * (gp[e] - pg) + zc * p;
-      for (int j = 0; j < k; ++j)
-        if (idx[(size_t)t * k + j] == e) g += tw[(size_t)t * k + j] * (dw[(size_t)t * k + j] - wd);
-      dz[(size_t)t * E + e] = g * inv_tau;
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    float z = kBad;
+    if (e < E) {
+      z = zin[(size_t)t * E + e] + (lbias ? lbias[e] : 0.f);
+      if (!isfinite(z)) z = kBad;
     }
+    zr[i] = z;
+    m = fmaxf(m, z);
   }
-}
-
-// dW_r [E, d] = dz^T x: a CTA per block of 32 experts x 64 columns, the tokens in chunks of 32
-// through shared memory, each output summed in token order.
-template <typename T>
-__global__ void __launch_bounds__(256) k_router_dwr(const float* __restrict__ dz, const T* __restrict__ x, int Tn,
-                                                    int d, int E, float* __restrict__ dwr) {
-  __shared__ float zsm[32][33];  // [token][expert]
-  __shared__ float xsm[32][65];  // [token][column]
-  const int e0 = blockIdx.y * 32, c0 = blockIdx.x * 64;
-  const int tid = threadIdx.x;
-  const int el = tid >> 3, cl = (tid & 7) * 8;  // this thread: expert e0 + el, columns c0 + cl .. + 7
-  float acc[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int t0 = 0; t0 < Tn; t0 += 32) {
-    for (int i = tid; i < 32 * 32; i += 256) {
-      const int tt = i >> 5, e = i & 31;
-      zsm[tt][e] = (t0 + tt < Tn && e0 + e < E) ? dz[(size_t)(t0 + tt) * E + e0 + e] : 0.f;
-    }
-    for (int i = tid; i < 32 * 64; i += 256) {
-      const int tt = i >> 6, c = i & 63;
-      xsm[tt][c] = (t0 + tt < Tn && c0 + c < d) ? to_f(x[(size_t)(t0 + tt) * d + c0 + c]) : 0.f;
-    }
-    __syncthreads();
-    for (int tt = 0; tt < 32; ++tt) {
-      const float g = zsm[tt][el];
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float p[8], s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, xsm[tt][cl + i], acc[i]);
-    }
-    __syncthreads();
+  for (int i = 0; i < 8; ++i) {
+    p[i] = lane + 32 * i < E ? __expf((zr[i] - m) * inv_tau) : 0.f;
+    s += p[i];
   }
-  if (e0 + el < E) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + cl + i < d) dwr[(size_t)(e0 + el) * d + c0 + cl + i] = acc[i];
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float inv_s = 1.f / s;
+  const float lse = m * inv_tau + __logf(s);
+  float pg = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    p[i] *= inv_s;
+    if (lane + 32 * i < E) pg = fmaf(p[i], gp[lane + 32 * i], pg);
   }
-}
-
-// dx [T, d] = dz W_r: a CTA per block of 32 tokens x 64 columns, the experts in order.
-template <typename T>
-__global__ void __launch_bounds__(256) k_router_dx(const float* __restrict__ dz, const T* __restrict__ wr, int Tn,
-                                                   int d, int E, float* __restrict__ dx) {
-  __shared__ float zsm[32][33];  // [token][expert chunk]
-  __shared__ float wsm[32][65];  // [expert chunk][column]
-  const int t0 = blockIdx.y * 32, c0 = blockIdx.x * 64;
-  const int tid = threadIdx.x;
-  const int tl = tid >> 3, cl = (tid & 7) * 8;
-  float acc[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int e0 = 0; e0 < E; e0 += 32) {
-    for (int i = tid; i < 32 * 32; i += 256) {
-      const int tt = i >> 5, e = i & 31;
-      zsm[tt][e] = (t0 + tt < Tn && e0 + e < E) ? dz[(size_t)(t0 + tt) * E + e0 + e] : 0.f;
-    }
-    for (int i = tid; i < 32 * 64; i += 256) {
-      const int e = i >> 6, c = i & 63;
-      wsm[e][c] = (e0 + e < E && c0 + c < d) ? to_f(wr[(size_t)(e0 + e) * d + c0 + c]) : 0.f;
-    }
-    __syncthreads();
-    for (int e = 0; e < 32; ++e) {
-      const float g = zsm[tl][e];
+  for (int o = 16; o; o >>= 1) pg += __shfl_xor_sync(0xffffffffu, pg, o);
+  float wd = 0.f;
+  for (int j = 0; j < k; ++j) wd = fmaf(tw[(size_t)t * k + j], dw[(size_t)t * k + j], wd);
+  const float zc = dzl * 2.f * z_coef * lse / (float)Tn;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, wsm[e][cl + i], acc[i]);
-    }
-    __syncthreads();
-  }
-  if (t0 + tl < Tn) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + cl + i < d) dx[(size_t)(t0 + tl) * d + c0 + cl + i] = acc[i];
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (e >= E) continue;
+    float g = p[i] * (gp[e] - pg) + zc * p[i];
+    for (int j = 0; j < k; ++j)
+      if (idx[(size_t)t * k + j] == e) g += tw[(size_t)t * k + j] * (dw[(size_t)t * k + j] - wd);
+    dz[(size_t)t * E + e] = g * inv_tau;
   }
 }
 
@@ -229,19 +205,37 @@ cudaError_t router_bwd_t(const void* x, const void* wr, const float* lbias, cons
   const T* xt = static_cast<const T*>(x);
   const T* wt = static_cast<const T*>(wr);
   if (T_ > 0) {
-    const size_t smem = sizeof(float) * ((size_t)BT * (BC + 1) + (size_t)E * (BC + 1) + (size_t)BT * (E + 1) + E);
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_router_dz<T>), smem);
+    // z [T, E] = x W_r^T into dz (then overwritten by the logits' gradient, token by token)
+    cudaError_t e = sgemm<T, T, true, false>(xt, d, wt, d, dz, E, T_, E, d, st);
     if (e != cudaSuccess) return e;
-    k_router_dz<T><<<(T_ + BT - 1) / BT, BTHREADS, smem, st>>>(xt, wt, lbias, idx, tw, counts, dw, T_, d, E, k,
-                                                               inv_tau, lb_coef, z_coef, dlb, dzl, dz);
+    k_router_dz2<T><<<(T_ + 7) / 8, 256, 0, st>>>(dz, lbias, idx, tw, counts, dw, T_, E, k, inv_tau, lb_coef, z_coef,
+                                                  dlb, dzl, dz);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_router_dx<T><<<dim3((d + 63) / 64, (T_ + 31) / 32), 256, 0, st>>>(dz, wt, T_, d, E, dx);
-    e = cudaGetLastError();
+    // dW_r = dz^T x: the tokens split into S slices (more CTAs than the E x d output alone gives),
+    // the slices' partials in the dx buffer (S E <= T floats per column), summed in slice order
+    const int S = T_ >= 8 * E ? 8 : (T_ >= 2 * E ? T_ / E : 1);
+    if (S == 1) {
+      e = sgemm<float, T, false, true>(dz, E, xt, d, dwr, d, E, d, T_, st);
+    } else {
+      const int ts = (T_ + S - 1) / S;
+      for (int q = 0; q < S && e == cudaSuccess; ++q) {
+        const int t0 = q * ts, tn = min(ts, T_ - t0);
+        if (tn > 0)
+          e = sgemm<float, T, false, true>(dz + (size_t)t0 * E, E, xt + (size_t)t0 * d, d, dx + (size_t)q * E * d, d, E,
+                                           d, tn, st);
+        else
+          e = cudaMemsetAsync(dx + (size_t)q * E * d, 0, sizeof(float) * (size_t)E * d, st);
+      }
+      if (e == cudaSuccess) {
+        k_sum_slices<<<592, 256, 0, st>>>(dx, S, (size_t)E * d, dwr);
+        e = cudaGetLastError();
+      }
+    }
     if (e != cudaSuccess) return e;
+    return sgemm<float, T, true, true>(dz, E, wt, d, dx, d, T_, d, E, st);  // dx = dz W_r (overwrites the partials)
   }
-  k_router_dwr<T><<<dim3((d + 63) / 64, (E + 31) / 32), 256, 0, st>>>(dz, xt, T_, d, E, dwr);
-  return cudaGetLastError();
+  return cudaMemsetAsync(dwr, 0, sizeof(float) * (size_t)E * d, st);
 }
 }  // namespace
 
