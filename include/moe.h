@@ -326,6 +326,37 @@ moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* 
                               const int32_t* counts, const float* dw, float dlb, float dzl, float* dz,
                               float* dw_router, float* dx, void* stream);
 
+/* Gradients of the expert FFN weights, fp32, in the layouts of the weights in moe_weights. */
+typedef struct {
+  float* dw_up;    /* [E,dff,d]                                      */
+  float* dw_gate;  /* [E,dff,d] (SwiGLU) or NULL                     */
+  float* dw_down;  /* [E,d,dff]                                      */
+  float* db_up;    /* [E,dff] (has_bias) or NULL                     */
+  float* db_down;  /* [E,d]   (has_bias) or NULL                     */
+  float* dws_up;   /* shared [S,dff,d] or NULL when n_shared == 0    */
+  float* dws_gate; /* shared [S,dff,d] (SwiGLU) or NULL              */
+  float* dws_down; /* shared [S,d,dff] or NULL                       */
+} moe_expert_grads;
+
+/* moe_expert_ffn_backward: the backward of the expert FFNs of moe_expert_ffn and of the shared
+ * experts (the GELU FFN of the GPT-4 2% article, sec. 3.1, and the SwiGLU FFN of the same section;
+ * shared experts see every token with weight 1, DeepSeekMoE in the OpenMythos article, sec. 3.2):
+ *   x [T,d], x_perm [A_max,d], offsets [E+1] and row_of [T,k] as moe_permute left them, dy [T,d]
+ *   the layer output's upstream gradient, dy_perm [A_max,d] from moe_combine_backward
+ *   -> every gradient of g (overwritten; an expert with no rows gets zeros) and dx [T,d] fp32, to
+ *      which the experts' part of the input gradient is ADDED (first the routed experts, each
+ *      token's kept slots in slot order, then the shared experts in order), so that dx after
+ *      moe_route_backward and this call is the layer's input gradient.
+ * The pre-activations are recomputed in fp32 from x_perm / x; every sum runs in a fixed order.
+ * scratch: moe_expert_backward_scratch_size bytes of device memory, 256-byte aligned.
+ * MOE_ERR_UNSUPPORTED with a backup expert or 8-bit expert weights; MOE_ERR_INVALID_ARG for a
+ * NULL or misaligned (16-byte) pointer that the config needs. */
+moe_status moe_expert_backward_scratch_size(const moe_config* cfg, size_t* bytes);
+moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, const void* x,
+                                   const void* x_perm, const int32_t* offsets, const int32_t* row_of,
+                                   const void* dy, const void* dy_perm, const moe_expert_grads* g,
+                                   float* dx, void* scratch, void* stream);
+
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);
 

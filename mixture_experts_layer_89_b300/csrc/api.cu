@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -119,6 +120,32 @@ WsLayout layout(const moe_config* c) {
   L.y_perm = take(A * d * 4);
   L.h_sh = take(T * S * f * elt(c));
   L.y_sh = take(S ? T * d * 4 : 0);
+  L.total = off;
+  return L;
+}
+
+// Scratch of the expert FFN backward: three [R, dff] fp32 buffers (pre-activations, then their
+// gradients and h) for R = max(A_max, T when there are shared experts) rows, and the permuted
+// rows' input gradients [A_max, d] fp32.
+struct ExpertBwdScratch {
+  size_t s0, s1, s2, dx_perm, total;
+};
+
+ExpertBwdScratch expert_bwd_scratch(const moe_config* c) {
+  ExpertBwdScratch L;
+  const size_t A = (size_t)a_max_of(c);
+  const size_t R = std::max(A, c->n_shared > 0 ? (size_t)c->T : (size_t)0);
+  const size_t f = (size_t)c->dff, d = (size_t)c->d;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t a = off;
+    off += align256(bytes);
+    return a;
+  };
+  L.s0 = take(R * f * 4);
+  L.s1 = take(c->act == MOE_ACT_SWIGLU ? R * f * 4 : 0);
+  L.s2 = take(R * f * 4);
+  L.dx_perm = take(A * d * 4);
   L.total = off;
   return L;
 }
@@ -661,6 +688,54 @@ moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* 
                                             cfg->T, cfg->d, cfg->E, cfg->k, inv_tau_of(cfg), cfg->lb_coef,
                                             cfg->z_coef, dlb, dzl, dz, dw_router, dx,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_backward_scratch_size(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  if (cfg->backup_expert || cfg->expert_weights != MOE_EXPERT_WEIGHTS_DTYPE) return MOE_ERR_UNSUPPORTED;
+  *bytes = expert_bwd_scratch(cfg).total;
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, const void* x, const void* x_perm,
+                                   const int32_t* offsets, const int32_t* row_of, const void* dy,
+                                   const void* dy_perm, const moe_expert_grads* g, float* dx, void* scratch,
+                                   void* stream) {
+  NvtxRange nvtx_range("moe_expert_ffn_backward");
+  MOE_TRY(validate(cfg));
+  if (cfg->backup_expert || cfg->expert_weights != MOE_EXPERT_WEIGHTS_DTYPE) return MOE_ERR_UNSUPPORTED;
+  if (!w || !g) return MOE_ERR_INVALID_ARG;
+  const bool glu = cfg->act == MOE_ACT_SWIGLU, routed = a_max_of(cfg) > 0, S = cfg->n_shared > 0;
+  if (!w->w_up || !w->w_down || !g->dw_up || !g->dw_down || (glu && (!w->w_gate || !g->dw_gate)))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->has_bias && (!w->b_up || !g->db_up || !g->db_down)) return MOE_ERR_INVALID_ARG;
+  if (S && (!w->ws_up || !w->ws_down || !g->dws_up || !g->dws_down || (glu && (!w->ws_gate || !g->dws_gate))))
+    return MOE_ERR_INVALID_ARG;
+  if (routed && (!x_perm || !offsets || !row_of || !dy_perm || !dx || !scratch)) return MOE_ERR_INVALID_ARG;
+  if (S && cfg->T > 0 && (!x || !dy || !dx || !scratch)) return MOE_ERR_INVALID_ARG;
+  const void* ps[] = {x, x_perm, offsets, row_of, dy, dy_perm, dx, scratch, w->w_up, w->w_gate, w->w_down,
+                      w->b_up, w->ws_up, w->ws_gate, w->ws_down, g->dw_up, g->dw_gate, g->dw_down, g->db_up,
+                      g->db_down, g->dws_up, g->dws_gate, g->dws_down};
+  for (const void* p : ps)
+    if (misaligned(p)) return MOE_ERR_INVALID_ARG;
+  const ExpertBwdScratch L = expert_bwd_scratch(cfg);
+  const int64_t cap = capacity_exact(cfg->capacity_factor, cfg->T, cfg->k, cfg->E);
+  ExpertBackward b{};
+  b.T = cfg->T, b.d = cfg->d, b.E = cfg->E, b.k = cfg->k, b.dff = cfg->dff, b.n_shared = cfg->n_shared;
+  b.act = glu ? ACT_SWIGLU : ACT_GELU;
+  b.rows_bound = routed ? (int)(cap >= 0 && cap < cfg->T ? cap : cfg->T) : 0;
+  b.x = x, b.x_perm = x_perm, b.dy = dy, b.dy_perm = dy_perm, b.offsets = offsets, b.row_of = row_of;
+  b.w_up = w->w_up, b.w_gate = glu ? w->w_gate : nullptr, b.w_down = w->w_down;
+  b.b_up = cfg->has_bias ? w->b_up : nullptr;
+  b.ws_up = w->ws_up, b.ws_gate = glu ? w->ws_gate : nullptr, b.ws_down = w->ws_down;
+  b.dw_up = g->dw_up, b.dw_gate = glu ? g->dw_gate : nullptr, b.dw_down = g->dw_down;
+  b.db_up = cfg->has_bias ? g->db_up : nullptr, b.db_down = cfg->has_bias ? g->db_down : nullptr;
+  b.dws_up = g->dws_up, b.dws_gate = glu ? g->dws_gate : nullptr, b.dws_down = g->dws_down;
+  b.dx = dx;
+  b.dx_perm = at<float>(scratch, L.dx_perm);
+  b.s0 = at<float>(scratch, L.s0), b.s1 = at<float>(scratch, L.s1), b.s2 = at<float>(scratch, L.s2);
+  return cuda_status(launch_expert_backward(is_bf16(cfg), b, static_cast<cudaStream_t>(stream)));
 }
 
 const char* moe_last_error(void) { return tc_last_error(); }

@@ -61,14 +61,42 @@ __global__ void __launch_bounds__(256) k_combine_bwd(const T* __restrict__ dy, c
 // shared-memory reads are conflict-free float4s), K in steps of 8 through shared memory.  Every
 // output is accumulated in k order.  A(m, k) = A[m lda + k] (AK: K contiguous) or A[k lda + m];
 // B(k, n) = B[k ldb + n] (BN: N contiguous) or B[n ldb + k].
+// Grouped form (blockIdx.z = group g, rows of g = [off[g], off[g + 1]) of the permuted rows):
+//   rows on M: A and C rows offset by off[g] (A K-contiguous), B offset by g b_stride, M = rows of g;
+//   rows on K: A and B rows offset by off[g] (A M-contiguous, B N-contiguous), C offset by
+//              g c_stride, K = rows of g.
+// beta = 1 adds the product to C instead of overwriting it.
+struct GemmGroups {
+  const int32_t* off;  // NULL: one plain problem
+  int rows_on_k;
+  int64_t b_stride, c_stride;
+  int beta;
+};
+
 template <typename TA, typename TB, bool AK, bool BN>
 __global__ void __launch_bounds__(256) k_sgemm(const TA* __restrict__ A, int64_t lda, const TB* __restrict__ B,
                                                int64_t ldb, float* __restrict__ C, int64_t ldc, int M, int N,
-                                               int K) {
+                                               int K, const GemmGroups gr) {
   __shared__ __align__(16) float As[8][128];
   __shared__ __align__(16) float Bs[8][128];
   const int tid = threadIdx.x;
   const int m0 = blockIdx.y * 128, n0 = blockIdx.x * 128;
+  if (gr.off) {
+    const int g = blockIdx.z;
+    const int lo = gr.off[g], hi = gr.off[g + 1];
+    if (gr.rows_on_k) {
+      K = hi - lo;
+      A += (size_t)lo * lda;
+      B += (size_t)lo * ldb;
+      C += (size_t)g * gr.c_stride;
+    } else {
+      M = hi - lo;
+      A += (size_t)lo * lda;
+      C += (size_t)lo * ldc;
+      B += (size_t)g * gr.b_stride;
+    }
+    if (m0 >= M) return;
+  }
   const int ty = tid >> 4, tx = tid & 15;
   float acc[8][8];
 #pragma unroll
@@ -111,16 +139,18 @@ __global__ void __launch_bounds__(256) k_sgemm(const TA* __restrict__ A, int64_t
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int gn = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
-      if (gn < N) C[(size_t)gm * ldc + gn] = acc[i][j];
+      if (gn < N) C[(size_t)gm * ldc + gn] = gr.beta ? C[(size_t)gm * ldc + gn] + acc[i][j] : acc[i][j];
     }
   }
 }
 
+// M: the rows (plain), or a bound on any group's rows (rows on M); G groups (1 when plain).
 template <typename TA, typename TB, bool AK, bool BN>
 cudaError_t sgemm(const TA* A, int64_t lda, const TB* B, int64_t ldb, float* C, int64_t ldc, int M, int N, int K,
-                  cudaStream_t st) {
-  if (M <= 0 || N <= 0) return cudaSuccess;
-  k_sgemm<TA, TB, AK, BN><<<dim3((N + 127) / 128, (M + 127) / 128), 256, 0, st>>>(A, lda, B, ldb, C, ldc, M, N, K);
+                  cudaStream_t st, const GemmGroups& gr = GemmGroups{nullptr, 0, 0, 0, 0}, int G = 1) {
+  if (M <= 0 || N <= 0 || G <= 0) return cudaSuccess;
+  k_sgemm<TA, TB, AK, BN><<<dim3((N + 127) / 128, (M + 127) / 128, G), 256, 0, st>>>(A, lda, B, ldb, C, ldc, M, N, K,
+                                                                                     gr);
   return cudaGetLastError();
 }
 
@@ -237,6 +267,166 @@ cudaError_t router_bwd_t(const void* x, const void* wr, const float* lbias, cons
   }
   return cudaMemsetAsync(dwr, 0, sizeof(float) * (size_t)E * d, st);
 }
+
+// Activation backward, elementwise over the rows of each group (blockIdx.y = group; rows
+// [off[g], off[g + 1]), or [0, rows) with off == NULL), in place:
+//   SwiGLU: gate and up pre-activations p0 = g, p1 = u and dh -> p0 = dg = dh u silu'(g),
+//           p1 = du = dh silu(g), dh = h = silu(g) u;
+//   GELU:   pre-activation p0 = a (bias b[g] not yet added) and dh -> p0 = da = dh gelu'(a + b),
+//           dh = h = gelu(a + b).
+// silu(g) = g sigma(g), silu'(g) = sigma(g) (1 + g (1 - sigma(g))); gelu(a) = a Phi(a),
+// gelu'(a) = Phi(a) + a phi(a) with the standard normal CDF Phi and density phi.
+template <int ACT, typename T>
+__global__ void __launch_bounds__(256) k_act_bwd(float* __restrict__ p0, float* __restrict__ p1,
+                                                 float* __restrict__ dh, const T* __restrict__ bias,
+                                                 const int32_t* __restrict__ off, int rows, int dff) {
+  const int g = blockIdx.y;
+  const int lo = off ? off[g] : 0, hi = off ? off[g + 1] : rows;
+  for (int r = lo + (int)blockIdx.x; r < hi; r += gridDim.x) {
+    const size_t base = (size_t)r * dff;
+    for (int c = threadIdx.x; c < dff; c += blockDim.x) {
+      const size_t i = base + c;
+      const float up = dh[i];
+      if (ACT == ACT_SWIGLU) {
+        const float gv = p0[i], uv = p1[i];
+        const float sg = 1.f / (1.f + expf(-gv));
+        const float si = gv * sg;
+        p0[i] = up * uv * (sg * (1.f + gv * (1.f - sg)));
+        p1[i] = up * si;
+        dh[i] = si * uv;
+      } else {
+        const float a = p0[i] + (bias ? to_f(bias[(size_t)g * dff + c]) : 0.f);
+        const float cdf = 0.5f * (1.f + erff(a * 0.70710678118654752f));
+        const float pdf = 0.39894228040143268f * expf(-0.5f * a * a);
+        p0[i] = up * (cdf + a * pdf);
+        dh[i] = a * cdf;
+      }
+    }
+  }
+}
+
+// dst [G, n] = the column sums of each group's rows of src [rows, ld] (rows summed in order).
+template <typename T>
+__global__ void __launch_bounds__(256) k_group_colsum(const T* __restrict__ src, int64_t ld,
+                                                      const int32_t* __restrict__ off, int n,
+                                                      float* __restrict__ dst) {
+  const int g = blockIdx.y, c = blockIdx.x * 256 + threadIdx.x;
+  if (c >= n) return;
+  float s = 0.f;
+  for (int r = off[g]; r < off[g + 1]; ++r) s += to_f(src[(size_t)r * ld + c]);
+  dst[(size_t)g * n + c] = s;
+}
+
+// dx [T, d] += the input gradients of each token's kept rows, in slot order.
+__global__ void __launch_bounds__(256) k_scatter_rows_add(const float* __restrict__ dxp,
+                                                          const int32_t* __restrict__ row_of, int k, int d,
+                                                          float* __restrict__ dx) {
+  const int t = blockIdx.x;
+  int rows[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) rows[j] = j < k ? row_of[(size_t)t * k + j] : -1;
+  for (int c = threadIdx.x; c < d; c += 256) {
+    float v = dx[(size_t)t * d + c];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (rows[j] >= 0) v += dxp[(size_t)rows[j] * d + c];
+    dx[(size_t)t * d + c] = v;
+  }
+}
+
+// The expert FFN backward of one set of rows: G groups of rows (the routed experts over the
+// permuted rows, by off) or one plain problem of `rows` rows (a shared expert, off == NULL), the
+// weights of group g at g * (dff d).  xr [rows, d] the FFN inputs, dyr [rows, d] the upstream
+// gradients of its outputs.  Writes dW_up, dW_gate, dW_down (and the bias gradients) of every
+// group, and dxr = du W_up + dg W_gate (beta_dx = 1: added to dxr).  s0, s1, s2 [rows, dff] fp32.
+template <typename T>
+cudaError_t ffn_bwd_rows(int act, const T* xr, const T* dyr, const int32_t* off, int G, int rows_bound, int d,
+                         int dff, const T* wu, const T* wg, const T* wd, const T* bu, float* dwu, float* dwg,
+                         float* dwd, float* dbu, float* dbd, float* dxr, int beta_dx, float* s0, float* s1,
+                         float* s2, cudaStream_t st) {
+  const bool glu = act == ACT_SWIGLU;
+  const int64_t wstride = (int64_t)dff * d;
+  const GemmGroups on_m{off, 0, wstride, 0, 0}, on_k{off, 1, 0, wstride, 0};
+  const GemmGroups on_m_acc{off, 0, wstride, 0, 1};
+  const GemmGroups plain{nullptr, 0, 0, 0, 0}, plain_acc{nullptr, 0, 0, 0, 1};
+  const bool grouped = off != nullptr;
+  // pre-activations (fp32, K = d in order): u or a = xr W_up^T, g = xr W_gate^T; dh = dyr W_down
+  float* pu = glu ? s1 : s0;
+  cudaError_t e = sgemm<T, T, true, false>(xr, d, wu, d, pu, dff, rows_bound, dff, d, st, grouped ? on_m : plain, G);
+  if (e == cudaSuccess && glu)
+    e = sgemm<T, T, true, false>(xr, d, wg, d, s0, dff, rows_bound, dff, d, st, grouped ? on_m : plain, G);
+  if (e == cudaSuccess)
+    e = sgemm<T, T, true, true>(dyr, d, wd, dff, s2, dff, rows_bound, dff, d, st, grouped ? on_m : plain, G);
+  if (e != cudaSuccess) return e;
+  const dim3 eg(grouped ? 64 : 592, G);
+  if (glu)
+    k_act_bwd<ACT_SWIGLU, T><<<eg, 256, 0, st>>>(s0, s1, s2, nullptr, off, rows_bound, dff);
+  else
+    k_act_bwd<ACT_GELU, T><<<eg, 256, 0, st>>>(s0, nullptr, s2, bu, off, rows_bound, dff);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (dbu) {  // biases: routed GELU experts only
+    k_group_colsum<float><<<dim3((dff + 255) / 256, G), 256, 0, st>>>(s0, dff, off, dff, dbu);
+    k_group_colsum<T><<<dim3((d + 255) / 256, G), 256, 0, st>>>(dyr, d, off, d, dbd);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // weight gradients (K = the group's rows, in row order): dW_down = dyr^T h, dW_up = du^T xr,
+  // dW_gate = dg^T xr
+  const int kr = grouped ? 0 : rows_bound;
+  e = sgemm<T, float, false, true>(dyr, d, s2, dff, dwd, dff, d, dff, kr, st, grouped ? on_k : plain, G);
+  if (e == cudaSuccess)
+    e = sgemm<float, T, false, true>(pu, dff, xr, d, dwu, d, dff, d, kr, st, grouped ? on_k : plain, G);
+  if (e == cudaSuccess && glu)
+    e = sgemm<float, T, false, true>(s0, dff, xr, d, dwg, d, dff, d, kr, st, grouped ? on_k : plain, G);
+  if (e != cudaSuccess) return e;
+  // input gradient (K = dff in order): dxr (+)= du W_up, then + dg W_gate
+  e = sgemm<float, T, true, true>(pu, dff, wu, d, dxr, d, rows_bound, d, dff, st,
+                                  grouped ? (beta_dx ? on_m_acc : on_m) : (beta_dx ? plain_acc : plain), G);
+  if (e == cudaSuccess && glu)
+    e = sgemm<float, T, true, true>(s0, dff, wg, d, dxr, d, rows_bound, d, dff, st, grouped ? on_m_acc : plain_acc,
+                                    G);
+  return e;
+}
+
+template <typename T>
+cudaError_t expert_bwd_t(const ExpertBackward& b, cudaStream_t st) {
+  const T* x = static_cast<const T*>(b.x);
+  const T* dy = static_cast<const T*>(b.dy);
+  cudaError_t e = cudaSuccess;
+  if (b.rows_bound > 0) {
+    e = ffn_bwd_rows<T>(b.act, static_cast<const T*>(b.x_perm), static_cast<const T*>(b.dy_perm), b.offsets, b.E,
+                        b.rows_bound, b.d, b.dff, static_cast<const T*>(b.w_up), static_cast<const T*>(b.w_gate),
+                        static_cast<const T*>(b.w_down), static_cast<const T*>(b.b_up), b.dw_up, b.dw_gate,
+                        b.dw_down, b.db_up, b.db_down, b.dx_perm, 0, b.s0, b.s1, b.s2, st);
+    if (e != cudaSuccess) return e;
+    k_scatter_rows_add<<<b.T, 256, 0, st>>>(b.dx_perm, b.row_of, b.k, b.d, b.dx);
+    e = cudaGetLastError();
+  } else {  // nothing routed: every expert's gradient is zero
+    const size_t wsz = sizeof(float) * (size_t)b.E * b.dff * b.d;
+    e = cudaMemsetAsync(b.dw_up, 0, wsz, st);
+    if (e == cudaSuccess && b.dw_gate) e = cudaMemsetAsync(b.dw_gate, 0, wsz, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b.dw_down, 0, wsz, st);
+    if (e == cudaSuccess && b.db_up) e = cudaMemsetAsync(b.db_up, 0, sizeof(float) * (size_t)b.E * b.dff, st);
+    if (e == cudaSuccess && b.db_down) e = cudaMemsetAsync(b.db_down, 0, sizeof(float) * (size_t)b.E * b.d, st);
+  }
+  // shared experts: every token, weight 1, added to dx one expert after another
+  const size_t sw = (size_t)b.dff * b.d;
+  for (int s = 0; s < b.n_shared && e == cudaSuccess; ++s) {
+    if (b.T == 0) {
+      e = cudaMemsetAsync(b.dws_up + s * sw, 0, sizeof(float) * sw, st);
+      if (e == cudaSuccess && b.dws_gate) e = cudaMemsetAsync(b.dws_gate + s * sw, 0, sizeof(float) * sw, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(b.dws_down + s * sw, 0, sizeof(float) * sw, st);
+      continue;
+    }
+    e = ffn_bwd_rows<T>(b.act, x, dy, nullptr, 1, b.T, b.d, b.dff, static_cast<const T*>(b.ws_up) + s * sw,
+                        b.ws_gate ? static_cast<const T*>(b.ws_gate) + s * sw : nullptr,
+                        static_cast<const T*>(b.ws_down) + s * sw, nullptr, b.dws_up + s * sw,
+                        b.dws_gate ? b.dws_gate + s * sw : nullptr, b.dws_down + s * sw, nullptr, nullptr, b.dx, 1,
+                        b.s0, b.s1, b.s2, st);
+  }
+  return e;
+}
 }  // namespace
 
 cudaError_t launch_combine_backward(bool bf16, const void* dy, const float* y_perm, const int32_t* row_of,
@@ -264,6 +454,11 @@ cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, con
                                        dzl, dz, dwr, dx, st);
   return router_bwd_t<float>(x, wr, lbias, idx, tw, counts, dw, T, d, E, k, inv_tau, lb_coef, z_coef, dlb, dzl, dz,
                              dwr, dx, st);
+}
+
+cudaError_t launch_expert_backward(bool bf16, const ExpertBackward& b, cudaStream_t st) {
+  if (b.k < 1 || b.k > 8) return cudaErrorInvalidValue;
+  return bf16 ? expert_bwd_t<__nv_bfloat16>(b, st) : expert_bwd_t<float>(b, st);
 }
 
 }  // namespace moe

@@ -129,6 +129,19 @@ cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, con
                                    const float* tw, const int32_t* counts, const float* dw, int T, int d, int E, int k,
                                    float inv_tau, float lb_coef, float z_coef, float dlb, float dzl, float* dz,
                                    float* dwr, float* dx, cudaStream_t st);
+// Backward of the expert FFNs (routed over the permuted rows, then the shared experts over all
+// tokens).  Weights and activations in the layer dtype, gradients fp32; act is ACT_GELU or
+// ACT_SWIGLU; rows_bound bounds any expert's rows (0: no routed rows); s0..s2 hold
+// max(A_max, T) x dff floats each (s1 SwiGLU only), dx_perm A_max x d.
+struct ExpertBackward {
+  int T, d, E, k, dff, n_shared, act, rows_bound;
+  const void *x, *x_perm, *dy, *dy_perm;
+  const int32_t *offsets, *row_of;
+  const void *w_up, *w_gate, *w_down, *b_up, *ws_up, *ws_gate, *ws_down;
+  float *dw_up, *dw_gate, *dw_down, *db_up, *db_down, *dws_up, *dws_gate, *dws_down;
+  float *dx, *dx_perm, *s0, *s1, *s2;
+};
+cudaError_t launch_expert_backward(bool bf16, const ExpertBackward& b, cudaStream_t st);
 // Per-row scaled 8-bit codes of w [blocks][rows][cols] (fmt 1 int8, 2 E4M3), one CTA per row.
 cudaError_t launch_quantize(bool bf16, int fmt, const void* w, int blocks, int rows, int cols, uint8_t* codes,
                             float* scale, int32_t* nonfinite, cudaStream_t st);

@@ -36,6 +36,12 @@ class MoeWeights(ctypes.Structure):
                 ("bb_down", _c_p), ("s_up", _c_p), ("s_gate", _c_p), ("s_down", _c_p), ("ss_up", _c_p),
                 ("ss_gate", _c_p), ("ss_down", _c_p), ("sb_up", _c_p), ("sb_gate", _c_p), ("sb_down", _c_p)]
 
+
+class MoeExpertGrads(ctypes.Structure):
+    _fields_ = [("dw_up", _c_p), ("dw_gate", _c_p), ("dw_down", _c_p), ("db_up", _c_p), ("db_down", _c_p),
+                ("dws_up", _c_p), ("dws_gate", _c_p), ("dws_down", _c_p)]
+
+
 # expert weight storage (moe_expert_weights)
 EXPERT_WEIGHTS = {"dtype": 0, "int8": 1, "e4m3": 2}
 
@@ -82,6 +88,9 @@ def lib() -> ctypes.CDLL:
         L.moe_combine_backward.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_route_backward.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float,
                                          ctypes.c_float, _c_p, _c_p, _c_p, _c_p]
+        L.moe_expert_backward_scratch_size.argtypes = [cfgp, P(ctypes.c_size_t)]
+        L.moe_expert_ffn_backward.argtypes = [cfgp, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                              P(MoeExpertGrads), _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_last_error.argtypes = []
@@ -90,7 +99,7 @@ def lib() -> ctypes.CDLL:
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
                      "moe_set_wait_limit", "moe_route_diagnostics", "moe_quantize_experts", "moe_combine_backward",
-                     "moe_route_backward"):
+                     "moe_route_backward", "moe_expert_backward_scratch_size", "moe_expert_ffn_backward"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -99,8 +108,8 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
             "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_route_diagnostics",
-            "moe_quantize_experts", "moe_combine_backward", "moe_route_backward", "moe_status_string",
-            "moe_last_error")
+            "moe_quantize_experts", "moe_combine_backward", "moe_route_backward",
+            "moe_expert_backward_scratch_size", "moe_expert_ffn_backward", "moe_status_string", "moe_last_error")
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -256,6 +265,29 @@ def moe_route_backward(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, d
     _check(lib().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx),
                                     _p(topk_w), _p(counts), _p(dw), float(dlb), float(dzl), _p(dz), _p(dw_router),
                                     _p(dx), _s(stream)), "moe_route_backward")
+
+
+def moe_expert_backward_scratch_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_expert_backward_scratch_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_expert_backward_scratch_size")
+    return int(n.value)
+
+
+def make_expert_grads(g: Dict[str, Optional[torch.Tensor]]) -> MoeExpertGrads:
+    """MoeExpertGrads over the fp32 tensors of ``g`` (keys dw_up, dw_gate, dw_down, db_up, db_down,
+    dws_up, dws_gate, dws_down; missing keys are NULL)."""
+    s = MoeExpertGrads(*[_p(g.get(n)) for n in ("dw_up", "dw_gate", "dw_down", "db_up", "db_down", "dws_up",
+                                                "dws_gate", "dws_down")])
+    s._keep = g
+    return s
+
+
+def moe_expert_ffn_backward(cfg, weights: MoeWeights, x, x_perm, offsets, row_of, dy, dy_perm,
+                            grads: MoeExpertGrads, dx, scratch, stream=None):
+    _check(lib().moe_expert_ffn_backward(ctypes.byref(cfg), ctypes.byref(weights), _p(x), _p(x_perm), _p(offsets),
+                                         _p(row_of), _p(dy), _p(dy_perm), ctypes.byref(grads), _p(dx),
+                                         _p(scratch), _s(stream)), "moe_expert_ffn_backward")
 
 
 # ----------------------------------------------------------------------------- convenience
