@@ -124,28 +124,49 @@ WsLayout layout(const moe_config* c) {
   return L;
 }
 
-// Scratch of the expert FFN backward: three [R, dff] fp32 buffers (pre-activations, then their
-// gradients and h) for R = max(A_max, T when there are shared experts) rows, and the permuted
-// rows' input gradients [A_max, d] fp32.
+// Scratch of the expert FFN backward: a status word; three [R, dff] fp32 buffers (pre-activations,
+// then their gradients and h) for R = max(A_max, T when there are shared experts) rows, and the
+// permuted rows' input gradients [A_max, d] fp32.  bf16 layers add the tensor-core operands: the
+// padded column offsets, the weights' transposes of one set of experts, D [R, Kd] and h [R, dff]
+// in bf16, and the transposed copies over Kp columns (every expert's rows padded to 64, or T
+// padded to 64).
 struct ExpertBwdScratch {
-  size_t s0, s1, s2, dx_perm, total;
+  size_t status, s0, s1, s2, dx_perm, koff, wdT, wcT, D, h, DT, hT, xT, dyT, total;
+  int64_t Kp;
 };
+
+int64_t round64(int64_t v) { return (v + 63) & ~(int64_t)63; }
 
 ExpertBwdScratch expert_bwd_scratch(const moe_config* c) {
   ExpertBwdScratch L;
   const size_t A = (size_t)a_max_of(c);
   const size_t R = std::max(A, c->n_shared > 0 ? (size_t)c->T : (size_t)0);
-  const size_t f = (size_t)c->dff, d = (size_t)c->d;
+  const size_t f = (size_t)c->dff, d = (size_t)c->d, E = (size_t)c->E;
+  const bool glu = c->act == MOE_ACT_SWIGLU, tc = is_bf16(c);
+  const size_t Kd = glu ? 2 * f : f;
+  L.Kp = std::max(A > 0 ? round64((int64_t)A + 63 * (int64_t)E) : (int64_t)0,
+                  c->n_shared > 0 ? round64(c->T) : (int64_t)0);
+  const size_t Kp = tc ? (size_t)L.Kp : 0;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t a = off;
     off += align256(bytes);
     return a;
   };
+  L.status = take(256);
   L.s0 = take(R * f * 4);
-  L.s1 = take(c->act == MOE_ACT_SWIGLU ? R * f * 4 : 0);
+  L.s1 = take(glu ? R * f * 4 : 0);
   L.s2 = take(R * f * 4);
   L.dx_perm = take(A * d * 4);
+  L.koff = take(tc ? (E + 1) * 4 : 0);
+  L.wdT = take(tc ? E * f * d * 2 : 0);
+  L.wcT = take(tc ? E * d * Kd * 2 : 0);
+  L.D = take(tc ? R * Kd * 2 : 0);
+  L.h = take(tc ? R * f * 2 : 0);
+  L.DT = take(Kd * Kp * 2);
+  L.hT = take(f * Kp * 2);
+  L.xT = take(d * Kp * 2);
+  L.dyT = take(d * Kp * 2);
   L.total = off;
   return L;
 }
@@ -714,6 +735,7 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, 
     return MOE_ERR_INVALID_ARG;
   if (routed && (!x_perm || !offsets || !row_of || !dy_perm || !dx || !scratch)) return MOE_ERR_INVALID_ARG;
   if (S && cfg->T > 0 && (!x || !dy || !dx || !scratch)) return MOE_ERR_INVALID_ARG;
+  if (!scratch) return MOE_ERR_INVALID_ARG;  // the status word lives there
   const void* ps[] = {x, x_perm, offsets, row_of, dy, dy_perm, dx, scratch, w->w_up, w->w_gate, w->w_down,
                       w->b_up, w->ws_up, w->ws_gate, w->ws_down, g->dw_up, g->dw_gate, g->dw_down, g->db_up,
                       g->db_down, g->dws_up, g->dws_gate, g->dws_down};
@@ -725,6 +747,8 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, 
   b.T = cfg->T, b.d = cfg->d, b.E = cfg->E, b.k = cfg->k, b.dff = cfg->dff, b.n_shared = cfg->n_shared;
   b.act = glu ? ACT_SWIGLU : ACT_GELU;
   b.rows_bound = routed ? (int)(cap >= 0 && cap < cfg->T ? cap : cfg->T) : 0;
+  b.rows_alloc = (int)a_max_of(cfg);
+  b.Kp = L.Kp;
   b.x = x, b.x_perm = x_perm, b.dy = dy, b.dy_perm = dy_perm, b.offsets = offsets, b.row_of = row_of;
   b.w_up = w->w_up, b.w_gate = glu ? w->w_gate : nullptr, b.w_down = w->w_down;
   b.b_up = cfg->has_bias ? w->b_up : nullptr;
@@ -735,6 +759,12 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, 
   b.dx = dx;
   b.dx_perm = at<float>(scratch, L.dx_perm);
   b.s0 = at<float>(scratch, L.s0), b.s1 = at<float>(scratch, L.s1), b.s2 = at<float>(scratch, L.s2);
+  b.status = at<uint32_t>(scratch, L.status);
+  b.koff = at<int32_t>(scratch, L.koff);
+  using bf = __nv_bfloat16;
+  b.wdT = at<bf>(scratch, L.wdT), b.wcT = at<bf>(scratch, L.wcT), b.D = at<bf>(scratch, L.D);
+  b.h = at<bf>(scratch, L.h), b.DT = at<bf>(scratch, L.DT), b.hT = at<bf>(scratch, L.hT);
+  b.xT = at<bf>(scratch, L.xT), b.dyT = at<bf>(scratch, L.dyT);
   return cuda_status(launch_expert_backward(is_bf16(cfg), b, static_cast<cudaStream_t>(stream)));
 }
 

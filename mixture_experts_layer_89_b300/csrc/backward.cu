@@ -276,6 +276,20 @@ cudaError_t router_bwd_t(const void* x, const void* wr, const float* lbias, cons
 //           dh = h = gelu(a + b).
 // silu(g) = g sigma(g), silu'(g) = sigma(g) (1 + g (1 - sigma(g))); gelu(a) = a Phi(a),
 // gelu'(a) = Phi(a) + a phi(a) with the standard normal CDF Phi and density phi.
+__device__ __forceinline__ void swiglu_bwd(float gv, float uv, float up, float& dg, float& du, float& h) {
+  const float sg = 1.f / (1.f + expf(-gv));
+  const float si = gv * sg;
+  dg = up * uv * (sg * (1.f + gv * (1.f - sg)));
+  du = up * si;
+  h = si * uv;
+}
+__device__ __forceinline__ void gelu_bwd(float a, float up, float& da, float& h) {
+  const float cdf = 0.5f * (1.f + erff(a * 0.70710678118654752f));
+  const float pdf = 0.39894228040143268f * expf(-0.5f * a * a);
+  da = up * (cdf + a * pdf);
+  h = a * cdf;
+}
+
 template <int ACT, typename T>
 __global__ void __launch_bounds__(256) k_act_bwd(float* __restrict__ p0, float* __restrict__ p1,
                                                  float* __restrict__ dh, const T* __restrict__ bias,
@@ -286,22 +300,126 @@ __global__ void __launch_bounds__(256) k_act_bwd(float* __restrict__ p0, float* 
     const size_t base = (size_t)r * dff;
     for (int c = threadIdx.x; c < dff; c += blockDim.x) {
       const size_t i = base + c;
-      const float up = dh[i];
       if (ACT == ACT_SWIGLU) {
-        const float gv = p0[i], uv = p1[i];
-        const float sg = 1.f / (1.f + expf(-gv));
-        const float si = gv * sg;
-        p0[i] = up * uv * (sg * (1.f + gv * (1.f - sg)));
-        p1[i] = up * si;
-        dh[i] = si * uv;
+        swiglu_bwd(p0[i], p1[i], dh[i], p0[i], p1[i], dh[i]);
       } else {
         const float a = p0[i] + (bias ? to_f(bias[(size_t)g * dff + c]) : 0.f);
-        const float cdf = 0.5f * (1.f + erff(a * 0.70710678118654752f));
-        const float pdf = 0.39894228040143268f * expf(-0.5f * a * a);
-        p0[i] = up * (cdf + a * pdf);
-        dh[i] = a * cdf;
+        gelu_bwd(a, dh[i], p0[i], dh[i]);
       }
     }
+  }
+}
+
+// The same for bf16 layers, whose next contractions run on the tensor cores: from the fp32
+// pre-activations p0 (g, or a without its bias), p1 (u) and dh, the bf16 operands D [rows][ldd]
+// (SwiGLU: du at column c and dg at dff + c; GELU: da) and h [rows][dff]; GELU also keeps the fp32
+// da in p0 for the bias sums.
+template <int ACT>
+__global__ void __launch_bounds__(256) k_act_bwd_tc(float* __restrict__ p0, const float* __restrict__ p1,
+                                                    const float* __restrict__ dh, const __nv_bfloat16* __restrict__ bias,
+                                                    const int32_t* __restrict__ off, int rows, int dff,
+                                                    __nv_bfloat16* __restrict__ D, int64_t ldd,
+                                                    __nv_bfloat16* __restrict__ h) {
+  const int g = blockIdx.y;
+  const int lo = off ? off[g] : 0, hi = off ? off[g + 1] : rows;
+  for (int r = lo + (int)blockIdx.x; r < hi; r += gridDim.x) {
+    for (int c = threadIdx.x; c < dff; c += blockDim.x) {
+      const size_t i = (size_t)r * dff + c;
+      float hv;
+      if (ACT == ACT_SWIGLU) {
+        float dg, du;
+        swiglu_bwd(p0[i], p1[i], dh[i], dg, du, hv);
+        D[(size_t)r * ldd + c] = __float2bfloat16_rn(du);
+        D[(size_t)r * ldd + dff + c] = __float2bfloat16_rn(dg);
+      } else {
+        const float a = p0[i] + (bias ? __bfloat162float(bias[(size_t)g * dff + c]) : 0.f);
+        float da;
+        gelu_bwd(a, dh[i], da, hv);
+        p0[i] = da;
+        D[(size_t)r * ldd + c] = __float2bfloat16_rn(da);
+      }
+      h[i] = __float2bfloat16_rn(hv);
+    }
+  }
+}
+
+// out_b[c ldo + col0 + r] = in_b[r C + c] for each b (in [nb][R][C], out_b = out + b ob): the
+// weights' transposes that the tensor-core contractions read K-major.  32 x 32 tiles through
+// shared memory.
+__global__ void __launch_bounds__(256) k_transpose_bf16(const __nv_bfloat16* __restrict__ in, int R, int C,
+                                                        __nv_bfloat16* __restrict__ out, int64_t ldo, int col0,
+                                                        int64_t ob) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const __nv_bfloat16* ib = in + (size_t)blockIdx.z * R * C;
+  __nv_bfloat16* obp = out + (size_t)blockIdx.z * ob;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[i][threadIdx.x] = ib[(size_t)r * C + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < R && c < C) obp[(size_t)c * ldo + col0 + r] = tile[threadIdx.x][i];
+  }
+}
+
+// koff[g] = sum over g' < g of the rows of g' rounded up to 64: each group's first column in the
+// transposed copies that the weight gradients contract over.
+__global__ void k_pad_offsets(const int32_t* __restrict__ off, int G, int32_t* __restrict__ koff) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int run = 0;
+  koff[0] = 0;
+  for (int g = 0; g < G; ++g) {
+    run += (off[g + 1] - off[g] + 63) & ~63;
+    koff[g + 1] = run;
+  }
+}
+
+// out [C][Kp]: padded column p of group g (koff[g] <= p < koff[g+1]) holds row off[g] + p - koff[g]
+// of in [rows][ldi] while that row is the group's, else zero.  off / koff NULL: one group of `rows`
+// rows, padded to a multiple of 64.  32 padded columns x 32 channels per block.
+__global__ void __launch_bounds__(256) k_transpose_pad(const __nv_bfloat16* __restrict__ in, int64_t ldi, int C,
+                                                       const int32_t* __restrict__ off,
+                                                       const int32_t* __restrict__ koff, int G, int rows,
+                                                       __nv_bfloat16* __restrict__ out, int64_t Kp) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  __shared__ int s_r0, s_hi, s_live;
+  const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  if (threadIdx.x == 0 && threadIdx.y == 0) {
+    int live = 0, r0 = 0, hi = 0;
+    if (off) {
+      if (p0 < koff[G]) {
+        int lo = 0, h = G - 1;  // the last group starting at or before p0
+        while (lo < h) {
+          const int mid = (lo + h + 1) >> 1;
+          if (koff[mid] <= p0) lo = mid;
+          else h = mid - 1;
+        }
+        live = 1;
+        r0 = off[lo] + (p0 - koff[lo]);
+        hi = off[lo + 1];
+      }
+    } else if (p0 < ((rows + 63) & ~63)) {
+      live = 1;
+      r0 = p0;
+      hi = rows;
+    }
+    s_live = live;
+    s_r0 = r0;
+    s_hi = hi;
+  }
+  __syncthreads();
+  if (!s_live) return;
+  const int r0 = s_r0, hi = s_hi;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (r < hi && c < C) ? in[(size_t)r * ldi + c] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i;
+    if (c < C) out[(size_t)c * Kp + p0 + threadIdx.x] = tile[threadIdx.x][i];
   }
 }
 
@@ -393,7 +511,8 @@ template <typename T>
 cudaError_t expert_bwd_t(const ExpertBackward& b, cudaStream_t st) {
   const T* x = static_cast<const T*>(b.x);
   const T* dy = static_cast<const T*>(b.dy);
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(b.status, 0, sizeof(uint32_t), st);  // no bounded waits on this path
+  if (e != cudaSuccess) return e;
   if (b.rows_bound > 0) {
     e = ffn_bwd_rows<T>(b.act, static_cast<const T*>(b.x_perm), static_cast<const T*>(b.dy_perm), b.offsets, b.E,
                         b.rows_bound, b.d, b.dff, static_cast<const T*>(b.w_up), static_cast<const T*>(b.w_gate),
@@ -424,6 +543,107 @@ cudaError_t expert_bwd_t(const ExpertBackward& b, cudaStream_t st) {
                         static_cast<const T*>(b.ws_down) + s * sw, nullptr, b.dws_up + s * sw,
                         b.dws_gate ? b.dws_gate + s * sw : nullptr, b.dws_down + s * sw, nullptr, nullptr, b.dx, 1,
                         b.s0, b.s1, b.s2, st);
+  }
+  return e;
+}
+// bf16 layers: every contraction on the tensor cores (k_gemm_bwd) with fp32 accumulation; the
+// operands the backward creates (du, dg or da, h and the transposed copies) are rounded to bf16.
+// One FFN backward over G groups of rows (off) or one plain problem of `rows` rows (off == NULL).
+cudaError_t ffn_bwd_tc(const ExpertBackward& b, bool glu, const __nv_bfloat16* xr, const __nv_bfloat16* dyr,
+                       const int32_t* off, int G, int rows_alloc, int rows, const __nv_bfloat16* wu,
+                       const __nv_bfloat16* wg, const __nv_bfloat16* wd, const __nv_bfloat16* bu, float* dwu,
+                       float* dwg, float* dwd, float* dbu, float* dbd, float* dxr, int beta_dx, cudaStream_t st) {
+  const int d = b.d, f = b.dff, Kd = glu ? 2 * f : f;
+  const int Gw = off ? G : 1;
+  // the weights' transposes: W_down^T [Gw][f][d], [W_up^T | W_gate^T] [Gw][d][Kd]
+  const dim3 tb(32, 8);
+  k_transpose_bf16<<<dim3((f + 31) / 32, (d + 31) / 32, Gw), tb, 0, st>>>(wd, d, f, b.wdT, d, 0, (int64_t)f * d);
+  k_transpose_bf16<<<dim3((d + 31) / 32, (f + 31) / 32, Gw), tb, 0, st>>>(wu, f, d, b.wcT, Kd, 0, (int64_t)d * Kd);
+  if (glu)
+    k_transpose_bf16<<<dim3((d + 31) / 32, (f + 31) / 32, Gw), tb, 0, st>>>(wg, f, d, b.wcT, Kd, f, (int64_t)d * Kd);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // pre-activations g (or a) into s0, u into s1; dh = dy W_down into s2
+  e = launch_gemm_bwd_rows_m(xr, rows_alloc, glu ? wg : wu, Gw, f, d, off, G, rows, b.s0, f, 0, b.status, st);
+  if (e == cudaSuccess && glu)
+    e = launch_gemm_bwd_rows_m(xr, rows_alloc, wu, Gw, f, d, off, G, rows, b.s1, f, 0, b.status, st);
+  if (e == cudaSuccess)
+    e = launch_gemm_bwd_rows_m(dyr, rows_alloc, b.wdT, Gw, f, d, off, G, rows, b.s2, f, 0, b.status, st);
+  if (e != cudaSuccess) return e;
+  const dim3 eg(off ? 64 : 592, off ? G : 1);
+  if (glu)
+    k_act_bwd_tc<ACT_SWIGLU><<<eg, 256, 0, st>>>(b.s0, b.s1, b.s2, nullptr, off, rows, f, b.D, Kd, b.h);
+  else
+    k_act_bwd_tc<ACT_GELU><<<eg, 256, 0, st>>>(b.s0, nullptr, b.s2, bu, off, rows, f, b.D, Kd, b.h);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (dbu) {
+    k_group_colsum<float><<<dim3((f + 255) / 256, G), 256, 0, st>>>(b.s0, f, off, f, dbu);
+    k_group_colsum<__nv_bfloat16><<<dim3((d + 255) / 256, G), 256, 0, st>>>(dyr, d, off, d, dbd);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // input gradient: [du | dg] [W_up^T | W_gate^T]^T, one contraction over K = Kd
+  e = launch_gemm_bwd_rows_m(b.D, rows_alloc, b.wcT, Gw, d, Kd, off, G, rows, dxr, d, beta_dx, b.status, st);
+  if (e != cudaSuccess) return e;
+  // weight gradients over each group's rows: transposed copies, each group zero-padded to 64
+  const int32_t* koff = nullptr;
+  if (off) {
+    k_pad_offsets<<<1, 32, 0, st>>>(off, G, b.koff);
+    koff = b.koff;
+  }
+  const int64_t Kp = b.Kp;
+  const int pad_cols = off ? (int)Kp : ((rows + 63) & ~63);
+  const dim3 tg((unsigned)(pad_cols / 32), 1);
+  k_transpose_pad<<<dim3(tg.x, (Kd + 31) / 32), tb, 0, st>>>(b.D, Kd, Kd, off, koff, G, rows, b.DT, Kp);
+  k_transpose_pad<<<dim3(tg.x, (f + 31) / 32), tb, 0, st>>>(b.h, f, f, off, koff, G, rows, b.hT, Kp);
+  k_transpose_pad<<<dim3(tg.x, (d + 31) / 32), tb, 0, st>>>(xr, d, d, off, koff, G, rows, b.xT, Kp);
+  k_transpose_pad<<<dim3(tg.x, (d + 31) / 32), tb, 0, st>>>(dyr, d, d, off, koff, G, rows, b.dyT, Kp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int cols = (rows + 63) & ~63;
+  e = launch_gemm_bwd_rows_k(b.dyT, d, b.hT, f, (int)Kp, koff, G, cols, dwd, f, (int64_t)d * f, 0, b.status, st);
+  if (e == cudaSuccess)
+    e = launch_gemm_bwd_rows_k(b.DT, f, b.xT, d, (int)Kp, koff, G, cols, dwu, d, (int64_t)f * d, 0, b.status, st);
+  if (e == cudaSuccess && glu)
+    e = launch_gemm_bwd_rows_k(b.DT + (size_t)f * Kp, f, b.xT, d, (int)Kp, koff, G, cols, dwg, d, (int64_t)f * d, 0,
+                               b.status, st);
+  return e;
+}
+
+cudaError_t expert_bwd_tc(const ExpertBackward& b, cudaStream_t st) {
+  using bf = __nv_bfloat16;
+  const bool glu = b.act == ACT_SWIGLU;
+  cudaError_t e = cudaMemsetAsync(b.status, 0, sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  if (b.rows_bound > 0) {
+    e = ffn_bwd_tc(b, glu, static_cast<const bf*>(b.x_perm), static_cast<const bf*>(b.dy_perm), b.offsets, b.E,
+                   b.rows_alloc, 0, static_cast<const bf*>(b.w_up), static_cast<const bf*>(b.w_gate),
+                   static_cast<const bf*>(b.w_down), static_cast<const bf*>(b.b_up), b.dw_up, b.dw_gate, b.dw_down,
+                   b.db_up, b.db_down, b.dx_perm, 0, st);
+    if (e != cudaSuccess) return e;
+    k_scatter_rows_add<<<b.T, 256, 0, st>>>(b.dx_perm, b.row_of, b.k, b.d, b.dx);
+    e = cudaGetLastError();
+  } else {
+    const size_t wsz = sizeof(float) * (size_t)b.E * b.dff * b.d;
+    e = cudaMemsetAsync(b.dw_up, 0, wsz, st);
+    if (e == cudaSuccess && b.dw_gate) e = cudaMemsetAsync(b.dw_gate, 0, wsz, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(b.dw_down, 0, wsz, st);
+    if (e == cudaSuccess && b.db_up) e = cudaMemsetAsync(b.db_up, 0, sizeof(float) * (size_t)b.E * b.dff, st);
+    if (e == cudaSuccess && b.db_down) e = cudaMemsetAsync(b.db_down, 0, sizeof(float) * (size_t)b.E * b.d, st);
+  }
+  const size_t sw = (size_t)b.dff * b.d;
+  for (int s = 0; s < b.n_shared && e == cudaSuccess; ++s) {
+    if (b.T == 0) {
+      e = cudaMemsetAsync(b.dws_up + s * sw, 0, sizeof(float) * sw, st);
+      if (e == cudaSuccess && b.dws_gate) e = cudaMemsetAsync(b.dws_gate + s * sw, 0, sizeof(float) * sw, st);
+      if (e == cudaSuccess) e = cudaMemsetAsync(b.dws_down + s * sw, 0, sizeof(float) * sw, st);
+      continue;
+    }
+    e = ffn_bwd_tc(b, glu, static_cast<const bf*>(b.x), static_cast<const bf*>(b.dy), nullptr, 1, b.T, b.T,
+                   static_cast<const bf*>(b.ws_up) + s * sw, glu ? static_cast<const bf*>(b.ws_gate) + s * sw : nullptr,
+                   static_cast<const bf*>(b.ws_down) + s * sw, nullptr, b.dws_up + s * sw,
+                   glu ? b.dws_gate + s * sw : nullptr, b.dws_down + s * sw, nullptr, nullptr, b.dx, 1, st);
   }
   return e;
 }
@@ -458,7 +678,7 @@ cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, con
 
 cudaError_t launch_expert_backward(bool bf16, const ExpertBackward& b, cudaStream_t st) {
   if (b.k < 1 || b.k > 8) return cudaErrorInvalidValue;
-  return bf16 ? expert_bwd_t<__nv_bfloat16>(b, st) : expert_bwd_t<float>(b, st);
+  return bf16 ? expert_bwd_tc(b, st) : expert_bwd_t<float>(b, st);
 }
 
 }  // namespace moe

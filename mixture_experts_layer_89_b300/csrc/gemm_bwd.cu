@@ -1,0 +1,368 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores for the backward pass of the expert FFNs:
+//
+//   C[m, n] (+)= sum_k A[m, k] B[n, k]      A, B bf16 and K-major; fp32 accumulators and output
+//
+// in two grouped forms (group g < G <= 256):
+//   rows on M (input gradients, recomputed pre-activations): group g owns rows [off[g], off[g+1])
+//     of A [rows, K] and of C [rows, ldc]; its B is B[g] of B [G][N][K]; K is fixed.
+//   rows on K (weight gradients): group g owns the columns [off[g], off[g+1]) of A [M][Kp] and of
+//     B [N][Kp] (the group's rows of the layer, transposed, each group zero-padded to a multiple
+//     of 64 columns); its C is C + g c_stride, [M, N] with ldc.
+// A NULL offset array means one group: rows [0, rows) (rows on M) or columns [0, rows) (on K).
+//
+// Persistent CTAs (one per SM: four 48 KB stages of a 128 x 64 A tile and a 256 x 64 B tile, both
+// written by TMA with the 128-byte swizzle) walk the 128 x 256 output tiles of all groups in
+// order.  Warp 0 loads the stages, warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16, one thread)
+// into one of two TMEM accumulators (2 x 256 columns), warps 2-5 drain the other one into C while
+// the next tile accumulates.  Each output is one accumulation in k order, so results do not depend
+// on scheduling.  Every wait is bounded: on a time-out the kernel records DEV_TIMEOUT in the status
+// word, lets its copies and MMAs in flight land, frees its tensor memory and returns.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+constexpr int GB_BM = 128, GB_BN = 256, GB_BK = 64, GB_STAGES = 4, GB_MAXG = 256;
+constexpr int GB_A_BYTES = GB_BM * GB_BK * 2;  // 16 KB
+constexpr int GB_B_BYTES = GB_BN * GB_BK * 2;  // 32 KB
+constexpr int GB_STAGE_BYTES = GB_A_BYTES + GB_B_BYTES;
+constexpr int GB_THREADS = 192;
+constexpr uint32_t GB_TMEM_COLS = 2 * GB_BN;
+constexpr size_t GB_SMEM = (size_t)GB_STAGES * GB_STAGE_BYTES + 1024;  // + alignment slack
+static_assert(GB_STAGE_BYTES % 1024 == 0 && GB_A_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+static_assert(GB_SMEM <= 227 * 1024, "stages fit the shared memory of one CTA");
+static_assert(GB_MAXG <= 32 * 8, "eight groups per lane in the tile count");
+
+struct GbCtl {
+  uint64_t full[GB_STAGES], empty[GB_STAGES], tfull[2], tempty[2], mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int pre[GB_MAXG + 1];  // tiles of the groups before g
+  int lo[GB_MAXG + 1];   // the group boundaries
+};
+
+struct GbArgs {
+  int rows_on_k;
+  const int32_t* off;  // [G + 1] or NULL (one group of `rows`)
+  int G, rows;
+  int M, N, K;  // rows on M: N and K; rows on K: M and N
+  float* C;
+  int64_t ldc, c_stride;
+  int beta;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void gb_drain(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const unsigned long long t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+}
+
+struct GbTile {
+  int g, m0, n0, mrows, kb, k0;
+};
+
+__global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constant__ CUtensorMap map_a,
+                                                            const __grid_constant__ CUtensorMap map_b,
+                                                            const GbArgs a) {
+  extern __shared__ uint8_t gb_raw[];
+  __shared__ GbCtl ctl;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gb_raw) + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort_flag = &ctl.abort_flag;
+  const int G = a.off ? a.G : 1;
+  const int nt = (a.N + GB_BN - 1) / GB_BN;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < GB_STAGES; ++s) {
+      mbar_init(smem_u32(&ctl.full[s]), 1);
+      mbar_init(smem_u32(&ctl.empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl.tfull[b]), 1);
+      mbar_init(smem_u32(&ctl.tempty[b]), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(smem_u32(&ctl.mma_done), 1);
+    ctl.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(&ctl.tmem_base), GB_TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 3) {  // tiles per group and their exclusive prefix; lane owns groups [8 lane, 8 lane + 8)
+    int cnt[8], local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      cnt[i] = 0;
+      if (g < G) {
+        const int lo = a.off ? a.off[g] : 0;
+        const int hi = a.off ? a.off[g + 1] : a.rows;
+        ctl.lo[g] = lo;
+        if (g == G - 1) ctl.lo[G] = hi;
+        const int mt = a.rows_on_k ? (a.M + GB_BM - 1) / GB_BM : (hi > lo ? (hi - lo + GB_BM - 1) / GB_BM : 0);
+        cnt[i] = mt * nt;
+        local += cnt[i];
+      }
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int g = lane * 8 + i;
+      if (g < G) ctl.pre[g] = run;
+      run += cnt[i];
+    }
+    if (lane == 31) ctl.pre[G] = incl;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.pre[G];
+
+  auto decode = [&](int u) {
+    int lo = 0, hi = G - 1;  // the last group whose first tile is at or before u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ctl.pre[mid] <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    GbTile t;
+    t.g = lo;
+    const int r = u - ctl.pre[lo];
+    const int mt = r / nt;
+    t.n0 = (r % nt) * GB_BN;
+    const int glo = ctl.lo[lo], ghi = ctl.lo[lo + 1];
+    if (a.rows_on_k) {
+      t.m0 = mt * GB_BM;
+      t.mrows = min(GB_BM, a.M - t.m0);
+      t.k0 = glo;
+      t.kb = (ghi - glo) / GB_BK;
+    } else {
+      t.m0 = glo + mt * GB_BM;
+      t.mrows = min(GB_BM, ghi - t.m0);
+      t.k0 = 0;
+      t.kb = a.K / GB_BK;
+    }
+    return t;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      bool aborted = false;
+      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
+        const GbTile t = decode(u);
+        for (int kb = 0; kb < t.kb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl.empty[s]), ph ^ 1u, abort_flag, a.status)) {
+            aborted = true;
+            break;
+          }
+          armed &= ~(1u << s);
+          const uint32_t sa = smem_u32(smem + (size_t)s * GB_STAGE_BYTES), sb = sa + GB_A_BYTES;
+          const uint32_t fb = smem_u32(&ctl.full[s]);
+          mbar_arrive_expect_tx(fb, GB_STAGE_BYTES);
+          const int kc = t.k0 + kb * GB_BK;
+          tma_load_2d(sa, &map_a, fb, kc, t.m0);
+          if (a.rows_on_k) tma_load_2d(sb, &map_b, fb, kc, t.n0);
+          else tma_load_3d(sb, &map_b, fb, kc, t.n0, t.g);
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          if (++s == GB_STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (aborted)  // every armed copy lands before the CTA leaves
+        for (int i = 0; i < GB_STAGES; ++i)
+          if ((armed >> i) & 1u) gb_drain(smem_u32(&ctl.full[i]), (armed_ph >> i) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0, it = 0;
+      uint32_t ph = 0;
+      bool aborted = false;
+      const uint32_t idesc = umma_idesc_bf16(GB_BM, GB_BN);
+      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x, ++it) {
+        const GbTile t = decode(u);
+        const int acc = it & 1;
+        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait_bounded(smem_u32(&ctl.tempty[acc]), aph ^ 1u, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * GB_BN);
+        for (int kb = 0; kb < t.kb; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&ctl.full[s]), ph, abort_flag, a.status)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + (size_t)s * GB_STAGE_BYTES), sb = sa + GB_A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < GB_BK / 16; ++kk)
+            umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(smem_u32(&ctl.empty[s]));  // the stage is free once these MMAs have read it
+          if (++s == GB_STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (aborted) break;
+        if (t.kb > 0) umma_commit(smem_u32(&ctl.tfull[acc]));
+        else mbar_arrive(smem_u32(&ctl.tfull[acc]));  // nothing to sum: the epilogue writes zeros
+      }
+      umma_commit(smem_u32(&ctl.mma_done));
+      gb_drain(smem_u32(&ctl.mma_done), 0);
+    }
+  } else {
+    const int q = warp & 3;  // this warp reads TMEM lanes 32 q .. 32 q + 31 (tile rows)
+    int it = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+      const GbTile t = decode(u);
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(smem_u32(&ctl.tfull[acc]), aph, abort_flag, a.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const int r = 32 * q + lane;
+      const bool valid = r < t.mrows;
+      float* crow = a.C + (a.rows_on_k ? (size_t)t.g * a.c_stride : 0) + (size_t)(t.m0 + (valid ? r : 0)) * a.ldc + t.n0;
+      const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * GB_BN);
+#pragma unroll 1
+      for (int c = 0; c < GB_BN / 32 && t.n0 + 32 * c < a.N; ++c) {
+        uint32_t v[32];
+        if (t.kb > 0) {
+          tmem_ld32(tb + 32 * c, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (valid) {
+          float4* dst = reinterpret_cast<float4*>(crow + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 x = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            if (a.beta) {
+              const float4 o = dst[j];
+              x.x += o.x;
+              x.y += o.y;
+              x.z += o.z;
+              x.w += o.w;
+            }
+            dst[j] = x;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ctl.tempty[acc]));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, GB_TMEM_COLS);
+  }
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+cudaError_t launch_gb(const CUtensorMap& ma, const CUtensorMap& mb, const GbArgs& a, long tiles_bound, cudaStream_t st) {
+  if (tiles_bound <= 0) return cudaSuccess;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_bwd), GB_SMEM);
+  if (e != cudaSuccess) return e;
+  const int nsm = sm_count();
+  if (nsm <= 0) return cudaErrorInvalidDevice;
+  const int grid = (int)(tiles_bound < nsm ? tiles_bound : nsm);
+  k_gemm_bwd<<<grid, GB_THREADS, GB_SMEM, st>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+cudaError_t launch_gemm_bwd_rows_m(const void* A, int rows_alloc, const void* B, int G_w, int N, int K,
+                                   const int32_t* off, int G, int rows, float* C, int64_t ldc, int beta,
+                                   uint32_t* status, cudaStream_t st) {
+  if (rows_alloc <= 0 || N <= 0) return cudaSuccess;
+  if (K <= 0 || K % GB_BK || N % 32 || ldc % 4 || (off && (G < 1 || G > GB_MAXG)) || G_w < 1 || !aligned16(A) ||
+      !aligned16(B) || !aligned16(C))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)rows_alloc};
+  const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t ba[2] = {GB_BK, GB_BM};
+  const cuuint64_t db[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)G_w};
+  const cuuint64_t sb[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
+  const cuuint32_t bb[3] = {GB_BK, GB_BN, 1};
+  if (!make_tmap_bf16(&ma, A, 2, da, sa, ba) || !make_tmap_bf16(&mb, B, 3, db, sb, bb)) return cudaErrorInvalidValue;
+  GbArgs a{};
+  a.rows_on_k = 0;
+  a.off = off;
+  a.G = off ? G : 1;
+  a.rows = rows;
+  a.N = N;
+  a.K = K;
+  a.C = C;
+  a.ldc = ldc;
+  a.beta = beta;
+  a.status = status;
+  const long nt = (N + GB_BN - 1) / GB_BN;
+  const long rt = off ? (long)(rows_alloc + GB_BM - 1) / GB_BM + G : (long)(rows + GB_BM - 1) / GB_BM;
+  return launch_gb(ma, mb, a, rt * nt, st);
+}
+
+cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, int Kp, const int32_t* off, int G,
+                                   int cols, float* C, int64_t ldc, int64_t c_stride, int beta, uint32_t* status,
+                                   cudaStream_t st) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  if (Kp <= 0 || Kp % GB_BK || (!off && cols % GB_BK) || N % 32 || ldc % 4 || c_stride % 4 ||
+      (off && (G < 1 || G > GB_MAXG)) || !aligned16(A) || !aligned16(B) || !aligned16(C))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  const cuuint64_t da[2] = {(cuuint64_t)Kp, (cuuint64_t)M};
+  const cuuint64_t db[2] = {(cuuint64_t)Kp, (cuuint64_t)N};
+  const cuuint64_t s[1] = {(cuuint64_t)Kp * 2};
+  const cuuint32_t ba[2] = {GB_BK, GB_BM}, bb[2] = {GB_BK, GB_BN};
+  if (!make_tmap_bf16(&ma, A, 2, da, s, ba) || !make_tmap_bf16(&mb, B, 2, db, s, bb)) return cudaErrorInvalidValue;
+  GbArgs a{};
+  a.rows_on_k = 1;
+  a.off = off;
+  a.G = off ? G : 1;
+  a.rows = cols;
+  a.M = M;
+  a.N = N;
+  a.C = C;
+  a.ldc = ldc;
+  a.c_stride = c_stride;
+  a.beta = beta;
+  a.status = status;
+  const long tiles = (long)(off ? G : 1) * ((M + GB_BM - 1) / GB_BM) * ((N + GB_BN - 1) / GB_BN);
+  return launch_gb(ma, mb, a, tiles, st);
+}
+
+}  // namespace moe

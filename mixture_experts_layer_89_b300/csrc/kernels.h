@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -131,16 +132,33 @@ cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, con
                                    float* dwr, float* dx, cudaStream_t st);
 // Backward of the expert FFNs (routed over the permuted rows, then the shared experts over all
 // tokens).  Weights and activations in the layer dtype, gradients fp32; act is ACT_GELU or
-// ACT_SWIGLU; rows_bound bounds any expert's rows (0: no routed rows); s0..s2 hold
-// max(A_max, T) x dff floats each (s1 SwiGLU only), dx_perm A_max x d.
+// ACT_SWIGLU; rows_bound bounds any expert's rows (0: no routed rows), rows_alloc = A_max; s0..s2
+// hold max(A_max, T) x dff floats each (s1 SwiGLU only), dx_perm A_max x d.  bf16 layers (tensor
+// cores) also use: status (one word, zeroed by the call), koff [E+1], wdT [E][dff][d] and
+// wcT [E][d][Kd] (Kd = 2 dff for SwiGLU, else dff), D [max(A_max, T)][Kd] and h [..][dff] bf16,
+// and the transposed copies DT [Kd][Kp], hT [dff][Kp], xT and dyT [d][Kp] (Kp a multiple of 64 at
+// least the rows padded per expert and T padded).
 struct ExpertBackward {
-  int T, d, E, k, dff, n_shared, act, rows_bound;
+  int T, d, E, k, dff, n_shared, act, rows_bound, rows_alloc;
+  int64_t Kp;
   const void *x, *x_perm, *dy, *dy_perm;
   const int32_t *offsets, *row_of;
   const void *w_up, *w_gate, *w_down, *b_up, *ws_up, *ws_gate, *ws_down;
   float *dw_up, *dw_gate, *dw_down, *db_up, *db_down, *dws_up, *dws_gate, *dws_down;
   float *dx, *dx_perm, *s0, *s1, *s2;
+  uint32_t* status;
+  int32_t* koff;
+  __nv_bfloat16 *wdT, *wcT, *D, *h, *DT, *hT, *xT, *dyT;
 };
+// Grouped bf16 tensor-core GEMM of the backward, C (+)= A B^T with fp32 output (gemm_bwd.cu):
+// rows on M (A [rows_alloc][K], B [G_w][N][K], group rows from off or [0, rows)) and rows on K
+// (A [M][Kp], B [N][Kp], group columns from off -- multiples of 64 -- or [0, cols)).
+cudaError_t launch_gemm_bwd_rows_m(const void* A, int rows_alloc, const void* B, int G_w, int N, int K,
+                                   const int32_t* off, int G, int rows, float* C, int64_t ldc, int beta,
+                                   uint32_t* status, cudaStream_t st);
+cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, int Kp, const int32_t* off, int G,
+                                   int cols, float* C, int64_t ldc, int64_t c_stride, int beta, uint32_t* status,
+                                   cudaStream_t st);
 cudaError_t launch_expert_backward(bool bf16, const ExpertBackward& b, cudaStream_t st);
 // Per-row scaled 8-bit codes of w [blocks][rows][cols] (fmt 1 int8, 2 E4M3), one CTA per row.
 cudaError_t launch_quantize(bool bf16, int fmt, const void* w, int blocks, int rows, int cols, uint8_t* codes,
