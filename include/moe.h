@@ -347,8 +347,13 @@ typedef struct {
  *      which the experts' part of the input gradient is ADDED (first the routed experts, each
  *      token's kept slots in slot order, then the shared experts in order), so that dx after
  *      moe_route_backward and this call is the layer's input gradient.
- * The pre-activations are recomputed in fp32 from x_perm / x; every sum runs in a fixed order.
- * scratch: moe_expert_backward_scratch_size bytes of device memory, 256-byte aligned.
+ * The pre-activations are recomputed from x_perm / x with fp32 accumulation; every sum runs in a
+ * fixed order (bit-identical repeats).  bf16 layers contract on the tensor cores, with the
+ * operands the backward creates (du, dg or da, h) rounded to bf16 and fp32 accumulation; fp32
+ * layers run in fp32 on the CUDA cores.
+ * scratch: moe_expert_backward_scratch_size bytes of device memory, 256-byte aligned; its first
+ * word is a device status word that the call zeroes and moe_read_device_status(scratch) reads
+ * (MOE_ERR_TIMEOUT when a bounded wait of the tensor-core kernel ran out).
  * MOE_ERR_UNSUPPORTED with a backup expert or 8-bit expert weights; MOE_ERR_INVALID_ARG for a
  * NULL or misaligned (16-byte) pointer that the config needs. */
 moe_status moe_expert_backward_scratch_size(const moe_config* cfg, size_t* bytes);
