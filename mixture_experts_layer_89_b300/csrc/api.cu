@@ -127,11 +127,10 @@ WsLayout layout(const moe_config* c) {
 // Scratch of the expert FFN backward: a status word; three [R, dff] fp32 buffers (pre-activations,
 // then their gradients and h) for R = max(A_max, T when there are shared experts) rows, and the
 // permuted rows' input gradients [A_max, d] fp32.  bf16 layers add the tensor-core operands: the
-// padded column offsets, the weights' transposes of one set of experts, D [R, Kd] and h [R, dff]
-// in bf16, and the transposed copies over Kp columns (every expert's rows padded to 64, or T
-// padded to 64).
+// padded column offsets, D [R, Kd] and h [R, dff] in bf16, and the transposed copies over Kp
+// columns (every expert's rows padded to 64, or T padded to 64).
 struct ExpertBwdScratch {
-  size_t status, s0, s1, s2, dx_perm, koff, wdT, wcT, D, h, DT, hT, xT, dyT, total;
+  size_t status, s0, s1, s2, dx_perm, koff, D, h, DT, hT, xT, dyT, total;
   int64_t Kp;
 };
 
@@ -159,8 +158,6 @@ ExpertBwdScratch expert_bwd_scratch(const moe_config* c) {
   L.s2 = take(R * f * 4);
   L.dx_perm = take(A * d * 4);
   L.koff = take(tc ? (E + 1) * 4 : 0);
-  L.wdT = take(tc ? E * f * d * 2 : 0);
-  L.wcT = take(tc ? E * d * Kd * 2 : 0);
   L.D = take(tc ? R * Kd * 2 : 0);
   L.h = take(tc ? R * f * 2 : 0);
   L.DT = take(Kd * Kp * 2);
@@ -762,7 +759,7 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, 
   b.status = at<uint32_t>(scratch, L.status);
   b.koff = at<int32_t>(scratch, L.koff);
   using bf = __nv_bfloat16;
-  b.wdT = at<bf>(scratch, L.wdT), b.wcT = at<bf>(scratch, L.wcT), b.D = at<bf>(scratch, L.D);
+  b.D = at<bf>(scratch, L.D);
   b.h = at<bf>(scratch, L.h), b.DT = at<bf>(scratch, L.DT), b.hT = at<bf>(scratch, L.hT);
   b.xT = at<bf>(scratch, L.xT), b.dyT = at<bf>(scratch, L.dyT);
   return cuda_status(launch_expert_backward(is_bf16(cfg), b, static_cast<cudaStream_t>(stream)));

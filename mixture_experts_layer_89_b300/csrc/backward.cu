@@ -343,27 +343,6 @@ __global__ void __launch_bounds__(256) k_act_bwd_tc(float* __restrict__ p0, cons
   }
 }
 
-// out_b[c ldo + col0 + r] = in_b[r C + c] for each b (in [nb][R][C], out_b = out + b ob): the
-// weights' transposes that the tensor-core contractions read K-major.  32 x 32 tiles through
-// shared memory.
-__global__ void __launch_bounds__(256) k_transpose_bf16(const __nv_bfloat16* __restrict__ in, int R, int C,
-                                                        __nv_bfloat16* __restrict__ out, int64_t ldo, int col0,
-                                                        int64_t ob) {
-  __shared__ __nv_bfloat16 tile[32][34];
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const __nv_bfloat16* ib = in + (size_t)blockIdx.z * R * C;
-  __nv_bfloat16* obp = out + (size_t)blockIdx.z * ob;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + threadIdx.x;
-    if (r < R && c < C) tile[i][threadIdx.x] = ib[(size_t)r * C + c];
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int c = c0 + i, r = r0 + threadIdx.x;
-    if (r < R && c < C) obp[(size_t)c * ldo + col0 + r] = tile[threadIdx.x][i];
-  }
-}
-
 // koff[g] = sum over g' < g of the rows of g' rounded up to 64: each group's first column in the
 // transposed copies that the weight gradients contract over.
 __global__ void k_pad_offsets(const int32_t* __restrict__ off, int G, int32_t* __restrict__ koff) {
@@ -548,6 +527,8 @@ cudaError_t expert_bwd_t(const ExpertBackward& b, cudaStream_t st) {
 }
 // bf16 layers: every contraction on the tensor cores (k_gemm_bwd) with fp32 accumulation; the
 // operands the backward creates (du, dg or da, h and the transposed copies) are rounded to bf16.
+// The weights are read as stored (K-major for the recomputed pre-activations, N-major for dh and
+// dx); the weight gradients contract over the rows, so their operands are transposed per expert.
 // One FFN backward over G groups of rows (off) or one plain problem of `rows` rows (off == NULL).
 cudaError_t ffn_bwd_tc(const ExpertBackward& b, bool glu, const __nv_bfloat16* xr, const __nv_bfloat16* dyr,
                        const int32_t* off, int G, int rows_alloc, int rows, const __nv_bfloat16* wu,
@@ -555,20 +536,15 @@ cudaError_t ffn_bwd_tc(const ExpertBackward& b, bool glu, const __nv_bfloat16* x
                        float* dwg, float* dwd, float* dbu, float* dbd, float* dxr, int beta_dx, cudaStream_t st) {
   const int d = b.d, f = b.dff, Kd = glu ? 2 * f : f;
   const int Gw = off ? G : 1;
-  // the weights' transposes: W_down^T [Gw][f][d], [W_up^T | W_gate^T] [Gw][d][Kd]
   const dim3 tb(32, 8);
-  k_transpose_bf16<<<dim3((f + 31) / 32, (d + 31) / 32, Gw), tb, 0, st>>>(wd, d, f, b.wdT, d, 0, (int64_t)f * d);
-  k_transpose_bf16<<<dim3((d + 31) / 32, (f + 31) / 32, Gw), tb, 0, st>>>(wu, f, d, b.wcT, Kd, 0, (int64_t)d * Kd);
-  if (glu)
-    k_transpose_bf16<<<dim3((d + 31) / 32, (f + 31) / 32, Gw), tb, 0, st>>>(wg, f, d, b.wcT, Kd, f, (int64_t)d * Kd);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // pre-activations g (or a) into s0, u into s1; dh = dy W_down into s2
-  e = launch_gemm_bwd_rows_m(xr, rows_alloc, glu ? wg : wu, Gw, f, d, off, G, rows, b.s0, f, 0, b.status, st);
+  // pre-activations g (or a) into s0, u into s1 (W [f][d]: K-major as stored); dh = dy W_down into
+  // s2 (W_down [d][f] read N-major)
+  cudaError_t e = launch_gemm_bwd_rows_m(xr, rows_alloc, glu ? wg : wu, Gw, f, d, off, G, rows, b.s0, f, 0, b.status, st);
   if (e == cudaSuccess && glu)
     e = launch_gemm_bwd_rows_m(xr, rows_alloc, wu, Gw, f, d, off, G, rows, b.s1, f, 0, b.status, st);
   if (e == cudaSuccess)
-    e = launch_gemm_bwd_rows_m(dyr, rows_alloc, b.wdT, Gw, f, d, off, G, rows, b.s2, f, 0, b.status, st);
+    e = launch_gemm_bwd_rows_m_nmajor(dyr, rows_alloc, wd, nullptr, d, Gw, f, d, off, G, rows, b.s2, f, 0, b.status,
+                                      st, true);
   if (e != cudaSuccess) return e;
   const dim3 eg(off ? 64 : 592, off ? G : 1);
   if (glu)
@@ -583,8 +559,10 @@ cudaError_t ffn_bwd_tc(const ExpertBackward& b, bool glu, const __nv_bfloat16* x
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // input gradient: [du | dg] [W_up^T | W_gate^T]^T, one contraction over K = Kd
-  e = launch_gemm_bwd_rows_m(b.D, rows_alloc, b.wcT, Gw, d, Kd, off, G, rows, dxr, d, beta_dx, b.status, st);
+  // input gradient du W_up + dg W_gate: one contraction over K = Kd of [du | dg], the weights
+  // [f][d] read N-major (W_up for k < f, W_gate beyond)
+  e = launch_gemm_bwd_rows_m_nmajor(b.D, rows_alloc, wu, glu ? wg : nullptr, f, Gw, d, Kd, off, G, rows, dxr, d,
+                                    beta_dx, b.status, st, true);
   if (e != cudaSuccess) return e;
   // weight gradients over each group's rows: transposed copies, each group zero-padded to 64
   const int32_t* koff = nullptr;

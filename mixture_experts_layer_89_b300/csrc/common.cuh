@@ -352,6 +352,17 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
          | ((uint64_t)2 << 61);                    // swizzle mode: 128 B
 }
 
+// The same for an MN-major tile (the operand's M or N dimension contiguous): TMA boxes of 64
+// M/N elements (128 bytes, swizzled) by K rows, 8-row swizzle atoms stacked 1024 bytes apart along
+// K, boxes of 64 M/N elements `mn_stride` bytes apart.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_stride) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4)       // start address / 16
+         | ((uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16)  // leading byte offset: next 64 M/N elements
+         | ((uint64_t)(1024 >> 4) << 32)           // stride byte offset: next 8 K rows
+         | ((uint64_t)1 << 46)                     // descriptor version for tcgen05
+         | ((uint64_t)2 << 61);                    // swizzle mode: 128 B
+}
+
 // 32 lanes x 32 consecutive 32-bit TMEM columns -> 32 registers per thread (thread i = lane i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

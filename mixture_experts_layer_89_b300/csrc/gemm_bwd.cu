@@ -1,6 +1,6 @@
 // Grouped bf16 GEMM on the 5th-generation tensor cores for the backward pass of the expert FFNs:
 //
-//   C[m, n] (+)= sum_k A[m, k] B[n, k]      A, B bf16 and K-major; fp32 accumulators and output
+//   C[m, n] (+)= sum_k A[m, k] B[n, k]      A, B bf16 (A K-major); fp32 accumulators and output
 //
 // in two grouped forms (group g < G <= 256):
 //   rows on M (input gradients, recomputed pre-activations): group g owns rows [off[g], off[g+1])
@@ -9,6 +9,9 @@
 //     B [N][Kp] (the group's rows of the layer, transposed, each group zero-padded to a multiple
 //     of 64 columns); its C is C + g c_stride, [M, N] with ldc.
 // A NULL offset array means one group: rows [0, rows) (rows on M) or columns [0, rows) (on K).
+// Rows on M may also read B N-major, straight from the weights as stored: B_g(n, k) at
+// [g][k][n] of one tensor for k < ksplit and of a second one (at k - ksplit) beyond, so that
+// dh = dy W_down and dx = du W_up + dg W_gate need no transposed copy of the weights.
 //
 // Persistent CTAs (one per SM: four 48 KB stages of a 128 x 64 A tile and a 256 x 64 B tile, both
 // written by TMA with the 128-byte swizzle) walk the 128 x 256 output tiles of all groups in
@@ -44,6 +47,7 @@ struct GbCtl {
 
 struct GbArgs {
   int rows_on_k;
+  int b_mn, ksplit;  // rows on M: B N-major (map_b for k < ksplit, map_b2 beyond)
   const int32_t* off;  // [G + 1] or NULL (one group of `rows`)
   int G, rows;
   int M, N, K;  // rows on M: N and K; rows on K: M and N
@@ -66,6 +70,7 @@ struct GbTile {
 
 __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constant__ CUtensorMap map_a,
                                                             const __grid_constant__ CUtensorMap map_b,
+                                                            const __grid_constant__ CUtensorMap map_b2,
                                                             const GbArgs a) {
   extern __shared__ uint8_t gb_raw[];
   __shared__ GbCtl ctl;
@@ -90,6 +95,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
+    if (a.b_mn && a.ksplit < a.K) tma_prefetch_desc(&map_b2);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(&ctl.tmem_base), GB_TMEM_COLS);
@@ -177,8 +183,17 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
           mbar_arrive_expect_tx(fb, GB_STAGE_BYTES);
           const int kc = t.k0 + kb * GB_BK;
           tma_load_2d(sa, &map_a, fb, kc, t.m0);
-          if (a.rows_on_k) tma_load_2d(sb, &map_b, fb, kc, t.n0);
-          else tma_load_3d(sb, &map_b, fb, kc, t.n0, t.g);
+          if (a.rows_on_k) {
+            tma_load_2d(sb, &map_b, fb, kc, t.n0);
+          } else if (a.b_mn) {  // four boxes of 64 n by 64 k, 8 KB apart
+            const bool lo_half = kc < a.ksplit;
+            const CUtensorMap* mb = lo_half ? &map_b : &map_b2;
+            const int kl = lo_half ? kc : kc - a.ksplit;
+#pragma unroll
+            for (int j = 0; j < GB_BN / 64; ++j) tma_load_3d(sb + j * 8192, mb, fb, t.n0 + 64 * j, kl, t.g);
+          } else {
+            tma_load_3d(sb, &map_b, fb, kc, t.n0, t.g);
+          }
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           if (++s == GB_STAGES) {
@@ -196,7 +211,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool aborted = false;
-      const uint32_t idesc = umma_idesc_bf16(GB_BM, GB_BN);
+      const uint32_t idesc = umma_idesc_bf16(GB_BM, GB_BN) | (a.b_mn ? (1u << 16) : 0u);  // bit 16: B MN-major
       for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x, ++it) {
         const GbTile t = decode(u);
         const int acc = it & 1;
@@ -212,9 +227,11 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + (size_t)s * GB_STAGE_BYTES), sb = sa + GB_A_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < GB_BK / 16; ++kk)
-            umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc,
-                      (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < GB_BK / 16; ++kk) {
+            // K-major: 16 k are 32 bytes along a row; N-major: 16 k are 16 rows of 128 bytes
+            const uint64_t bdesc = a.b_mn ? sdesc_mn_sw128(sb + kk * 2048, 8192) : sdesc_k_sw128(sb + kk * 32);
+            umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
           umma_commit(smem_u32(&ctl.empty[s]));  // the stage is free once these MMAs have read it
           if (++s == GB_STAGES) {
             s = 0;
@@ -291,37 +308,68 @@ int sm_count() {
   return n;
 }
 
-cudaError_t launch_gb(const CUtensorMap& ma, const CUtensorMap& mb, const GbArgs& a, long tiles_bound, cudaStream_t st) {
+cudaError_t launch_gb(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2, const GbArgs& a,
+                      long tiles_bound, cudaStream_t st) {
   if (tiles_bound <= 0) return cudaSuccess;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_bwd), GB_SMEM);
   if (e != cudaSuccess) return e;
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
   const int grid = (int)(tiles_bound < nsm ? tiles_bound : nsm);
-  k_gemm_bwd<<<grid, GB_THREADS, GB_SMEM, st>>>(ma, mb, a);
+  k_gemm_bwd<<<grid, GB_THREADS, GB_SMEM, st>>>(ma, mb, mb2, a);
   return cudaGetLastError();
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
 
+cudaError_t launch_gemm_bwd_rows_m_nmajor(const void* A, int rows_alloc, const void* B, const void* B2, int ksplit,
+                                          int G_w, int N, int K, const int32_t* off, int G, int rows, float* C,
+                                          int64_t ldc, int beta, uint32_t* status, cudaStream_t st, bool nmajor);
+
 cudaError_t launch_gemm_bwd_rows_m(const void* A, int rows_alloc, const void* B, int G_w, int N, int K,
                                    const int32_t* off, int G, int rows, float* C, int64_t ldc, int beta,
                                    uint32_t* status, cudaStream_t st) {
+  return launch_gemm_bwd_rows_m_nmajor(A, rows_alloc, B, nullptr, 0, G_w, N, K, off, G, rows, C, ldc, beta, status,
+                                       st, false);
+}
+
+cudaError_t launch_gemm_bwd_rows_m_nmajor(const void* A, int rows_alloc, const void* B, const void* B2, int ksplit,
+                                          int G_w, int N, int K, const int32_t* off, int G, int rows, float* C,
+                                          int64_t ldc, int beta, uint32_t* status, cudaStream_t st, bool nmajor) {
   if (rows_alloc <= 0 || N <= 0) return cudaSuccess;
   if (K <= 0 || K % GB_BK || N % 32 || ldc % 4 || (off && (G < 1 || G > GB_MAXG)) || G_w < 1 || !aligned16(A) ||
       !aligned16(B) || !aligned16(C))
     return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
+  if (nmajor && (N % 8 || ksplit <= 0 || ksplit % GB_BK || ksplit > K || (ksplit < K && !aligned16(B2))))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb, mb2;
   const cuuint64_t da[2] = {(cuuint64_t)K, (cuuint64_t)rows_alloc};
   const cuuint64_t sa[1] = {(cuuint64_t)K * 2};
   const cuuint32_t ba[2] = {GB_BK, GB_BM};
-  const cuuint64_t db[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)G_w};
-  const cuuint64_t sb[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
-  const cuuint32_t bb[3] = {GB_BK, GB_BN, 1};
-  if (!make_tmap_bf16(&ma, A, 2, da, sa, ba) || !make_tmap_bf16(&mb, B, 3, db, sb, bb)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&ma, A, 2, da, sa, ba)) return cudaErrorInvalidValue;
+  if (nmajor) {  // B_g(n, k) at [g][k][n]: boxes of 64 n by 64 k; the second tensor holds k >= ksplit
+    const cuuint32_t bb[3] = {64, GB_BK, 1};
+    const cuuint64_t db[3] = {(cuuint64_t)N, (cuuint64_t)ksplit, (cuuint64_t)G_w};
+    const cuuint64_t sb[2] = {(cuuint64_t)N * 2, (cuuint64_t)N * ksplit * 2};
+    if (!make_tmap_bf16(&mb, B, 3, db, sb, bb)) return cudaErrorInvalidValue;
+    mb2 = mb;
+    if (ksplit < K) {
+      const cuuint64_t db2[3] = {(cuuint64_t)N, (cuuint64_t)(K - ksplit), (cuuint64_t)G_w};
+      const cuuint64_t sb2[2] = {(cuuint64_t)N * 2, (cuuint64_t)N * (K - ksplit) * 2};
+      if (!make_tmap_bf16(&mb2, B2, 3, db2, sb2, bb)) return cudaErrorInvalidValue;
+    }
+  } else {
+    const cuuint64_t db[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)G_w};
+    const cuuint64_t sb[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
+    const cuuint32_t bb[3] = {GB_BK, GB_BN, 1};
+    if (!make_tmap_bf16(&mb, B, 3, db, sb, bb)) return cudaErrorInvalidValue;
+    mb2 = mb;
+  }
   GbArgs a{};
   a.rows_on_k = 0;
+  a.b_mn = nmajor ? 1 : 0;
+  a.ksplit = nmajor ? ksplit : K;
   a.off = off;
   a.G = off ? G : 1;
   a.rows = rows;
@@ -333,7 +381,7 @@ cudaError_t launch_gemm_bwd_rows_m(const void* A, int rows_alloc, const void* B,
   a.status = status;
   const long nt = (N + GB_BN - 1) / GB_BN;
   const long rt = off ? (long)(rows_alloc + GB_BM - 1) / GB_BM + G : (long)(rows + GB_BM - 1) / GB_BM;
-  return launch_gb(ma, mb, a, rt * nt, st);
+  return launch_gb(ma, mb, mb2, a, rt * nt, st);
 }
 
 cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, int Kp, const int32_t* off, int G,
@@ -361,8 +409,9 @@ cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, i
   a.c_stride = c_stride;
   a.beta = beta;
   a.status = status;
+  a.ksplit = 0;
   const long tiles = (long)(off ? G : 1) * ((M + GB_BM - 1) / GB_BM) * ((N + GB_BN - 1) / GB_BN);
-  return launch_gb(ma, mb, a, tiles, st);
+  return launch_gb(ma, mb, mb, a, tiles, st);
 }
 
 }  // namespace moe

@@ -134,10 +134,10 @@ cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, con
 // tokens).  Weights and activations in the layer dtype, gradients fp32; act is ACT_GELU or
 // ACT_SWIGLU; rows_bound bounds any expert's rows (0: no routed rows), rows_alloc = A_max; s0..s2
 // hold max(A_max, T) x dff floats each (s1 SwiGLU only), dx_perm A_max x d.  bf16 layers (tensor
-// cores) also use: status (one word, zeroed by the call), koff [E+1], wdT [E][dff][d] and
-// wcT [E][d][Kd] (Kd = 2 dff for SwiGLU, else dff), D [max(A_max, T)][Kd] and h [..][dff] bf16,
-// and the transposed copies DT [Kd][Kp], hT [dff][Kp], xT and dyT [d][Kp] (Kp a multiple of 64 at
-// least the rows padded per expert and T padded).
+// cores) also use: status (one word, zeroed by the call), koff [E+1], D [max(A_max, T)][Kd]
+// (Kd = 2 dff for SwiGLU, else dff) and h [..][dff] bf16, and the transposed copies DT [Kd][Kp],
+// hT [dff][Kp], xT and dyT [d][Kp] (Kp a multiple of 64 at least the rows padded per expert and T
+// padded).
 struct ExpertBackward {
   int T, d, E, k, dff, n_shared, act, rows_bound, rows_alloc;
   int64_t Kp;
@@ -148,7 +148,7 @@ struct ExpertBackward {
   float *dx, *dx_perm, *s0, *s1, *s2;
   uint32_t* status;
   int32_t* koff;
-  __nv_bfloat16 *wdT, *wcT, *D, *h, *DT, *hT, *xT, *dyT;
+  __nv_bfloat16 *D, *h, *DT, *hT, *xT, *dyT;
 };
 // Grouped bf16 tensor-core GEMM of the backward, C (+)= A B^T with fp32 output (gemm_bwd.cu):
 // rows on M (A [rows_alloc][K], B [G_w][N][K], group rows from off or [0, rows)) and rows on K
@@ -156,6 +156,11 @@ struct ExpertBackward {
 cudaError_t launch_gemm_bwd_rows_m(const void* A, int rows_alloc, const void* B, int G_w, int N, int K,
                                    const int32_t* off, int G, int rows, float* C, int64_t ldc, int beta,
                                    uint32_t* status, cudaStream_t st);
+// Rows on M with B read N-major from the weights as stored: B_g(n, k) = B[g][k][n] for k < ksplit,
+// B2[g][k - ksplit][n] beyond (B2 unused when ksplit == K).
+cudaError_t launch_gemm_bwd_rows_m_nmajor(const void* A, int rows_alloc, const void* B, const void* B2, int ksplit,
+                                          int G_w, int N, int K, const int32_t* off, int G, int rows, float* C,
+                                          int64_t ldc, int beta, uint32_t* status, cudaStream_t st, bool nmajor);
 cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, int Kp, const int32_t* off, int G,
                                    int cols, float* C, int64_t ldc, int64_t c_stride, int beta, uint32_t* status,
                                    cudaStream_t st);
