@@ -17,7 +17,7 @@
 // written by TMA with the 128-byte swizzle) walk the 128 x 256 output tiles of all groups in
 // order.  Warp 0 loads the stages, warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16, one thread)
 // into one of two TMEM accumulators (2 x 256 columns), warps 2-5 drain the other one into C while
-// the next tile accumulates.  Each output is one accumulation in k order, so results do not depend
+// the next tile accumulates (32 x 32 blocks staged in shared memory for coalesced stores).  Each output is one accumulation in k order, so results do not depend
 // on scheduling.  Every wait is bounded: on a time-out the kernel records DEV_TIMEOUT in the status
 // word, lets its copies and MMAs in flight land, frees its tensor memory and returns.
 #include "common.cuh"
@@ -32,7 +32,8 @@ constexpr int GB_B_BYTES = GB_BN * GB_BK * 2;  // 32 KB
 constexpr int GB_STAGE_BYTES = GB_A_BYTES + GB_B_BYTES;
 constexpr int GB_THREADS = 192;
 constexpr uint32_t GB_TMEM_COLS = 2 * GB_BN;
-constexpr size_t GB_SMEM = (size_t)GB_STAGES * GB_STAGE_BYTES + 1024;  // + alignment slack
+constexpr int GB_EPI_BYTES = 4 * 32 * 32 * 4;  // one 32 x 32 fp32 staging block per epilogue warp
+constexpr size_t GB_SMEM = (size_t)GB_STAGES * GB_STAGE_BYTES + GB_EPI_BYTES + 1024;  // + alignment slack
 static_assert(GB_STAGE_BYTES % 1024 == 0 && GB_A_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 static_assert(GB_SMEM <= 227 * 1024, "stages fit the shared memory of one CTA");
 static_assert(GB_MAXG <= 32 * 8, "eight groups per lane in the tile count");
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
   extern __shared__ uint8_t gb_raw[];
   __shared__ GbCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gb_raw) + 1023) & ~(uintptr_t)1023);
+  float* epi = reinterpret_cast<float*>(smem + (size_t)GB_STAGES * GB_STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &ctl.abort_flag;
   const int G = a.off ? a.G : 1;
@@ -257,10 +259,13 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const int r = 32 * q + lane;
-      const bool valid = r < t.mrows;
-      float* crow = a.C + (a.rows_on_k ? (size_t)t.g * a.c_stride : 0) + (size_t)(t.m0 + (valid ? r : 0)) * a.ldc + t.n0;
+      // each 32 x 32 block goes through shared memory (16-byte chunks XOR-swizzled by row, so both
+      // the row-wise writes and the column-wise reads are conflict-free): lane = row on the way
+      // in, then 8 lanes per 128-byte row segment on the way out (coalesced stores)
+      float* cbase = a.C + (a.rows_on_k ? (size_t)t.g * a.c_stride : 0) + (size_t)t.m0 * a.ldc + t.n0;
+      const int rows_here = t.mrows - 32 * q;  // valid rows of this warp's quarter (may be <= 0)
       const uint32_t tb = tmem_base + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * GB_BN);
+      float4* stg = reinterpret_cast<float4*>(epi + (size_t)q * 32 * 32);
 #pragma unroll 1
       for (int c = 0; c < GB_BN / 32 && t.n0 + 32 * c < a.N; ++c) {
         uint32_t v[32];
@@ -271,22 +276,28 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (valid) {
-          float4* dst = reinterpret_cast<float4*>(crow + 32 * c);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4 x = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        for (int j = 0; j < 8; ++j)
+          stg[lane * 8 + (j ^ (lane & 7))] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = i * 4 + (lane >> 3), ch = lane & 7;
+          if (rr < rows_here) {
+            float4 x = stg[rr * 8 + (ch ^ (rr & 7))];
+            float4* dst = reinterpret_cast<float4*>(cbase + (size_t)(32 * q + rr) * a.ldc + 32 * c) + ch;
             if (a.beta) {
-              const float4 o = dst[j];
+              const float4 o = *dst;
               x.x += o.x;
               x.y += o.y;
               x.z += o.z;
               x.w += o.w;
             }
-            dst[j] = x;
+            *dst = x;
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
