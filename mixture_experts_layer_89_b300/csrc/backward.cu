@@ -313,7 +313,14 @@ __global__ void __launch_bounds__(256) k_act_bwd(float* __restrict__ p0, float* 
 // The same for bf16 layers, whose next contractions run on the tensor cores: from the fp32
 // pre-activations p0 (g, or a without its bias), p1 (u) and dh, the bf16 operands D [rows][ldd]
 // (SwiGLU: du at column c and dg at dff + c; GELU: da) and h [rows][dff]; GELU also keeps the fp32
-// da in p0 for the bias sums.
+// da in p0 for the bias sums.  Four columns per thread (dff is a multiple of 64).
+__device__ __forceinline__ void st_bf16x4(__nv_bfloat16* p, float a, float b, float c, float d) {
+  uint2 v;
+  v.x = pack_bf16x2(a, b);
+  v.y = pack_bf16x2(c, d);
+  *reinterpret_cast<uint2*>(p) = v;
+}
+
 template <int ACT>
 __global__ void __launch_bounds__(256) k_act_bwd_tc(float* __restrict__ p0, const float* __restrict__ p1,
                                                     const float* __restrict__ dh, const __nv_bfloat16* __restrict__ bias,
@@ -323,22 +330,33 @@ __global__ void __launch_bounds__(256) k_act_bwd_tc(float* __restrict__ p0, cons
   const int g = blockIdx.y;
   const int lo = off ? off[g] : 0, hi = off ? off[g + 1] : rows;
   for (int r = lo + (int)blockIdx.x; r < hi; r += gridDim.x) {
-    for (int c = threadIdx.x; c < dff; c += blockDim.x) {
+    for (int c = 4 * threadIdx.x; c < dff; c += 4 * blockDim.x) {
       const size_t i = (size_t)r * dff + c;
-      float hv;
+      const float4 up = *reinterpret_cast<const float4*>(dh + i);
+      const float4 x0 = *reinterpret_cast<const float4*>(p0 + i);
+      float hv[4];
       if (ACT == ACT_SWIGLU) {
-        float dg, du;
-        swiglu_bwd(p0[i], p1[i], dh[i], dg, du, hv);
-        D[(size_t)r * ldd + c] = __float2bfloat16_rn(du);
-        D[(size_t)r * ldd + dff + c] = __float2bfloat16_rn(dg);
+        const float4 x1 = *reinterpret_cast<const float4*>(p1 + i);
+        float dg[4], du[4];
+        swiglu_bwd(x0.x, x1.x, up.x, dg[0], du[0], hv[0]);
+        swiglu_bwd(x0.y, x1.y, up.y, dg[1], du[1], hv[1]);
+        swiglu_bwd(x0.z, x1.z, up.z, dg[2], du[2], hv[2]);
+        swiglu_bwd(x0.w, x1.w, up.w, dg[3], du[3], hv[3]);
+        st_bf16x4(D + (size_t)r * ldd + c, du[0], du[1], du[2], du[3]);
+        st_bf16x4(D + (size_t)r * ldd + dff + c, dg[0], dg[1], dg[2], dg[3]);
       } else {
-        const float a = p0[i] + (bias ? __bfloat162float(bias[(size_t)g * dff + c]) : 0.f);
-        float da;
-        gelu_bwd(a, dh[i], da, hv);
-        p0[i] = da;
-        D[(size_t)r * ldd + c] = __float2bfloat16_rn(da);
+        float b4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (bias)
+          for (int j = 0; j < 4; ++j) b4[j] = __bfloat162float(bias[(size_t)g * dff + c + j]);
+        float4 da;
+        gelu_bwd(x0.x + b4[0], up.x, da.x, hv[0]);
+        gelu_bwd(x0.y + b4[1], up.y, da.y, hv[1]);
+        gelu_bwd(x0.z + b4[2], up.z, da.z, hv[2]);
+        gelu_bwd(x0.w + b4[3], up.w, da.w, hv[3]);
+        *reinterpret_cast<float4*>(p0 + i) = da;
+        st_bf16x4(D + (size_t)r * ldd + c, da.x, da.y, da.z, da.w);
       }
-      h[i] = __float2bfloat16_rn(hv);
+      st_bf16x4(h + i, hv[0], hv[1], hv[2], hv[3]);
     }
   }
 }
@@ -357,15 +375,17 @@ __global__ void k_pad_offsets(const int32_t* __restrict__ off, int G, int32_t* _
 
 // out [C][Kp]: padded column p of group g (koff[g] <= p < koff[g+1]) holds row off[g] + p - koff[g]
 // of in [rows][ldi] while that row is the group's, else zero.  off / koff NULL: one group of `rows`
-// rows, padded to a multiple of 64.  32 padded columns x 32 channels per block.
+// rows, padded to a multiple of 64.  64 padded columns x 64 channels per block, moved as bf16 pairs
+// (C, ldi and Kp even; each block's 64 columns lie in one group).
 __global__ void __launch_bounds__(256) k_transpose_pad(const __nv_bfloat16* __restrict__ in, int64_t ldi, int C,
                                                        const int32_t* __restrict__ off,
                                                        const int32_t* __restrict__ koff, int G, int rows,
                                                        __nv_bfloat16* __restrict__ out, int64_t Kp) {
-  __shared__ __nv_bfloat16 tile[32][34];
+  __shared__ uint32_t tw[64][33];  // [padded column][channel pair]
   __shared__ int s_r0, s_hi, s_live;
-  const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
-  if (threadIdx.x == 0 && threadIdx.y == 0) {
+  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  if (tx == 0 && ty == 0) {
     int live = 0, r0 = 0, hi = 0;
     if (off) {
       if (p0 < koff[G]) {
@@ -391,14 +411,18 @@ __global__ void __launch_bounds__(256) k_transpose_pad(const __nv_bfloat16* __re
   __syncthreads();
   if (!s_live) return;
   const int r0 = s_r0, hi = s_hi;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (r < hi && c < C) ? in[(size_t)r * ldi + c] : __float2bfloat16_rn(0.f);
+  for (int i = ty; i < 64; i += 8) {
+    const int r = r0 + i, c = c0 + 2 * tx;
+    tw[i][tx] = (r < hi && c < C) ? *reinterpret_cast<const uint32_t*>(in + (size_t)r * ldi + c) : 0u;
   }
   __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int c = c0 + i;
-    if (c < C) out[(size_t)c * Kp + p0 + threadIdx.x] = tile[threadIdx.x][i];
+  for (int j = ty; j < 64; j += 8) {
+    const int c = c0 + j;
+    if (c >= C) break;
+    const uint32_t w0 = tw[2 * tx][j >> 1], w1 = tw[2 * tx + 1][j >> 1];
+    const uint32_t lo = (j & 1) ? (w0 >> 16) : (w0 & 0xFFFFu);
+    const uint32_t hi2 = (j & 1) ? (w1 >> 16) : (w1 & 0xFFFFu);
+    *reinterpret_cast<uint32_t*>(out + (size_t)c * Kp + p0 + 2 * tx) = lo | (hi2 << 16);
   }
 }
 
@@ -572,11 +596,11 @@ cudaError_t ffn_bwd_tc(const ExpertBackward& b, bool glu, const __nv_bfloat16* x
   }
   const int64_t Kp = b.Kp;
   const int pad_cols = off ? (int)Kp : ((rows + 63) & ~63);
-  const dim3 tg((unsigned)(pad_cols / 32), 1);
-  k_transpose_pad<<<dim3(tg.x, (Kd + 31) / 32), tb, 0, st>>>(b.D, Kd, Kd, off, koff, G, rows, b.DT, Kp);
-  k_transpose_pad<<<dim3(tg.x, (f + 31) / 32), tb, 0, st>>>(b.h, f, f, off, koff, G, rows, b.hT, Kp);
-  k_transpose_pad<<<dim3(tg.x, (d + 31) / 32), tb, 0, st>>>(xr, d, d, off, koff, G, rows, b.xT, Kp);
-  k_transpose_pad<<<dim3(tg.x, (d + 31) / 32), tb, 0, st>>>(dyr, d, d, off, koff, G, rows, b.dyT, Kp);
+  const unsigned px = (unsigned)(pad_cols / 64);
+  k_transpose_pad<<<dim3(px, (Kd + 63) / 64), tb, 0, st>>>(b.D, Kd, Kd, off, koff, G, rows, b.DT, Kp);
+  k_transpose_pad<<<dim3(px, (f + 63) / 64), tb, 0, st>>>(b.h, f, f, off, koff, G, rows, b.hT, Kp);
+  k_transpose_pad<<<dim3(px, (d + 63) / 64), tb, 0, st>>>(xr, d, d, off, koff, G, rows, b.xT, Kp);
+  k_transpose_pad<<<dim3(px, (d + 63) / 64), tb, 0, st>>>(dyr, d, d, off, koff, G, rows, b.dyT, Kp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int cols = (rows + 63) & ~63;

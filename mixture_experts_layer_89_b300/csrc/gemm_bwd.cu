@@ -72,6 +72,7 @@ struct GbTile {
 __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constant__ CUtensorMap map_a,
                                                             const __grid_constant__ CUtensorMap map_b,
                                                             const __grid_constant__ CUtensorMap map_b2,
+                                                            const __grid_constant__ CUtensorMap map_c,
                                                             const GbArgs a) {
   extern __shared__ uint8_t gb_raw[];
   __shared__ GbCtl ctl;
@@ -276,10 +277,26 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
+        if (a.rows_on_k) {  // the store that last read the staging block has finished reading it
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           stg[lane * 8 + (j ^ (lane & 7))] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
                                                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        if (a.rows_on_k) {
+          // weight gradients: one asynchronous TMA store of the block (the layout above is the
+          // tensor map's 128-byte swizzle); rows past M are clipped by the map
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && 32 * q < t.mrows) {
+            tma_store_3d(&map_c, smem_u32(stg), t.n0 + 32 * c, t.m0 + 32 * q, t.g);
+            bulk_commit();
+          }
+          __syncwarp();
+          continue;
+        }
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -303,6 +320,8 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&ctl.tempty[acc]));
     }
+    if (lane == 0) bulk_wait_all();  // every tile store has completed before the CTA leaves
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -319,15 +338,15 @@ int sm_count() {
   return n;
 }
 
-cudaError_t launch_gb(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2, const GbArgs& a,
-                      long tiles_bound, cudaStream_t st) {
+cudaError_t launch_gb(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mb2, const CUtensorMap& mc,
+                      const GbArgs& a, long tiles_bound, cudaStream_t st) {
   if (tiles_bound <= 0) return cudaSuccess;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_bwd), GB_SMEM);
   if (e != cudaSuccess) return e;
   const int nsm = sm_count();
   if (nsm <= 0) return cudaErrorInvalidDevice;
   const int grid = (int)(tiles_bound < nsm ? tiles_bound : nsm);
-  k_gemm_bwd<<<grid, GB_THREADS, GB_SMEM, st>>>(ma, mb, mb2, a);
+  k_gemm_bwd<<<grid, GB_THREADS, GB_SMEM, st>>>(ma, mb, mb2, mc, a);
   return cudaGetLastError();
 }
 
@@ -392,17 +411,23 @@ cudaError_t launch_gemm_bwd_rows_m_nmajor(const void* A, int rows_alloc, const v
   a.status = status;
   const long nt = (N + GB_BN - 1) / GB_BN;
   const long rt = off ? (long)(rows_alloc + GB_BM - 1) / GB_BM + G : (long)(rows + GB_BM - 1) / GB_BM;
-  return launch_gb(ma, mb, mb2, a, rt * nt, st);
+  return launch_gb(ma, mb, mb2, mb, a, rt * nt, st);  // (the C map is unused on rows on M)
 }
 
 cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, int Kp, const int32_t* off, int G,
                                    int cols, float* C, int64_t ldc, int64_t c_stride, int beta, uint32_t* status,
                                    cudaStream_t st) {
   if (M <= 0 || N <= 0) return cudaSuccess;
-  if (Kp <= 0 || Kp % GB_BK || (!off && cols % GB_BK) || N % 32 || ldc % 4 || c_stride % 4 ||
+  if (Kp <= 0 || Kp % GB_BK || (!off && cols % GB_BK) || N % 32 || ldc % 4 || c_stride % 4 || beta ||
       (off && (G < 1 || G > GB_MAXG)) || !aligned16(A) || !aligned16(B) || !aligned16(C))
     return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mc;
+  {  // C as [G][M][N] fp32 for the epilogue's 32 x 32 TMA stores
+    const cuuint64_t dc[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)(off ? G : 1)};
+    const cuuint64_t sc[2] = {(cuuint64_t)ldc * 4, (cuuint64_t)(c_stride > 0 ? c_stride : (int64_t)M * ldc) * 4};
+    const cuuint32_t bc[3] = {32, 32, 1};
+    if (!make_tmap_f32(&mc, C, 3, dc, sc, bc)) return cudaErrorInvalidValue;
+  }
   const cuuint64_t da[2] = {(cuuint64_t)Kp, (cuuint64_t)M};
   const cuuint64_t db[2] = {(cuuint64_t)Kp, (cuuint64_t)N};
   const cuuint64_t s[1] = {(cuuint64_t)Kp * 2};
@@ -422,7 +447,7 @@ cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, i
   a.status = status;
   a.ksplit = 0;
   const long tiles = (long)(off ? G : 1) * ((M + GB_BM - 1) / GB_BM) * ((N + GB_BN - 1) / GB_BN);
-  return launch_gb(ma, mb, mb, a, tiles, st);
+  return launch_gb(ma, mb, mb, mc, a, tiles, st);
 }
 
 }  // namespace moe

@@ -953,6 +953,11 @@ bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t*
   return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ptr, rank, dims, strides, box);
 }
 
+bool make_tmap_f32(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box) {
+  return make_tmap(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ptr, rank, dims, strides, box);
+}
+
 namespace {
 // Largest number of co-resident 2-CTA clusters of a kernel (0 if none), per device.
 template <typename K>

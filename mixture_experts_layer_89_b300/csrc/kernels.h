@@ -181,5 +181,8 @@ cudaError_t ensure_smem_attr(const void* kernel, size_t bytes);
 // out-of-range elements of a box read as zero.  False (message in tc_last_error) on failure.
 bool make_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                     const cuuint32_t* box);
+// The same for fp32 tensors (32 floats per 128-byte swizzle row).
+bool make_tmap_f32(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box);
 
 }  // namespace moe
