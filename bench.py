@@ -383,7 +383,7 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
         res["eager"] = {"value": round(T * ws_n / (ms_eager * 1e-3), 1), "ms_per_step": round(ms_eager, 5),
                         "note": "moe_layer_forward issued from Python every step (host launch cost included)"}
         res["route_stats"] = route_stats_of(moe, wl, cfg, inp, layer, drops, dev, stream)
-        res["routing_backward"] = routing_backward_of(moe, wl, cfg, inp, dev, stream)
+        res["backward"] = backward_of(moe, wl, cfg, inp, dev, stream)
         res["e2e"] = e2e_of(moe, args, wl, cfg, inp, layer, y, counts, drops, dev, stream, ws_n)
         res["gpu_launches"] = moe.moe_layer_forward_launches(cfg) * args.steps
     del graph
@@ -399,31 +399,45 @@ def measure(args, wl, ws_n, local, full: bool, cpu_flops: float = 0.0):
     return res
 
 
-def routing_backward_of(moe, wl, cfg, inp, dev, stream, n=5):
-    """The routing half of the backward pass on this workload: moe_combine_backward and
-    moe_route_backward on the forward steps' own outputs (routing, rows, y_perm), timed alone with
-    CUDA events (n calls after two warm-ups), outside the layer's figures."""
-    T, d, E, k = wl.T, wl.d, wl.E, wl.k
+def backward_of(moe, wl, cfg, inp, dev, stream, n=5):
+    """The backward pass on this workload: moe_combine_backward, moe_route_backward and
+    moe_expert_ffn_backward on the forward steps' own outputs (routing, rows, y_perm), each timed
+    alone with CUDA events (n calls after two warm-ups), outside the layer's figures."""
+    T, d, E, k, f, S = wl.T, wl.d, wl.E, wl.k, wl.dff, wl.n_shared
     cap, amax = moe.moe_capacity(cfg)
     ws = moe.alloc_workspace(cfg, dev)
     i32 = dict(dtype=torch.int32, device=dev)
-    idx, tw = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
-    counts, losses = torch.empty(E, **i32), torch.empty(2, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    idx, tw = torch.empty((T, k), **i32), torch.empty((T, k), **f32)
+    counts, losses = torch.empty(E, **i32), torch.empty(2, **f32)
     moe.moe_route(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), idx, tw, counts, losses, ws, stream)
     offsets, kept, row_of = torch.empty(E + 1, **i32), torch.empty(E, **i32), torch.empty((T, k), **i32)
     tok_of = torch.empty(max(amax, 1), **i32)
     x_perm = torch.empty((max(amax, 1), d), dtype=inp["x"].dtype, device=dev)
     moe.moe_permute(cfg, inp["x"], idx, counts, offsets, kept, row_of, tok_of, x_perm, ws, stream)
-    y_perm = torch.empty((max(amax, 1), d), dtype=torch.float32, device=dev)
-    y_sh = torch.empty((T, d), dtype=torch.float32, device=dev) if wl.n_shared else None
-    moe.moe_expert_ffn(cfg, x_perm, offsets, moe.make_weights(inp), y_perm, inp["x"], y_sh, ws, stream)
+    y_perm = torch.empty((max(amax, 1), d), **f32)
+    y_sh = torch.empty((T, d), **f32) if S else None
+    weights = moe.make_weights(inp)
+    moe.moe_expert_ffn(cfg, x_perm, offsets, weights, y_perm, inp["x"], y_sh, ws, stream)
     g = torch.Generator(device=dev).manual_seed(12345)
     dy = torch.randn((T, d), generator=g, device=dev).to(inp["x"].dtype)
-    dw = torch.empty((T, k), dtype=torch.float32, device=dev)
+    dw = torch.empty((T, k), **f32)
     dy_perm = torch.empty_like(x_perm)
-    dz = torch.empty((T, E), dtype=torch.float32, device=dev)
-    dwr = torch.empty((E, d), dtype=torch.float32, device=dev)
-    dx = torch.empty((T, d), dtype=torch.float32, device=dev)
+    dz = torch.empty((T, E), **f32)
+    dwr = torch.empty((E, d), **f32)
+    dx = torch.empty((T, d), **f32)
+    glu = wl.act == "swiglu"
+    grads = {"dw_up": torch.empty((E, f, d), **f32), "dw_down": torch.empty((E, d, f), **f32)}
+    if glu:
+        grads["dw_gate"] = torch.empty((E, f, d), **f32)
+    if wl.bias:
+        grads["db_up"], grads["db_down"] = torch.empty((E, f), **f32), torch.empty((E, d), **f32)
+    if S:
+        grads["dws_up"], grads["dws_down"] = torch.empty((S, f, d), **f32), torch.empty((S, d, f), **f32)
+        if glu:
+            grads["dws_gate"] = torch.empty((S, f, d), **f32)
+    scratch = torch.empty(max(moe.moe_expert_backward_scratch_size(cfg), 256), dtype=torch.uint8, device=dev)
+    gstruct = moe.make_expert_grads(grads)
 
     def comb():
         moe.moe_combine_backward(cfg, dy, y_perm, row_of, tw, dw, dy_perm, stream)
@@ -431,6 +445,10 @@ def routing_backward_of(moe, wl, cfg, inp, dev, stream, n=5):
     def rout():
         moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), idx, tw, counts, dw, 1.0, 1.0,
                                dz, dwr, dx, stream)
+
+    def expert():
+        moe.moe_expert_ffn_backward(cfg, weights, inp["x"], x_perm, offsets, row_of, dy, dy_perm, gstruct, dx,
+                                    scratch, stream)
 
     def time_it(fn):
         for _ in range(2):
@@ -444,16 +462,24 @@ def routing_backward_of(moe, wl, cfg, inp, dev, stream, n=5):
         torch.cuda.synchronize(dev)
         return t0.elapsed_time(t1) / n
 
-    ms_c, ms_r = time_it(comb), time_it(rout)
+    ms_c, ms_r, ms_e = time_it(comb), time_it(rout), time_it(expert)
+    status = moe.moe_read_device_status(scratch)
     elt = 2 if wl.dtype == "bf16" else 4
     rows = int(offsets[E].item())
     comb_bytes = T * d * elt + rows * d * (4 + elt)          # dy in, kept rows of y_perm in, dy_perm out
     rout_flops = 3 * 2.0 * T * E * d                         # logits recomputed, dz^T x, dz W_r
-    del ws, x_perm, y_perm, y_sh, dy_perm, dx
+    units = 7 if glu else 5                                  # recomputed pre-activations, dh, dW (x2-3), dx
+    exp_flops = 2.0 * d * f * units * (rows + S * T)
+    del ws, x_perm, y_perm, y_sh, dy_perm, dx, grads, scratch
     return {"combine_backward_ms": round(ms_c, 4), "combine_backward_GB/s": round(comb_bytes / (ms_c * 1e-3) / 1e9, 1),
             "route_backward_ms": round(ms_r, 4),
             "route_backward_TFLOP/s": round(rout_flops / (ms_r * 1e-3) / 1e12, 2),
-            "note": "routing half of the backward pass (fp32 CUDA-core contractions), timed alone, n=%d" % n}
+            "expert_backward_ms": round(ms_e, 4),
+            "expert_backward_TFLOP/s": round(exp_flops / (ms_e * 1e-3) / 1e12, 1),
+            "expert_backward_status": int(status),
+            "note": "backward pass, each call timed alone, n=%d: routing half on fp32 CUDA cores; expert FFNs %s"
+                    % (n, "on the tensor cores (bf16 operands, fp32 accumulators and gradients)" if wl.dtype == "bf16"
+                       else "on fp32 CUDA cores")}
 
 
 def route_stats_of(moe, wl, cfg, inp, layer, drops, dev, stream):
@@ -565,7 +591,7 @@ def run_ours(args, wl, ws_n, rank, local):
         "config": arm_config(wl, ws_n),
     }
     for key in ("expert_tflops", "expert_frac_of_burst_peak", "expert_frac_of_sustained_peak", "stage_ms",
-                "kept_rows", "drops", "roofline", "weight_stream", "route_stats", "routing_backward", "e2e",
+                "kept_rows", "drops", "roofline", "weight_stream", "route_stats", "backward", "e2e",
                 "gpu_launches", "clocks", "stage_clocks", "cpu_baseline"):
         if key in head:
             res[key] = head[key]
