@@ -437,6 +437,8 @@ def backward_of(moe, wl, cfg, inp, dev, stream, n=5):
         if glu:
             grads["dws_gate"] = torch.empty((S, f, d), **f32)
     scratch = torch.empty(max(moe.moe_expert_backward_scratch_size(cfg), 256), dtype=torch.uint8, device=dev)
+    n_rs = moe.moe_route_backward_scratch_size(cfg)
+    rscratch = torch.empty(n_rs, dtype=torch.uint8, device=dev) if n_rs else None
     gstruct = moe.make_expert_grads(grads)
 
     def comb():
@@ -444,7 +446,7 @@ def backward_of(moe, wl, cfg, inp, dev, stream, n=5):
 
     def rout():
         moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), idx, tw, counts, dw, 1.0, 1.0,
-                               dz, dwr, dx, stream)
+                               dz, dwr, dx, rscratch, stream)
 
     def expert():
         moe.moe_expert_ffn_backward(cfg, weights, inp["x"], x_perm, offsets, row_of, dy, dy_perm, gstruct, dx,
@@ -470,15 +472,17 @@ def backward_of(moe, wl, cfg, inp, dev, stream, n=5):
     rout_flops = 3 * 2.0 * T * E * d                         # logits recomputed, dz^T x, dz W_r
     units = 7 if glu else 5                                  # recomputed pre-activations, dh, dW (x2-3), dx
     exp_flops = 2.0 * d * f * units * (rows + S * T)
-    del ws, x_perm, y_perm, y_sh, dy_perm, dx, grads, scratch
+    del ws, x_perm, y_perm, y_sh, dy_perm, dx, grads, scratch, rscratch
     return {"combine_backward_ms": round(ms_c, 4), "combine_backward_GB/s": round(comb_bytes / (ms_c * 1e-3) / 1e9, 1),
             "route_backward_ms": round(ms_r, 4),
             "route_backward_TFLOP/s": round(rout_flops / (ms_r * 1e-3) / 1e12, 2),
             "expert_backward_ms": round(ms_e, 4),
             "expert_backward_TFLOP/s": round(exp_flops / (ms_e * 1e-3) / 1e12, 1),
             "expert_backward_status": int(status),
-            "note": "backward pass, each call timed alone, n=%d: routing half on fp32 CUDA cores; expert FFNs %s"
-                    % (n, "on the tensor cores (bf16 operands, fp32 accumulators and gradients)" if wl.dtype == "bf16"
+            "note": "backward pass, each call timed alone, n=%d: combine backward on CUDA cores; router backward "
+                    "%s; expert FFNs %s"
+                    % (n, "on the tensor cores (dz as bf16 hi + lo)" if n_rs else "on fp32 CUDA cores",
+                       "on the tensor cores (bf16 operands, fp32 accumulators and gradients)" if wl.dtype == "bf16"
                        else "on fp32 CUDA cores")}
 
 

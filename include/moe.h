@@ -314,17 +314,24 @@ moe_status moe_quantize_experts(const void* w, int32_t dtype, int32_t format, in
  *   x [T,d], w_router [E,d], logit_bias [E] or NULL, topk_idx / topk_w [T,k] and counts [E] as
  *   moe_route returned them, dw [T,k] from moe_combine_backward, dlb / dzl the weights of the two
  *   losses in the objective
- *   -> dz [T,E] fp32, the gradient of the logits (z recomputed in fp32); dw_router [E,d] fp32 =
- *      dz^T x; dx [T,d] fp32 = dz W_r, the router's part of the input gradient (overwritten).
+ *   -> dz [T,E] fp32, the gradient of the logits (z recomputed with fp32 accumulation);
+ *      dw_router [E,d] fp32 = dz^T x; dx [T,d] fp32 = dz W_r, the router's part of the input
+ *      gradient (overwritten).
+ *   scratch: NULL, or moe_route_backward_scratch_size bytes of device memory (256-byte aligned).
+ *   With it, a bf16 layer whose E is a multiple of 64 runs the three contractions on the tensor
+ *   cores (dz entering them as two bf16 parts, hi + lo, so within ~2^-17 of fp32); its first word
+ *   is then a device status word (moe_read_device_status).  Without it, or for other layers
+ *   (size 0), they run in fp32 on the CUDA cores.
  * MOE_ERR_INVALID_ARG for NULL or misaligned pointers, MOE_ERR_UNSUPPORTED outside the shape
  * limits of the forward. */
 moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const float* y_perm,
                                 const int32_t* row_of, const float* topk_w, float* dw, void* dy_perm,
                                 void* stream);
+moe_status moe_route_backward_scratch_size(const moe_config* cfg, size_t* bytes);
 moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* w_router,
                               const float* logit_bias, const int32_t* topk_idx, const float* topk_w,
                               const int32_t* counts, const float* dw, float dlb, float dzl, float* dz,
-                              float* dw_router, float* dx, void* stream);
+                              float* dw_router, float* dx, void* scratch, void* stream);
 
 /* Gradients of the expert FFN weights, fp32, in the layouts of the weights in moe_weights. */
 typedef struct {

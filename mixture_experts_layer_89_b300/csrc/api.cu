@@ -168,6 +168,31 @@ ExpertBwdScratch expert_bwd_scratch(const moe_config* c) {
   return L;
 }
 
+// Scratch of the router backward's tensor-core path: bf16 layers with E a multiple of 64 and T > 0;
+// 0 bytes otherwise (the CUDA-core path needs none).
+struct RouterBwdLayout {
+  size_t status, dzs, dzsT, xT, part, total;
+};
+
+RouterBwdLayout route_bwd_layout(const moe_config* c) {
+  RouterBwdLayout L{};
+  if (!is_bf16(c) || c->E % 64 || c->T <= 0) return L;
+  const size_t Tp = (size_t)round64(c->T), E = (size_t)c->E, d = (size_t)c->d;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t a = off;
+    off += align256(bytes);
+    return a;
+  };
+  L.status = take(256);
+  L.dzs = take((size_t)c->T * 2 * E * 2);
+  L.dzsT = take(2 * E * Tp * 2);
+  L.xT = take(d * Tp * 2);
+  L.part = take(2 * E * d * 4);
+  L.total = off;
+  return L;
+}
+
 template <typename P>
 inline P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
@@ -691,20 +716,38 @@ moe_status moe_combine_backward(const moe_config* cfg, const void* dy, const flo
                                              dy_perm, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_route_backward_scratch_size(const moe_config* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = route_bwd_layout(cfg).total;
+  return MOE_OK;
+}
+
 moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* w_router, const float* logit_bias,
                               const int32_t* topk_idx, const float* topk_w, const int32_t* counts, const float* dw,
-                              float dlb, float dzl, float* dz, float* dw_router, float* dx, void* stream) {
+                              float dlb, float dzl, float* dz, float* dw_router, float* dx, void* scratch,
+                              void* stream) {
   NvtxRange nvtx_range("moe_route_backward");
   MOE_TRY(validate(cfg));
   if (!w_router || !counts || !dw_router) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!x || !topk_idx || !topk_w || !dw || !dz || !dx)) return MOE_ERR_INVALID_ARG;
   if (!isfinite(dlb) || !isfinite(dzl)) return MOE_ERR_INVALID_ARG;
-  const void* ps[] = {x, w_router, logit_bias, topk_idx, topk_w, counts, dw, dz, dw_router, dx};
+  const void* ps[] = {x, w_router, logit_bias, topk_idx, topk_w, counts, dw, dz, dw_router, dx, scratch};
   for (const void* p : ps)
     if (misaligned(p)) return MOE_ERR_INVALID_ARG;
+  const RouterBwdLayout L = route_bwd_layout(cfg);
+  RouterBwdScratch sc{};
+  const bool tc = scratch && L.total > 0;
+  if (tc) {
+    sc.status = at<uint32_t>(scratch, L.status);
+    sc.dzs = at<__nv_bfloat16>(scratch, L.dzs);
+    sc.dzsT = at<__nv_bfloat16>(scratch, L.dzsT);
+    sc.xT = at<__nv_bfloat16>(scratch, L.xT);
+    sc.part = at<float>(scratch, L.part);
+  }
   return cuda_status(launch_router_backward(is_bf16(cfg), x, w_router, logit_bias, topk_idx, topk_w, counts, dw,
                                             cfg->T, cfg->d, cfg->E, cfg->k, inv_tau_of(cfg), cfg->lb_coef,
-                                            cfg->z_coef, dlb, dzl, dz, dw_router, dx,
+                                            cfg->z_coef, dlb, dzl, dz, dw_router, dx, tc ? &sc : nullptr,
                                             static_cast<cudaStream_t>(stream)));
 }
 

@@ -227,6 +227,66 @@ __global__ void __launch_bounds__(256) k_router_dz2(const float* zin, const floa
   }
 }
 
+__global__ void k_transpose_pad(const __nv_bfloat16* __restrict__ in, int64_t ldi, int C,
+                                const int32_t* __restrict__ off, const int32_t* __restrict__ koff, int G, int rows,
+                                __nv_bfloat16* __restrict__ out, int64_t Kp);
+
+// dz [T, E] fp32 -> dzs [T, 2E] bf16: hi = bf16(dz) at column e, lo = bf16(dz - hi) at E + e
+// (hi + lo carries 16 significant bits: |dz - hi - lo| <= 2^-17 |dz|).
+__global__ void __launch_bounds__(256) k_split_hi_lo(const float* __restrict__ dz, int Tn, int E,
+                                                     __nv_bfloat16* __restrict__ dzs) {
+  const size_t n = (size_t)Tn * E;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / E, e = i % E;
+    const float v = dz[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    dzs[t * 2 * E + e] = hi;
+    dzs[t * 2 * E + E + e] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+}
+
+// out[i] = part[i] + part[n + i]: the hi and lo halves of dW_r summed.
+__global__ void __launch_bounds__(256) k_sum_halves(const float* __restrict__ part, size_t n, float* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+    out[i] = part[i] + part[n + i];
+}
+
+// bf16 layers with E a multiple of 64 and a scratch: the three contractions on the tensor cores
+// (k_gemm_bwd).  The logits are recomputed with fp32 accumulation from the bf16 x and W_r as on
+// the CUDA cores; dz enters dW_r = dz^T x and dx = dz W_r as its bf16 hi and lo parts side by side
+// along K (so both keep ~2^-17 relative accuracy): dx = [hi | lo] [W_r; W_r] in one contraction
+// (W_r read N-major twice), and [hi^T; lo^T] x as a 2E x d product whose halves are summed.
+// scratch: status word, dzs [T, 2E] and its transpose [2E, Tp] bf16, x^T [d, Tp] bf16 (Tp = T
+// padded to 64), the 2E x d fp32 product.
+cudaError_t router_bwd_tc(const __nv_bfloat16* x, const __nv_bfloat16* wr, const float* lbias, const int32_t* idx,
+                          const float* tw, const int32_t* counts, const float* dw, int T_, int d, int E, int k,
+                          float inv_tau, float lb_coef, float z_coef, float dlb, float dzl, float* dz, float* dwr,
+                          float* dx, const RouterBwdScratch& sc, cudaStream_t st) {
+  const int Tp = (T_ + 63) & ~63;
+  cudaError_t e = cudaMemsetAsync(sc.status, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess)  // z [T, E] = x W_r^T
+    e = launch_gemm_bwd_rows_m(x, T_, wr, 1, E, d, nullptr, 1, T_, dz, E, 0, sc.status, st);
+  if (e != cudaSuccess) return e;
+  k_router_dz2<__nv_bfloat16><<<(T_ + 7) / 8, 256, 0, st>>>(dz, lbias, idx, tw, counts, dw, T_, E, k, inv_tau, lb_coef,
+                                                            z_coef, dlb, dzl, dz);
+  k_split_hi_lo<<<592, 256, 0, st>>>(dz, T_, E, sc.dzs);
+  const dim3 tb(32, 8);
+  k_transpose_pad<<<dim3(Tp / 64, (2 * E + 63) / 64), tb, 0, st>>>(sc.dzs, 2 * E, 2 * E, nullptr, nullptr, 1, T_,
+                                                                   sc.dzsT, Tp);
+  k_transpose_pad<<<dim3(Tp / 64, (d + 63) / 64), tb, 0, st>>>(x, d, d, nullptr, nullptr, 1, T_, sc.xT, Tp);
+  e = cudaGetLastError();
+  if (e == cudaSuccess)  // [hi^T; lo^T] x over the tokens
+    e = launch_gemm_bwd_rows_k(sc.dzsT, 2 * E, sc.xT, d, Tp, nullptr, 1, Tp, sc.part, d, (int64_t)2 * E * d, 0,
+                               sc.status, st);
+  if (e != cudaSuccess) return e;
+  k_sum_halves<<<592, 256, 0, st>>>(sc.part, (size_t)E * d, dwr);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // dx = [hi | lo] [W_r; W_r]
+  return launch_gemm_bwd_rows_m_nmajor(sc.dzs, T_, wr, wr, E, 1, d, 2 * E, nullptr, 1, T_, dx, d, 0, sc.status, st,
+                                       true);
+}
+
 template <typename T>
 cudaError_t router_bwd_t(const void* x, const void* wr, const float* lbias, const int32_t* idx, const float* tw,
                          const int32_t* counts, const float* dw, int T_, int d, int E, int k, float inv_tau,
@@ -669,8 +729,11 @@ cudaError_t launch_combine_backward(bool bf16, const void* dy, const float* y_pe
 cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, const float* lbias, const int32_t* idx,
                                    const float* tw, const int32_t* counts, const float* dw, int T, int d, int E, int k,
                                    float inv_tau, float lb_coef, float z_coef, float dlb, float dzl, float* dz,
-                                   float* dwr, float* dx, cudaStream_t st) {
+                                   float* dwr, float* dx, const RouterBwdScratch* sc, cudaStream_t st) {
   if (E < 1 || E > 256 || k < 1 || k > 8 || k > E) return cudaErrorInvalidValue;
+  if (sc && bf16 && T > 0)
+    return router_bwd_tc(static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(wr), lbias, idx, tw,
+                         counts, dw, T, d, E, k, inv_tau, lb_coef, z_coef, dlb, dzl, dz, dwr, dx, *sc, st);
   if (bf16)
     return router_bwd_t<__nv_bfloat16>(x, wr, lbias, idx, tw, counts, dw, T, d, E, k, inv_tau, lb_coef, z_coef, dlb,
                                        dzl, dz, dwr, dx, st);

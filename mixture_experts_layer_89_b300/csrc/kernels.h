@@ -126,10 +126,18 @@ struct Projection {
 cudaError_t launch_combine_backward(bool bf16, const void* dy, const float* y_perm, const int32_t* row_of,
                                     const float* topk_w, int T, int d, int k, float* dw, void* dy_perm,
                                     cudaStream_t st);
+// Scratch of the router backward's tensor-core path (bf16 layers, E a multiple of 64): status
+// word, dzs [T][2E] and dzsT [2E][Tp] bf16, xT [d][Tp] bf16, part [2E][d] fp32 (Tp = T padded to 64).
+struct RouterBwdScratch {
+  uint32_t* status;
+  __nv_bfloat16 *dzs, *dzsT, *xT;
+  float* part;
+};
+// sc == NULL (or an fp32 layer): the CUDA-core path.
 cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, const float* lbias, const int32_t* idx,
                                    const float* tw, const int32_t* counts, const float* dw, int T, int d, int E, int k,
                                    float inv_tau, float lb_coef, float z_coef, float dlb, float dzl, float* dz,
-                                   float* dwr, float* dx, cudaStream_t st);
+                                   float* dwr, float* dx, const RouterBwdScratch* sc, cudaStream_t st);
 // Backward of the expert FFNs (routed over the permuted rows, then the shared experts over all
 // tokens).  Weights and activations in the layer dtype, gradients fp32; act is ACT_GELU or
 // ACT_SWIGLU; rows_bound bounds any expert's rows (0: no routed rows), rows_alloc = A_max; s0..s2

@@ -87,7 +87,8 @@ def lib() -> ctypes.CDLL:
         L.moe_quantize_experts.argtypes = [_c_p, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_p, _c_p, _c_p, _c_p]
         L.moe_combine_backward.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_route_backward.argtypes = [cfgp, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p, ctypes.c_float,
-                                         ctypes.c_float, _c_p, _c_p, _c_p, _c_p]
+                                         ctypes.c_float, _c_p, _c_p, _c_p, _c_p, _c_p]
+        L.moe_route_backward_scratch_size.argtypes = [cfgp, P(ctypes.c_size_t)]
         L.moe_expert_backward_scratch_size.argtypes = [cfgp, P(ctypes.c_size_t)]
         L.moe_expert_ffn_backward.argtypes = [cfgp, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                                               P(MoeExpertGrads), _c_p, _c_p, _c_p]
@@ -99,7 +100,8 @@ def lib() -> ctypes.CDLL:
                      "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_layer_forward_timed",
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
                      "moe_set_wait_limit", "moe_route_diagnostics", "moe_quantize_experts", "moe_combine_backward",
-                     "moe_route_backward", "moe_expert_backward_scratch_size", "moe_expert_ffn_backward"):
+                     "moe_route_backward", "moe_route_backward_scratch_size", "moe_expert_backward_scratch_size",
+                     "moe_expert_ffn_backward"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -108,7 +110,7 @@ def lib() -> ctypes.CDLL:
 EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_ffn",
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
             "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_route_diagnostics",
-            "moe_quantize_experts", "moe_combine_backward", "moe_route_backward",
+            "moe_quantize_experts", "moe_combine_backward", "moe_route_backward", "moe_route_backward_scratch_size",
             "moe_expert_backward_scratch_size", "moe_expert_ffn_backward", "moe_status_string", "moe_last_error")
 
 
@@ -260,11 +262,17 @@ def moe_combine_backward(cfg, dy, y_perm, row_of, topk_w, dw, dy_perm, stream=No
                                       _p(dy_perm), _s(stream)), "moe_combine_backward")
 
 
+def moe_route_backward_scratch_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_route_backward_scratch_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_route_backward_scratch_size")
+    return int(n.value)
+
+
 def moe_route_backward(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, dw, dlb, dzl, dz, dw_router, dx,
-                       stream=None):
+                       scratch=None, stream=None):
     _check(lib().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx),
                                     _p(topk_w), _p(counts), _p(dw), float(dlb), float(dzl), _p(dz), _p(dw_router),
-                                    _p(dx), _s(stream)), "moe_route_backward")
+                                    _p(dx), _p(scratch), _s(stream)), "moe_route_backward")
 
 
 def moe_expert_backward_scratch_size(cfg: MoeConfig) -> int:

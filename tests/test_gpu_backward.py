@@ -1,6 +1,7 @@
 """GPU backward of the routing half of the layer against the oracle (needs a B300).
 
-moe_combine_backward and moe_route_backward run on the forward steps' own outputs (routing,
+moe_combine_backward and moe_route_backward (both of its paths: fp32 CUDA cores, and the tensor
+cores with dz split into bf16 hi + lo parts) run on the forward steps' own outputs (routing,
 rows, y_perm from moe_route / moe_permute / moe_expert_ffn); the oracle's combine_backward and
 router_backward get the same routing and rows (so near-tie tokens need no exemption), and its own
 fp64 logits for the softmax.  Acceptance: fp32 gradients normwise, max|d| <= 1e-4 max|ref|; the
@@ -55,11 +56,6 @@ def test_routing_backward_matches_oracle(case):
     dy_perm = torch.zeros_like(st["x_perm"])
     moe.moe_combine_backward(cfg, dy, st["y_perm"], st["row_of"], st["topk_w"], dw, dy_perm)
     dlb, dzl = 1.3, 0.7
-    dz = torch.empty((T, E), dtype=torch.float32, device="cuda")
-    dwr = torch.empty((E, d), dtype=torch.float32, device="cuda")
-    dx = torch.empty((T, d), dtype=torch.float32, device="cuda")
-    moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), st["topk_idx"], st["topk_w"],
-                           st["counts"], dw, dlb, dzl, dz, dwr, dx)
     torch.cuda.synchronize()
 
     row_of = st["row_of"].cpu().numpy()
@@ -81,15 +77,29 @@ def test_routing_backward_matches_oracle(case):
     rb = B.router_backward(O._f64(inp_cpu["x"]), O._f64(inp_cpu["w_router"]), P, lse,
                            st["topk_idx"].cpu().numpy(), tw, to_np(dw), st["counts"].cpu().numpy(), E=E, k=k,
                            lb_coef=wl.lb_coef, z_coef=wl.z_coef, dlb=dlb, dzl=dzl, temperature=wl.temperature)
-    _close(to_np(dz), rb["dz"], "dz")
-    _close(to_np(dwr), rb["dw_router"], "dw_router")
-    _close(to_np(dx), rb["dx"], "dx")
-    # deterministic: a second call gives the same bits
-    dz2, dwr2, dx2 = torch.empty_like(dz), torch.empty_like(dwr), torch.empty_like(dx)
-    moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), st["topk_idx"], st["topk_w"],
-                           st["counts"], dw, dlb, dzl, dz2, dwr2, dx2)
-    torch.cuda.synchronize()
-    assert torch.equal(dz, dz2) and torch.equal(dwr, dwr2) and torch.equal(dx, dx2)
+    n_scratch = moe.moe_route_backward_scratch_size(cfg)
+    # bf16 layers with E a multiple of 64 have a tensor-core path (taken when a scratch is given);
+    # every layer has the CUDA-core one
+    assert (n_scratch > 0) == (wl.dtype == "bf16" and E % 64 == 0)
+    for scratch in ([None, torch.empty(n_scratch, dtype=torch.uint8, device="cuda")] if n_scratch else [None]):
+        path = "CUDA cores" if scratch is None else "tensor cores"
+        outs = []
+        for _ in range(2):  # deterministic: a second call gives the same bits
+            dz = torch.full((T, E), float("nan"), dtype=torch.float32, device="cuda")
+            dwr = torch.full((E, d), float("nan"), dtype=torch.float32, device="cuda")
+            dx = torch.full((T, d), float("nan"), dtype=torch.float32, device="cuda")
+            moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), st["topk_idx"],
+                                   st["topk_w"], st["counts"], dw, dlb, dzl, dz, dwr, dx, scratch)
+            torch.cuda.synchronize()
+            outs.append((dz, dwr, dx))
+        dz, dwr, dx = outs[0]
+        print(f"  {path}:")
+        _close(to_np(dz), rb["dz"], "dz")
+        _close(to_np(dwr), rb["dw_router"], "dw_router")
+        _close(to_np(dx), rb["dx"], "dx")
+        assert all(torch.equal(a, b) for a, b in zip(outs[0], outs[1]))
+        if scratch is not None:
+            assert moe.moe_read_device_status(scratch) == moe.MOE_OK
 
 
 def test_routing_backward_empty_batch_and_arguments():
@@ -105,4 +115,5 @@ def test_routing_backward_empty_batch_and_arguments():
     import ctypes
     L = moe.lib()
     assert L.moe_route_backward(ctypes.byref(moe.config_from_workload(CASES["bf16_swiglu_cap"])), None, None, None,
-                                None, None, None, None, 1.0, 1.0, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+                                None, None, None, None, 1.0, 1.0, None, None, None, None,
+                                None) == moe.MOE_ERR_INVALID_ARG
