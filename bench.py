@@ -38,11 +38,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # kernel, from ncu captures (profiles/k_proj_tc_skewed_e16_bf16.md), keyed by workload; valid only
 # while gemm_tc.cu and common.cuh hash to src_sha1.  skewed_e16_bf16 is measured; skewed_bf16 is
 # too large to capture under a full metric set, so its figure is the stand-in's traffic per
-# algorithmic byte (1.0146) times the full launch's algorithmic bytes (weights of 128 experts,
+# algorithmic byte (1.0143) times the full launch's algorithmic bytes (weights of 128 experts,
 # token rows in, hidden rows out).
 NCU_TRAFFIC = {
-    "skewed_e16_bf16": {"bytes": 1669744896 + 49454336, "src_sha1": "825df9e24e918d1025eac665d225029d1cd08c7e"},
-    "skewed_bf16": {"bytes": 13753593856, "src_sha1": "825df9e24e918d1025eac665d225029d1cd08c7e",
+    "skewed_e16_bf16": {"bytes": 1669249536 + 49530112, "src_sha1": "4289058b31e7b631343f91ba81d028ca6d3e9552"},
+    "skewed_bf16": {"bytes": 13750237184, "src_sha1": "4289058b31e7b631343f91ba81d028ca6d3e9552",
                     "scaled_from": "skewed_e16_bf16"},
 }
 
