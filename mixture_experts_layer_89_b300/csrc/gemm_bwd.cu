@@ -13,11 +13,16 @@
 // [g][k][n] of one tensor for k < ksplit and of a second one (at k - ksplit) beyond, so that
 // dh = dy W_down and dx = du W_up + dg W_gate need no transposed copy of the weights.
 //
-// Persistent CTAs (one per SM: four 48 KB stages of a 128 x 64 A tile and a 256 x 64 B tile, both
-// written by TMA with the 128-byte swizzle) walk the 128 x 256 output tiles of all groups in
-// order.  Warp 0 loads the stages, warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16, one thread)
-// into one of two TMEM accumulators (2 x 256 columns), warps 2-5 drain the other one into C while
-// the next tile accumulates (32 x 32 blocks staged in shared memory for coalesced stores).  Each output is one accumulation in k order, so results do not depend
+// Persistent 2-SM pairs (a cluster of two CTAs, one per SM, issuing tcgen05.mma with
+// cta_group::2): a pair owns a 256 x 256 output tile, each CTA 128 rows of it.  Per 64-deep K step
+// each CTA holds its 128 rows of A and its 128-row half of B (32 KB, written by TMA with the
+// 128-byte swizzle), so the operand stream per SM is 2/3 of what one SM alone would need for a
+// 128 x 256 tile.  The pairs walk the tiles of all groups in order.  In each CTA warp 0 loads the
+// stages (both CTAs' copies complete on the leader's barrier); the leader's warp 1 issues the MMAs
+// (M = 256, N = 256, K = 16) into one of two TMEM accumulators (2 x 256 columns in each CTA) and
+// its commits reach both CTAs; warps 2-5 of each CTA drain its own 128 rows of the other
+// accumulator into C (32 x 32 blocks staged in shared memory for coalesced or TMA stores) while
+// the next tile accumulates.  Each output is one accumulation in k order, so results do not depend
 // on scheduling.  Every wait is bounded: on a time-out the kernel records DEV_TIMEOUT in the status
 // word, lets its copies and MMAs in flight land, frees its tensor memory and returns.
 #include "common.cuh"
@@ -26,16 +31,18 @@
 namespace moe {
 
 namespace {
-constexpr int GB_BM = 128, GB_BN = 256, GB_BK = 64, GB_STAGES = 4, GB_MAXG = 256;
-constexpr int GB_A_BYTES = GB_BM * GB_BK * 2;  // 16 KB
-constexpr int GB_B_BYTES = GB_BN * GB_BK * 2;  // 32 KB
+constexpr int GB_BM = 128;   // rows of C per CTA (256 per pair)
+constexpr int GB_BN = 256;   // columns of C per tile (each CTA holds half of B's 256 rows)
+constexpr int GB_BK = 64, GB_STAGES = 6, GB_MAXG = 256;
+constexpr int GB_A_BYTES = GB_BM * GB_BK * 2;        // 16 KB
+constexpr int GB_B_BYTES = (GB_BN / 2) * GB_BK * 2;  // 16 KB
 constexpr int GB_STAGE_BYTES = GB_A_BYTES + GB_B_BYTES;
 constexpr int GB_THREADS = 192;
 constexpr uint32_t GB_TMEM_COLS = 2 * GB_BN;
 constexpr int GB_EPI_BYTES = 4 * 32 * 32 * 4;  // one 32 x 32 fp32 staging block per epilogue warp
 constexpr size_t GB_SMEM = (size_t)GB_STAGES * GB_STAGE_BYTES + GB_EPI_BYTES + 1024;  // + alignment slack
 static_assert(GB_STAGE_BYTES % 1024 == 0 && GB_A_BYTES % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-static_assert(GB_SMEM <= 227 * 1024, "stages fit the shared memory of one CTA");
+static_assert(GB_SMEM <= 227 * 1024 - 4096, "stages fit the shared memory of one CTA");
 static_assert(GB_MAXG <= 32 * 8, "eight groups per lane in the tile count");
 
 struct GbCtl {
@@ -69,27 +76,29 @@ struct GbTile {
   int g, m0, n0, mrows, kb, k0;
 };
 
-__global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constant__ CUtensorMap map_a,
-                                                            const __grid_constant__ CUtensorMap map_b,
-                                                            const __grid_constant__ CUtensorMap map_b2,
-                                                            const __grid_constant__ CUtensorMap map_c,
-                                                            const GbArgs a) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GB_THREADS, 1)
+    k_gemm_bwd(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+               const __grid_constant__ CUtensorMap map_b2, const __grid_constant__ CUtensorMap map_c,
+               const GbArgs a) {
   extern __shared__ uint8_t gb_raw[];
   __shared__ GbCtl ctl;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gb_raw) + 1023) & ~(uintptr_t)1023);
   float* epi = reinterpret_cast<float*>(smem + (size_t)GB_STAGES * GB_STAGE_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const bool leader = crank == 0;
+  constexpr uint16_t kPair = 0x3;
   volatile int* abort_flag = &ctl.abort_flag;
   const int G = a.off ? a.G : 1;
   const int nt = (a.N + GB_BN - 1) / GB_BN;
   if (threadIdx.x == 0) {
     for (int s = 0; s < GB_STAGES; ++s) {
-      mbar_init(smem_u32(&ctl.full[s]), 1);
+      mbar_init(smem_u32(&ctl.full[s]), 1);  // the leader's arrive_expect_tx (both CTAs' bytes)
       mbar_init(smem_u32(&ctl.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl.tfull[b]), 1);
-      mbar_init(smem_u32(&ctl.tempty[b]), 4);  // one arrive per epilogue warp
+      mbar_init(smem_u32(&ctl.tempty[b]), 8);  // one arrive per epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl.mma_done), 1);
     ctl.abort_flag = 0;
@@ -100,9 +109,9 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
     tma_prefetch_desc(&map_b);
     if (a.b_mn && a.ksplit < a.K) tma_prefetch_desc(&map_b2);
   }
-  if (warp == 2) {
-    tmem_alloc(smem_u32(&ctl.tmem_base), GB_TMEM_COLS);
-    tmem_relinquish();
+  if (warp == 2) {  // both CTAs of the pair allocate together and receive the same address
+    tmem_alloc_cg2(smem_u32(&ctl.tmem_base), GB_TMEM_COLS);
+    tmem_relinquish_cg2();
   }
   if (warp == 3) {  // tiles per group and their exclusive prefix; lane owns groups [8 lane, 8 lane + 8)
     int cnt[8], local = 0;
@@ -115,8 +124,8 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
         const int hi = a.off ? a.off[g + 1] : a.rows;
         ctl.lo[g] = lo;
         if (g == G - 1) ctl.lo[G] = hi;
-        const int mt = a.rows_on_k ? (a.M + GB_BM - 1) / GB_BM : (hi > lo ? (hi - lo + GB_BM - 1) / GB_BM : 0);
-        cnt[i] = mt * nt;
+        const int span = a.rows_on_k ? a.M : (hi > lo ? hi - lo : 0);
+        cnt[i] = (span + 2 * GB_BM - 1) / (2 * GB_BM) * nt;
         local += cnt[i];
       }
     }
@@ -137,10 +146,13 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = ctl.tmem_base;
   const int total = ctl.pre[G];
+  const int pair = (int)blockIdx.x >> 1, npairs = (int)gridDim.x >> 1;
 
+  // this CTA's part of tile u: its 128 rows of the pair's 256, the pair's 256 columns
   auto decode = [&](int u) {
     int lo = 0, hi = G - 1;  // the last group whose first tile is at or before u
     while (lo < hi) {
@@ -155,13 +167,13 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
     t.n0 = (r % nt) * GB_BN;
     const int glo = ctl.lo[lo], ghi = ctl.lo[lo + 1];
     if (a.rows_on_k) {
-      t.m0 = mt * GB_BM;
-      t.mrows = min(GB_BM, a.M - t.m0);
+      t.m0 = mt * 2 * GB_BM + (int)crank * GB_BM;
+      t.mrows = max(0, min(GB_BM, a.M - t.m0));
       t.k0 = glo;
       t.kb = (ghi - glo) / GB_BK;
     } else {
-      t.m0 = glo + mt * GB_BM;
-      t.mrows = min(GB_BM, ghi - t.m0);
+      t.m0 = glo + mt * 2 * GB_BM + (int)crank * GB_BM;
+      t.mrows = max(0, min(GB_BM, ghi - t.m0));
       t.k0 = 0;
       t.kb = a.K / GB_BK;
     }
@@ -173,49 +185,52 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
       bool aborted = false;
-      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x) {
+      for (int u = pair; u < total && !aborted; u += npairs) {
         const GbTile t = decode(u);
+        const int nb = t.n0 + (int)crank * (GB_BN / 2);  // this CTA's half of B
         for (int kb = 0; kb < t.kb; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&ctl.empty[s]), ph ^ 1u, abort_flag, a.status)) {
             aborted = true;
             break;
           }
-          armed &= ~(1u << s);
           const uint32_t sa = smem_u32(smem + (size_t)s * GB_STAGE_BYTES), sb = sa + GB_A_BYTES;
           const uint32_t fb = smem_u32(&ctl.full[s]);
-          mbar_arrive_expect_tx(fb, GB_STAGE_BYTES);
+          const uint32_t lb = mapa_rank(fb, 0);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, 2u * GB_STAGE_BYTES);
+            armed |= 1u << s;
+            armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          }
           const int kc = t.k0 + kb * GB_BK;
-          tma_load_2d(sa, &map_a, fb, kc, t.m0);
+          tma_load_2d_cg2(sa, &map_a, lb, kc, t.m0);
           if (a.rows_on_k) {
-            tma_load_2d(sb, &map_b, fb, kc, t.n0);
-          } else if (a.b_mn) {  // four boxes of 64 n by 64 k, 8 KB apart
+            tma_load_2d_cg2(sb, &map_b, lb, kc, nb);
+          } else if (a.b_mn) {  // two boxes of 64 n by 64 k, 8 KB apart
             const bool lo_half = kc < a.ksplit;
             const CUtensorMap* mb = lo_half ? &map_b : &map_b2;
             const int kl = lo_half ? kc : kc - a.ksplit;
 #pragma unroll
-            for (int j = 0; j < GB_BN / 64; ++j) tma_load_3d(sb + j * 8192, mb, fb, t.n0 + 64 * j, kl, t.g);
+            for (int j = 0; j < GB_BN / 2 / 64; ++j) tma_load_3d_cg2(sb + j * 8192, mb, lb, nb + 64 * j, kl, t.g);
           } else {
-            tma_load_3d(sb, &map_b, fb, kc, t.n0, t.g);
+            tma_load_3d_cg2(sb, &map_b, lb, kc, nb, t.g);
           }
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           if (++s == GB_STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
       }
-      if (aborted)  // every armed copy lands before the CTA leaves
+      if (aborted && leader)  // both CTAs' armed copies land (or the wait runs out) before leaving
         for (int i = 0; i < GB_STAGES; ++i)
           if ((armed >> i) & 1u) gb_drain(smem_u32(&ctl.full[i]), (armed_ph >> i) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int s = 0, it = 0;
       uint32_t ph = 0;
       bool aborted = false;
-      const uint32_t idesc = umma_idesc_bf16(GB_BM, GB_BN) | (a.b_mn ? (1u << 16) : 0u);  // bit 16: B MN-major
-      for (int u = blockIdx.x; u < total && !aborted; u += gridDim.x, ++it) {
+      const uint32_t idesc = umma_idesc_bf16(2 * GB_BM, GB_BN) | (a.b_mn ? (1u << 16) : 0u);  // bit 16: B MN-major
+      for (int u = pair; u < total && !aborted; u += npairs, ++it) {
         const GbTile t = decode(u);
         const int acc = it & 1;
         const uint32_t aph = (uint32_t)(it >> 1) & 1u;
@@ -233,25 +248,29 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
           for (int kk = 0; kk < GB_BK / 16; ++kk) {
             // K-major: 16 k are 32 bytes along a row; N-major: 16 k are 16 rows of 128 bytes
             const uint64_t bdesc = a.b_mn ? sdesc_mn_sw128(sb + kk * 2048, 8192) : sdesc_k_sw128(sb + kk * 32);
-            umma_bf16(d_tmem, sdesc_k_sw128(sa + kk * 32), bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_cg2(d_tmem, sdesc_k_sw128(sa + kk * 32), bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&ctl.empty[s]));  // the stage is free once these MMAs have read it
+          umma_commit_cg2_mc(smem_u32(&ctl.empty[s]), kPair);  // both CTAs' copies of the stage are free
           if (++s == GB_STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (aborted) break;
-        if (t.kb > 0) umma_commit(smem_u32(&ctl.tfull[acc]));
-        else mbar_arrive(smem_u32(&ctl.tfull[acc]));  // nothing to sum: the epilogue writes zeros
+        if (t.kb > 0) {
+          umma_commit_cg2_mc(smem_u32(&ctl.tfull[acc]), kPair);  // both CTAs' accumulators are full
+        } else {  // nothing to sum: both epilogues write zeros
+          mbar_arrive_cluster(mapa_rank(smem_u32(&ctl.tfull[acc]), 0));
+          mbar_arrive_cluster(mapa_rank(smem_u32(&ctl.tfull[acc]), 1));
+        }
       }
-      umma_commit(smem_u32(&ctl.mma_done));
+      umma_commit_cg2_mc(smem_u32(&ctl.mma_done), kPair);
       gb_drain(smem_u32(&ctl.mma_done), 0);
     }
   } else {
-    const int q = warp & 3;  // this warp reads TMEM lanes 32 q .. 32 q + 31 (tile rows)
+    const int q = warp & 3;  // this warp reads TMEM lanes 32 q .. 32 q + 31 (its CTA's tile rows)
     int it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+    for (int u = pair; u < total; u += npairs, ++it) {
       const GbTile t = decode(u);
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
@@ -290,7 +309,7 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
           // tensor map's 128-byte swizzle); rows past M are clipped by the map
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && 32 * q < t.mrows) {
+          if (lane == 0 && rows_here > 0) {
             tma_store_3d(&map_c, smem_u32(stg), t.n0 + 32 * c, t.m0 + 32 * q, t.g);
             bulk_commit();
           }
@@ -316,25 +335,51 @@ __global__ void __launch_bounds__(GB_THREADS, 1) k_gemm_bwd(const __grid_constan
         }
         __syncwarp();
       }
+      // the accumulator's reads have completed (tcgen05.wait::ld above): a plain remote arrive (no
+      // cluster-wide release, which costs ~0.5 us) tells the leader it may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&ctl.tempty[acc]));
+      if (lane == 0) mbar_arrive_remote(mapa_rank(smem_u32(&ctl.tempty[acc]), 0));
     }
     if (lane == 0) bulk_wait_all();  // every tile store has completed before the CTA leaves
     __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
+  // no signal of the peer can still be in flight towards this CTA, and neither CTA's TMEM is in
+  // use, when the pair frees its TMEM together
+  cluster_sync_all();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, GB_TMEM_COLS);
+    tmem_dealloc_cg2(tmem_base, GB_TMEM_COLS);
   }
 }
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+// Pairs that fit the GPU at once (one CTA per SM): co-resident 2-CTA clusters of this kernel,
+// asked once per device.
+int max_pairs() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  if (ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_bwd), GB_SMEM) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(GB_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GB_SMEM;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_bwd, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
     return 0;
+  }
+  cached[dev] = n;
   return n;
 }
 
@@ -343,10 +388,10 @@ cudaError_t launch_gb(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
   if (tiles_bound <= 0) return cudaSuccess;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k_gemm_bwd), GB_SMEM);
   if (e != cudaSuccess) return e;
-  const int nsm = sm_count();
-  if (nsm <= 0) return cudaErrorInvalidDevice;
-  const int grid = (int)(tiles_bound < nsm ? tiles_bound : nsm);
-  k_gemm_bwd<<<grid, GB_THREADS, GB_SMEM, st>>>(ma, mb, mb2, mc, a);
+  const int npairs_max = max_pairs();
+  if (npairs_max <= 0) return cudaErrorInvalidDevice;
+  const long pairs = tiles_bound < npairs_max ? tiles_bound : npairs_max;
+  k_gemm_bwd<<<(unsigned)(2 * pairs), GB_THREADS, GB_SMEM, st>>>(ma, mb, mb2, mc, a);  // cluster dims (2, 1, 1)
   return cudaGetLastError();
 }
 
@@ -392,7 +437,7 @@ cudaError_t launch_gemm_bwd_rows_m_nmajor(const void* A, int rows_alloc, const v
   } else {
     const cuuint64_t db[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)G_w};
     const cuuint64_t sb[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
-    const cuuint32_t bb[3] = {GB_BK, GB_BN, 1};
+    const cuuint32_t bb[3] = {GB_BK, GB_BN / 2, 1};
     if (!make_tmap_bf16(&mb, B, 3, db, sb, bb)) return cudaErrorInvalidValue;
     mb2 = mb;
   }
@@ -410,7 +455,7 @@ cudaError_t launch_gemm_bwd_rows_m_nmajor(const void* A, int rows_alloc, const v
   a.beta = beta;
   a.status = status;
   const long nt = (N + GB_BN - 1) / GB_BN;
-  const long rt = off ? (long)(rows_alloc + GB_BM - 1) / GB_BM + G : (long)(rows + GB_BM - 1) / GB_BM;
+  const long rt = off ? (long)(rows_alloc + 2 * GB_BM - 1) / (2 * GB_BM) + G : (long)(rows + 2 * GB_BM - 1) / (2 * GB_BM);
   return launch_gb(ma, mb, mb2, mb, a, rt * nt, st);  // (the C map is unused on rows on M)
 }
 
@@ -431,7 +476,7 @@ cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, i
   const cuuint64_t da[2] = {(cuuint64_t)Kp, (cuuint64_t)M};
   const cuuint64_t db[2] = {(cuuint64_t)Kp, (cuuint64_t)N};
   const cuuint64_t s[1] = {(cuuint64_t)Kp * 2};
-  const cuuint32_t ba[2] = {GB_BK, GB_BM}, bb[2] = {GB_BK, GB_BN};
+  const cuuint32_t ba[2] = {GB_BK, GB_BM}, bb[2] = {GB_BK, GB_BN / 2};
   if (!make_tmap_bf16(&ma, A, 2, da, s, ba) || !make_tmap_bf16(&mb, B, 2, db, s, bb)) return cudaErrorInvalidValue;
   GbArgs a{};
   a.rows_on_k = 1;
@@ -446,7 +491,7 @@ cudaError_t launch_gemm_bwd_rows_k(const void* A, int M, const void* B, int N, i
   a.beta = beta;
   a.status = status;
   a.ksplit = 0;
-  const long tiles = (long)(off ? G : 1) * ((M + GB_BM - 1) / GB_BM) * ((N + GB_BN - 1) / GB_BN);
+  const long tiles = (long)(off ? G : 1) * ((M + 2 * GB_BM - 1) / (2 * GB_BM)) * ((N + GB_BN - 1) / GB_BN);
   return launch_gb(ma, mb, mb, mc, a, tiles, st);
 }
 

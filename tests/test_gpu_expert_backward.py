@@ -42,6 +42,12 @@ CASES = {
                                 n_shared=1, seed=75, wseed=75),
     "fp32_swiglu_E64": Workload("ebw_fp32_swiglu_E64", T=200, d=192, E=64, k=6, dff=128, act="swiglu",
                                 dtype="f32", n_shared=1, seed=76, wseed=76),
+    # the largest expert count (256 groups in the tensor-core GEMM's tile table), top-8
+    "bf16_E256_k8": Workload("ebw_bf16_E256_k8", T=96, d=128, E=256, k=8, dff=64, act="swiglu", dtype="bf16",
+                             seed=77, wseed=77),
+    # decode-shaped: 32 tokens, d = 2048 (32 K steps per tile), 64 experts, two shared experts
+    "bf16_decode": Workload("ebw_bf16_decode", T=32, d=2048, E=64, k=6, dff=256, act="swiglu", dtype="bf16",
+                            n_shared=2, seed=78, wseed=78),
 }
 
 # bf16 layers contract on the tensor cores with the operands the backward creates (du, dg or da,
