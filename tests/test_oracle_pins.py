@@ -390,6 +390,23 @@ def check_backward(o, b=None):
     g = b.moe_layer_backward(inp, np.zeros((6, 4)), E=3, k=3, act="gelu", z_coef=0.5, dlb=0.0, dzl=1.0)
     P, lse = o.softmax_lse(inp["x"] @ inp["w_router"].T)
     np.testing.assert_allclose(g["dw_router"], ((2 * 0.5 * lse / 6)[:, None] * P).T @ inp["x"], rtol=1e-12, atol=1e-14)
+    # the task loss <dy, y> is a sum over tokens, and dropless routing treats each token alone: its
+    # gradient over a batch is the sum of the gradients over any split of the batch (what a data-
+    # parallel all-reduce of per-rank gradients relies on); dx is the halves' rows side by side
+    inp = _bwd_case(rng, 10, 5, 4, 2, 3, "swiglu", False, 1)
+    dy = rng.standard_normal((10, 5))
+    kw = dict(E=4, k=2, act="swiglu", n_shared=1, dlb=0.0, dzl=0.0)
+    whole = b.moe_layer_backward(inp, dy, **kw)
+    halves = []
+    for sl in (slice(0, 4), slice(4, 10)):
+        part = dict(inp)
+        part["x"] = inp["x"][sl]
+        halves.append(b.moe_layer_backward(part, dy[sl], **kw))
+    for name, v in whole.items():
+        if name == "dx":
+            np.testing.assert_allclose(np.concatenate([halves[0]["dx"], halves[1]["dx"]]), v, rtol=1e-12, atol=1e-12)
+        else:
+            np.testing.assert_allclose(halves[0][name] + halves[1][name], v, rtol=1e-12, atol=1e-12, err_msg=name)
 
 
 def check_fp8(o):
