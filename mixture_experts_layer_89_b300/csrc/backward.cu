@@ -271,9 +271,9 @@ cudaError_t router_bwd_tc(const __nv_bfloat16* x, const __nv_bfloat16* wr, const
                                                             z_coef, dlb, dzl, dz);
   k_split_hi_lo<<<592, 256, 0, st>>>(dz, T_, E, sc.dzs);
   const dim3 tb(32, 8);
-  k_transpose_pad<<<dim3(Tp / 64, (2 * E + 63) / 64), tb, 0, st>>>(sc.dzs, 2 * E, 2 * E, nullptr, nullptr, 1, T_,
+  k_transpose_pad<<<dim3(Tp / 64, (2 * E + 127) / 128), tb, 0, st>>>(sc.dzs, 2 * E, 2 * E, nullptr, nullptr, 1, T_,
                                                                    sc.dzsT, Tp);
-  k_transpose_pad<<<dim3(Tp / 64, (d + 63) / 64), tb, 0, st>>>(x, d, d, nullptr, nullptr, 1, T_, sc.xT, Tp);
+  k_transpose_pad<<<dim3(Tp / 64, (d + 127) / 128), tb, 0, st>>>(x, d, d, nullptr, nullptr, 1, T_, sc.xT, Tp);
   e = cudaGetLastError();
   if (e == cudaSuccess)  // [hi^T; lo^T] x over the tokens
     e = launch_gemm_bwd_rows_k(sc.dzsT, 2 * E, sc.xT, d, Tp, nullptr, 1, Tp, sc.part, d, (int64_t)2 * E * d, 0,
@@ -435,17 +435,19 @@ __global__ void k_pad_offsets(const int32_t* __restrict__ off, int G, int32_t* _
 
 // out [C][Kp]: padded column p of group g (koff[g] <= p < koff[g+1]) holds row off[g] + p - koff[g]
 // of in [rows][ldi] while that row is the group's, else zero.  off / koff NULL: one group of `rows`
-// rows, padded to a multiple of 64.  64 padded columns x 64 channels per block, moved as bf16 pairs
-// (C, ldi and Kp even; each block's 64 columns lie in one group).
+// rows, padded to a multiple of 64.  A block moves 64 padded columns x 128 channels: 16-byte loads
+// of 8 channels of a row (all four issued before the shared-memory writes), bf16 pairs in shared
+// memory, 16-byte stores of 8 padded columns of a channel (C, ldi a multiple of 8; Kp of 64; each
+// block's 64 columns lie in one group).
 __global__ void __launch_bounds__(256) k_transpose_pad(const __nv_bfloat16* __restrict__ in, int64_t ldi, int C,
                                                        const int32_t* __restrict__ off,
                                                        const int32_t* __restrict__ koff, int G, int rows,
                                                        __nv_bfloat16* __restrict__ out, int64_t Kp) {
-  __shared__ uint32_t tw[64][33];  // [padded column][channel pair]
+  __shared__ uint32_t tw[64][65];  // [padded column][channel pair]
   __shared__ int s_r0, s_hi, s_live;
-  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  if (tx == 0 && ty == 0) {
+  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 128;
+  const int tid = threadIdx.y * 32 + threadIdx.x;
+  if (tid == 0) {
     int live = 0, r0 = 0, hi = 0;
     if (off) {
       if (p0 < koff[G]) {
@@ -471,18 +473,35 @@ __global__ void __launch_bounds__(256) k_transpose_pad(const __nv_bfloat16* __re
   __syncthreads();
   if (!s_live) return;
   const int r0 = s_r0, hi = s_hi;
-  for (int i = ty; i < 64; i += 8) {
-    const int r = r0 + i, c = c0 + 2 * tx;
-    tw[i][tx] = (r < hi && c < C) ? *reinterpret_cast<const uint32_t*>(in + (size_t)r * ldi + c) : 0u;
+  const int cc = (tid & 15) * 8;  // this thread's 8 channels of a row
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rl = i * 16 + (tid >> 4), r = r0 + rl;
+    v[i] = (r < hi && c0 + cc < C) ? *reinterpret_cast<const uint4*>(in + (size_t)r * ldi + c0 + cc)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rl = i * 16 + (tid >> 4);
+    tw[rl][cc / 2 + 0] = v[i].x;
+    tw[rl][cc / 2 + 1] = v[i].y;
+    tw[rl][cc / 2 + 2] = v[i].z;
+    tw[rl][cc / 2 + 3] = v[i].w;
   }
   __syncthreads();
-  for (int j = ty; j < 64; j += 8) {
-    const int c = c0 + j;
-    if (c >= C) break;
-    const uint32_t w0 = tw[2 * tx][j >> 1], w1 = tw[2 * tx + 1][j >> 1];
-    const uint32_t lo = (j & 1) ? (w0 >> 16) : (w0 & 0xFFFFu);
-    const uint32_t hi2 = (j & 1) ? (w1 >> 16) : (w1 & 0xFFFFu);
-    *reinterpret_cast<uint32_t*>(out + (size_t)c * Kp + p0 + 2 * tx) = lo | (hi2 << 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int o = i * 256 + tid;
+    const int ch = o >> 3, pc = o & 7;  // channel of the tile, 8-column chunk of the output row
+    const int c = c0 + ch;
+    if (c >= C) continue;
+    const int j = ch >> 1, sh = (ch & 1) * 16;
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) w[q] = (tw[8 * pc + q][j] >> sh) & 0xFFFFu;
+    const uint4 pk = make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16), w[6] | (w[7] << 16));
+    *reinterpret_cast<uint4*>(out + (size_t)c * Kp + p0 + 8 * pc) = pk;
   }
 }
 
@@ -657,10 +676,10 @@ cudaError_t ffn_bwd_tc(const ExpertBackward& b, bool glu, const __nv_bfloat16* x
   const int64_t Kp = b.Kp;
   const int pad_cols = off ? (int)Kp : ((rows + 63) & ~63);
   const unsigned px = (unsigned)(pad_cols / 64);
-  k_transpose_pad<<<dim3(px, (Kd + 63) / 64), tb, 0, st>>>(b.D, Kd, Kd, off, koff, G, rows, b.DT, Kp);
-  k_transpose_pad<<<dim3(px, (f + 63) / 64), tb, 0, st>>>(b.h, f, f, off, koff, G, rows, b.hT, Kp);
-  k_transpose_pad<<<dim3(px, (d + 63) / 64), tb, 0, st>>>(xr, d, d, off, koff, G, rows, b.xT, Kp);
-  k_transpose_pad<<<dim3(px, (d + 63) / 64), tb, 0, st>>>(dyr, d, d, off, koff, G, rows, b.dyT, Kp);
+  k_transpose_pad<<<dim3(px, (Kd + 127) / 128), tb, 0, st>>>(b.D, Kd, Kd, off, koff, G, rows, b.DT, Kp);
+  k_transpose_pad<<<dim3(px, (f + 127) / 128), tb, 0, st>>>(b.h, f, f, off, koff, G, rows, b.hT, Kp);
+  k_transpose_pad<<<dim3(px, (d + 127) / 128), tb, 0, st>>>(xr, d, d, off, koff, G, rows, b.xT, Kp);
+  k_transpose_pad<<<dim3(px, (d + 127) / 128), tb, 0, st>>>(dyr, d, d, off, koff, G, rows, b.dyT, Kp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int cols = (rows + 63) & ~63;
