@@ -171,7 +171,7 @@ ExpertBwdScratch expert_bwd_scratch(const moe_config* c) {
 // Scratch of the router backward's tensor-core path: bf16 layers with E a multiple of 64 and T > 0;
 // 0 bytes otherwise (the CUDA-core path needs none).
 struct RouterBwdLayout {
-  size_t status, dzs, dzsT, xT, part, total;
+  size_t status, dzs, dzsT, xT, part, koff, total;
 };
 
 RouterBwdLayout route_bwd_layout(const moe_config* c) {
@@ -188,7 +188,8 @@ RouterBwdLayout route_bwd_layout(const moe_config* c) {
   L.dzs = take((size_t)c->T * 2 * E * 2);
   L.dzsT = take(2 * E * Tp * 2);
   L.xT = take(d * Tp * 2);
-  L.part = take(2 * E * d * 4);
+  L.part = take((size_t)kRouterBwdSlices * 2 * E * d * 4);
+  L.koff = take((kRouterBwdSlices + 1) * 4);
   L.total = off;
   return L;
 }
@@ -744,6 +745,7 @@ moe_status moe_route_backward(const moe_config* cfg, const void* x, const void* 
     sc.dzsT = at<__nv_bfloat16>(scratch, L.dzsT);
     sc.xT = at<__nv_bfloat16>(scratch, L.xT);
     sc.part = at<float>(scratch, L.part);
+    sc.koff = at<int32_t>(scratch, L.koff);
   }
   return cuda_status(launch_router_backward(is_bf16(cfg), x, w_router, logit_bias, topk_idx, topk_w, counts, dw,
                                             cfg->T, cfg->d, cfg->E, cfg->k, inv_tau_of(cfg), cfg->lb_coef,

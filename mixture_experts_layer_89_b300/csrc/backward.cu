@@ -245,10 +245,21 @@ __global__ void __launch_bounds__(256) k_split_hi_lo(const float* __restrict__ d
   }
 }
 
-// out[i] = part[i] + part[n + i]: the hi and lo halves of dW_r summed.
-__global__ void __launch_bounds__(256) k_sum_halves(const float* __restrict__ part, size_t n, float* __restrict__ out) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-    out[i] = part[i] + part[n + i];
+// out[i] = the hi and lo halves of dW_r over the S token slices, summed in slice order:
+// part [S][2][n] (hi rows first, then lo rows, per slice).
+__global__ void __launch_bounds__(256) k_sum_halves(const float* __restrict__ part, int S, size_t n,
+                                                    float* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int q = 0; q < S; ++q) v += part[(size_t)q * 2 * n + i] + part[(size_t)q * 2 * n + n + i];
+    out[i] = v;
+  }
+}
+
+// koff[s] = the first padded token column of slice s of [0, Tp) (multiples of 64), koff[S] = Tp.
+__global__ void k_slice_offsets(int Tp, int S, int32_t* __restrict__ koff) {
+  const int s = threadIdx.x;
+  if (s <= S) koff[s] = (int)((int64_t)(Tp / 64) * s / S) * 64;
 }
 
 // bf16 layers with E a multiple of 64 and a scratch: the three contractions on the tensor cores
@@ -274,12 +285,19 @@ cudaError_t router_bwd_tc(const __nv_bfloat16* x, const __nv_bfloat16* wr, const
   k_transpose_pad<<<dim3(Tp / 64, (2 * E + 127) / 128), tb, 0, st>>>(sc.dzs, 2 * E, 2 * E, nullptr, nullptr, 1, T_,
                                                                    sc.dzsT, Tp);
   k_transpose_pad<<<dim3(Tp / 64, (d + 127) / 128), tb, 0, st>>>(x, d, d, nullptr, nullptr, 1, T_, sc.xT, Tp);
-  e = cudaGetLastError();
-  if (e == cudaSuccess)  // [hi^T; lo^T] x over the tokens
-    e = launch_gemm_bwd_rows_k(sc.dzsT, 2 * E, sc.xT, d, Tp, nullptr, 1, Tp, sc.part, d, (int64_t)2 * E * d, 0,
-                               sc.status, st);
+  // [hi^T; lo^T] x over the tokens, split into S slices of the token columns (groups of the GEMM)
+  // so that enough pairs share the few 2E x d output tiles; partials summed in slice order
+  const int tiles = ((2 * E + 255) / 256) * ((d + 255) / 256);
+  const int S = max(1, min(min(kRouterBwdSlices, 64 / tiles), Tp / 64));
+  if (S > 1) {
+    k_slice_offsets<<<1, 32, 0, st>>>(Tp, S, sc.koff);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess)  // one slice: a single group of Tp columns, no offsets array
+    e = launch_gemm_bwd_rows_k(sc.dzsT, 2 * E, sc.xT, d, Tp, S > 1 ? sc.koff : nullptr, S, Tp, sc.part, d,
+                               (int64_t)2 * E * d, 0, sc.status, st);
   if (e != cudaSuccess) return e;
-  k_sum_halves<<<592, 256, 0, st>>>(sc.part, (size_t)E * d, dwr);
+  k_sum_halves<<<592, 256, 0, st>>>(sc.part, S, (size_t)E * d, dwr);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // dx = [hi | lo] [W_r; W_r]

@@ -127,11 +127,14 @@ cudaError_t launch_combine_backward(bool bf16, const void* dy, const float* y_pe
                                     const float* topk_w, int T, int d, int k, float* dw, void* dy_perm,
                                     cudaStream_t st);
 // Scratch of the router backward's tensor-core path (bf16 layers, E a multiple of 64): status
-// word, dzs [T][2E] and dzsT [2E][Tp] bf16, xT [d][Tp] bf16, part [2E][d] fp32 (Tp = T padded to 64).
+// word, dzs [T][2E] and dzsT [2E][Tp] bf16, xT [d][Tp] bf16, part [kRouterBwdSlices][2E][d] fp32
+// and koff [kRouterBwdSlices + 1] (Tp = T padded to 64).
+constexpr int kRouterBwdSlices = 8;
 struct RouterBwdScratch {
   uint32_t* status;
   __nv_bfloat16 *dzs, *dzsT, *xT;
   float* part;
+  int32_t* koff;
 };
 // sc == NULL (or an fp32 layer): the CUDA-core path.
 cudaError_t launch_router_backward(bool bf16, const void* x, const void* wr, const float* lbias, const int32_t* idx,

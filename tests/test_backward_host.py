@@ -39,7 +39,9 @@ def _route_scratch(wl):
     if wl.dtype != "bf16" or wl.E % 64 or wl.T <= 0:
         return 0
     Tp, E, d, T = _r64(wl.T), wl.E, wl.d, wl.T
-    return sum(_r256(p) for p in (256, T * 2 * E * 2, 2 * E * Tp * 2, d * Tp * 2, 2 * E * d * 4))
+    slices = 8  # the token slices the dW_r contraction may be split into
+    return sum(_r256(p) for p in (256, T * 2 * E * 2, 2 * E * Tp * 2, d * Tp * 2, slices * 2 * E * d * 4,
+                                  (slices + 1) * 4))
 
 
 NAMES = ["tiny_fp32", "flash_bf16", "finegrained_bf16", "decode_bf16", "skewed_bf16", "skewed_cf1_bf16"]
