@@ -1,6 +1,6 @@
 /*
- * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN layer: the forward pass,
- * and the backward of its routing half.
+ * moe.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts FFN layer: the forward pass and
+ * the backward pass (routing half and expert FFNs).
  *
  * The layer (mini-moe tutorial, sec. 3.1 MoELayer; OpenMythos article, sec. 3.1; FLAME-MoE
  * summary, sec. 2) maps T tokens x[T,d] to y[T,d]:
@@ -298,11 +298,11 @@ moe_status moe_quantize_experts(const void* w, int32_t dtype, int32_t format, in
                                 int32_t rows, int32_t cols, void* codes, float* scale,
                                 int32_t* nonfinite, void* stream);
 
-/* Backward of the routing half of the layer (a first part of the backward pass; the expert FFNs'
- * gradients are not provided).  The objective is L = sum_t <dy_t, y_t> + dlb lb + dzl zl (the pages
- * train with the load-balance loss and the router z-loss added: mini-moe tutorial, training loop;
- * FLAME-MoE summary, sec. 2).  Top-k selection, capacity drops and the expert counts pass no
- * gradient.  All sums in a fixed order; fp32 on CUDA cores.
+/* Backward pass of the layer, in three calls: moe_combine_backward, moe_route_backward and
+ * moe_expert_ffn_backward (below).  The objective is L = sum_t <dy_t, y_t> + dlb lb + dzl zl (the
+ * pages train with the load-balance loss and the router z-loss added: mini-moe tutorial, training
+ * loop; FLAME-MoE summary, sec. 2).  Top-k selection, capacity drops and the expert counts pass no
+ * gradient.  All sums in a fixed order (bit-identical repeats).
  *
  * moe_combine_backward (FLAME-MoE summary sec. 2: y = routing-weighted sum of the experts):
  *   dy [T,d] (layer dtype), y_perm [A_max,d] fp32, row_of [T,k], topk_w [T,k] as the forward

@@ -1,6 +1,5 @@
-// Backward of the routing half of the layer (a first part of the backward pass: the pages train
-// these layers with the load-balance and z-loss terms in the objective, the mini-moe tutorial's
-// training loop and the FLAME-MoE summary, sec. 2).
+// Backward pass of the layer (the pages train these layers with the load-balance and z-loss terms
+// in the objective: the mini-moe tutorial's training loop and the FLAME-MoE summary, sec. 2).
 //
 //   combine:  y_t = sum over kept slots j of w_tj y_perm[row_of[t, j]]  (+ shared experts)
 //             dL/dw_tj = <dy_t, y_perm[row]>   (0 for a dropped slot)
@@ -11,10 +10,13 @@
 //             (f_e = counts_e / (T k); top-k selection and counts pass no gradient); the z-loss
 //             beta mean_t lse_t^2 adds dzl 2 beta lse_t P_te / T; everything is divided by tau;
 //             then dW_r = dz^T x and dx = dz W_r.
-// Every sum runs in a fixed order (results do not depend on scheduling).  fp32 arithmetic on CUDA
-// cores (the three contractions -- logits, dz^T x, dz W_r -- through one register-tiled SGEMM):
-// they are small next to the expert GEMMs (E <= 256 columns), and fp32 keeps the gradients within
-// ~1e-6 of the exact ones.
+//   experts:  pre-activations recomputed from the permuted rows; dh = dy_perm W_down; the
+//             activation backward (du, dg or da, and h); dx_perm = du W_up + dg W_gate; the weight
+//             gradients dW_down = dy_perm^T h, dW_up = du^T x_perm, dW_gate = dg^T x_perm (and the
+//             bias sums) per expert; each token's rows added into dx; shared experts over all tokens.
+// Every sum runs in a fixed order (results do not depend on scheduling).  bf16 layers run the
+// contractions on the tensor cores (the grouped GEMM of gemm_bwd.cu); fp32 layers, and the router
+// without its scratch, on CUDA cores through one register-tiled SGEMM in fp32.
 #include <float.h>
 
 #include "common.cuh"
