@@ -17,8 +17,10 @@ counts and pass none either, which leaves its gradient on the mean probabilities
 
 Pins (tests/test_oracle_pins.py, check_backward): central finite differences of L, computed with
 the pinned forward oracle, on small layers whose top-k margins are far larger than the step, for
-every parameter tensor and the input; and k = E with identical experts, where the output does not
-depend on the router, so the router's gradient is exactly that of the two losses.
+every parameter tensor and the input; k = E with identical experts, where the output does not
+depend on the router, so the router's gradient is exactly that of the two losses; and the task
+loss's gradients over a dropless batch equal the sums of those over any split of it.  The routing
+half also against torch autograd (check_routing_backward).
 """
 from __future__ import annotations
 
