@@ -369,6 +369,25 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, 
                                    const void* dy, const void* dy_perm, const moe_expert_grads* g,
                                    float* dx, void* scratch, void* stream);
 
+/* Device pointers to the forward's intermediates inside a workspace (host-only pointer arithmetic,
+ * no GPU work).  After moe_layer_forward(cfg, ..., ws) they hold that call's topk_idx and topk_w
+ * [T,k], counts [E] (only when the call's counts_out was NULL: otherwise that array holds them),
+ * offsets [E+1], row_of [T,k], tok_of [A_max], x_perm [A_max,d] (layer dtype) and y_perm
+ * [A_max,d] fp32 -- what moe_combine_backward, moe_route_backward and moe_expert_ffn_backward
+ * take -- until the next call that uses the workspace.  MOE_ERR_INVALID_ARG for a NULL or
+ * misaligned workspace or a NULL v. */
+typedef struct {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_of;
+  int32_t* tok_of;
+  void* x_perm;
+  float* y_perm;
+} moe_forward_views;
+moe_status moe_workspace_views(const moe_config* cfg, void* ws, moe_forward_views* v);
+
 /* Static string for a status code. */
 const char* moe_status_string(moe_status s);
 

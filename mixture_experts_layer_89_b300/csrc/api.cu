@@ -810,6 +810,21 @@ moe_status moe_expert_ffn_backward(const moe_config* cfg, const moe_weights* w, 
   return cuda_status(launch_expert_backward(is_bf16(cfg), b, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_workspace_views(const moe_config* cfg, void* ws, moe_forward_views* v) {
+  MOE_TRY(validate(cfg));
+  if (!ws || !v || misaligned(ws)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = layout(cfg);
+  v->topk_idx = at<int32_t>(ws, L.topk_idx);
+  v->topk_w = at<float>(ws, L.topk_w);
+  v->counts = at<int32_t>(ws, L.counts);
+  v->offsets = at<int32_t>(ws, L.offsets);
+  v->row_of = at<int32_t>(ws, L.row_of);
+  v->tok_of = at<int32_t>(ws, L.tok_of);
+  v->x_perm = at<char>(ws, L.x_perm);
+  v->y_perm = at<float>(ws, L.y_perm);
+  return MOE_OK;
+}
+
 const char* moe_last_error(void) { return tc_last_error(); }
 
 const char* moe_status_string(moe_status s) {

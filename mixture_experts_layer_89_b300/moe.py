@@ -37,6 +37,11 @@ class MoeWeights(ctypes.Structure):
                 ("ss_gate", _c_p), ("ss_down", _c_p), ("sb_up", _c_p), ("sb_gate", _c_p), ("sb_down", _c_p)]
 
 
+class MoeForwardViews(ctypes.Structure):
+    _fields_ = [("topk_idx", _c_p), ("topk_w", _c_p), ("counts", _c_p), ("offsets", _c_p), ("row_of", _c_p),
+                ("tok_of", _c_p), ("x_perm", _c_p), ("y_perm", _c_p)]
+
+
 class MoeExpertGrads(ctypes.Structure):
     _fields_ = [("dw_up", _c_p), ("dw_gate", _c_p), ("dw_down", _c_p), ("db_up", _c_p), ("db_down", _c_p),
                 ("dws_up", _c_p), ("dws_gate", _c_p), ("dws_down", _c_p)]
@@ -90,6 +95,7 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_float, _c_p, _c_p, _c_p, _c_p, _c_p]
         L.moe_route_backward_scratch_size.argtypes = [cfgp, P(ctypes.c_size_t)]
         L.moe_expert_backward_scratch_size.argtypes = [cfgp, P(ctypes.c_size_t)]
+        L.moe_workspace_views.argtypes = [cfgp, _c_p, P(MoeForwardViews)]
         L.moe_expert_ffn_backward.argtypes = [cfgp, P(MoeWeights), _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                                               P(MoeExpertGrads), _c_p, _c_p, _c_p]
         L.moe_status_string.argtypes = [_c_i32]
@@ -101,7 +107,7 @@ def lib() -> ctypes.CDLL:
                      "moe_read_device_status", "moe_layer_forward_launches", "moe_route_stats",
                      "moe_set_wait_limit", "moe_route_diagnostics", "moe_quantize_experts", "moe_combine_backward",
                      "moe_route_backward", "moe_route_backward_scratch_size", "moe_expert_backward_scratch_size",
-                     "moe_expert_ffn_backward"):
+                     "moe_expert_ffn_backward", "moe_workspace_views"):
             getattr(L, name).restype = _c_i32
         _LIB = L
     return _LIB
@@ -111,7 +117,8 @@ EXPORTED = ("moe_workspace_size", "moe_capacity", "moe_route", "moe_route_noallo
             "moe_combine", "moe_layer_forward", "moe_layer_forward_timed", "moe_read_device_status",
             "moe_layer_forward_launches", "moe_route_stats", "moe_set_wait_limit", "moe_route_diagnostics",
             "moe_quantize_experts", "moe_combine_backward", "moe_route_backward", "moe_route_backward_scratch_size",
-            "moe_expert_backward_scratch_size", "moe_expert_ffn_backward", "moe_status_string", "moe_last_error")
+            "moe_expert_backward_scratch_size", "moe_expert_ffn_backward", "moe_workspace_views", "moe_status_string",
+            "moe_last_error")
 
 
 # ----------------------------------------------------------------------------- marshalling
@@ -273,6 +280,13 @@ def moe_route_backward(cfg, x, w_router, logit_bias, topk_idx, topk_w, counts, d
     _check(lib().moe_route_backward(ctypes.byref(cfg), _p(x), _p(w_router), _p(logit_bias), _p(topk_idx),
                                     _p(topk_w), _p(counts), _p(dw), float(dlb), float(dzl), _p(dz), _p(dw_router),
                                     _p(dx), _p(scratch), _s(stream)), "moe_route_backward")
+
+
+def moe_workspace_views(cfg: MoeConfig, ws) -> Dict[str, int]:
+    """Device addresses of the forward's intermediates inside workspace ``ws`` (see moe.h)."""
+    v = MoeForwardViews()
+    _check(lib().moe_workspace_views(ctypes.byref(cfg), _p(ws), ctypes.byref(v)), "moe_workspace_views")
+    return {name: getattr(v, name) for name, _ in MoeForwardViews._fields_}
 
 
 def moe_expert_backward_scratch_size(cfg: MoeConfig) -> int:

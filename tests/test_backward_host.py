@@ -104,3 +104,27 @@ def test_route_backward_argument_checks():
                                 None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_route_backward(ctypes.byref(cfg), *args, 1.0, 1.0, None, fake, fake, None,
                                 None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_views_lie_inside_the_workspace_and_do_not_overlap():
+    for name in ("flash_bf16", "decode_bf16", "tiny_fp32"):
+        wl = WORKLOADS[name]
+        cfg = moe.config_from_workload(wl)
+        base = 1 << 20  # 256-byte aligned, never dereferenced: the call is pointer arithmetic only
+        size = moe.moe_workspace_size(cfg)
+        v = moe.moe_workspace_views(cfg, base)
+        _, A = moe.moe_capacity(cfg)
+        elt = 2 if wl.dtype == "bf16" else 4
+        extent = {"topk_idx": wl.T * wl.k * 4, "topk_w": wl.T * wl.k * 4, "counts": wl.E * 4,
+                  "offsets": (wl.E + 1) * 4, "row_of": wl.T * wl.k * 4, "tok_of": A * 4, "x_perm": A * wl.d * elt,
+                  "y_perm": A * wl.d * 4}
+        spans = sorted((v[n], v[n] + extent[n], n) for n in extent)
+        for lo, hi, n in spans:
+            assert base <= lo and hi <= base + size and lo % 16 == 0, (name, n)
+        for (lo0, hi0, n0), (lo1, hi1, n1) in zip(spans, spans[1:]):
+            assert hi0 <= lo1, (name, n0, n1)
+    L = moe.lib()
+    cfg = moe.config_from_workload(WORKLOADS["flash_bf16"])
+    out = moe.MoeForwardViews()
+    assert L.moe_workspace_views(ctypes.byref(cfg), None, ctypes.byref(out)) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_workspace_views(ctypes.byref(cfg), (1 << 20) + 4, ctypes.byref(out)) == moe.MOE_ERR_INVALID_ARG

@@ -261,3 +261,39 @@ def test_expert_backward_empty_batch_and_arguments():
     for bad in (CASES["bf16_sparse_E64"].replace(backup=True), CASES["bf16_sparse_E64"].replace(weights8="int8")):
         c = moe.config_from_workload(bad)
         assert L.moe_expert_backward_scratch_size(ctypes.byref(c), ctypes.byref(n)) == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_backward_from_the_fused_forward_workspace():
+    """moe_layer_forward keeps its routing, rows and y_perm in the workspace; the backward calls fed
+    from moe_workspace_views give the same bits as when fed from the forward steps."""
+    wl = CASES["bf16_swiglu_cap_shared"]
+    inp_cpu = make_inputs(wl, "cpu")
+    inp = {k: (v.cuda() if v is not None else None) for k, v in inp_cpu.items()}
+    cfg = moe.config_from_workload(wl)
+    T, d, E, k = wl.T, wl.d, wl.E, wl.k
+    dy = torch.randn((T, d), generator=torch.Generator().manual_seed(5)).to(inp_cpu["x"].dtype).cuda()
+
+    def backward(topk_idx, topk_w, counts, offsets, row_of, x_perm, y_perm):
+        dw = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        dy_perm = torch.zeros(x_perm_shape, dtype=inp["x"].dtype, device="cuda")
+        moe.moe_combine_backward(cfg, dy, y_perm, row_of, topk_w, dw, dy_perm)
+        dz = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        dwr = torch.empty((E, d), dtype=torch.float32, device="cuda")
+        dx = torch.empty((T, d), dtype=torch.float32, device="cuda")
+        moe.moe_route_backward(cfg, inp["x"], inp["w_router"], inp.get("logit_bias"), topk_idx, topk_w, counts, dw,
+                               1.0, 1.0, dz, dwr, dx)
+        grads = _grad_tensors(wl, "cuda")
+        _run_expert_backward(cfg, inp, x_perm, offsets, row_of, dy, dy_perm, grads, dx)
+        torch.cuda.synchronize()
+        return dict(dw=dw, dz=dz, dw_router=dwr, dx=dx, **grads)
+
+    st = run_steps(wl, inp)
+    x_perm_shape = tuple(st["x_perm"].shape)
+    ref = backward(st["topk_idx"], st["topk_w"], st["counts"], st["offsets"], st["row_of"], st["x_perm"],
+                   st["y_perm"])
+    layer = moe.MoELayer(cfg, inp)
+    _, _, counts, _ = layer.forward(inp["x"])
+    v = moe.moe_workspace_views(cfg, layer.ws)
+    got = backward(v["topk_idx"], v["topk_w"], counts, v["offsets"], v["row_of"], v["x_perm"], v["y_perm"])
+    for name in ref:
+        assert torch.equal(ref[name], got[name]), name
